@@ -1,0 +1,427 @@
+"""Decode-step benchmark for the paged FP8-KV GQA path.
+
+One step = kv_append_fp8 of the step's new tokens (1 per sequence where the
+workload appends) + paged_gqa_decode over every cached token, on one batch of
+synthetic Llama-3-shaped inputs already resident in HBM.  Prints ONE JSON line
+(rank 0):
+
+  value      effective HBM GB/s of the decode step: algorithmic KV bytes
+             (sum_b L_b * Hkv * 2 * 128) / device time per step
+  e2e        the same metric through the public Python API with the step's
+             inputs copied from pinned host memory and the output copied back
+  roofline   the decode call (partial + combine kernels) against the measured
+             HBM copy bandwidth
+  cpu_baseline  the CPU oracle on a bounded sample of the same workload
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1] [--page 16]
+    python bench.py --impl reference ...      # the oracle as the reference arm
+
+With N > 1 (torchrun) every rank runs an independent replica: the path has no
+exchange step, so there is no collective beyond the timing barrier.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "paged FP8-KV GQA decode: µs/step and effective HBM GB/s (% of GB300 peak)"
+L2_BYTES = 129 * 1024 * 1024
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def _kernel_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("decode.cu", "device.cuh", "internal.h"):
+        with open(os.path.join(ROOT, "paged_fp8_kv_03_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(workload_name: str):
+    """dram bytes per decode launch from the committed ncu summary, if it was
+    taken on this exact kernel source and workload (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        t = json.load(fh)
+    ent = t.get(workload_name)
+    if not ent or ent.get("kernel_sha") != _kernel_sha():
+        return None
+    return ent.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled while the timed loop runs."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.path = tempfile.mktemp(prefix="pkv_clocks_", suffix=".csv")
+        self.proc = None
+        self.dev = device_index
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons, n = [], [], set(), 0
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for line in fh:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 10:
+                    continue
+                try:
+                    sm.append(float(parts[2]))
+                    smax.append(float(parts[3]))
+                except ValueError:
+                    continue
+                n += 1
+                for name, val in zip(names, parts[6:10]):
+                    if val.lower().startswith("active"):
+                        reasons.add(name)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": n}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def _fill_layer(pkv, wl, layer, dev):
+    P, H, D = wl.page_size, wl.hkv, wl.head_dim
+    ks, vs = wl.scales(layer, device=dev)
+    kc = torch.zeros((wl.num_pages, H, P, D), dtype=torch.uint8, device=dev)
+    vc = torch.zeros_like(kc)
+    chunk = 1 << 15
+    for b, L in enumerate(wl.prefill_lens):
+        for t0 in range(0, L, chunk):
+            t1 = min(L, t0 + chunk)
+            pkv.kv_append_fp8(wl.kv_rows(layer, 0, b, t0, t1, device=dev), wl.kv_rows(layer, 1, b, t0, t1, device=dev),
+                              wl.slots(b, t0, t1).to(dev), ks, vs, kc, vc)
+    return {"kc": kc, "vc": vc, "ks": ks, "vs": vs}
+
+
+def _step_inputs(wl, layer, dev):
+    """The per-step inputs: new K/V rows of the appended tokens, their slots, q."""
+    A = wl.append
+    if A:
+        k_new = torch.cat([wl.kv_rows(layer, 0, b, L, L + A, device=dev) for b, L in enumerate(wl.prefill_lens)])
+        v_new = torch.cat([wl.kv_rows(layer, 1, b, L, L + A, device=dev) for b, L in enumerate(wl.prefill_lens)])
+        slots = torch.cat([wl.slots(b, L, L + A) for b, L in enumerate(wl.prefill_lens)]).to(dev)
+    else:
+        k_new = v_new = slots = None
+    return {"k_new": k_new, "v_new": v_new, "slots": slots, "q": wl.q(layer, 0, device=dev)}
+
+
+def run_gpu(args, rank, world):
+    import paged_fp8_kv_03_gb300 as pkv
+    from paged_fp8_kv_03_gb300 import build as pbuild
+
+    if rank == 0 or not os.path.exists(pbuild.LIB):
+        pbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    pkv.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl = workloads.config(args.config, page_size=args.page)
+    kv_bytes = wl.kv_bytes()
+    # distinct layer caches rotated step by step so a step never finds the
+    # previous step's KV in L2 (each cache alone is already larger than L2)
+    n_layers = max(1, args.rotate or int(math.ceil(3 * L2_BYTES / kv_bytes)))
+    free, _ = torch.cuda.mem_get_info(dev)
+    n_layers = max(1, min(n_layers, int(0.8 * free // (kv_bytes + (1 << 20)))))
+    layers = [_fill_layer(pkv, wl, l, dev) for l in range(n_layers)]
+    steps_in = [_step_inputs(wl, l, dev) for l in range(n_layers)]
+    bt = wl.block_table().to(dev)
+    lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev)
+    out = torch.empty((wl.batch, wl.hq, wl.head_dim), dtype=torch.bfloat16, device=dev)
+    ws = pkv.decode_workspace(wl.batch, wl.hq, wl.hkv, wl.page_size, dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        c = layers[i % n_layers]
+        s = steps_in[i % n_layers]
+        if s["k_new"] is not None:
+            pkv.pkv_kv_append_fp8(s["k_new"], s["v_new"], s["slots"], c["ks"], c["vs"], c["kc"], c["vc"], err)
+        if ev is not None:
+            ev[0].record(stream)
+        pkv.pkv_paged_gqa_decode(s["q"], c["kc"], c["vc"], c["ks"], c["vs"], bt, lens, out, ws, device_error=err)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index)
+    if rank == 0:
+        clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i, evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if rank == 0 else None
+    total_ms = t_start.elapsed_time(t_end)
+    decode_ms = [a.elapsed_time(b) for a, b in evs]
+    if world > 1:
+        t = torch.tensor([total_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    assert int(err.item()) == 0, f"device error word {int(err.item())}"
+
+    # ---- end to end through the public API with host buffers
+    e2e_steps = min(args.steps, args.e2e_steps)
+    host = []
+    for l in range(n_layers):
+        s = steps_in[l]
+        h = {"q": s["q"].cpu().pin_memory(), "bt": bt.cpu().pin_memory(), "lens": lens.cpu().pin_memory()}
+        if s["k_new"] is not None:
+            h.update(k_new=s["k_new"].cpu().pin_memory(), v_new=s["v_new"].cpu().pin_memory(),
+                     slots=s["slots"].cpu().pin_memory())
+        host.append(h)
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host[0].values())
+    d2h = out.numel() * out.element_size()
+
+    def e2e_step(i):
+        c = layers[i % n_layers]
+        h = host[i % n_layers]
+        d = {k: v.to(dev, non_blocking=True) for k, v in h.items()}
+        if "k_new" in d:
+            pkv.kv_append_fp8(d["k_new"], d["v_new"], d["slots"], c["ks"], c["vs"], c["kc"], c["vc"])
+        o = pkv.paged_gqa_decode(d["q"], c["kc"], c["vc"], c["ks"], c["vs"], d["bt"], d["lens"], workspace=ws)
+        out_host.copy_(o, non_blocking=True)
+
+    for i in range(3):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    ms_per_step = total_ms / args.steps
+    value = world * kv_bytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    dec_ms = statistics.mean(decode_ms)
+    achieved = kv_bytes / (dec_ms * 1e-3) / 1e9
+    traffic = _traffic(wl.name)
+    launches_per_step = (1 if wl.append else 0) + 2
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 6),
+        "us_per_step": round(ms_per_step * 1e3, 3),
+        "frac_of_peak": round(value / world / peak, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "kv_dtype": "e4m3",
+        "data": "synthetic",
+        "config": {**wl.describe(), "kv_bytes_per_step": kv_bytes, "layer_caches_rotated": n_layers,
+                   "l2": "inputs larger than L2: each layer cache exceeds the 129 MB L2 and "
+                         f"{n_layers} distinct caches rotate step by step",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "kernel": "paged_gqa_decode (partial + split-K combine)",
+                     "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes,
+                     "avg_launch_us": round(dec_ms * 1e3, 3)},
+        "e2e": {"value": round(world * kv_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
+                "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, scale_device=dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+class OracleRig:
+    """The CPU oracle on this workload.  Pools, scales and prefill pages are
+    prepared once from host-generated inputs (untimed); step() times the
+    oracle's append of the step's tokens and its decode of whole sequences."""
+
+    def __init__(self, wl, scale_device="cpu"):
+        import oracle
+        self.oracle = oracle
+        self.wl = wl
+        ks, vs = wl.scales(0, device=scale_device)
+        self.ks, self.vs = ks.cpu().numpy(), vs.cpu().numpy()
+        shape = (wl.num_pages, wl.hkv, wl.page_size, wl.head_dim)
+        self.kc = np.zeros(shape, np.uint8)
+        self.vc = np.zeros(shape, np.uint8)
+        self.q = wl.q().view(torch.uint16).numpy()
+        self.bt = wl.block_table().numpy()
+        self.lens = np.array(wl.seq_lens, np.int32)
+        self.filled = set()
+
+    def fill(self, b):
+        if b in self.filled:
+            return
+        wl, L = self.wl, self.wl.prefill_lens[b]
+        sl = wl.slots(b, 0, L).numpy()
+        self.oracle.kv_append(wl.kv_rows(0, 0, b, 0, L).numpy(), sl, self.ks, self.kc)
+        self.oracle.kv_append(wl.kv_rows(0, 1, b, 0, L).numpy(), sl, self.vs, self.vc)
+        self.filled.add(b)
+
+    def step(self, seqs, threads):
+        wl = self.wl
+        for b in seqs:
+            self.fill(b)
+        new = [(wl.kv_rows(0, 0, b, wl.prefill_lens[b], wl.seq_lens[b]).numpy(),
+                wl.kv_rows(0, 1, b, wl.prefill_lens[b], wl.seq_lens[b]).numpy(),
+                wl.slots(b, wl.prefill_lens[b], wl.seq_lens[b]).numpy()) for b in seqs]
+        sel = np.array([[b, i] for b in seqs for i in range(wl.hq)], np.int32)
+        t0 = time.perf_counter()
+        for kn, vn, sl in new:
+            if len(sl):
+                self.oracle.kv_append(kn, sl, self.ks, self.kc)
+                self.oracle.kv_append(vn, sl, self.vs, self.vc)
+        self.oracle.paged_decode(self.q, self.kc, self.vc, self.ks, self.vs, self.bt, self.lens, sel=sel,
+                                 threads=threads)
+        dt = time.perf_counter() - t0
+        return dt, sum(wl.seq_lens[b] for b in seqs) * wl.hkv * 2 * wl.head_dim
+
+
+def cpu_baseline(wl, budget_s: float, scale_device="cpu") -> dict:
+    threads = len(os.sched_getaffinity(0))
+    rig = OracleRig(wl, scale_device)
+    done, secs, nbytes = [], 0.0, 0
+    for b in range(wl.batch):
+        if secs >= budget_s:
+            break
+        dt, nb = rig.step([b], threads)
+        done.append(b)
+        secs += dt
+        nbytes += nb
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"sequences {done[0]}..{done[-1]} ({len(done)} of {wl.batch}), all {wl.hq} query heads, "
+                      f"fp64 C oracle append+decode, {secs:.1f} s timed"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    wl = workloads.config(args.config, page_size=args.page)
+    threads = len(os.sched_getaffinity(0))
+    rig = OracleRig(wl)
+    per = []
+    nbytes = 0
+    for i in range(args.warmup + args.steps):
+        b = i % wl.batch
+        dt, nb = rig.step([b], threads)
+        if i >= args.warmup:
+            per.append(dt)
+            nbytes = nb
+    ms = 1e3 * statistics.mean(per)
+    value = nbytes / (ms * 1e-3) / 1e9
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {**wl.describe(), "kv_bytes_per_step": wl.kv_bytes()},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": "each step: one sequence (all query heads) of the workload, "
+                                       "fp64 C oracle append + decode"},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=3000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--page", type=int, default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--rotate", type=int, default=0, help="distinct layer caches (0 = auto)")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        backend = "nccl" if args.impl == "ours" else "gloo"
+        if args.impl == "ours":
+            torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
+        torch.distributed.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_gpu(args, rank, world)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,181 @@
+/*
+ * pagedfp8 -- paged FP8 (E4M3) KV cache and grouped-query decode attention
+ * for sm_103a (GB300).  Plain C ABI: device pointers, sizes, a CUDA stream.
+ *
+ * Sources for what the calls compute (prior art; no kernel API is given
+ * there):
+ *   [G]  "FP8量化与长上下文实测：Llama 3 70B部署优化指南" (sheratonhq.com/news/163163):
+ *        §1.1 the E4M3 format (max 448, smallest step 2^-9); §1.2 GQA, 8 KV
+ *        heads serving 64 query heads, and quantising the KV cache to FP8;
+ *        §2.2 the KV size 2 x layers x kv_heads x head_dim x tokens x bytes;
+ *        §3.1 quantisation as a division by an absmax/448 scale; §3.2 one KV
+ *        scale per attention layer, applied to every new K/V during decode.
+ *   [N]  Llama 3 FP8 + 128K production notes (0539edu.com/news/5628500):
+ *        §2.2 PagedAttention keeps the KV cache in fixed 16-token pages;
+ *        §3.2 decode at 128K re-reads the whole cache every step, so it is
+ *        bound by memory bandwidth; §3.3 block_size 16, kv_cache_dtype fp8;
+ *        §5.2 one block-table entry per 16 tokens (8000 for 128000 tokens).
+ *   [S]  Llama 3 8B notes (mlqm.cn/news/162512), §3.3: block size 32 option.
+ *
+ * Memory layout (part of the ABI, so page bytes compare bit for bit):
+ *   k_cache, v_cache : uint8  [num_pages][num_kv_heads][page_size][head_dim]
+ *                      one pair per layer; a page holds page_size tokens of
+ *                      every kv head, each kv head's tokens contiguous.
+ *   block_table      : int32  [batch][max_pages_per_seq]; entry p of row b is
+ *                      the physical page holding tokens p*P .. p*P+P-1.
+ *   slot             : physical_page * page_size + row within the page.
+ *
+ * Ownership: the caller owns every buffer (caches, tables, outputs, the
+ * decode workspace).  The library allocates no device memory, keeps no state
+ * between calls beyond a per-device cache of device properties and the
+ * driver entry point it uses to describe tensors for the TMA unit, and never
+ * synchronises the stream.  Calls are asynchronous on `stream`; the status
+ * reports argument errors found on the host and launch errors only.
+ *
+ * Device-side error word: kernels OR bits into *device_error (int32, device
+ * memory, may be NULL) instead of reading or writing out of bounds:
+ *   PKV_DEVERR_SLOT      a slot outside the pool (token skipped)
+ *   PKV_DEVERR_PAGE      a block-table entry outside [0, num_pages) (its
+ *                        page is read as zeros)
+ *   PKV_DEVERR_SEQLEN    seq_lens[b] < 0 or beyond max_pages_per_seq pages
+ *                        (clamped)
+ *   PKV_DEVERR_TIMEOUT   a pipeline wait exceeded its time limit (the kernel
+ *                        stopped issuing work, drained its copies and
+ *                        returned; outputs are undefined)
+ * The word is sticky: clear it (e.g. cudaMemsetAsync) before a call whose
+ * errors you want to attribute.
+ */
+#ifndef PAGEDFP8_H
+#define PAGEDFP8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int pkv_status;
+
+enum {
+    PKV_OK = 0,
+    PKV_ERR_NULL = 1,         /* a required pointer is NULL                  */
+    PKV_ERR_SHAPE = 2,        /* a size is negative, zero or inconsistent     */
+    PKV_ERR_DTYPE = 3,        /* unknown dtype code                           */
+    PKV_ERR_UNSUPPORTED = 4,  /* valid but not built: head_dim, page size, G  */
+    PKV_ERR_WORKSPACE = 5,    /* workspace too small or misaligned            */
+    PKV_ERR_CUDA = 6,         /* a CUDA runtime/driver call or launch failed  */
+    PKV_ERR_ALIGN = 7         /* a pointer is not 16-byte aligned             */
+};
+
+/* Activation dtype codes. */
+enum { PKV_F32 = 0, PKV_BF16 = 1 };
+
+/* Device error bits (see above). */
+enum {
+    PKV_DEVERR_SLOT = 1,
+    PKV_DEVERR_PAGE = 2,
+    PKV_DEVERR_SEQLEN = 4,
+    PKV_DEVERR_TIMEOUT = 8
+};
+
+/* Build limits. */
+#define PKV_HEAD_DIM 128      /* the only head_dim built (Llama 3)            */
+#define PKV_MAX_GROUP 8       /* query heads per kv head, 1..8                */
+#define PKV_MAX_BATCH 8192    /* sequences per decode call                    */
+
+/*
+ * kv_append_fp8 -- quantise new K and V tokens to E4M3 and write them into
+ * their pages ([G] §3.1/§3.2 quantisation by division by the scale; [G] §1.1
+ * format; [N] §2.2 pages).
+ *
+ * For every token t < num_tokens with slot = slot_mapping[t] >= 0, every kv
+ * head h and every d < head_dim:
+ *     k_cache[slot / P][h][slot % P][d] = E4M3(k_new[t][h][d] / k_scale[h])
+ * and the same for V.  The division is IEEE fp32 (correctly rounded); E4M3 is
+ * round-to-nearest-even from fp32 with saturation to +-448 (+-Inf -> +-448,
+ * NaN -> a NaN code).
+ *
+ *   k_new, v_new   device, [num_tokens][num_kv_heads][head_dim], contiguous,
+ *                  dtype in_dtype (PKV_F32 or PKV_BF16), 16-byte aligned.
+ *   slot_mapping   device int64 [num_tokens]; negative = do not write.
+ *   k_scale, v_scale device fp32 [num_kv_heads], > 0.
+ *   k_cache, v_cache device uint8 pools as laid out above, 16-byte aligned.
+ *   device_error   device int32 or NULL; PKV_DEVERR_SLOT for slots outside
+ *                  [0, num_pages * page_size) (the token is skipped).
+ * num_tokens == 0 is a no-op.  Two tokens with the same slot race.
+ */
+pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, int in_dtype,
+                             int64_t num_tokens, int num_kv_heads, int head_dim,
+                             const int64_t *slot_mapping,
+                             const float *k_scale, const float *v_scale,
+                             uint8_t *k_cache, uint8_t *v_cache,
+                             int64_t num_pages, int page_size,
+                             int32_t *device_error, cudaStream_t stream);
+
+/*
+ * Workspace bytes pkv_paged_gqa_decode needs for these sizes on the current
+ * device (partial softmax states of the split-K pass).  Returns 0 for sizes
+ * the library rejects.  max_ctas as in pkv_paged_gqa_decode.
+ */
+size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
+                                 int head_dim, int page_size, int max_ctas);
+
+/*
+ * paged_gqa_decode -- one decode step of grouped-query attention over the
+ * paged FP8 cache ([G] §1.2 GQA; [N] §2.2/§5.2 paging; [N] §3.2 the whole
+ * cache is read every step).
+ *
+ * For every sequence b < batch and query head i < num_q_heads, with
+ * G = num_q_heads / num_kv_heads, h = i / G and L = seq_lens[b]:
+ *     s_t = sm_scale * sum_d q[b][i][d] * E4M3(k_cache[pg(t)][h][t % P][d]) * k_scale[h]
+ *     w_t = softmax_t(s_t)                              for t < L
+ *     out[b][i][d] = sum_t w_t * E4M3(v_cache[pg(t)][h][t % P][d]) * v_scale[h]
+ * where pg(t) = block_table[b][t / P].  L == 0 gives a zero row.  Long
+ * contexts are split across CTAs (split-K / flash-decoding) and the partial
+ * softmax states are merged exactly (log-sum-exp) in a second pass, in a
+ * fixed order: results are deterministic run to run and independent of
+ * where the pages sit in the pool.
+ *
+ *   q              device bf16 [batch][num_q_heads][head_dim] (|q| < 65504).
+ *   k_cache, v_cache device uint8 pools (layout above), 16-byte aligned.
+ *   k_scale, v_scale device fp32 [num_kv_heads].
+ *   block_table    device int32 [batch][max_pages_per_seq].
+ *   seq_lens       device int32 [batch]; must satisfy
+ *                  0 <= seq_lens[b] <= max_pages_per_seq * page_size
+ *                  (violations set PKV_DEVERR_SEQLEN and are clamped).
+ *   head_dim       128.  page_size 16 or 32.  G in 1..8.
+ *   sm_scale       softmax scale, normally 1/sqrt(head_dim).
+ *   out            device [batch][num_q_heads][head_dim], out_dtype
+ *                  PKV_BF16 (bf16, RNE of the fp32 result) or PKV_F32.
+ *   workspace      device, >= pkv_decode_workspace_size(...) bytes, 256-byte
+ *                  aligned; contents need no initialisation; one workspace
+ *                  must not be shared by calls that overlap on the GPU.
+ *   device_error   device int32 or NULL (bits above).
+ *   max_ctas       0 = one persistent CTA per resident slot on the device;
+ *                  > 0 caps the CTA count (changes the split, not the math).
+ */
+pkv_status pkv_paged_gqa_decode(const void *q,
+                                const uint8_t *k_cache, const uint8_t *v_cache,
+                                const float *k_scale, const float *v_scale,
+                                const int32_t *block_table, int max_pages_per_seq,
+                                const int32_t *seq_lens,
+                                int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                int page_size, int64_t num_pages, float sm_scale,
+                                void *out, int out_dtype,
+                                void *workspace, size_t workspace_bytes,
+                                int32_t *device_error, int max_ctas, cudaStream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *pkv_status_string(pkv_status status);
+
+/* Library ABI version: (major << 16) | minor. */
+int pkv_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDFP8_H */

@@ -1,0 +1,219 @@
+"""Python binding of libpagedfp8 (paged FP8 KV cache + GQA decode, sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels of ``libpagedfp8.so``.  torch supplies device memory and the current
+stream.  The entry points mirror the C ABI in ``include/pagedfp8.h``:
+
+* ``pkv_kv_append_fp8``       -- quantise new K/V rows into their pages
+* ``pkv_paged_gqa_decode``    -- grouped-query decode attention over the pages
+* ``pkv_decode_workspace_size``, ``pkv_status_string``, ``pkv_version``
+
+``kv_append_fp8`` / ``paged_gqa_decode`` are the same calls with the output
+and workspace allocated by torch when not given.  There is no CPU fallback:
+if the library is not built, loading raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+PKV_F32, PKV_BF16 = 0, 1
+DEVERR_SLOT, DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT = 1, 2, 4, 8
+HEAD_DIM = 128
+MAX_GROUP = 8
+MAX_BATCH = 8192
+
+_lib = None
+_lock = threading.Lock()
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: status {status} ({pkv_status_string(status)})")
+        self.status = status
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load libpagedfp8.so (built in-tree by build()); raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"{path} is missing: build the CUDA library first "
+                               "(python -m paged_fp8_kv_03_gb300.build)")
+        lib = ctypes.CDLL(path)
+        vp, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+        lib.pkv_kv_append_fp8.restype = i32
+        lib.pkv_kv_append_fp8.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp, vp, vp, i64, i32, vp, vp]
+        lib.pkv_decode_workspace_size.restype = sz
+        lib.pkv_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.pkv_paged_gqa_decode.restype = i32
+        lib.pkv_paged_gqa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64,
+                                             f32, vp, i32, vp, sz, vp, i32, vp]
+        lib.pkv_status_string.restype = ctypes.c_char_p
+        lib.pkv_status_string.argtypes = [i32]
+        lib.pkv_version.restype = i32
+        lib.pkv_version.argtypes = []
+        _lib = lib
+        return lib
+
+
+def pkv_status_string(status: int) -> str:
+    return load().pkv_status_string(int(status)).decode()
+
+
+def pkv_version() -> int:
+    return int(load().pkv_version())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return ctypes.c_void_p(stream.cuda_stream)
+    return ctypes.c_void_p(int(stream))
+
+
+def _need(t, name, dtype=None, dim=None, cuda=True):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if cuda and not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dims, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _act_code(t) -> int:
+    if t.dtype == torch.float32:
+        return PKV_F32
+    if t.dtype == torch.bfloat16:
+        return PKV_BF16
+    raise TypeError(f"activations must be float32 or bfloat16, got {t.dtype}")
+
+
+def pkv_kv_append_fp8(k_new, v_new, slot_mapping, k_scale, v_scale, k_cache, v_cache,
+                      device_error=None, stream=None) -> None:
+    """k_new/v_new [T, Hkv, 128] fp32|bf16; slot_mapping int64 [T]; scales fp32
+    [Hkv]; caches uint8 [num_pages, Hkv, P, 128] (written in place)."""
+    _need(k_new, "k_new", dim=3)
+    _need(v_new, "v_new", dtype=k_new.dtype, dim=3)
+    _need(slot_mapping, "slot_mapping", torch.int64, 1)
+    _need(k_scale, "k_scale", torch.float32, 1)
+    _need(v_scale, "v_scale", torch.float32, 1)
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    if device_error is not None:
+        _need(device_error, "device_error", torch.int32)
+    T, H, D = k_new.shape
+    NP, H2, P, D2 = k_cache.shape
+    if v_new.shape != k_new.shape or v_cache.shape != k_cache.shape or H2 != H or D2 != D:
+        raise ValueError("k/v shapes disagree")
+    if slot_mapping.shape[0] != T or k_scale.shape[0] != H or v_scale.shape[0] != H:
+        raise ValueError("slot_mapping / scale shapes disagree")
+    st = load().pkv_kv_append_fp8(_ptr(k_new), _ptr(v_new), _act_code(k_new), T, H, D, _ptr(slot_mapping),
+                                  _ptr(k_scale), _ptr(v_scale), _ptr(k_cache), _ptr(v_cache), NP, P,
+                                  _ptr(device_error), _stream(stream))
+    if st != 0:
+        raise PkvError(st, "pkv_kv_append_fp8")
+
+
+def pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim=HEAD_DIM, page_size=16,
+                              max_ctas=0) -> int:
+    return int(load().pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, page_size,
+                                                max_ctas))
+
+
+def pkv_paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace,
+                         sm_scale=None, device_error=None, max_ctas=0, stream=None) -> None:
+    """q bf16 [B, Hq, 128]; caches uint8 [num_pages, Hkv, P, 128]; scales fp32
+    [Hkv]; block_table int32 [B, max_pages]; seq_lens int32 [B]; out
+    [B, Hq, 128] bf16 or fp32; workspace uint8 (pkv_decode_workspace_size bytes)."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    _need(k_scale, "k_scale", torch.float32, 1)
+    _need(v_scale, "v_scale", torch.float32, 1)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(out, "out", dim=3)
+    _need(workspace, "workspace", torch.uint8)
+    if device_error is not None:
+        _need(device_error, "device_error", torch.int32)
+    B, Hq, D = q.shape
+    NP, Hkv, P, D2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or D2 != D or out.shape != q.shape:
+        raise ValueError("q / cache / out shapes disagree")
+    if block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_table / seq_lens shapes disagree with q")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    st = load().pkv_paged_gqa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                     _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, Hq, Hkv, D, P,
+                                     NP, float(sm_scale), _ptr(out), _act_code(out), _ptr(workspace),
+                                     workspace.numel(), _ptr(device_error), int(max_ctas), _stream(stream))
+    if st != 0:
+        raise PkvError(st, "pkv_paged_gqa_decode")
+
+
+_ws_cache: dict = {}
+
+
+def decode_workspace(batch, num_q_heads, num_kv_heads, page_size, device=None, max_ctas=0) -> torch.Tensor:
+    """A workspace tensor for these sizes, cached per (device, stream, sizes).
+    Calls that use it must not overlap on the GPU (same stream is fine)."""
+    device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    stream = torch.cuda.current_stream(device).cuda_stream
+    key = (device.index, stream, batch, num_q_heads, num_kv_heads, page_size, max_ctas)
+    ws = _ws_cache.get(key)
+    if ws is None:
+        with torch.cuda.device(device):
+            n = pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, HEAD_DIM, page_size, max_ctas)
+        if n == 0:
+            raise PkvError(4, "pkv_decode_workspace_size")
+        ws = torch.empty(n, dtype=torch.uint8, device=device)
+        _ws_cache[key] = ws
+    return ws
+
+
+def kv_append_fp8(k_new, v_new, slot_mapping, k_scale, v_scale, k_cache, v_cache, device_error=None,
+                  stream=None) -> None:
+    pkv_kv_append_fp8(k_new, v_new, slot_mapping, k_scale, v_scale, k_cache, v_cache, device_error, stream)
+
+
+def paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out=None,
+                     out_dtype=torch.bfloat16, workspace=None, sm_scale=None, device_error=None, max_ctas=0,
+                     stream=None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(q.shape[0], q.shape[1], k_cache.shape[1], k_cache.shape[2], q.device,
+                                     max_ctas)
+    pkv_paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace,
+                         sm_scale, device_error, max_ctas, stream)
+    return out
+
+
+__all__ = ["load", "lib_path", "pkv_kv_append_fp8", "pkv_paged_gqa_decode", "pkv_decode_workspace_size",
+           "pkv_status_string", "pkv_version", "kv_append_fp8", "paged_gqa_decode", "decode_workspace",
+           "PkvError", "PKV_F32", "PKV_BF16", "DEVERR_SLOT", "DEVERR_PAGE", "DEVERR_SEQLEN",
+           "DEVERR_TIMEOUT"]

@@ -1,0 +1,289 @@
+// C entry points: argument checks on the host, TMA tensor descriptions of the
+// page pools, grid sizing and launches.  Nothing here allocates device memory.
+#include <math.h>
+
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "internal.h"
+
+namespace pkv {
+
+namespace {
+
+std::mutex g_mu;
+std::map<int, int> g_sm_count;                              // device -> SMs
+std::map<std::tuple<int, int, size_t>, int> g_occupancy;     // (device, P, smem) -> CTAs per SM
+std::map<std::tuple<int, int>, size_t> g_smem_attr;          // (device, P) -> max dynamic smem set
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+EncodeTiledFn g_encode = nullptr;
+
+EncodeTiledFn encode_fn()
+{
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(fn);
+    }
+    return g_encode;
+}
+
+// A pool [num_pages][hkv][P][128] bytes seen as a 3-D tensor (128 bytes, P rows,
+// num_pages*hkv tiles); one box = one page of one kv head, 128-byte swizzled.
+bool make_page_map(CUtensorMap *tm, const uint8_t *pool, int64_t num_pages, int hkv, int P)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(P),
+                                static_cast<cuuint64_t>(num_pages) * static_cast<cuuint64_t>(hkv)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(P) * kHeadDim};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(P), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(pool), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void *p, uintptr_t a)
+{
+    return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+int current_device()
+{
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return -1;
+    return dev;
+}
+
+}  // namespace
+
+int device_sm_count()
+{
+    const int dev = current_device();
+    if (dev < 0)
+        return 0;
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_sm_count.find(dev);
+    if (it != g_sm_count.end())
+        return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return 0;
+    g_sm_count[dev] = n;
+    return n;
+}
+
+// Persistent grid: every resident CTA slot on the device (capped by max_ctas).
+int decode_num_ctas(int page_size, int batch, int max_ctas)
+{
+    const int dev = current_device();
+    const int sms = device_sm_count();
+    if (dev < 0 || sms <= 0)
+        return 0;
+    const size_t smem = decode_smem_bytes(page_size, batch);
+    const void *kern = decode_kernel_for(page_size);
+    int per_sm = 0;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto key_attr = std::make_tuple(dev, page_size);
+        auto ia = g_smem_attr.find(key_attr);
+        if (ia == g_smem_attr.end() || ia->second < smem) {
+            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+                cudaSuccess)
+                return 0;
+            g_smem_attr[key_attr] = smem;
+        }
+        auto key = std::make_tuple(dev, page_size, smem);
+        auto it = g_occupancy.find(key);
+        if (it != g_occupancy.end()) {
+            per_sm = it->second;
+        } else {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
+                return 0;
+            g_occupancy[key] = per_sm;
+        }
+    }
+    if (per_sm <= 0)
+        return 0;
+    int c = per_sm * sms;
+    if (max_ctas > 0 && max_ctas < c)
+        c = max_ctas;
+    return c;
+}
+
+}  // namespace pkv
+
+using namespace pkv;
+
+namespace {
+
+pkv_status check_decode_shape(int batch, int hq, int hkv, int head_dim, int page_size, int max_pages,
+                              int64_t num_pages)
+{
+    if (batch < 0 || hq <= 0 || hkv <= 0 || max_pages <= 0 || num_pages <= 0)
+        return PKV_ERR_SHAPE;
+    if (hq % hkv != 0)
+        return PKV_ERR_SHAPE;
+    if (head_dim != kHeadDim || (page_size != 16 && page_size != 32))
+        return PKV_ERR_UNSUPPORTED;
+    if (hq / hkv > PKV_MAX_GROUP || batch > PKV_MAX_BATCH)
+        return PKV_ERR_UNSUPPORTED;
+    if (num_pages * static_cast<int64_t>(hkv) >= (int64_t(1) << 31) - 1)
+        return PKV_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(max_pages) * page_size >= (int64_t(1) << 31))
+        return PKV_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(batch) * max_pages >= (int64_t(1) << 40))
+        return PKV_ERR_UNSUPPORTED;
+    return PKV_OK;
+}
+
+size_t workspace_bytes_for(int batch, int hq, int hkv, int num_ctas)
+{
+    const size_t slots = static_cast<size_t>(num_ctas) + static_cast<size_t>(batch) * hkv;
+    const size_t bytes = slots * static_cast<size_t>(hq / hkv) * kPartialStride * sizeof(float);
+    return (bytes + 255) & ~size_t(255);
+}
+
+}  // namespace
+
+extern "C" {
+
+int pkv_version(void)
+{
+    return (1 << 16) | 0;
+}
+
+const char *pkv_status_string(pkv_status s)
+{
+    switch (s) {
+    case PKV_OK: return "ok";
+    case PKV_ERR_NULL: return "a required pointer is NULL";
+    case PKV_ERR_SHAPE: return "invalid or inconsistent sizes";
+    case PKV_ERR_DTYPE: return "unknown dtype code";
+    case PKV_ERR_UNSUPPORTED: return "unsupported configuration (head_dim, page size, group, batch or pool size)";
+    case PKV_ERR_WORKSPACE: return "workspace missing, too small or not 256-byte aligned";
+    case PKV_ERR_CUDA: return "CUDA call or kernel launch failed";
+    case PKV_ERR_ALIGN: return "pointer not aligned as required";
+    default: return "unknown status";
+    }
+}
+
+pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, int in_dtype, int64_t num_tokens,
+                             int num_kv_heads, int head_dim, const int64_t *slot_mapping, const float *k_scale,
+                             const float *v_scale, uint8_t *k_cache, uint8_t *v_cache, int64_t num_pages,
+                             int page_size, int32_t *device_error, cudaStream_t stream)
+{
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_pages <= 0)
+        return PKV_ERR_SHAPE;
+    if (in_dtype != PKV_F32 && in_dtype != PKV_BF16)
+        return PKV_ERR_DTYPE;
+    if (head_dim != kHeadDim || (page_size != 16 && page_size != 32))
+        return PKV_ERR_UNSUPPORTED;
+    if (num_tokens == 0)
+        return PKV_OK;
+    if (!k_new || !v_new || !slot_mapping || !k_scale || !v_scale || !k_cache || !v_cache)
+        return PKV_ERR_NULL;
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
+        !aligned(slot_mapping, 8) || !aligned(k_scale, 4) || !aligned(v_scale, 4) ||
+        !aligned(device_error, 4))
+        return PKV_ERR_ALIGN;
+    AppendArgs a;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.in_bf16 = in_dtype == PKV_BF16;
+    a.num_tokens = num_tokens;
+    a.hkv = num_kv_heads;
+    a.slots = slot_mapping;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.num_pages = num_pages;
+    a.page_size = page_size;
+    a.err = device_error;
+    return launch_kv_append(a, stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                                 int max_ctas)
+{
+    if (check_decode_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, 1, 1) != PKV_OK)
+        return 0;
+    const int ctas = decode_num_ctas(page_size, batch, max_ctas);
+    if (ctas <= 0)
+        return 0;
+    return workspace_bytes_for(batch, num_q_heads, num_kv_heads, ctas);
+}
+
+pkv_status pkv_paged_gqa_decode(const void *q, const uint8_t *k_cache, const uint8_t *v_cache, const float *k_scale,
+                                const float *v_scale, const int32_t *block_table, int max_pages_per_seq,
+                                const int32_t *seq_lens, int batch, int num_q_heads, int num_kv_heads,
+                                int head_dim, int page_size, int64_t num_pages, float sm_scale, void *out,
+                                int out_dtype, void *workspace, size_t workspace_bytes, int32_t *device_error,
+                                int max_ctas, cudaStream_t stream)
+{
+    pkv_status st = check_decode_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_seq,
+                                       num_pages);
+    if (st != PKV_OK)
+        return st;
+    if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
+        return PKV_ERR_DTYPE;
+    if (!(sm_scale == sm_scale) || isinf(sm_scale))
+        return PKV_ERR_SHAPE;
+    if (batch == 0)
+        return PKV_OK;
+    if (!q || !k_cache || !v_cache || !k_scale || !v_scale || !block_table || !seq_lens || !out)
+        return PKV_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4) ||
+        !aligned(device_error, 4))
+        return PKV_ERR_ALIGN;
+    if (!workspace || !aligned(workspace, 256))
+        return PKV_ERR_WORKSPACE;
+
+    const int ctas = decode_num_ctas(page_size, batch, max_ctas);
+    if (ctas <= 0)
+        return PKV_ERR_CUDA;
+    if (workspace_bytes < workspace_bytes_for(batch, num_q_heads, num_kv_heads, ctas))
+        return PKV_ERR_WORKSPACE;
+
+    alignas(64) CUtensorMap tm_k;
+    alignas(64) CUtensorMap tm_v;
+    if (!make_page_map(&tm_k, k_cache, num_pages, num_kv_heads, page_size) ||
+        !make_page_map(&tm_v, v_cache, num_pages, num_kv_heads, page_size))
+        return PKV_ERR_CUDA;
+
+    DecodeArgs a;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.block_table = block_table;
+    a.max_pages = max_pages_per_seq;
+    a.seq_lens = seq_lens;
+    a.batch = batch;
+    a.hq = num_q_heads;
+    a.hkv = num_kv_heads;
+    a.group = num_q_heads / num_kv_heads;
+    a.num_pages = num_pages;
+    a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+    a.out = out;
+    a.out_f32 = out_dtype == PKV_F32;
+    a.partials = static_cast<float *>(workspace);
+    a.err = device_error;
+    a.num_ctas = ctas;
+    return launch_paged_decode(a, tm_k, tm_v, page_size, stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
+}  // extern "C"

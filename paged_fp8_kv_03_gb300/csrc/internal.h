@@ -1,0 +1,61 @@
+// Declarations shared by the library's translation units (not installed).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pagedfp8.h"
+#include "device.cuh"
+
+namespace pkv {
+
+constexpr int kHeadDim = PKV_HEAD_DIM;
+
+// Decode kernel shape (shared by the launcher and the workspace sizing).
+constexpr int kConsumerWarps = 4;                       // warps that compute
+constexpr int kThreads = (kConsumerWarps + 1) * 32;     // + one TMA producer warp
+constexpr int kStages = 8;                              // pages in flight per CTA
+constexpr int kPartialStride = kHeadDim + 4;            // floats per (slot, head): acc, m, l, pad
+
+struct AppendArgs {
+    const void *k_new, *v_new;
+    int in_bf16;
+    int64_t num_tokens;
+    int hkv;
+    const int64_t *slots;
+    const float *k_scale, *v_scale;
+    uint8_t *k_cache, *v_cache;
+    int64_t num_pages;
+    int page_size;
+    int32_t *err;
+};
+
+struct DecodeArgs {
+    const __nv_bfloat16 *q;
+    const float *k_scale, *v_scale;
+    const int32_t *block_table;
+    int max_pages;
+    const int32_t *seq_lens;
+    int batch, hq, hkv, group;
+    int64_t num_pages;
+    float sm_scale_log2;        // sm_scale * log2(e): scores live in the exp2 domain
+    void *out;
+    int out_f32;
+    float *partials;            // [num_ctas + batch * hkv][group][kPartialStride]
+    int32_t *err;
+    int num_ctas;
+};
+
+// Host helpers (api.cu).
+int device_sm_count();
+
+// Launchers.
+cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t stream);
+size_t decode_smem_bytes(int page_size, int batch);
+const void *decode_kernel_for(int page_size);
+int decode_num_ctas(int page_size, int batch, int max_ctas);
+cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
+                                int page_size, cudaStream_t stream);
+
+}  // namespace pkv

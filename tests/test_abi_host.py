@@ -1,0 +1,124 @@
+"""The C ABI without a GPU: the library loads, exports every function the
+header declares, and rejects bad arguments on the host with the documented
+status codes (no CUDA call is reached by any of these)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_fp8_kv_03_gb300 as pkv
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "pagedfp8.h")
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text)))
+
+
+def _status_codes():
+    text = open(HEADER).read()
+    return {m.group(1): int(m.group(2)) for m in re.finditer(r"(PKV_ERR_[A-Z]+|PKV_OK)\s*=\s*(\d+)", text)}
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return pkv.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"pkv_kv_append_fp8", "pkv_paged_gqa_decode", "pkv_decode_workspace_size",
+            "pkv_status_string", "pkv_version"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings_and_version(lib):
+    codes = _status_codes()
+    assert codes["PKV_OK"] == 0 and len(codes) == 8
+    for name, c in codes.items():
+        s = pkv.pkv_status_string(c)
+        assert s and s != "unknown status", name
+    assert pkv.pkv_status_string(12345) == "unknown status"
+    assert pkv.pkv_version() >> 16 == 1
+
+
+A16 = ctypes.c_void_p(0x10000)      # fake, 16-byte-aligned addresses: never dereferenced on these paths
+A16b = ctypes.c_void_p(0x20000)
+
+
+def _append(lib, **kw):
+    args = dict(k=A16, v=A16, dtype=0, T=4, H=8, D=128, slots=A16, ks=A16, vs=A16, kc=A16, vc=A16b,
+                np_=10, P=16, err=None)
+    args.update(kw)
+    return lib.pkv_kv_append_fp8(args["k"], args["v"], args["dtype"], args["T"], args["H"], args["D"],
+                                 args["slots"], args["ks"], args["vs"], args["kc"], args["vc"], args["np_"],
+                                 args["P"], args["err"], None)
+
+
+def test_append_argument_errors(lib):
+    c = _status_codes()
+    assert _append(lib, T=-1) == c["PKV_ERR_SHAPE"]
+    assert _append(lib, H=0) == c["PKV_ERR_SHAPE"]
+    assert _append(lib, np_=0) == c["PKV_ERR_SHAPE"]
+    assert _append(lib, dtype=7) == c["PKV_ERR_DTYPE"]
+    assert _append(lib, D=64) == c["PKV_ERR_UNSUPPORTED"]
+    assert _append(lib, P=8) == c["PKV_ERR_UNSUPPORTED"]
+    assert _append(lib, P=64) == c["PKV_ERR_UNSUPPORTED"]
+    assert _append(lib, k=None) == c["PKV_ERR_NULL"]
+    assert _append(lib, slots=None) == c["PKV_ERR_NULL"]
+    assert _append(lib, kc=ctypes.c_void_p(0x10008)) == c["PKV_ERR_ALIGN"]
+    assert _append(lib, k=ctypes.c_void_p(0x10004)) == c["PKV_ERR_ALIGN"]
+    assert _append(lib, err=ctypes.c_void_p(0x10002)) == c["PKV_ERR_ALIGN"]
+    assert _append(lib, T=0, k=None, v=None, slots=None) == c["PKV_OK"]     # empty append is a no-op
+
+
+def _decode(lib, **kw):
+    a = dict(q=A16, kc=A16, vc=A16b, ks=A16, vs=A16, bt=A16, maxp=4, lens=A16, B=2, Hq=16, Hkv=2, D=128,
+             P=16, np_=8, sm=0.088, out=A16, odt=1, ws=A16, wsb=1 << 20, err=None, ctas=0)
+    a.update(kw)
+    return lib.pkv_paged_gqa_decode(a["q"], a["kc"], a["vc"], a["ks"], a["vs"], a["bt"], a["maxp"], a["lens"],
+                                    a["B"], a["Hq"], a["Hkv"], a["D"], a["P"], a["np_"], a["sm"], a["out"],
+                                    a["odt"], a["ws"], a["wsb"], a["err"], a["ctas"], None)
+
+
+def test_decode_argument_errors(lib):
+    c = _status_codes()
+    assert _decode(lib, Hq=12, Hkv=8) == c["PKV_ERR_SHAPE"]          # Hq % Hkv
+    assert _decode(lib, B=-1) == c["PKV_ERR_SHAPE"]
+    assert _decode(lib, maxp=0) == c["PKV_ERR_SHAPE"]
+    assert _decode(lib, np_=0) == c["PKV_ERR_SHAPE"]
+    assert _decode(lib, Hq=32, Hkv=2) == c["PKV_ERR_UNSUPPORTED"]    # G = 16
+    assert _decode(lib, D=64) == c["PKV_ERR_UNSUPPORTED"]
+    assert _decode(lib, P=64) == c["PKV_ERR_UNSUPPORTED"]
+    assert _decode(lib, B=pkv.MAX_BATCH + 1) == c["PKV_ERR_UNSUPPORTED"]
+    assert _decode(lib, np_=1 << 30, Hkv=2) == c["PKV_ERR_UNSUPPORTED"]   # tile index would overflow int32
+    assert _decode(lib, odt=5) == c["PKV_ERR_DTYPE"]
+    assert _decode(lib, sm=float("nan")) == c["PKV_ERR_SHAPE"]
+    assert _decode(lib, sm=float("inf")) == c["PKV_ERR_SHAPE"]
+    assert _decode(lib, q=None) == c["PKV_ERR_NULL"]
+    assert _decode(lib, bt=None) == c["PKV_ERR_NULL"]
+    assert _decode(lib, out=None) == c["PKV_ERR_NULL"]
+    assert _decode(lib, kc=ctypes.c_void_p(0x10001)) == c["PKV_ERR_ALIGN"]
+    assert _decode(lib, out=ctypes.c_void_p(0x10008)) == c["PKV_ERR_ALIGN"]
+    assert _decode(lib, ws=None) == c["PKV_ERR_WORKSPACE"]
+    assert _decode(lib, ws=ctypes.c_void_p(0x10010)) == c["PKV_ERR_WORKSPACE"]
+    assert _decode(lib, B=0, q=None, bt=None, lens=None, out=None) == c["PKV_OK"]
+
+
+def test_workspace_size_rejects_unsupported(lib):
+    assert pkv.pkv_decode_workspace_size(2, 12, 8) == 0
+    assert pkv.pkv_decode_workspace_size(2, 16, 8, head_dim=64) == 0
+    assert pkv.pkv_decode_workspace_size(2, 16, 8, page_size=8) == 0
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+    x = torch.zeros(1, 1, 128)
+    with pytest.raises(ValueError):
+        pkv.pkv_kv_append_fp8(x, x, torch.zeros(1, dtype=torch.int64), torch.ones(1), torch.ones(1),
+                              torch.zeros(1, 1, 16, 128, dtype=torch.uint8),
+                              torch.zeros(1, 1, 16, 128, dtype=torch.uint8))
