@@ -556,13 +556,21 @@ __global__ void __launch_bounds__(kCombineThreads) splitk_combine_kernel(const D
     if (c0 == c1)
         return;
     const float vsc = __ldg(a.v_scale + h);
+    // CTAs between c0 and c1 whose range is empty (more CTAs than page-heads)
+    // wrote nothing: skip their slots.
+    auto has_piece = [&](int c) {
+        return static_cast<int64_t>(c) * total / a.num_ctas != static_cast<int64_t>(c + 1) * total / a.num_ctas;
+    };
     for (int e = threadIdx.x; e < a.group * kHeadDim; e += kCombineThreads) {
         const int g = e >> 7, d = e & (kHeadDim - 1);
         float M = -INFINITY;
         for (int c = c0; c <= c1; ++c)
-            M = fmaxf(M, a.partials[(static_cast<int64_t>(c + seg) * a.group + g) * kPartialStride + kHeadDim]);
+            if (has_piece(c))
+                M = fmaxf(M, a.partials[(static_cast<int64_t>(c + seg) * a.group + g) * kPartialStride + kHeadDim]);
         float Ls = 0.f, A = 0.f;
         for (int c = c0; c <= c1; ++c) {
+            if (!has_piece(c))
+                continue;
             const float *slot = a.partials + (static_cast<int64_t>(c + seg) * a.group + g) * kPartialStride;
             const float f = exp2f(slot[kHeadDim] - M);
             Ls += slot[kHeadDim + 1] * f;

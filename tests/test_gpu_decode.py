@@ -16,11 +16,18 @@ from tests.gpu_fill import (assert_close, bf16_ulp, fill_gpu, oracle_rows, sampl
 pytestmark = pytest.mark.gpu
 
 
+def _poisoned_workspace(pkv, f, max_ctas):
+    """A workspace full of NaN bytes: reading a slot nobody wrote shows up."""
+    wl = f.wl
+    n = pkv.pkv_decode_workspace_size(wl.batch, wl.hq, wl.hkv, 128, wl.page_size, max_ctas)
+    return torch.full((n,), 0xFF, dtype=torch.uint8, device=f.q.device)
+
+
 def _decode(pkv, f, out_dtype=torch.float32, max_ctas=0, err=None, bt=None, lens=None, kc=None, vc=None):
     out = pkv.paged_gqa_decode(f.q, f.kc if kc is None else kc, f.vc if vc is None else vc, f.ks, f.vs,
                                f.bt if bt is None else bt, f.lens if lens is None else lens,
                                out_dtype=out_dtype, device_error=err if err is not None else f.err,
-                               max_ctas=max_ctas)
+                               max_ctas=max_ctas, workspace=_poisoned_workspace(pkv, f, max_ctas))
     torch.cuda.synchronize()
     return out
 
