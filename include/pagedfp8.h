@@ -168,6 +168,40 @@ pkv_status pkv_paged_gqa_decode(const void *q,
                                 void *workspace, size_t workspace_bytes,
                                 int32_t *device_error, int max_ctas, cudaStream_t stream);
 
+/*
+ * paged_gqa_decode without a caller workspace, for callers that cannot
+ * allocate device memory (a serving engine that owns every byte of device
+ * memory through its own pool, a plugin that must not bypass its host
+ * runtime's allocator, a latency-critical loop that cannot pay for an
+ * allocation).  No counterpart on the pages: it is an interface variant, the
+ * computation is exactly pkv_paged_gqa_decode's.
+ *
+ * Same arguments and results as pkv_paged_gqa_decode minus the workspace.
+ * The split-K scratch lives in a fixed array inside the library image,
+ * pkv_decode_noalloc_scratch_bytes() bytes (8 MiB), which every GPU that
+ * loads the library keeps until the process exits.  The call allocates
+ * nothing.  Sizes whose scratch would not fit return PKV_ERR_WORKSPACE
+ * (at G = 8 that is num_ctas + batch * num_kv_heads > 1985 partial slots).
+ * All calls share the array: calls that overlap on the GPU (two streams, or
+ * unordered host threads) race and corrupt each other's results; calls
+ * ordered on one stream are safe.  The array keeps the previous call's
+ * contents, which the decode never reads before writing.  The first call on
+ * each device looks up the array's device address (with that device
+ * current) and caches it: make that first call before any stream capture.
+ */
+pkv_status pkv_paged_gqa_decode_noalloc(const void *q,
+                                        const uint8_t *k_cache, const uint8_t *v_cache,
+                                        const float *k_scale, const float *v_scale,
+                                        const int32_t *block_table, int max_pages_per_seq,
+                                        const int32_t *seq_lens,
+                                        int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                        int page_size, int64_t num_pages, float sm_scale,
+                                        void *out, int out_dtype,
+                                        int32_t *device_error, int max_ctas, cudaStream_t stream);
+
+/* Size in bytes of the fixed scratch array pkv_paged_gqa_decode_noalloc uses. */
+size_t pkv_decode_noalloc_scratch_bytes(void);
+
 /* Human-readable name of a status code (static string). */
 const char *pkv_status_string(pkv_status status);
 

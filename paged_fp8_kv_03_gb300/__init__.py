@@ -62,6 +62,11 @@ def load() -> ctypes.CDLL:
         lib.pkv_paged_gqa_decode.restype = i32
         lib.pkv_paged_gqa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64,
                                              f32, vp, i32, vp, sz, vp, i32, vp]
+        lib.pkv_paged_gqa_decode_noalloc.restype = i32
+        lib.pkv_paged_gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
+                                                     i64, f32, vp, i32, vp, i32, vp]
+        lib.pkv_decode_noalloc_scratch_bytes.restype = sz
+        lib.pkv_decode_noalloc_scratch_bytes.argtypes = []
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_status_string.argtypes = [i32]
         lib.pkv_version.restype = i32
@@ -175,6 +180,42 @@ def pkv_paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq
         raise PkvError(st, "pkv_paged_gqa_decode")
 
 
+def pkv_paged_gqa_decode_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out,
+                                 sm_scale=None, device_error=None, max_ctas=0, stream=None) -> None:
+    """pkv_paged_gqa_decode without a workspace, for callers that cannot
+    allocate device memory: the split-K scratch is a fixed array inside the
+    library (see pkv_decode_noalloc_scratch_bytes).  Calls that overlap on the
+    GPU share that array and race; calls on one stream are safe."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    _need(k_scale, "k_scale", torch.float32, 1)
+    _need(v_scale, "v_scale", torch.float32, 1)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(out, "out", dim=3)
+    if device_error is not None:
+        _need(device_error, "device_error", torch.int32)
+    B, Hq, D = q.shape
+    NP, Hkv, P, D2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or D2 != D or out.shape != q.shape:
+        raise ValueError("q / cache / out shapes disagree")
+    if block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_table / seq_lens shapes disagree with q")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    st = load().pkv_paged_gqa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                             _ptr(v_scale), _ptr(block_table), block_table.shape[1],
+                                             _ptr(seq_lens), B, Hq, Hkv, D, P, NP, float(sm_scale), _ptr(out),
+                                             _act_code(out), _ptr(device_error), int(max_ctas), _stream(stream))
+    if st != 0:
+        raise PkvError(st, "pkv_paged_gqa_decode_noalloc")
+
+
+def pkv_decode_noalloc_scratch_bytes() -> int:
+    return int(load().pkv_decode_noalloc_scratch_bytes())
+
+
 _ws_cache: dict = {}
 
 
@@ -214,6 +255,7 @@ def paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_len
 
 
 __all__ = ["load", "lib_path", "pkv_kv_append_fp8", "pkv_paged_gqa_decode", "pkv_decode_workspace_size",
+           "pkv_paged_gqa_decode_noalloc", "pkv_decode_noalloc_scratch_bytes",
            "pkv_status_string", "pkv_version", "kv_append_fp8", "paged_gqa_decode", "decode_workspace",
            "PkvError", "PKV_F32", "PKV_BF16", "DEVERR_SLOT", "DEVERR_PAGE", "DEVERR_SEQLEN",
            "DEVERR_TIMEOUT"]
