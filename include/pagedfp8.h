@@ -27,9 +27,9 @@
  *
  * Ownership: the caller owns every buffer (caches, tables, outputs, the
  * decode workspace).  The library allocates no device memory, keeps no state
- * between calls beyond a per-device cache of device properties and the
- * driver entry point it uses to describe tensors for the TMA unit, and never
- * synchronises the stream.  Calls are asynchronous on `stream`; the status
+ * between calls beyond a per-device cache of device properties, the driver
+ * entry point it uses to describe tensors for the TMA unit and a process-wide
+ * call counter, and never synchronises the stream.  Calls are asynchronous on `stream`; the status
  * reports argument errors found on the host and launch errors only.
  *
  * Device-side error word: kernels OR bits into *device_error (int32, device
@@ -134,10 +134,10 @@ size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
  *     w_t = softmax_t(s_t)                              for t < L
  *     out[b][i][d] = sum_t w_t * E4M3(v_cache[pg(t)][h][t % P][d]) * v_scale[h]
  * where pg(t) = block_table[b][t / P].  L == 0 gives a zero row.  Long
- * contexts are split across CTAs (split-K / flash-decoding) and the partial
- * softmax states are merged exactly (log-sum-exp) in a second pass, in a
- * fixed order: results are deterministic run to run and independent of
- * where the pages sit in the pool.
+ * contexts are split across CTAs (split-K / flash-decoding); the CTA that
+ * finishes a sequence's last piece merges the partial softmax states exactly
+ * (log-sum-exp) in a fixed order: results are deterministic run to run and
+ * independent of where the pages sit in the pool.  One kernel launch.
  *
  *   q              device bf16 [batch][num_q_heads][head_dim] (|q| < 65504).
  *   k_cache, v_cache device uint8 pools (layout above), 16-byte aligned.
@@ -151,7 +151,9 @@ size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
  *   out            device [batch][num_q_heads][head_dim], out_dtype
  *                  PKV_BF16 (bf16, RNE of the fp32 result) or PKV_F32.
  *   workspace      device, >= pkv_decode_workspace_size(...) bytes, 256-byte
- *                  aligned; contents need no initialisation; one workspace
+ *                  aligned: per-(sequence, kv head) arrival counters, then the
+ *                  partial states.  Contents need no initialisation (the
+ *                  counters are tagged with a per-call epoch); one workspace
  *                  must not be shared by calls that overlap on the GPU.
  *   device_error   device int32 or NULL (bits above).
  *   max_ctas       0 = one persistent CTA per resident slot on the device;
@@ -180,8 +182,10 @@ pkv_status pkv_paged_gqa_decode(const void *q,
  * The split-K scratch lives in a fixed array inside the library image,
  * pkv_decode_noalloc_scratch_bytes() bytes (8 MiB), which every GPU that
  * loads the library keeps until the process exits.  The call allocates
- * nothing.  Sizes whose scratch would not fit return PKV_ERR_WORKSPACE
- * (at G = 8 that is num_ctas + batch * num_kv_heads > 1985 partial slots).
+ * nothing.  Sizes whose scratch would not fit return PKV_ERR_WORKSPACE (the
+ * scratch holds 8 bytes per (sequence, kv head) plus, at G = 8, 4224 bytes per
+ * partial slot, num_ctas + batch * num_kv_heads slots; with 304 CTAs that
+ * allows batch * num_kv_heads up to about 1660).
  * All calls share the array: calls that overlap on the GPU (two streams, or
  * unordered host threads) race and corrupt each other's results; calls
  * ordered on one stream are safe.  The array keeps the previous call's

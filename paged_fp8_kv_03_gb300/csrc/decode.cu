@@ -16,13 +16,15 @@
 // the sequence lengths (flash-decoding split-K with perfect balance).  A CTA
 // range cuts segments into pieces; a piece that covers a whole segment writes
 // the final output, the others write a partial softmax state (running max m,
-// sum l, unnormalised accumulator) into workspace slot (cta + segment), and
-// a second small kernel merges the pieces of each segment in CTA order.
+// sum l, unnormalised accumulator) into workspace slot (cta + segment) and
+// bump the segment's arrival counter; the CTA that brings the count to the
+// number of pieces merges them, in CTA order (deterministic), and writes the
+// output.  Counters carry a per-call epoch so they never need clearing.
 //
 // Inside a CTA: one producer warp walks the CTA's pages, fetches block-table
 // entries 32 at a time one batch ahead, and issues two TMA tensor loads per
-// page (K tile, V tile; 128-byte swizzled, evict-first in L2) into an
-// 8-stage shared-memory ring guarded by full/empty mbarriers.  Four consumer
+// page (K tile, V tile; 128-byte swizzled, evict-first in L2) into a 96 KB
+// shared-memory ring (24 pages at P = 16) guarded by full/empty mbarriers.  Four consumer
 // warps take the pages round-robin.  Each warp reads a 16-token tile with
 // ldmatrix (conflict-free thanks to the swizzle), widens E4M3 to f16 exactly
 // in registers, and runs both products on the tensor cores with mma.sync
@@ -50,7 +52,6 @@ namespace {
 constexpr uint64_t kTimeoutNs = 2000000000ull;
 constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr unsigned kFull = 0xffffffffu;
-constexpr int kCombineThreads = 128;
 
 struct Loc {
     int b, h, pg;   // sequence, kv head, page index within the sequence
@@ -109,12 +110,34 @@ __device__ __forceinline__ int cta_of(int64_t x, int64_t total, int ctas)
     return static_cast<int>(((x + 1) * ctas - 1) / total);
 }
 
+__device__ __forceinline__ bool cta_has_range(int c, int64_t total, int ctas)
+{
+    return static_cast<int64_t>(c) * total / ctas != static_cast<int64_t>(c + 1) * total / ctas;
+}
+
+// Counts one more finished piece of a segment for this call's epoch; true for
+// the piece that completes the segment.  Lock-free: every failed CAS means
+// another piece succeeded.
+__device__ __forceinline__ bool arrive_last(unsigned long long *cnt, unsigned long long epoch, unsigned n)
+{
+    unsigned long long old = __ldcg(cnt);
+    for (;;) {
+        const unsigned long long nv = ((old >> 24) == epoch) ? old + 1 : ((epoch << 24) | 1ull);
+        const unsigned long long prev = atomicCAS(cnt, old, nv);
+        if (prev == old)
+            return (nv & 0xFFFFFFull) == n;
+        old = prev;
+    }
+}
+
 template <int P>
 struct Smem {
     static constexpr int kTile = P * kHeadDim;              // bytes of one K (or V) tile
     static constexpr int kStageBytes = 2 * kTile;
+    static constexpr int kStages = P == 16 ? 20 : 8;           // 80 KB / 64 KB ring
+    static_assert(kStages % kConsumerWarps == 0, "each consumer warp owns a fixed subset of stages");
     static constexpr int kBar = kStages * kStageBytes;      // full[kStages], empty[kStages]
-    static constexpr int kFlag = kBar + 2 * kStages * 8;    // abort flag
+    static constexpr int kFlag = kBar + 2 * kStages * 8;    // abort flag, last-piece flag, c0, c1
     static constexpr int kWarpSum = kFlag + 16;             // scan scratch (5 ints)
     static constexpr int kCm = kWarpSum + 32;               // [warps][8] running max
     static constexpr int kCl = kCm + kConsumerWarps * 8 * 4;        // [warps][8] sums
@@ -184,33 +207,44 @@ __device__ __forceinline__ void store_out(const DecodeArgs &a, int64_t row, int 
         static_cast<__nv_bfloat16 *>(a.out)[row * kHeadDim + d] = __float2bfloat16_rn(v);
 }
 
+// Per-lane byte offsets of the ldmatrix rows inside a 16-token tile (128-byte
+// rows, 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r & 7)).
+// x4 load q covers: K -> matrices (j, sg) = (mi & 1, 2q + (mi >> 1)), rows
+// 8j..8j+7; V -> the same pattern over (token half, dim segment).
+struct TileOffsets {
+    uint32_t ld[4];
+};
+
+__device__ __forceinline__ TileOffsets tile_offsets(int lane)
+{
+    TileOffsets o;
+    const int r = lane & 7, mi = lane >> 3;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const int half = mi & 1, sg = 2 * q + (mi >> 1), tok = 8 * half + r;
+        o.ld[q] = static_cast<uint32_t>(tok * kHeadDim + ((sg ^ r) << 4));
+    }
+    return o;
+}
+
 // One 16-token tile: scores, online softmax update, P.V accumulation.
-// kt / vt: shared addresses of the tile's K and V rows (128 B each, 128-byte
-// swizzle, tile base 1024-byte aligned).  nv: valid tokens in the tile (1..16).
-__device__ __forceinline__ void process_tile(uint32_t kt, uint32_t vt, int nv, const uint32_t (&qa)[8][2],
-                                             float scale2, float &m_ref, float &lsum, float (&acc)[8][4],
-                                             int lane)
+// kt / vt: shared addresses of the tile's K and V rows (tile base 1024-byte
+// aligned).  nv: valid tokens in the tile (1..16); kPartial when nv < 16.
+template <bool kPartial>
+__device__ __forceinline__ void process_tile(uint32_t kt, uint32_t vt, int nv, const TileOffsets &off,
+                                             const uint32_t (&qa)[8][2], float scale2, float &m_ref, float &lsum,
+                                             float (&acc)[8][4], int lane)
 {
     const int t4 = lane & 3;
-    const int r = lane & 7;
-    const int mi = lane >> 3;
 
-    // K fragments: matrix (j, sg) = tokens 8j..8j+7, dims 16sg..16sg+15.
-    uint32_t kf[2][8];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int j = mi & 1, sg = 2 * q + (mi >> 1), tok = 8 * j + r;
-        ldsm_x4(kt + tok * kHeadDim + ((sg ^ r) << 4), kf[0][2 * q], kf[1][2 * q], kf[0][2 * q + 1],
-                kf[1][2 * q + 1]);
-    }
-    // V fragments (transposed): matrix (hh, sg) = tokens 8hh..8hh+7, dims 16sg..16sg+15.
+    uint32_t kf[2][8];   // [token half j][dim segment]
     uint32_t vf[2][8];
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        const int hh = mi & 1, sg = 2 * q + (mi >> 1), tok = 8 * hh + r;
-        ldsm_x4_trans(vt + tok * kHeadDim + ((sg ^ r) << 4), vf[0][2 * q], vf[1][2 * q],
-                      vf[0][2 * q + 1], vf[1][2 * q + 1]);
-    }
+    for (int q = 0; q < 4; ++q)
+        ldsm_x4(kt + off.ld[q], kf[0][2 * q], kf[1][2 * q], kf[0][2 * q + 1], kf[1][2 * q + 1]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        ldsm_x4_trans(vt + off.ld[q], vf[0][2 * q], vf[1][2 * q], vf[0][2 * q + 1], vf[1][2 * q + 1]);
 
     // S = Q K^T.  Thread (gid, t4) gets S[head gid][tokens 8j + 2t4, 8j + 2t4 + 1].
     float sc[2][4];
@@ -222,21 +256,25 @@ __device__ __forceinline__ void process_tile(uint32_t kt, uint32_t vt, int nv, c
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
 #pragma unroll
-        for (int j = 0; j < 2; ++j)
-            mma_16816(sc[j], qa[kk][0], 0u, qa[kk][1], 0u, e4m3x2_to_f16x2(kf[j][kk]),
-                      e4m3x2_to_f16x2(kf[j][kk] >> 16));
+        for (int j = 0; j < 2; ++j) {
+            uint32_t b0, b1;
+            e4m3x4_to_f16x4(kf[j][kk], b0, b1);
+            mma_16816(sc[j], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+        }
 
-    float y[4];
-    y[0] = (2 * t4 < nv) ? sc[0][0] * scale2 : -INFINITY;
-    y[1] = (2 * t4 + 1 < nv) ? sc[0][1] * scale2 : -INFINITY;
-    y[2] = (8 + 2 * t4 < nv) ? sc[1][0] * scale2 : -INFINITY;
-    y[3] = (9 + 2 * t4 < nv) ? sc[1][1] * scale2 : -INFINITY;
+    float y[4] = {sc[0][0] * scale2, sc[0][1] * scale2, sc[1][0] * scale2, sc[1][1] * scale2};
+    if (kPartial) {
+        if (2 * t4 >= nv) y[0] = -INFINITY;
+        if (2 * t4 + 1 >= nv) y[1] = -INFINITY;
+        if (8 + 2 * t4 >= nv) y[2] = -INFINITY;
+        if (9 + 2 * t4 >= nv) y[3] = -INFINITY;
+    }
     float tmax = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
     tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 1));
     tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 2));
     if (__any_sync(kFull, tmax > m_ref + kRescaleThreshold)) {
         const float m_new = fmaxf(m_ref, tmax);
-        const float alpha = exp2f(m_ref - m_new);
+        const float alpha = ex2_approx(m_ref - m_new);
         lsum *= alpha;
         m_ref = m_new;
         // The accumulator of this thread belongs to heads 2*t4 and 2*t4+1.
@@ -250,15 +288,15 @@ __device__ __forceinline__ void process_tile(uint32_t kt, uint32_t vt, int nv, c
             acc[sg][3] *= a1;
         }
     }
-    const float p0 = exp2f(y[0] - m_ref), p1 = exp2f(y[1] - m_ref);
-    const float p2 = exp2f(y[2] - m_ref), p3 = exp2f(y[3] - m_ref);
+    const float p0 = ex2_approx(y[0] - m_ref), p1 = ex2_approx(y[1] - m_ref);
+    const float p2 = ex2_approx(y[2] - m_ref), p3 = ex2_approx(y[3] - m_ref);
     lsum += (p0 + p1) + (p2 + p3);
     const uint32_t h01 = f32x2_to_f16x2(p0, p1), h23 = f32x2_to_f16x2(p2, p3);
     const float2 b01 = f16x2_to_f32x2(h01), b23 = f16x2_to_f32x2(h23);
     const uint32_t l01 = f32x2_to_f16x2(p0 - b01.x, p1 - b01.y);
     const uint32_t l23 = f32x2_to_f16x2(p2 - b23.x, p3 - b23.y);
 
-    if (nv < 16) {   // rows past the sequence end may hold anything (even NaN codes)
+    if (kPartial) {   // rows past the sequence end may hold anything (even NaN codes)
         const uint32_t m0 = (2 * t4 < nv ? 0x0000FFFFu : 0u) | (2 * t4 + 1 < nv ? 0xFFFF0000u : 0u);
         const uint32_t m1 = (8 + 2 * t4 < nv ? 0x0000FFFFu : 0u) | (9 + 2 * t4 < nv ? 0xFFFF0000u : 0u);
 #pragma unroll
@@ -270,21 +308,21 @@ __device__ __forceinline__ void process_tile(uint32_t kt, uint32_t vt, int nv, c
     // O^T[d][g] += V^T[d][t] P^T[t][g]; dims of m-tile sg: rows gid -> 16sg+2gid, gid+8 -> 16sg+2gid+1.
 #pragma unroll
     for (int sg = 0; sg < 8; ++sg) {
-        const uint32_t x0 = __byte_perm(vf[0][sg], 0, 0x3120);
-        const uint32_t x1 = __byte_perm(vf[1][sg], 0, 0x3120);
-        const uint32_t a0 = e4m3x2_to_f16x2(x0), a1 = e4m3x2_to_f16x2(x0 >> 16);
-        const uint32_t a2 = e4m3x2_to_f16x2(x1), a3 = e4m3x2_to_f16x2(x1 >> 16);
+        uint32_t a0, a1, a2, a3;
+        e4m3x4_to_f16x4(__byte_perm(vf[0][sg], 0, 0x3120), a0, a1);
+        e4m3x4_to_f16x4(__byte_perm(vf[1][sg], 0, 0x3120), a2, a3);
         mma_16816(acc[sg], a0, a1, a2, a3, h01, h23);
         mma_16816(acc[sg], a0, a1, a2, a3, l01, l23);
     }
 }
 
 template <int P>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                             const DecodeArgs a)
 {
     using S = Smem<P>;
+    constexpr int kStages = S::kStages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -338,6 +376,16 @@ __global__ void __launch_bounds__(kThreads, 3)
         __syncthreads();
     }
 
+    // Sequences with no tokens: nobody streams them, so write their zero rows here.
+    for (int sg = blockIdx.x; sg < a.batch * a.hkv; sg += a.num_ctas) {
+        const int b = sg / a.hkv;
+        if (pages_of(pstart, b) == 0) {
+            const int64_t row0 = static_cast<int64_t>(b) * a.hq + static_cast<int64_t>(sg % a.hkv) * a.group;
+            for (int e = tid; e < a.group * kHeadDim; e += kThreads)
+                store_out(a, row0 + (e >> 7), e & (kHeadDim - 1), 0.f);
+        }
+    }
+
     const int64_t total = static_cast<int64_t>(pstart[a.batch]) * a.hkv;
     const int64_t lo = static_cast<int64_t>(blockIdx.x) * total / a.num_ctas;
     const int64_t hi = static_cast<int64_t>(blockIdx.x + 1) * total / a.num_ctas;
@@ -362,7 +410,9 @@ __global__ void __launch_bounds__(kThreads, 3)
         int my_z = 0;
         if (lane < n_total)
             my_z = tile_z(advance(pstart, a.batch, a.hkv, base, lane));
-        int64_t issued = 0;
+        int issued = 0;
+        int st = 0;            // stage of page i
+        uint32_t use = 0;      // how many times stage st has been filled before page i
         for (int64_t i0 = 0; i0 < n_total; i0 += 32) {
             const int n = static_cast<int>(min(static_cast<int64_t>(32), n_total - i0));
             const Loc next = advance(pstart, a.batch, a.hkv, base, 32);
@@ -372,19 +422,20 @@ __global__ void __launch_bounds__(kThreads, 3)
             for (int j = 0; j < n; ++j) {
                 const int z = __shfl_sync(kFull, my_z, j);
                 if (lane == 0 && !*abort_flag) {
-                    const int64_t i = i0 + j;
-                    const int s = static_cast<int>(i % kStages);
-                    const uint32_t u = static_cast<uint32_t>(i / kStages);
                     bool ok = true;
-                    if (u > 0)
-                        ok = wait_thread(bar_empty + 8 * s, (u - 1) & 1u, abort_flag, a.err, true);
+                    if (use > 0)
+                        ok = wait_thread(bar_empty + 8 * st, (use - 1) & 1u, abort_flag, a.err, true);
                     if (ok) {
-                        const uint32_t dst = ring + s * S::kStageBytes;
-                        mbar_arrive_expect_tx(bar_full + 8 * s, 2 * S::kTile);
-                        tma_load_3d(dst, &tm_k, 0, 0, z, bar_full + 8 * s, policy);
-                        tma_load_3d(dst + S::kTile, &tm_v, 0, 0, z, bar_full + 8 * s, policy);
-                        issued = i + 1;
+                        const uint32_t dst = ring + st * S::kStageBytes;
+                        mbar_arrive_expect_tx(bar_full + 8 * st, 2 * S::kTile);
+                        tma_load_3d(dst, &tm_k, 0, 0, z, bar_full + 8 * st, policy);
+                        tma_load_3d(dst + S::kTile, &tm_v, 0, 0, z, bar_full + 8 * st, policy);
+                        issued = static_cast<int>(i0) + j + 1;
                     }
+                }
+                if (++st == kStages) {
+                    st = 0;
+                    ++use;
                 }
             }
             my_z = next_z;
@@ -393,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 3)
         // Drain: never leave the CTA with a copy still writing shared memory.
         if (lane == 0) {
             for (int s = 0; s < kStages && s < issued; ++s) {
-                const uint32_t u = static_cast<uint32_t>((issued - 1 - s) / kStages);
+                const uint32_t u = static_cast<uint32_t>((issued - 1 - s) / kStages);   // last fill of stage s
                 wait_thread(bar_full + 8 * s, u & 1u, abort_flag, a.err, false);
             }
         }
@@ -405,8 +456,12 @@ __global__ void __launch_bounds__(kThreads, 3)
     float *cm = reinterpret_cast<float *>(smem + S::kCm);
     float *cl = reinterpret_cast<float *>(smem + S::kCl);
     float *ca = reinterpret_cast<float *>(smem + S::kCa);
+    const TileOffsets off = tile_offsets(lane);
     Loc loc = locate(pstart, a.batch, a.hkv, lo);
-    int64_t cur = lo, ibase = 0;
+    int64_t cur = lo;
+    int ibase = 0;             // CTA page counter at the start of the piece
+    int st = warp;             // stage of this warp's next page (pages w, w+4, ... go to this warp)
+    uint32_t par = 0;          // its fill parity
     while (cur < hi) {
         const int np = pages_of(pstart, loc.b);
         const int n_piece = static_cast<int>(min(static_cast<int64_t>(np - loc.pg), hi - cur));
@@ -439,21 +494,30 @@ __global__ void __launch_bounds__(kThreads, 3)
             for (int c = 0; c < 4; ++c)
                 acc[sg][c] = 0.f;
 
-        const int64_t iend = ibase + n_piece;
-        for (int64_t i = ibase + (warp - ibase % kConsumerWarps + kConsumerWarps) % kConsumerWarps; i < iend;
+        const int iend = ibase + n_piece;
+        for (int i = ibase + (warp - ibase % kConsumerWarps + kConsumerWarps) % kConsumerWarps; i < iend;
              i += kConsumerWarps) {
-            const int page = loc.pg + static_cast<int>(i - ibase);
+            const int page = loc.pg + (i - ibase);
             const int nv = min(P, L - page * P);
-            const int s = static_cast<int>(i % kStages);
-            const uint32_t par = static_cast<uint32_t>(i / kStages) & 1u;
-            if (!wait_warp(bar_full + 8 * s, par, abort_flag, a.err, lane))
+            const int s = st;
+            const uint32_t ph = par;
+            st += kConsumerWarps;
+            if (st >= kStages) {
+                st -= kStages;
+                par ^= 1u;
+            }
+            if (!wait_warp(bar_full + 8 * s, ph, abort_flag, a.err, lane))
                 continue;
             const uint32_t kt = ring + s * S::kStageBytes;
 #pragma unroll
-            for (int sub = 0; sub < P / 16; ++sub)
-                if (sub * 16 < nv)
-                    process_tile(kt + sub * 16 * kHeadDim, kt + S::kTile + sub * 16 * kHeadDim, nv - sub * 16,
-                                 qa, scale2, m_ref, lsum, acc, lane);
+            for (int sub = 0; sub < P / 16; ++sub) {
+                const int nvs = nv - sub * 16;
+                const uint32_t kts = kt + sub * 16 * kHeadDim, vts = kts + S::kTile;
+                if (nvs >= 16)
+                    process_tile<false>(kts, vts, 16, off, qa, scale2, m_ref, lsum, acc, lane);
+                else if (nvs > 0)
+                    process_tile<true>(kts, vts, nvs, off, qa, scale2, m_ref, lsum, acc, lane);
+            }
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar_empty + 8 * s);
@@ -485,7 +549,7 @@ __global__ void __launch_bounds__(kThreads, 3)
             float Ls = 0.f, A = 0.f;
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) {
-                const float f = exp2f(cm[w * 8 + g] - M);
+                const float f = ex2_approx(cm[w * 8 + g] - M);
                 Ls += cl[w * 8 + g] * f;
                 A += ca[(w * 8 + g) * kHeadDim + d] * f;
             }
@@ -501,82 +565,51 @@ __global__ void __launch_bounds__(kThreads, 3)
                 }
             }
         }
+        if (!whole) {
+            // ---- split-K: the CTA finishing the segment's last piece merges all of them
+            int *flags = reinterpret_cast<int *>(smem + S::kFlag);    // [1] last, [2] c0, [3] c1
+            __threadfence();
+            named_barrier(1, kConsumerWarps * 32);
+            if (tid == 0) {
+                const int64_t start = static_cast<int64_t>(pstart[loc.b]) * a.hkv + static_cast<int64_t>(loc.h) * np;
+                const int c0 = cta_of(start, total, a.num_ctas);
+                const int c1 = cta_of(start + np - 1, total, a.num_ctas);
+                unsigned n = 0;
+                for (int c = c0; c <= c1; ++c)
+                    n += cta_has_range(c, total, a.num_ctas) ? 1u : 0u;
+                flags[1] = arrive_last(a.counters + seg, a.epoch, n) ? 1 : 0;
+                flags[2] = c0;
+                flags[3] = c1;
+            }
+            named_barrier(1, kConsumerWarps * 32);
+            if (flags[1]) {
+                __threadfence();
+                const int c0 = flags[2], c1 = flags[3];
+                for (int e = tid; e < a.group * kHeadDim; e += kConsumerWarps * 32) {
+                    const int g = e >> 7, d = e & (kHeadDim - 1);
+                    float M = -INFINITY;
+                    for (int c = c0; c <= c1; ++c)
+                        if (cta_has_range(c, total, a.num_ctas))
+                            M = fmaxf(M, __ldcg(a.partials + (static_cast<int64_t>(c + seg) * a.group + g) *
+                                                                 kPartialStride + kHeadDim));
+                    float Ls = 0.f, A = 0.f;
+                    for (int c = c0; c <= c1; ++c) {
+                        if (!cta_has_range(c, total, a.num_ctas))
+                            continue;
+                        const float *slot = a.partials + (static_cast<int64_t>(c + seg) * a.group + g) * kPartialStride;
+                        const float f = ex2_approx(__ldcg(slot + kHeadDim) - M);
+                        Ls += __ldcg(slot + kHeadDim + 1) * f;
+                        A += __ldcg(slot + d) * f;
+                    }
+                    store_out(a, row0 + g, d, A / Ls * vsc);
+                }
+            }
+        }
         named_barrier(1, kConsumerWarps * 32);
 
         cur += n_piece;
         ibase += n_piece;
         loc = advance(pstart, a.batch, a.hkv, loc, n_piece);
-    }
-}
-
-// Merges the pieces of every segment that more than one CTA touched, writes
-// zeros for empty sequences, and leaves single-piece segments alone.
-__global__ void __launch_bounds__(kCombineThreads) splitk_combine_kernel(const DecodeArgs a, int P)
-{
-    __shared__ int red[2][kCombineThreads / 32];
-    const int seg = blockIdx.x;
-    const int b = seg / a.hkv, h = seg % a.hkv;
-    const int cap = a.max_pages * P;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int before = 0, all = 0;
-    for (int bb = threadIdx.x; bb < a.batch; bb += kCombineThreads) {
-        const int np = (clamp_len(__ldg(a.seq_lens + bb), cap) + P - 1) / P;
-        all += np;
-        if (bb < b)
-            before += np;
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        before += __shfl_xor_sync(kFull, before, o);
-        all += __shfl_xor_sync(kFull, all, o);
-    }
-    if (lane == 0) {
-        red[0][warp] = before;
-        red[1][warp] = all;
-    }
-    __syncthreads();
-    before = 0;
-    all = 0;
-#pragma unroll
-    for (int w = 0; w < kCombineThreads / 32; ++w) {
-        before += red[0][w];
-        all += red[1][w];
-    }
-    const int np = (clamp_len(__ldg(a.seq_lens + b), cap) + P - 1) / P;
-    const int64_t row0 = static_cast<int64_t>(b) * a.hq + static_cast<int64_t>(h) * a.group;
-    if (np == 0) {
-        for (int e = threadIdx.x; e < a.group * kHeadDim; e += kCombineThreads)
-            store_out(a, row0 + (e >> 7), e & (kHeadDim - 1), 0.f);
-        return;
-    }
-    const int64_t total = static_cast<int64_t>(all) * a.hkv;
-    const int64_t start = static_cast<int64_t>(before) * a.hkv + static_cast<int64_t>(h) * np;
-    const int c0 = cta_of(start, total, a.num_ctas);
-    const int c1 = cta_of(start + np - 1, total, a.num_ctas);
-    if (c0 == c1)
-        return;
-    const float vsc = __ldg(a.v_scale + h);
-    // CTAs between c0 and c1 whose range is empty (more CTAs than page-heads)
-    // wrote nothing: skip their slots.
-    auto has_piece = [&](int c) {
-        return static_cast<int64_t>(c) * total / a.num_ctas != static_cast<int64_t>(c + 1) * total / a.num_ctas;
-    };
-    for (int e = threadIdx.x; e < a.group * kHeadDim; e += kCombineThreads) {
-        const int g = e >> 7, d = e & (kHeadDim - 1);
-        float M = -INFINITY;
-        for (int c = c0; c <= c1; ++c)
-            if (has_piece(c))
-                M = fmaxf(M, a.partials[(static_cast<int64_t>(c + seg) * a.group + g) * kPartialStride + kHeadDim]);
-        float Ls = 0.f, A = 0.f;
-        for (int c = c0; c <= c1; ++c) {
-            if (!has_piece(c))
-                continue;
-            const float *slot = a.partials + (static_cast<int64_t>(c + seg) * a.group + g) * kPartialStride;
-            const float f = exp2f(slot[kHeadDim] - M);
-            Ls += slot[kHeadDim + 1] * f;
-            A += slot[d] * f;
-        }
-        store_out(a, row0 + g, d, A / Ls * vsc);
     }
 }
 
@@ -602,16 +635,12 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, co
                                 int page_size, cudaStream_t stream)
 {
     const size_t smem = decode_smem_bytes(page_size, a.batch);
-    if (a.num_ctas > 0) {
+    {
         if (page_size == 32)
             paged_gqa_decode_kernel<32><<<a.num_ctas, kThreads, smem, stream>>>(tm_k, tm_v, a);
         else
             paged_gqa_decode_kernel<16><<<a.num_ctas, kThreads, smem, stream>>>(tm_k, tm_v, a);
-        const cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess)
-            return e;
     }
-    splitk_combine_kernel<<<a.batch * a.hkv, kCombineThreads, 0, stream>>>(a, page_size);
     return cudaGetLastError();
 }
 

@@ -107,12 +107,24 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], uint32_t a0, uint32_t a
 }
 
 // ---------------------------------------------------------------- conversions
-// Two E4M3 bytes (low byte -> low half) to two exact f16 values.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16)
+// Four E4M3 bytes -> two f16x2 registers (bytes 0,1 -> lo; bytes 2,3 -> hi),
+// exact; the 16-bit halves feed the conversions directly.
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t &lo, uint32_t &hi)
 {
-    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair16 & 0xFFFFu),
-                                               __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(x));
+}
+
+// 2^x with the hardware approximation (relative error about 2^-22; -inf -> 0).
+__device__ __forceinline__ float ex2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi)

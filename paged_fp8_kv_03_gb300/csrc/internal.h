@@ -15,7 +15,7 @@ constexpr int kHeadDim = PKV_HEAD_DIM;
 // Decode kernel shape (shared by the launcher and the workspace sizing).
 constexpr int kConsumerWarps = 4;                       // warps that compute
 constexpr int kThreads = (kConsumerWarps + 1) * 32;     // + one TMA producer warp
-constexpr int kStages = 8;                              // pages in flight per CTA
+constexpr int kCtasPerSm = 2;                           // resident decode CTAs per SM
 constexpr int kPartialStride = kHeadDim + 4;            // floats per (slot, head): acc, m, l, pad
 
 struct AppendArgs {
@@ -42,10 +42,18 @@ struct DecodeArgs {
     float sm_scale_log2;        // sm_scale * log2(e): scores live in the exp2 domain
     void *out;
     int out_f32;
-    float *partials;            // [num_ctas + batch * hkv][group][kPartialStride]
+    unsigned long long *counters;   // [batch * hkv] arrival counters: (epoch << 24) | pieces seen
+    float *partials;                // [num_ctas + batch * hkv][group][kPartialStride]
+    unsigned long long epoch;       // unique per call (40 bits), so counters never need clearing
     int32_t *err;
     int num_ctas;
 };
+
+// Workspace = counters (rounded to 256 bytes) followed by the partial slots.
+inline size_t decode_counter_bytes(int batch, int hkv)
+{
+    return (static_cast<size_t>(batch) * hkv * sizeof(unsigned long long) + 255) & ~size_t(255);
+}
 
 // Host helpers (api.cu).
 int device_sm_count();
