@@ -180,12 +180,13 @@ pkv_status pkv_paged_gqa_decode(const void *q,
  *
  * Same arguments and results as pkv_paged_gqa_decode minus the workspace.
  * The split-K scratch lives in a fixed array inside the library image,
- * pkv_decode_noalloc_scratch_bytes() bytes (8 MiB), which every GPU that
+ * pkv_decode_noalloc_scratch_bytes() bytes (16 MiB), which every GPU that
  * loads the library keeps until the process exits.  The call allocates
  * nothing.  Sizes whose scratch would not fit return PKV_ERR_WORKSPACE (the
- * scratch holds 8 bytes per (sequence, kv head) plus, at G = 8, 4224 bytes per
- * partial slot, num_ctas + batch * num_kv_heads slots; with 304 CTAs that
- * allows batch * num_kv_heads up to about 1660).
+ * scratch holds 8 bytes per (sequence, kv head) plus G * 528 bytes per
+ * partial slot, one slot per worker warp (1824 on a 152-SM GPU) plus one per
+ * (sequence, kv head); at G = 8 that allows batch * num_kv_heads up to about
+ * 2100).
  * All calls share the array: calls that overlap on the GPU (two streams, or
  * unordered host threads) race and corrupt each other's results; calls
  * ordered on one stream are safe.  The array keeps the previous call's

@@ -152,7 +152,7 @@ pkv_status check_decode_shape(int batch, int hq, int hkv, int head_dim, int page
 
 size_t workspace_bytes_for(int batch, int hq, int hkv, int num_ctas)
 {
-    const size_t slots = static_cast<size_t>(num_ctas) + static_cast<size_t>(batch) * hkv;
+    const size_t slots = static_cast<size_t>(num_ctas) * kWarps + static_cast<size_t>(batch) * hkv;
     const size_t bytes = slots * static_cast<size_t>(hq / hkv) * kPartialStride * sizeof(float);
     return decode_counter_bytes(batch, hkv) + ((bytes + 255) & ~size_t(255));
 }

@@ -11,21 +11,23 @@
 // design streams every KV byte exactly once at full HBM rate.
 //
 // Work split.  The (sequence, kv head) segments are laid end to end as one
-// list of "page-heads" (one page of one kv head, 2 x P x 128 bytes).  Each of
-// C persistent CTAs takes an equal contiguous range of that list, whatever
-// the sequence lengths (flash-decoding split-K with perfect balance).  A CTA
-// range cuts segments into pieces; a piece that covers a whole segment writes
-// the final output, the others write a partial softmax state (running max m,
-// sum l, unnormalised accumulator) into workspace slot (cta + segment) and
-// bump the segment's arrival counter; the CTA that brings the count to the
-// number of pieces merges them, in CTA order (deterministic), and writes the
-// output.  Counters carry a per-call epoch so they never need clearing.
+// list of "page-heads" (one page of one kv head, 2 x P x 128 bytes).  Every
+// warp of the persistent grid is an independent worker that takes an equal
+// contiguous range of that list, whatever the sequence lengths (split-K /
+// flash-decoding with exact balance).  A worker's range cuts segments into
+// pieces; a piece covering a whole segment writes the final output, the
+// others write a partial softmax state (running max m, sum l, unnormalised
+// accumulator) into workspace slot (worker + segment) and bump the segment's
+// arrival counter; the worker that brings the count to the number of pieces
+// merges them, in worker order (deterministic), and writes the output.
+// Counters carry a per-call epoch so they never need clearing.
 //
-// Inside a CTA: one producer warp walks the CTA's pages, fetches block-table
-// entries 32 at a time one batch ahead, and issues two TMA tensor loads per
-// page (K tile, V tile; 128-byte swizzled, evict-first in L2) into a 96 KB
-// shared-memory ring (24 pages at P = 16) guarded by full/empty mbarriers.  Four consumer
-// warps take the pages round-robin.  Each warp reads a 16-token tile with
+// Inside a worker (one warp): lane 0 issues two TMA tensor loads per page
+// (K tile, V tile; 128-byte swizzled, evict-first in L2) into the warp's own
+// 4-stage shared-memory ring (2 stages of 32-token pages), each stage guarded
+// by one mbarrier; the warp refills a stage as soon as it has consumed it, so
+// no cross-warp handshake sits on the load path.  Block-table entries come in
+// 32 at a time, one batch ahead.  The warp reads a 16-token tile with
 // ldmatrix (conflict-free thanks to the swizzle), widens E4M3 to f16 exactly
 // in registers, and runs both products on the tensor cores with mma.sync
 // m16n8k16 (f16 in, f32 accumulate):
@@ -35,8 +37,7 @@
 // probabilities never leave registers.  P is split into f16 hi + lo parts
 // (two PV products) so the probabilities keep ~22 significant bits.  The
 // online softmax runs in the exp2 domain with a lazy rescale (only when a
-// running max grows by more than 2^8).  At the end of a piece the four warps
-// merge their states through shared memory.
+// running max grows by more than 2^8).
 //
 // Every wait on an mbarrier is bounded (2 s on the global timer): on expiry
 // the kernel raises PKV_DEVERR_TIMEOUT, stops issuing copies, drains the ones
@@ -104,15 +105,15 @@ __device__ Loc advance(const int *ps, int batch, int hkv, Loc l, int64_t n)
     return l;
 }
 
-// CTA whose range holds list position x (ranges are [c*T/C, (c+1)*T/C)).
-__device__ __forceinline__ int cta_of(int64_t x, int64_t total, int ctas)
+// Worker whose range holds list position x (ranges are [w*T/W, (w+1)*T/W)).
+__device__ __forceinline__ int worker_of(int64_t x, int64_t total, int workers)
 {
-    return static_cast<int>(((x + 1) * ctas - 1) / total);
+    return static_cast<int>(((x + 1) * workers - 1) / total);
 }
 
-__device__ __forceinline__ bool cta_has_range(int c, int64_t total, int ctas)
+__device__ __forceinline__ bool worker_has_range(int w, int64_t total, int workers)
 {
-    return static_cast<int64_t>(c) * total / ctas != static_cast<int64_t>(c + 1) * total / ctas;
+    return static_cast<int64_t>(w) * total / workers != static_cast<int64_t>(w + 1) * total / workers;
 }
 
 // Counts one more finished piece of a segment for this call's epoch; true for
@@ -134,16 +135,12 @@ template <int P>
 struct Smem {
     static constexpr int kTile = P * kHeadDim;              // bytes of one K (or V) tile
     static constexpr int kStageBytes = 2 * kTile;
-    static constexpr int kStages = P == 16 ? 20 : 8;           // 80 KB / 64 KB ring
-    static_assert(kStages % kConsumerWarps == 0, "each consumer warp owns a fixed subset of stages");
-    static constexpr int kBar = kStages * kStageBytes;      // full[kStages], empty[kStages]
-    static constexpr int kFlag = kBar + 2 * kStages * 8;    // abort flag, last-piece flag, c0, c1
-    static constexpr int kWarpSum = kFlag + 16;             // scan scratch (5 ints)
-    static constexpr int kCm = kWarpSum + 32;               // [warps][8] running max
-    static constexpr int kCl = kCm + kConsumerWarps * 8 * 4;        // [warps][8] sums
-    static constexpr int kCa = kCl + kConsumerWarps * 8 * 4;        // [warps][8][128] accumulators
-    static constexpr int kPstart = kCa + kConsumerWarps * 8 * kHeadDim * 4;
-    static_assert(kCa % 16 == 0, "accumulator scratch must be 16-byte aligned");
+    static constexpr int kStages = P == 16 ? 4 : 2;         // per warp: 16 KB ring
+    static constexpr int kWarpRing = kStages * kStageBytes;
+    static constexpr int kBar = kWarps * kWarpRing;         // full[kWarps][kStages]
+    static constexpr int kFlag = kBar + kWarps * kStages * 8;   // abort flag
+    static constexpr int kWarpSum = kFlag + 16;             // scan scratch (kWarps ints)
+    static constexpr int kPstart = kWarpSum + 32;
     static size_t bytes(int batch) { return static_cast<size_t>(kPstart) + 4u * (batch + 1) + 1024u; }
 };
 
@@ -205,6 +202,57 @@ __device__ __forceinline__ void store_out(const DecodeArgs &a, int64_t row, int 
         static_cast<float *>(a.out)[row * kHeadDim + d] = v;
     else
         static_cast<__nv_bfloat16 *>(a.out)[row * kHeadDim + d] = __float2bfloat16_rn(v);
+}
+
+__device__ __forceinline__ void store_pair(const DecodeArgs &a, int64_t row, int d, float v0, float v1)
+{
+    if (a.out_f32)
+        *reinterpret_cast<float2 *>(static_cast<float *>(a.out) + row * kHeadDim + d) = make_float2(v0, v1);
+    else
+        *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(a.out) + row * kHeadDim + d) =
+            __floats2bfloat162_rn(v0, v1);
+}
+
+// Merges the partial states of one segment written by workers w0..w1 (in
+// worker order) and writes its G output rows.  One warp; lanes split the
+// pieces for the max and the sum, then the 128 dims.
+__device__ __noinline__ void merge_pieces(const DecodeArgs &a, int seg, int w0, int w1, bool dense, int64_t total,
+                                          int workers, int64_t row0, float vsc, int lane)
+{
+    for (int g = 0; g < a.group; ++g) {
+        auto slot = [&](int w) {
+            return a.partials + (static_cast<int64_t>(w + seg) * a.group + g) * kPartialStride;
+        };
+        float mloc = -INFINITY;
+        for (int w = w0 + lane; w <= w1; w += 32)
+            if (dense || worker_has_range(w, total, workers))
+                mloc = fmaxf(mloc, __ldcg(slot(w) + kHeadDim));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, o));
+        const float M = mloc;
+        float lloc = 0.f;
+        for (int w = w0 + lane; w <= w1; w += 32)
+            if (dense || worker_has_range(w, total, workers))
+                lloc += __ldcg(slot(w) + kHeadDim + 1) * ex2_approx(__ldcg(slot(w) + kHeadDim) - M);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            lloc += __shfl_xor_sync(kFull, lloc, o);
+        const float inv = vsc / lloc;
+        float A[4] = {0.f, 0.f, 0.f, 0.f};
+        for (int w = w0; w <= w1; ++w) {
+            if (!dense && !worker_has_range(w, total, workers))
+                continue;
+            const float *sl = slot(w);
+            const float f = ex2_approx(__ldcg(sl + kHeadDim) - M);
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                A[j] += __ldcg(sl + lane + 32 * j) * f;
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            store_out(a, row0 + g, lane + 32 * j, A[j] * inv);
+    }
 }
 
 // Per-lane byte offsets of the ldmatrix rows inside a 16-token tile (128-byte
@@ -330,9 +378,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int *pstart = reinterpret_cast<int *>(smem + S::kPstart);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kFlag);
     int *warp_sum = reinterpret_cast<int *>(smem + S::kWarpSum);
-    const uint32_t ring = smem_addr(smem);
-    const uint32_t bar_full = smem_addr(smem + S::kBar);
-    const uint32_t bar_empty = bar_full + 8 * kStages;
     const int cap = a.max_pages * P;
 
     // ---- per-sequence page offsets (every CTA computes them; B ints from L2)
@@ -353,10 +398,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             warp_sum[warp] = incl;
         if (tid == 0) {
             *abort_flag = 0;
-            for (int s = 0; s < kStages; ++s) {
-                mbar_init(bar_full + 8 * s, 1);
-                mbar_init(bar_empty + 8 * s, 1);
-            }
+            const uint32_t bar0 = smem_addr(smem + S::kBar);
+            for (int s = 0; s < kWarps * kStages; ++s)
+                mbar_init(bar0 + 8 * s, 1);
             fence_barrier_init();
         }
         __syncthreads();
@@ -386,96 +430,76 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         }
     }
 
+    const int workers = a.num_ctas * kWarps;
+    const int worker = blockIdx.x * kWarps + warp;
     const int64_t total = static_cast<int64_t>(pstart[a.batch]) * a.hkv;
-    const int64_t lo = static_cast<int64_t>(blockIdx.x) * total / a.num_ctas;
-    const int64_t hi = static_cast<int64_t>(blockIdx.x + 1) * total / a.num_ctas;
+    const int64_t lo = static_cast<int64_t>(worker) * total / workers;
+    const int64_t hi = static_cast<int64_t>(worker + 1) * total / workers;
     if (lo >= hi)
-        return;
+        return;                                  // warp-level: no CTA barrier follows
+    const int n_total = static_cast<int>(hi - lo);
 
-    if (warp == kConsumerWarps) {
-        // ================= producer warp =================
-        const uint64_t policy = l2_policy_evict_first();
-        const int64_t n_total = hi - lo;
-        const int zoob = static_cast<int>(a.num_pages * a.hkv);   // first out-of-pool tile: reads zeros
-        auto tile_z = [&](Loc l) -> int {
-            const int phys = __ldg(a.block_table + static_cast<int64_t>(l.b) * a.max_pages + l.pg);
-            if (phys < 0 || phys >= a.num_pages) {
-                if (a.err)
-                    atomicOr(a.err, PKV_DEVERR_PAGE);
-                return zoob;
-            }
-            return phys * a.hkv + l.h;
-        };
-        Loc base = locate(pstart, a.batch, a.hkv, lo);
-        int my_z = 0;
-        if (lane < n_total)
-            my_z = tile_z(advance(pstart, a.batch, a.hkv, base, lane));
-        int issued = 0;
-        int st = 0;            // stage of page i
-        uint32_t use = 0;      // how many times stage st has been filled before page i
-        for (int64_t i0 = 0; i0 < n_total; i0 += 32) {
-            const int n = static_cast<int>(min(static_cast<int64_t>(32), n_total - i0));
-            const Loc next = advance(pstart, a.batch, a.hkv, base, 32);
-            int next_z = 0;
-            if (i0 + 32 + lane < n_total)
-                next_z = tile_z(advance(pstart, a.batch, a.hkv, next, lane));
-            for (int j = 0; j < n; ++j) {
-                const int z = __shfl_sync(kFull, my_z, j);
-                if (lane == 0 && !*abort_flag) {
-                    bool ok = true;
-                    if (use > 0)
-                        ok = wait_thread(bar_empty + 8 * st, (use - 1) & 1u, abort_flag, a.err, true);
-                    if (ok) {
-                        const uint32_t dst = ring + st * S::kStageBytes;
-                        mbar_arrive_expect_tx(bar_full + 8 * st, 2 * S::kTile);
-                        tma_load_3d(dst, &tm_k, 0, 0, z, bar_full + 8 * st, policy);
-                        tma_load_3d(dst + S::kTile, &tm_v, 0, 0, z, bar_full + 8 * st, policy);
-                        issued = static_cast<int>(i0) + j + 1;
-                    }
-                }
-                if (++st == kStages) {
-                    st = 0;
-                    ++use;
-                }
-            }
-            my_z = next_z;
-            base = next;
+    const uint32_t ring = smem_addr(smem) + warp * S::kWarpRing;
+    const uint32_t bars = smem_addr(smem + S::kBar) + warp * kStages * 8;
+    const uint64_t policy = l2_policy_evict_first();
+    const int zoob = static_cast<int>(a.num_pages * a.hkv);   // first out-of-pool tile: reads zeros
+    auto tile_z = [&](Loc l) -> int {
+        const int phys = __ldg(a.block_table + static_cast<int64_t>(l.b) * a.max_pages + l.pg);
+        if (phys < 0 || phys >= a.num_pages) {
+            if (a.err)
+                atomicOr(a.err, PKV_DEVERR_PAGE);
+            return zoob;
         }
-        // Drain: never leave the CTA with a copy still writing shared memory.
-        if (lane == 0) {
-            for (int s = 0; s < kStages && s < issued; ++s) {
-                const uint32_t u = static_cast<uint32_t>((issued - 1 - s) / kStages);   // last fill of stage s
-                wait_thread(bar_full + 8 * s, u & 1u, abort_flag, a.err, false);
-            }
-        }
-        return;
-    }
+        return phys * a.hkv + l.h;
+    };
 
-    // ================= consumer warps =================
+    // ---- block-table batches: zcur holds pages [32*fb, 32*fb+32), znext the next 32
+    Loc cons = locate(pstart, a.batch, a.hkv, lo);
+    Loc nbase = advance(pstart, a.batch, a.hkv, cons, 32);
+    int zcur = lane < n_total ? tile_z(advance(pstart, a.batch, a.hkv, cons, lane)) : 0;
+    int znext = 32 + lane < n_total ? tile_z(advance(pstart, a.batch, a.hkv, nbase, lane)) : 0;
+    int fb = 0;
+    int issued_hi = 0;                           // pages [0, issued_hi) had their loads issued
+
+    auto issue = [&](int f) {                    // warp-uniform; page f goes to stage f % kStages
+        if (f >= 32 * (fb + 1)) {
+            zcur = znext;
+            ++fb;
+            nbase = advance(pstart, a.batch, a.hkv, nbase, 32);
+            znext = 32 * (fb + 1) + lane < n_total ? tile_z(advance(pstart, a.batch, a.hkv, nbase, lane)) : 0;
+        }
+        const int z = __shfl_sync(kFull, zcur, f & 31);
+        if (lane == 0 && !*abort_flag) {
+            const int s = f % kStages;
+            const uint32_t dst = ring + s * S::kStageBytes;
+            mbar_arrive_expect_tx(bars + 8 * s, 2 * S::kTile);
+            tma_load_3d(dst, &tm_k, 0, 0, z, bars + 8 * s, policy);
+            tma_load_3d(dst + S::kTile, &tm_v, 0, 0, z, bars + 8 * s, policy);
+            issued_hi = f + 1;
+        }
+    };
+    for (int f = 0; f < kStages && f < n_total; ++f)
+        issue(f);
+
     const int gid = lane >> 2, t4 = lane & 3;
-    float *cm = reinterpret_cast<float *>(smem + S::kCm);
-    float *cl = reinterpret_cast<float *>(smem + S::kCl);
-    float *ca = reinterpret_cast<float *>(smem + S::kCa);
     const TileOffsets off = tile_offsets(lane);
-    Loc loc = locate(pstart, a.batch, a.hkv, lo);
-    int64_t cur = lo;
-    int ibase = 0;             // CTA page counter at the start of the piece
-    int st = warp;             // stage of this warp's next page (pages w, w+4, ... go to this warp)
-    uint32_t par = 0;          // its fill parity
-    while (cur < hi) {
-        const int np = pages_of(pstart, loc.b);
-        const int n_piece = static_cast<int>(min(static_cast<int64_t>(np - loc.pg), hi - cur));
-        const int L = clamp_len(__ldg(a.seq_lens + loc.b), cap);
-        const bool whole = (loc.pg == 0) && (n_piece == np);
-        const int seg = loc.b * a.hkv + loc.h;
-        const float scale2 = __ldg(a.k_scale + loc.h) * a.sm_scale_log2;
+    int st = 0;                                  // stage of page k
+    uint32_t ph = 0;                             // its fill parity
+    int k = 0;
+    while (k < n_total) {
+        const int np = pages_of(pstart, cons.b);
+        const int n_piece = min(np - cons.pg, n_total - k);
+        const int L = clamp_len(__ldg(a.seq_lens + cons.b), cap);
+        const bool whole = (cons.pg == 0) && (n_piece == np);
+        const int seg = cons.b * a.hkv + cons.h;
+        const float scale2 = __ldg(a.k_scale + cons.h) * a.sm_scale_log2;
 
         // Q fragment for k-step kk: head gid, dims 16kk + 4t4 + {0,1} and {2,3}.
         uint32_t qa[8][2];
         {
             const bool valid = gid < a.group;
             const __nv_bfloat16 *qrow =
-                a.q + (static_cast<int64_t>(loc.b) * a.hq + loc.h * a.group + (valid ? gid : 0)) * kHeadDim;
+                a.q + (static_cast<int64_t>(cons.b) * a.hq + cons.h * a.group + (valid ? gid : 0)) * kHeadDim;
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 uint2 v = make_uint2(0u, 0u);
@@ -494,122 +518,95 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             for (int c = 0; c < 4; ++c)
                 acc[sg][c] = 0.f;
 
-        const int iend = ibase + n_piece;
-        for (int i = ibase + (warp - ibase % kConsumerWarps + kConsumerWarps) % kConsumerWarps; i < iend;
-             i += kConsumerWarps) {
-            const int page = loc.pg + (i - ibase);
-            const int nv = min(P, L - page * P);
+        for (int j = 0; j < n_piece; ++j, ++k) {
+            const int nv = min(P, L - (cons.pg + j) * P);
             const int s = st;
-            const uint32_t ph = par;
-            st += kConsumerWarps;
-            if (st >= kStages) {
-                st -= kStages;
-                par ^= 1u;
+            const uint32_t par = ph;
+            if (++st == kStages) {
+                st = 0;
+                ph ^= 1u;
             }
-            if (!wait_warp(bar_full + 8 * s, ph, abort_flag, a.err, lane))
-                continue;
-            const uint32_t kt = ring + s * S::kStageBytes;
+            if (wait_warp(bars + 8 * s, par, abort_flag, a.err, lane)) {
+                const uint32_t kt = ring + s * S::kStageBytes;
 #pragma unroll
-            for (int sub = 0; sub < P / 16; ++sub) {
-                const int nvs = nv - sub * 16;
-                const uint32_t kts = kt + sub * 16 * kHeadDim, vts = kts + S::kTile;
-                if (nvs >= 16)
-                    process_tile<false>(kts, vts, 16, off, qa, scale2, m_ref, lsum, acc, lane);
-                else if (nvs > 0)
-                    process_tile<true>(kts, vts, nvs, off, qa, scale2, m_ref, lsum, acc, lane);
+                for (int sub = 0; sub < P / 16; ++sub) {
+                    const int nvs = nv - sub * 16;
+                    const uint32_t kts = kt + sub * 16 * kHeadDim, vts = kts + S::kTile;
+                    if (nvs >= 16)
+                        process_tile<false>(kts, vts, 16, off, qa, scale2, m_ref, lsum, acc, lane);
+                    else if (nvs > 0)
+                        process_tile<true>(kts, vts, nvs, off, qa, scale2, m_ref, lsum, acc, lane);
+                }
             }
+            // Stage s is free again: order this warp's reads before the async-proxy refill.
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             __syncwarp();
-            if (lane == 0)
-                mbar_arrive(bar_empty + 8 * s);
+            if (k + kStages < n_total)
+                issue(k + kStages);
         }
 
-        // ---- merge the four warps' states of this piece
+        // ---- end of piece
         lsum += __shfl_xor_sync(kFull, lsum, 1);
         lsum += __shfl_xor_sync(kFull, lsum, 2);
-        if (t4 == 0) {
-            cm[warp * 8 + gid] = m_ref;
-            cl[warp * 8 + gid] = lsum;
-        }
+        const float vsc = __ldg(a.v_scale + cons.h);
+        const int64_t row0 = static_cast<int64_t>(cons.b) * a.hq + cons.h * a.group;
+        const bool h0 = 2 * t4 < a.group, h1 = 2 * t4 + 1 < a.group;
+        if (whole) {
+            const float l0 = __shfl_sync(kFull, lsum, 8 * t4), l1 = __shfl_sync(kFull, lsum, 8 * t4 + 4);
+            const float s0 = vsc / l0, s1 = vsc / l1;
 #pragma unroll
-        for (int sg = 0; sg < 8; ++sg) {
-            const int d = 16 * sg + 2 * gid;
-            *reinterpret_cast<float2 *>(ca + (warp * 8 + 2 * t4) * kHeadDim + d) = make_float2(acc[sg][0], acc[sg][2]);
-            *reinterpret_cast<float2 *>(ca + (warp * 8 + 2 * t4 + 1) * kHeadDim + d) =
-                make_float2(acc[sg][1], acc[sg][3]);
-        }
-        named_barrier(1, kConsumerWarps * 32);
-        const float vsc = __ldg(a.v_scale + loc.h);
-        const int64_t row0 = static_cast<int64_t>(loc.b) * a.hq + loc.h * a.group;
-        for (int e = tid; e < a.group * kHeadDim; e += kConsumerWarps * 32) {
-            const int g = e >> 7, d = e & (kHeadDim - 1);
-            float M = -INFINITY;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w)
-                M = fmaxf(M, cm[w * 8 + g]);
-            float Ls = 0.f, A = 0.f;
-#pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float f = ex2_approx(cm[w * 8 + g] - M);
-                Ls += cl[w * 8 + g] * f;
-                A += ca[(w * 8 + g) * kHeadDim + d] * f;
+            for (int sg = 0; sg < 8; ++sg) {
+                const int d = 16 * sg + 2 * gid;
+                if (h0)
+                    store_pair(a, row0 + 2 * t4, d, acc[sg][0] * s0, acc[sg][2] * s0);
+                if (h1)
+                    store_pair(a, row0 + 2 * t4 + 1, d, acc[sg][1] * s1, acc[sg][3] * s1);
             }
-            if (whole) {
-                store_out(a, row0 + g, d, A / Ls * vsc);
-            } else {
-                float *slot = a.partials +
-                              (static_cast<int64_t>(blockIdx.x + seg) * a.group + g) * kPartialStride;
-                slot[d] = A;
-                if (d == 0) {
-                    slot[kHeadDim] = M;
-                    slot[kHeadDim + 1] = Ls;
-                }
+        } else {
+            float *slot = a.partials + static_cast<int64_t>(worker + seg) * a.group * kPartialStride;
+#pragma unroll
+            for (int sg = 0; sg < 8; ++sg) {
+                const int d = 16 * sg + 2 * gid;
+                if (h0)
+                    *reinterpret_cast<float2 *>(slot + (2 * t4) * kPartialStride + d) = make_float2(acc[sg][0], acc[sg][2]);
+                if (h1)
+                    *reinterpret_cast<float2 *>(slot + (2 * t4 + 1) * kPartialStride + d) =
+                        make_float2(acc[sg][1], acc[sg][3]);
             }
-        }
-        if (!whole) {
-            // ---- split-K: the CTA finishing the segment's last piece merges all of them
-            int *flags = reinterpret_cast<int *>(smem + S::kFlag);    // [1] last, [2] c0, [3] c1
+            if (t4 == 0 && gid < a.group) {
+                slot[gid * kPartialStride + kHeadDim] = m_ref;
+                slot[gid * kPartialStride + kHeadDim + 1] = lsum;
+            }
+            // The worker completing the segment's last piece merges all of them.
             __threadfence();
-            named_barrier(1, kConsumerWarps * 32);
-            if (tid == 0) {
-                const int64_t start = static_cast<int64_t>(pstart[loc.b]) * a.hkv + static_cast<int64_t>(loc.h) * np;
-                const int c0 = cta_of(start, total, a.num_ctas);
-                const int c1 = cta_of(start + np - 1, total, a.num_ctas);
+            __syncwarp();
+            const int64_t start = static_cast<int64_t>(pstart[cons.b]) * a.hkv + static_cast<int64_t>(cons.h) * np;
+            const int w0 = worker_of(start, total, workers);
+            const int w1 = worker_of(start + np - 1, total, workers);
+            const bool dense = total >= workers;          // then every worker range is non-empty
+            int last = 0;
+            if (lane == 0) {
                 unsigned n = 0;
-                for (int c = c0; c <= c1; ++c)
-                    n += cta_has_range(c, total, a.num_ctas) ? 1u : 0u;
-                flags[1] = arrive_last(a.counters + seg, a.epoch, n) ? 1 : 0;
-                flags[2] = c0;
-                flags[3] = c1;
+                if (dense)
+                    n = static_cast<unsigned>(w1 - w0 + 1);
+                else
+                    for (int w = w0; w <= w1; ++w)
+                        n += worker_has_range(w, total, workers) ? 1u : 0u;
+                last = arrive_last(a.counters + seg, a.epoch, n) ? 1 : 0;
             }
-            named_barrier(1, kConsumerWarps * 32);
-            if (flags[1]) {
+            if (__shfl_sync(kFull, last, 0)) {
                 __threadfence();
-                const int c0 = flags[2], c1 = flags[3];
-                for (int e = tid; e < a.group * kHeadDim; e += kConsumerWarps * 32) {
-                    const int g = e >> 7, d = e & (kHeadDim - 1);
-                    float M = -INFINITY;
-                    for (int c = c0; c <= c1; ++c)
-                        if (cta_has_range(c, total, a.num_ctas))
-                            M = fmaxf(M, __ldcg(a.partials + (static_cast<int64_t>(c + seg) * a.group + g) *
-                                                                 kPartialStride + kHeadDim));
-                    float Ls = 0.f, A = 0.f;
-                    for (int c = c0; c <= c1; ++c) {
-                        if (!cta_has_range(c, total, a.num_ctas))
-                            continue;
-                        const float *slot = a.partials + (static_cast<int64_t>(c + seg) * a.group + g) * kPartialStride;
-                        const float f = ex2_approx(__ldcg(slot + kHeadDim) - M);
-                        Ls += __ldcg(slot + kHeadDim + 1) * f;
-                        A += __ldcg(slot + d) * f;
-                    }
-                    store_out(a, row0 + g, d, A / Ls * vsc);
-                }
+                merge_pieces(a, seg, w0, w1, dense, total, workers, row0, vsc, lane);
             }
         }
-        named_barrier(1, kConsumerWarps * 32);
+        cons = advance(pstart, a.batch, a.hkv, cons, n_piece);
+    }
 
-        cur += n_piece;
-        ibase += n_piece;
-        loc = advance(pstart, a.batch, a.hkv, loc, n_piece);
+    // Drain: never leave with a copy still writing this warp's ring (only
+    // possible after a timeout: normally every issued page was waited for).
+    if (*abort_flag && lane == 0) {
+        for (int f = max(0, issued_hi - kStages); f < issued_hi; ++f)
+            wait_thread(bars + 8 * (f % kStages), static_cast<uint32_t>(f / kStages) & 1u, abort_flag, a.err, false);
     }
 }
 

@@ -13,9 +13,9 @@ namespace pkv {
 constexpr int kHeadDim = PKV_HEAD_DIM;
 
 // Decode kernel shape (shared by the launcher and the workspace sizing).
-constexpr int kConsumerWarps = 4;                       // warps that compute
-constexpr int kThreads = (kConsumerWarps + 1) * 32;     // + one TMA producer warp
-constexpr int kCtasPerSm = 2;                           // resident decode CTAs per SM
+constexpr int kWarps = 4;                               // independent workers per CTA
+constexpr int kThreads = kWarps * 32;
+constexpr int kCtasPerSm = 3;                           // resident decode CTAs per SM
 constexpr int kPartialStride = kHeadDim + 4;            // floats per (slot, head): acc, m, l, pad
 
 struct AppendArgs {
@@ -43,7 +43,7 @@ struct DecodeArgs {
     void *out;
     int out_f32;
     unsigned long long *counters;   // [batch * hkv] arrival counters: (epoch << 24) | pieces seen
-    float *partials;                // [num_ctas + batch * hkv][group][kPartialStride]
+    float *partials;                // [num_ctas * kWarps + batch * hkv][group][kPartialStride]
     unsigned long long epoch;       // unique per call (40 bits), so counters never need clearing
     int32_t *err;
     int num_ctas;

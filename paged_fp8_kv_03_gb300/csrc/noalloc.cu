@@ -17,8 +17,9 @@
 //   * all calls share it: two calls that overlap on the GPU (different streams,
 //     or different host threads without ordering) race on it and give wrong
 //     results.  Calls on one stream are ordered and safe.
-//   * it keeps the last call's contents; the decode writes every slot it
-//     later reads, so nothing needs clearing between calls;
+//   * it keeps the last call's contents; the decode writes every partial slot
+//     before reading it and tags its arrival counters with a per-call epoch,
+//     so nothing needs clearing between calls;
 //   * sizes whose scratch would exceed the array are rejected with
 //     PKV_ERR_WORKSPACE.
 //
@@ -31,7 +32,7 @@
 
 namespace {
 
-constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;   // 8 MiB
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
 
 // Host code must not take this symbol's address as a device pointer: on the
 // host it names a stand-in object.  The device address comes from
