@@ -275,52 +275,70 @@ __device__ __forceinline__ TileOffsets tile_offsets(int lane)
     return o;
 }
 
-// One 16-token tile: scores, online softmax update, P.V accumulation.
-// kt / vt: shared addresses of the tile's K and V rows (tile base 1024-byte
-// aligned).  nv: valid tokens in the tile (1..16); kPartial when nv < 16.
+// One 16-token tile (already in registers, see load_tile): scores, online
+// softmax update, P.V accumulation.  nv: valid tokens in the tile (1..16);
+// kPartial when nv < 16.
+// Instruction order keeps dependent tensor-core ops apart: QK^T runs as four
+// independent accumulator chains, and the two PV products of an accumulator
+// are four MMAs apart.
+struct TileFrags {
+    uint32_t kf[2][8];   // K: [token half j][dim segment]
+    uint32_t vf[2][8];   // V (transposed pairs): [token half][dim segment]
+};
+
+// Copies one 16-token tile from the ring into registers.
+__device__ __forceinline__ void load_tile(uint32_t kt, uint32_t vt, const TileOffsets &off, TileFrags &f)
+{
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        ldsm_x4(kt + off.ld[q], f.kf[0][2 * q], f.kf[1][2 * q], f.kf[0][2 * q + 1], f.kf[1][2 * q + 1]);
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+        ldsm_x4_trans(vt + off.ld[q], f.vf[0][2 * q], f.vf[1][2 * q], f.vf[0][2 * q + 1], f.vf[1][2 * q + 1]);
+}
+
 template <bool kPartial>
-__device__ __forceinline__ void process_tile(uint32_t kt, uint32_t vt, int nv, const TileOffsets &off,
-                                             const uint32_t (&qa)[8][2], float scale2, float &m_ref, float &lsum,
-                                             float (&acc)[8][4], int lane)
+__device__ __forceinline__ void process_tile(TileFrags &fr, int nv, const uint32_t (&qa)[8][2], float scale2,
+                                             float &m_ref, float &lsum, float (&acc)[8][4], int lane)
 {
     const int t4 = lane & 3;
+    uint32_t (&kf)[2][8] = fr.kf;
+    uint32_t (&vf)[2][8] = fr.vf;
 
-    uint32_t kf[2][8];   // [token half j][dim segment]
-    uint32_t vf[2][8];
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        ldsm_x4(kt + off.ld[q], kf[0][2 * q], kf[1][2 * q], kf[0][2 * q + 1], kf[1][2 * q + 1]);
-#pragma unroll
-    for (int q = 0; q < 4; ++q)
-        ldsm_x4_trans(vt + off.ld[q], vf[0][2 * q], vf[1][2 * q], vf[0][2 * q + 1], vf[1][2 * q + 1]);
-
-    // S = Q K^T.  Thread (gid, t4) gets S[head gid][tokens 8j + 2t4, 8j + 2t4 + 1].
-    float sc[2][4];
+    // S = Q K^T.  Thread (gid, t4) gets S[head gid][tokens 8j + 2t4, 8j + 2t4 + 1];
+    // even and odd k-steps accumulate separately and are added at the end.
+    float sc[2][2][4];
 #pragma unroll
     for (int j = 0; j < 2; ++j)
 #pragma unroll
-        for (int c = 0; c < 4; ++c)
-            sc[j][c] = 0.f;
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                sc[j][h][c] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk)
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
             uint32_t b0, b1;
             e4m3x4_to_f16x4(kf[j][kk], b0, b1);
-            mma_16816(sc[j], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+            mma_16816(sc[j][kk & 1], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
         }
 
-    float y[4] = {sc[0][0] * scale2, sc[0][1] * scale2, sc[1][0] * scale2, sc[1][1] * scale2};
+    float y[4] = {(sc[0][0][0] + sc[0][1][0]) * scale2, (sc[0][0][1] + sc[0][1][1]) * scale2,
+                  (sc[1][0][0] + sc[1][1][0]) * scale2, (sc[1][0][1] + sc[1][1][1]) * scale2};
     if (kPartial) {
         if (2 * t4 >= nv) y[0] = -INFINITY;
         if (2 * t4 + 1 >= nv) y[1] = -INFINITY;
         if (8 + 2 * t4 >= nv) y[2] = -INFINITY;
         if (9 + 2 * t4 >= nv) y[3] = -INFINITY;
     }
-    float tmax = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
-    tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 1));
-    tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 2));
-    if (__any_sync(kFull, tmax > m_ref + kRescaleThreshold)) {
+    // Lazy rescale: the running reference m_ref (shared by the 4 lanes of a
+    // head) moves only when some score exceeds it by more than 2^8, so the
+    // common path needs no cross-lane max.
+    const float lmax = fmaxf(fmaxf(y[0], y[1]), fmaxf(y[2], y[3]));
+    if (__any_sync(kFull, lmax > m_ref + kRescaleThreshold)) {
+        float tmax = fmaxf(lmax, __shfl_xor_sync(kFull, lmax, 1));
+        tmax = fmaxf(tmax, __shfl_xor_sync(kFull, tmax, 2));
         const float m_new = fmaxf(m_ref, tmax);
         const float alpha = ex2_approx(m_ref - m_new);
         lsum *= alpha;
@@ -355,12 +373,19 @@ __device__ __forceinline__ void process_tile(uint32_t kt, uint32_t vt, int nv, c
     }
     // O^T[d][g] += V^T[d][t] P^T[t][g]; dims of m-tile sg: rows gid -> 16sg+2gid, gid+8 -> 16sg+2gid+1.
 #pragma unroll
-    for (int sg = 0; sg < 8; ++sg) {
-        uint32_t a0, a1, a2, a3;
-        e4m3x4_to_f16x4(__byte_perm(vf[0][sg], 0, 0x3120), a0, a1);
-        e4m3x4_to_f16x4(__byte_perm(vf[1][sg], 0, 0x3120), a2, a3);
-        mma_16816(acc[sg], a0, a1, a2, a3, h01, h23);
-        mma_16816(acc[sg], a0, a1, a2, a3, l01, l23);
+    for (int g4 = 0; g4 < 8; g4 += 4) {
+        uint32_t va[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            e4m3x4_to_f16x4(__byte_perm(vf[0][g4 + i], 0, 0x3120), va[i][0], va[i][1]);
+            e4m3x4_to_f16x4(__byte_perm(vf[1][g4 + i], 0, 0x3120), va[i][2], va[i][3]);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            mma_16816(acc[g4 + i], va[i][0], va[i][1], va[i][2], va[i][3], h01, h23);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            mma_16816(acc[g4 + i], va[i][0], va[i][1], va[i][2], va[i][3], l01, l23);
     }
 }
 
@@ -526,23 +551,31 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 st = 0;
                 ph ^= 1u;
             }
-            if (wait_warp(bars + 8 * s, par, abort_flag, a.err, lane)) {
-                const uint32_t kt = ring + s * S::kStageBytes;
+            const bool ready = wait_warp(bars + 8 * s, par, abort_flag, a.err, lane);
+            const uint32_t kt = ring + s * S::kStageBytes;
+            // Copy the page into registers, then hand the stage straight back
+            // to the TMA unit so every stage stays in flight during the math.
+            TileFrags fr[P / 16];
+            if (ready) {
+#pragma unroll
+                for (int sub = 0; sub < P / 16; ++sub)
+                    load_tile(kt + sub * 16 * kHeadDim, kt + S::kTile + sub * 16 * kHeadDim, off, fr[sub]);
+            }
+            if (k + kStages < n_total) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                issue(k + kStages);
+            }
+            if (ready) {
 #pragma unroll
                 for (int sub = 0; sub < P / 16; ++sub) {
                     const int nvs = nv - sub * 16;
-                    const uint32_t kts = kt + sub * 16 * kHeadDim, vts = kts + S::kTile;
                     if (nvs >= 16)
-                        process_tile<false>(kts, vts, 16, off, qa, scale2, m_ref, lsum, acc, lane);
+                        process_tile<false>(fr[sub], 16, qa, scale2, m_ref, lsum, acc, lane);
                     else if (nvs > 0)
-                        process_tile<true>(kts, vts, nvs, off, qa, scale2, m_ref, lsum, acc, lane);
+                        process_tile<true>(fr[sub], nvs, qa, scale2, m_ref, lsum, acc, lane);
                 }
             }
-            // Stage s is free again: order this warp's reads before the async-proxy refill.
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            if (k + kStages < n_total)
-                issue(k + kStages);
         }
 
         // ---- end of piece
