@@ -28,8 +28,8 @@
  * Ownership: the caller owns every buffer (caches, tables, outputs, the
  * decode workspace).  The library allocates no device memory, keeps no state
  * between calls beyond a per-device cache of device properties, the driver
- * entry point it uses to describe tensors for the TMA unit and a process-wide
- * call counter, and never synchronises the stream.  Calls are asynchronous on `stream`; the status
+ * entry point it uses to describe tensors for the TMA unit, and never
+ * synchronises the stream.  Calls are asynchronous on `stream`; the status
  * reports argument errors found on the host and launch errors only.
  *
  * Device-side error word: kernels OR bits into *device_error (int32, device
@@ -134,10 +134,11 @@ size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
  *     w_t = softmax_t(s_t)                              for t < L
  *     out[b][i][d] = sum_t w_t * E4M3(v_cache[pg(t)][h][t % P][d]) * v_scale[h]
  * where pg(t) = block_table[b][t / P].  L == 0 gives a zero row.  Long
- * contexts are split across CTAs (split-K / flash-decoding); the CTA that
- * finishes a sequence's last piece merges the partial softmax states exactly
- * (log-sum-exp) in a fixed order: results are deterministic run to run and
- * independent of where the pages sit in the pool.  One kernel launch.
+ * contexts are split across warps (split-K / flash-decoding) and a second
+ * kernel merges the partial softmax states exactly (log-sum-exp) in a fixed
+ * order: results are deterministic run to run and independent of where the
+ * pages sit in the pool.  Two kernel launches (the second is a programmatic
+ * dependent launch that overlaps the first one's tail).
  *
  *   q              device bf16 [batch][num_q_heads][head_dim] (|q| < 65504).
  *   k_cache, v_cache device uint8 pools (layout above), 16-byte aligned.
@@ -151,10 +152,10 @@ size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
  *   out            device [batch][num_q_heads][head_dim], out_dtype
  *                  PKV_BF16 (bf16, RNE of the fp32 result) or PKV_F32.
  *   workspace      device, >= pkv_decode_workspace_size(...) bytes, 256-byte
- *                  aligned: per-(sequence, kv head) arrival counters, then the
- *                  partial states.  Contents need no initialisation (the
- *                  counters are tagged with a per-call epoch); one workspace
- *                  must not be shared by calls that overlap on the GPU.
+ *                  aligned: per-(sequence, kv head) piece ranges, then the
+ *                  partial states.  Contents need no initialisation; one
+ *                  workspace must not be shared by calls that overlap on the
+ *                  GPU.
  *   device_error   device int32 or NULL (bits above).
  *   max_ctas       0 = one persistent CTA per resident slot on the device;
  *                  > 0 caps the CTA count (changes the split, not the math).

@@ -2,7 +2,6 @@
 // page pools, grid sizing and launches.  Nothing here allocates device memory.
 #include <math.h>
 
-#include <atomic>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -154,21 +153,7 @@ size_t workspace_bytes_for(int batch, int hq, int hkv, int num_ctas)
 {
     const size_t slots = static_cast<size_t>(num_ctas) * kWarps + static_cast<size_t>(batch) * hkv;
     const size_t bytes = slots * static_cast<size_t>(hq / hkv) * kPartialStride * sizeof(float);
-    return decode_counter_bytes(batch, hkv) + ((bytes + 255) & ~size_t(255));
-}
-
-// Process-wide call counter: each decode call tags its split-K arrival
-// counters with a fresh 40-bit epoch, so stale counts from earlier calls (or
-// a workspace never cleared) are recognised and restarted.
-std::atomic<unsigned long long> g_epoch{0};
-
-unsigned long long next_epoch()
-{
-    for (;;) {
-        const unsigned long long e = (g_epoch.fetch_add(1) + 1) & ((1ull << 40) - 1);
-        if (e != 0)
-            return e;
-    }
+    return decode_segment_bytes(batch, hkv) + ((bytes + 255) & ~size_t(255));
 }
 
 }  // namespace
@@ -295,9 +280,8 @@ pkv_status pkv_paged_gqa_decode(const void *q, const uint8_t *k_cache, const uin
     a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
     a.out = out;
     a.out_f32 = out_dtype == PKV_F32;
-    a.counters = static_cast<unsigned long long *>(workspace);
-    a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + decode_counter_bytes(batch, num_kv_heads));
-    a.epoch = next_epoch();
+    a.seg_pieces = static_cast<int2 *>(workspace);
+    a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + decode_segment_bytes(batch, num_kv_heads));
     a.err = device_error;
     a.num_ctas = ctas;
     return launch_paged_decode(a, tm_k, tm_v, page_size, stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;

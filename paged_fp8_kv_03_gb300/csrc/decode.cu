@@ -17,10 +17,10 @@
 // flash-decoding with exact balance).  A worker's range cuts segments into
 // pieces; a piece covering a whole segment writes the final output, the
 // others write a partial softmax state (running max m, sum l, unnormalised
-// accumulator) into workspace slot (worker + segment) and bump the segment's
-// arrival counter; the worker that brings the count to the number of pieces
-// merges them, in worker order (deterministic), and writes the output.
-// Counters carry a per-call epoch so they never need clearing.
+// accumulator) into workspace slot (worker + segment).  A second kernel, one
+// CTA per (segment, head) with a thread per dimension, merges the pieces in
+// worker order (deterministic); it is a programmatic dependent launch, so it
+// is already resident when the first kernel's last warps finish.
 //
 // Inside a worker (one warp): lane 0 issues two TMA tensor loads per page
 // (K tile, V tile; 128-byte swizzled, evict-first in L2) into the warp's own
@@ -116,21 +116,6 @@ __device__ __forceinline__ bool worker_has_range(int w, int64_t total, int worke
     return static_cast<int64_t>(w) * total / workers != static_cast<int64_t>(w + 1) * total / workers;
 }
 
-// Counts one more finished piece of a segment for this call's epoch; true for
-// the piece that completes the segment.  Lock-free: every failed CAS means
-// another piece succeeded.
-__device__ __forceinline__ bool arrive_last(unsigned long long *cnt, unsigned long long epoch, unsigned n)
-{
-    unsigned long long old = __ldcg(cnt);
-    for (;;) {
-        const unsigned long long nv = ((old >> 24) == epoch) ? old + 1 : ((epoch << 24) | 1ull);
-        const unsigned long long prev = atomicCAS(cnt, old, nv);
-        if (prev == old)
-            return (nv & 0xFFFFFFull) == n;
-        old = prev;
-    }
-}
-
 template <int P>
 struct Smem {
     static constexpr int kTile = P * kHeadDim;              // bytes of one K (or V) tile
@@ -211,48 +196,6 @@ __device__ __forceinline__ void store_pair(const DecodeArgs &a, int64_t row, int
     else
         *reinterpret_cast<__nv_bfloat162 *>(static_cast<__nv_bfloat16 *>(a.out) + row * kHeadDim + d) =
             __floats2bfloat162_rn(v0, v1);
-}
-
-// Merges the partial states of one segment written by workers w0..w1 (in
-// worker order) and writes its G output rows.  One warp; lanes split the
-// pieces for the max and the sum, then the 128 dims.
-__device__ __noinline__ void merge_pieces(const DecodeArgs &a, int seg, int w0, int w1, bool dense, int64_t total,
-                                          int workers, int64_t row0, float vsc, int lane)
-{
-    for (int g = 0; g < a.group; ++g) {
-        auto slot = [&](int w) {
-            return a.partials + (static_cast<int64_t>(w + seg) * a.group + g) * kPartialStride;
-        };
-        float mloc = -INFINITY;
-        for (int w = w0 + lane; w <= w1; w += 32)
-            if (dense || worker_has_range(w, total, workers))
-                mloc = fmaxf(mloc, __ldcg(slot(w) + kHeadDim));
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, o));
-        const float M = mloc;
-        float lloc = 0.f;
-        for (int w = w0 + lane; w <= w1; w += 32)
-            if (dense || worker_has_range(w, total, workers))
-                lloc += __ldcg(slot(w) + kHeadDim + 1) * ex2_approx(__ldcg(slot(w) + kHeadDim) - M);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            lloc += __shfl_xor_sync(kFull, lloc, o);
-        const float inv = vsc / lloc;
-        float A[4] = {0.f, 0.f, 0.f, 0.f};
-        for (int w = w0; w <= w1; ++w) {
-            if (!dense && !worker_has_range(w, total, workers))
-                continue;
-            const float *sl = slot(w);
-            const float f = ex2_approx(__ldcg(sl + kHeadDim) - M);
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                A[j] += __ldcg(sl + lane + 32 * j) * f;
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            store_out(a, row0 + g, lane + 32 * j, A[j] * inv);
-    }
 }
 
 // Per-lane byte offsets of the ldmatrix rows inside a 16-token tile (128-byte
@@ -458,6 +401,26 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int workers = a.num_ctas * kWarps;
     const int worker = blockIdx.x * kWarps + warp;
     const int64_t total = static_cast<int64_t>(pstart[a.batch]) * a.hkv;
+
+    // Piece table for the merge kernel: first and last worker of every
+    // segment that more than one worker touches (-1: nothing to merge).
+    if (blockIdx.x == 0) {
+        for (int sg = tid; sg < a.batch * a.hkv; sg += kThreads) {
+            const int b = sg / a.hkv, h = sg % a.hkv, np = pages_of(pstart, b);
+            int2 r = make_int2(-1, -1);
+            if (np > 0) {
+                const int64_t start = static_cast<int64_t>(pstart[b]) * a.hkv + static_cast<int64_t>(h) * np;
+                const int w0 = worker_of(start, total, workers), w1 = worker_of(start + np - 1, total, workers);
+                if (w0 != w1)
+                    r = make_int2(w0, w1);
+            }
+            a.seg_pieces[sg] = r;
+        }
+        if (tid == 0)
+            a.seg_pieces[a.batch * a.hkv] = make_int2(static_cast<int>(total & 0x7FFFFFFF), static_cast<int>(total >> 31));
+    }
+    // Let the merge kernel get scheduled now; it waits for this grid to finish.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int64_t lo = static_cast<int64_t>(worker) * total / workers;
     const int64_t hi = static_cast<int64_t>(worker + 1) * total / workers;
     if (lo >= hi)
@@ -610,27 +573,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 slot[gid * kPartialStride + kHeadDim] = m_ref;
                 slot[gid * kPartialStride + kHeadDim + 1] = lsum;
             }
-            // The worker completing the segment's last piece merges all of them.
-            __threadfence();
-            __syncwarp();
-            const int64_t start = static_cast<int64_t>(pstart[cons.b]) * a.hkv + static_cast<int64_t>(cons.h) * np;
-            const int w0 = worker_of(start, total, workers);
-            const int w1 = worker_of(start + np - 1, total, workers);
-            const bool dense = total >= workers;          // then every worker range is non-empty
-            int last = 0;
-            if (lane == 0) {
-                unsigned n = 0;
-                if (dense)
-                    n = static_cast<unsigned>(w1 - w0 + 1);
-                else
-                    for (int w = w0; w <= w1; ++w)
-                        n += worker_has_range(w, total, workers) ? 1u : 0u;
-                last = arrive_last(a.counters + seg, a.epoch, n) ? 1 : 0;
-            }
-            if (__shfl_sync(kFull, last, 0)) {
-                __threadfence();
-                merge_pieces(a, seg, w0, w1, dense, total, workers, row0, vsc, lane);
-            }
         }
         cons = advance(pstart, a.batch, a.hkv, cons, n_piece);
     }
@@ -641,6 +583,78 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         for (int f = max(0, issued_hi - kStages); f < issued_hi; ++f)
             wait_thread(bars + 8 * (f % kStages), static_cast<uint32_t>(f / kStages) & 1u, abort_flag, a.err, false);
     }
+}
+
+constexpr int kMergeThreads = kHeadDim;   // one thread per dimension
+
+// One CTA per (segment, head g): merges the partial states that workers
+// w0..w1 wrote for that head, in worker order, and writes the output row.
+__global__ void __launch_bounds__(kMergeThreads) splitk_merge_kernel(const DecodeArgs a)
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid has finished
+    const int seg = blockIdx.x, g = blockIdx.y, d = threadIdx.x;
+    const int2 r = a.seg_pieces[seg];
+    if (r.x < 0)
+        return;
+    const int2 tw = a.seg_pieces[a.batch * a.hkv];
+    const int64_t total = static_cast<int64_t>(tw.x) | (static_cast<int64_t>(tw.y) << 31);
+    const int workers = a.num_ctas * kWarps;
+    const bool dense = total >= workers;          // then every worker range is non-empty
+    const int b = seg / a.hkv, h = seg % a.hkv;
+    const int lane = d & 31, warp = d >> 5;
+    __shared__ float f_sh[kMergeThreads];
+    __shared__ float red[kMergeThreads / 32];
+    auto slot = [&](int w) { return a.partials + (static_cast<int64_t>(w + seg) * a.group + g) * kPartialStride; };
+    auto valid = [&](int w) { return dense || worker_has_range(w, total, workers); };
+
+    float mloc = -INFINITY;
+    for (int w = r.x + d; w <= r.y; w += kMergeThreads)
+        if (valid(w))
+            mloc = fmaxf(mloc, slot(w)[kHeadDim]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, o));
+    if (lane == 0)
+        red[warp] = mloc;
+    __syncthreads();
+    float M = red[0];
+#pragma unroll
+    for (int w = 1; w < kMergeThreads / 32; ++w)
+        M = fmaxf(M, red[w]);
+    __syncthreads();
+
+    float L = 0.f, A = 0.f;
+    for (int c0 = r.x; c0 <= r.y; c0 += kMergeThreads) {
+        const int n = min(kMergeThreads, r.y - c0 + 1);
+        float f = 0.f, lw = 0.f;
+        if (d < n && valid(c0 + d)) {
+            const float *sl = slot(c0 + d);
+            f = ex2_approx(sl[kHeadDim] - M);
+            lw = sl[kHeadDim + 1] * f;
+        }
+        f_sh[d] = f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            lw += __shfl_xor_sync(kFull, lw, o);
+        if (lane == 0)
+            red[warp] = lw;
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < kMergeThreads / 32; ++w)
+            L += red[w];
+        if (dense) {
+#pragma unroll 8
+            for (int i = 0; i < n; ++i)
+                A += slot(c0 + i)[d] * f_sh[i];
+        } else {
+            for (int i = 0; i < n; ++i)             // workers with empty ranges wrote nothing: skip them
+                if (valid(c0 + i))
+                    A += slot(c0 + i)[d] * f_sh[i];
+        }
+        __syncthreads();
+    }
+    const float vsc = __ldg(a.v_scale + h);
+    store_out(a, static_cast<int64_t>(b) * a.hq + static_cast<int64_t>(h) * a.group + g, d, A * (vsc / L));
 }
 
 template <int P>
@@ -665,13 +679,24 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, co
                                 int page_size, cudaStream_t stream)
 {
     const size_t smem = decode_smem_bytes(page_size, a.batch);
-    {
-        if (page_size == 32)
-            paged_gqa_decode_kernel<32><<<a.num_ctas, kThreads, smem, stream>>>(tm_k, tm_v, a);
-        else
-            paged_gqa_decode_kernel<16><<<a.num_ctas, kThreads, smem, stream>>>(tm_k, tm_v, a);
-    }
-    return cudaGetLastError();
+    if (page_size == 32)
+        paged_gqa_decode_kernel<32><<<a.num_ctas, kThreads, smem, stream>>>(tm_k, tm_v, a);
+    else
+        paged_gqa_decode_kernel<16><<<a.num_ctas, kThreads, smem, stream>>>(tm_k, tm_v, a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(a.batch * a.hkv), static_cast<unsigned>(a.group), 1);
+    cfg.blockDim = dim3(kMergeThreads, 1, 1);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitk_merge_kernel, a);
 }
 
 }  // namespace pkv

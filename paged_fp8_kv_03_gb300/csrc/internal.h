@@ -42,17 +42,18 @@ struct DecodeArgs {
     float sm_scale_log2;        // sm_scale * log2(e): scores live in the exp2 domain
     void *out;
     int out_f32;
-    unsigned long long *counters;   // [batch * hkv] arrival counters: (epoch << 24) | pieces seen
+    int2 *seg_pieces;               // [batch * hkv + 1] first/last worker of each segment (-1: nothing
+                                    // to merge), then the list length split in two 31-bit halves
     float *partials;                // [num_ctas * kWarps + batch * hkv][group][kPartialStride]
-    unsigned long long epoch;       // unique per call (40 bits), so counters never need clearing
     int32_t *err;
     int num_ctas;
 };
 
-// Workspace = counters (rounded to 256 bytes) followed by the partial slots.
-inline size_t decode_counter_bytes(int batch, int hkv)
+// Workspace = per-segment piece ranges + the list length (rounded to 256
+// bytes), then the partial slots.
+inline size_t decode_segment_bytes(int batch, int hkv)
 {
-    return (static_cast<size_t>(batch) * hkv * sizeof(unsigned long long) + 255) & ~size_t(255);
+    return ((static_cast<size_t>(batch) * hkv + 1) * sizeof(int2) + 255) & ~size_t(255);
 }
 
 // Host helpers (api.cu).

@@ -17,9 +17,8 @@
 //   * all calls share it: two calls that overlap on the GPU (different streams,
 //     or different host threads without ordering) race on it and give wrong
 //     results.  Calls on one stream are ordered and safe.
-//   * it keeps the last call's contents; the decode writes every partial slot
-//     before reading it and tags its arrival counters with a per-call epoch,
-//     so nothing needs clearing between calls;
+//   * it keeps the last call's contents; the decode writes every value it
+//     later reads, so nothing needs clearing between calls;
 //   * sizes whose scratch would exceed the array are rejected with
 //     PKV_ERR_WORKSPACE.
 //
