@@ -111,11 +111,6 @@ __device__ __forceinline__ int worker_of(int64_t x, int64_t total, int workers)
     return static_cast<int>(((x + 1) * workers - 1) / total);
 }
 
-__device__ __forceinline__ bool worker_has_range(int w, int64_t total, int workers)
-{
-    return static_cast<int64_t>(w) * total / workers != static_cast<int64_t>(w + 1) * total / workers;
-}
-
 template <int P>
 struct Smem {
     static constexpr int kTile = P * kHeadDim;              // bytes of one K (or V) tile
@@ -587,8 +582,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
 constexpr int kMergeThreads = kHeadDim;   // one thread per dimension
 
-// One CTA per (segment, head g): merges the partial states that workers
-// w0..w1 wrote for that head, in worker order, and writes the output row.
+// One CTA per (segment, head g): merges the partial states that the workers
+// covering the segment wrote for that head, in worker order, and writes the
+// output row.  When the list has at least as many page-heads as workers, the
+// pieces come from the contiguous workers w0..w1; otherwise every worker owns
+// at most one page-head and piece i comes from the worker owning position
+// x0 + i.
 __global__ void __launch_bounds__(kMergeThreads) splitk_merge_kernel(const DecodeArgs a)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid has finished
@@ -599,18 +598,21 @@ __global__ void __launch_bounds__(kMergeThreads) splitk_merge_kernel(const Decod
     const int2 tw = a.seg_pieces[a.batch * a.hkv];
     const int64_t total = static_cast<int64_t>(tw.x) | (static_cast<int64_t>(tw.y) << 31);
     const int workers = a.num_ctas * kWarps;
-    const bool dense = total >= workers;          // then every worker range is non-empty
+    const bool dense = total >= workers;
+    const int64_t x0 = dense ? 0 : static_cast<int64_t>(r.x) * total / workers;
+    const int n_pieces = dense ? r.y - r.x + 1
+                               : static_cast<int>(static_cast<int64_t>(r.y) * total / workers - x0 + 1);
     const int b = seg / a.hkv, h = seg % a.hkv;
     const int lane = d & 31, warp = d >> 5;
     __shared__ float f_sh[kMergeThreads];
+    __shared__ int w_sh[kMergeThreads];
     __shared__ float red[kMergeThreads / 32];
+    auto piece_worker = [&](int i) { return dense ? r.x + i : worker_of(x0 + i, total, workers); };
     auto slot = [&](int w) { return a.partials + (static_cast<int64_t>(w + seg) * a.group + g) * kPartialStride; };
-    auto valid = [&](int w) { return dense || worker_has_range(w, total, workers); };
 
     float mloc = -INFINITY;
-    for (int w = r.x + d; w <= r.y; w += kMergeThreads)
-        if (valid(w))
-            mloc = fmaxf(mloc, slot(w)[kHeadDim]);
+    for (int i = d; i < n_pieces; i += kMergeThreads)
+        mloc = fmaxf(mloc, slot(piece_worker(i))[kHeadDim]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
         mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, o));
@@ -624,15 +626,18 @@ __global__ void __launch_bounds__(kMergeThreads) splitk_merge_kernel(const Decod
     __syncthreads();
 
     float L = 0.f, A = 0.f;
-    for (int c0 = r.x; c0 <= r.y; c0 += kMergeThreads) {
-        const int n = min(kMergeThreads, r.y - c0 + 1);
+    for (int c0 = 0; c0 < n_pieces; c0 += kMergeThreads) {
+        const int n = min(kMergeThreads, n_pieces - c0);
         float f = 0.f, lw = 0.f;
-        if (d < n && valid(c0 + d)) {
-            const float *sl = slot(c0 + d);
+        int wk = 0;
+        if (d < n) {
+            wk = piece_worker(c0 + d);
+            const float *sl = slot(wk);
             f = ex2_approx(sl[kHeadDim] - M);
             lw = sl[kHeadDim + 1] * f;
         }
         f_sh[d] = f;
+        w_sh[d] = wk;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
             lw += __shfl_xor_sync(kFull, lw, o);
@@ -642,15 +647,9 @@ __global__ void __launch_bounds__(kMergeThreads) splitk_merge_kernel(const Decod
 #pragma unroll
         for (int w = 0; w < kMergeThreads / 32; ++w)
             L += red[w];
-        if (dense) {
 #pragma unroll 8
-            for (int i = 0; i < n; ++i)
-                A += slot(c0 + i)[d] * f_sh[i];
-        } else {
-            for (int i = 0; i < n; ++i)             // workers with empty ranges wrote nothing: skip them
-                if (valid(c0 + i))
-                    A += slot(c0 + i)[d] * f_sh[i];
-        }
+        for (int i = 0; i < n; ++i)
+            A += slot(w_sh[i])[d] * f_sh[i];
         __syncthreads();
     }
     const float vsc = __ldg(a.v_scale + h);
