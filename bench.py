@@ -1,8 +1,10 @@
 """Decode-step benchmark for the paged FP8-KV GQA path.
 
-One step = kv_append_fp8 of the step's new tokens (1 per sequence where the
-workload appends) + paged_gqa_decode over every cached token, on one batch of
-synthetic Llama-3-shaped inputs already resident in HBM.  Prints ONE JSON line
+One step = the step's new tokens appended to the FP8 cache (1 per sequence
+where the workload appends) + decode attention over every cached token, on
+one batch of synthetic Llama-3-shaped inputs already resident in HBM: by
+default one append_decode_fp8 call (append fused into the decode launch),
+with --separate kv_append_fp8 followed by paged_gqa_decode.  Prints ONE JSON line
 (rank 0):
 
   value      effective HBM GB/s of the decode step: algorithmic KV bytes
@@ -142,11 +144,12 @@ def _fill_layer(pkv, wl, layer, dev):
 
 
 def _step_inputs(wl, layer, dev):
-    """The per-step inputs: new K/V rows of the appended tokens, their slots, q."""
+    """The per-step inputs: new K/V rows of the appended tokens [B, A, Hkv, D],
+    their slots (for the two-call path), q."""
     A = wl.append
     if A:
-        k_new = torch.cat([wl.kv_rows(layer, 0, b, L, L + A, device=dev) for b, L in enumerate(wl.prefill_lens)])
-        v_new = torch.cat([wl.kv_rows(layer, 1, b, L, L + A, device=dev) for b, L in enumerate(wl.prefill_lens)])
+        k_new = torch.stack([wl.kv_rows(layer, 0, b, L, L + A, device=dev) for b, L in enumerate(wl.prefill_lens)])
+        v_new = torch.stack([wl.kv_rows(layer, 1, b, L, L + A, device=dev) for b, L in enumerate(wl.prefill_lens)])
         slots = torch.cat([wl.slots(b, L, L + A) for b, L in enumerate(wl.prefill_lens)]).to(dev)
     else:
         k_new = v_new = slots = None
@@ -187,12 +190,17 @@ def run_gpu(args, rank, world):
             g = i * per_step + l
             c = layers[g % n_layers]
             s = steps_in[g % n_layers]
-            if s["k_new"] is not None:
-                pkv.pkv_kv_append_fp8(s["k_new"], s["v_new"], s["slots"], c["ks"], c["vs"], c["kc"], c["vc"], err)
+            if s["k_new"] is not None and args.separate:
+                pkv.pkv_kv_append_fp8(s["k_new"].flatten(0, 1), s["v_new"].flatten(0, 1), s["slots"], c["ks"], c["vs"],
+                                      c["kc"], c["vc"], err)
             if evs is not None:
                 evs[l][0].record(stream)
-            pkv.pkv_paged_gqa_decode(s["q"], c["kc"], c["vc"], c["ks"], c["vs"], bt, lens, out, ws,
-                                     device_error=err)
+            if s["k_new"] is not None and not args.separate:
+                pkv.pkv_append_decode_fp8(s["k_new"], s["v_new"], s["q"], c["kc"], c["vc"], c["ks"], c["vs"], bt, lens,
+                                          out, ws, device_error=err)
+            else:
+                pkv.pkv_paged_gqa_decode(s["q"], c["kc"], c["vc"], c["ks"], c["vs"], bt, lens, out, ws,
+                                         device_error=err)
             if evs is not None:
                 evs[l][1].record(stream)
 
@@ -245,9 +253,14 @@ def run_gpu(args, rank, world):
             c = layers[g % n_layers]
             h = host[g % n_layers]
             d = {k: v.to(dev, non_blocking=True) for k, v in h.items()}
-            if "k_new" in d:
-                pkv.kv_append_fp8(d["k_new"], d["v_new"], d["slots"], c["ks"], c["vs"], c["kc"], c["vc"])
-            o = pkv.paged_gqa_decode(d["q"], c["kc"], c["vc"], c["ks"], c["vs"], d["bt"], d["lens"], workspace=ws)
+            if "k_new" in d and args.separate:
+                pkv.kv_append_fp8(d["k_new"].flatten(0, 1), d["v_new"].flatten(0, 1), d["slots"], c["ks"], c["vs"],
+                                  c["kc"], c["vc"])
+            if "k_new" in d and not args.separate:
+                o = pkv.append_decode_fp8(d["k_new"], d["v_new"], d["q"], c["kc"], c["vc"], c["ks"], c["vs"], d["bt"],
+                                          d["lens"], workspace=ws)
+            else:
+                o = pkv.paged_gqa_decode(d["q"], c["kc"], c["vc"], c["ks"], c["vs"], d["bt"], d["lens"], workspace=ws)
             out_host.copy_(o, non_blocking=True)
 
     for i in range(3):
@@ -273,7 +286,7 @@ def run_gpu(args, rank, world):
     dec_ms = statistics.mean(decode_ms)
     achieved = kv_bytes / (dec_ms * 1e-3) / 1e9
     traffic = _traffic(wl.name)
-    launches_per_step = per_step * ((1 if wl.append else 0) + 2)
+    launches_per_step = per_step * ((1 if (wl.append and args.separate) else 0) + 2)
     line = {
         "metric": METRIC,
         "value": round(value, 2),
@@ -295,7 +308,9 @@ def run_gpu(args, rank, world):
                    "l2": "inputs larger than L2: each layer cache exceeds the 129 MB L2 and "
                          f"{n_layers} distinct caches rotate layer pass by layer pass",
                    "parallelism": f"replicas x{world}"},
-        "roofline": {"bound": "hbm", "kernel": "paged_gqa_decode (partial + split-K combine)",
+        "path": ("kv_append_fp8 + paged_gqa_decode (two calls)" if (wl.append and args.separate) else
+                 "append_decode_fp8 (append fused into the decode launch)" if wl.append else "paged_gqa_decode"),
+        "roofline": {"bound": "hbm", "kernel": "decode call: paged_gqa_decode_kernel + splitk_merge_kernel",
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes,
@@ -414,6 +429,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--separate", action="store_true",
+                    help="time kv_append_fp8 and paged_gqa_decode as two calls instead of the fused step")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))

@@ -172,6 +172,40 @@ pkv_status pkv_paged_gqa_decode(const void *q,
                                 int32_t *device_error, int max_ctas, cudaStream_t stream);
 
 /*
+ * append_decode_fp8 -- one whole decode step in one call: the kv_append_fp8
+ * of the step's new tokens fused into paged_gqa_decode ([G] §3.2: new K/V are
+ * quantised with the layer's scale as they are produced; [N] §3.2 decode).
+ *
+ * For every sequence b with L = seq_lens[b] (the length AFTER this step's
+ * tokens) and j < n_new, token position t = L - n_new + j:
+ *     k_cache[pg(t)][h][t % P][d] = E4M3(k_new[b][j][h][d] / k_scale[h])
+ * (same for V, same rounding as pkv_kv_append_fp8), then exactly the
+ * attention of pkv_paged_gqa_decode over t < L.  Page bytes and outputs are
+ * bit-identical to calling pkv_kv_append_fp8 with slot = pg(t) * P + t % P
+ * followed by pkv_paged_gqa_decode.  Each new token is written by the warp
+ * that later reads its page, so no extra launch or grid-wide ordering is
+ * needed.
+ *
+ *   k_new, v_new   device [batch][n_new][num_kv_heads][head_dim], in_dtype
+ *                  PKV_F32 or PKV_BF16, 16-byte aligned (unused if n_new == 0).
+ *   n_new          tokens appended per sequence (>= 0); seq_lens[b] < n_new
+ *                  drops the missing positions and sets PKV_DEVERR_SEQLEN.
+ *   The pages receiving new tokens must not be shared with another sequence
+ *   of the same call (prefix-shared pages are read-only).
+ *   Everything else as in pkv_paged_gqa_decode (the caches are written).
+ */
+pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dtype, int n_new,
+                                 const void *q, uint8_t *k_cache, uint8_t *v_cache,
+                                 const float *k_scale, const float *v_scale,
+                                 const int32_t *block_table, int max_pages_per_seq,
+                                 const int32_t *seq_lens,
+                                 int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                 int page_size, int64_t num_pages, float sm_scale,
+                                 void *out, int out_dtype,
+                                 void *workspace, size_t workspace_bytes,
+                                 int32_t *device_error, int max_ctas, cudaStream_t stream);
+
+/*
  * paged_gqa_decode without a caller workspace, for callers that cannot
  * allocate device memory (a serving engine that owns every byte of device
  * memory through its own pool, a plugin that must not bypass its host

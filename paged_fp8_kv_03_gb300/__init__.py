@@ -6,6 +6,7 @@ stream.  The entry points mirror the C ABI in ``include/pagedfp8.h``:
 
 * ``pkv_kv_append_fp8``       -- quantise new K/V rows into their pages
 * ``pkv_paged_gqa_decode``    -- grouped-query decode attention over the pages
+* ``pkv_append_decode_fp8``    -- both in one launch (one whole decode step)
 * ``pkv_decode_workspace_size``, ``pkv_status_string``, ``pkv_version``
 
 ``kv_append_fp8`` / ``paged_gqa_decode`` are the same calls with the output
@@ -62,6 +63,9 @@ def load() -> ctypes.CDLL:
         lib.pkv_paged_gqa_decode.restype = i32
         lib.pkv_paged_gqa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64,
                                              f32, vp, i32, vp, sz, vp, i32, vp]
+        lib.pkv_append_decode_fp8.restype = i32
+        lib.pkv_append_decode_fp8.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
+                                              i32, i64, f32, vp, i32, vp, sz, vp, i32, vp]
         lib.pkv_paged_gqa_decode_noalloc.restype = i32
         lib.pkv_paged_gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
                                                      i64, f32, vp, i32, vp, i32, vp]
@@ -180,6 +184,57 @@ def pkv_paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq
         raise PkvError(st, "pkv_paged_gqa_decode")
 
 
+def pkv_append_decode_fp8(k_new, v_new, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out,
+                          workspace, sm_scale=None, device_error=None, max_ctas=0, stream=None) -> None:
+    """One fused decode step: k_new/v_new [B, n_new, Hkv, 128] (fp32|bf16) are
+    quantised into the cache at positions seq_lens[b] - n_new .. seq_lens[b] - 1
+    (seq_lens counts them), then attention as pkv_paged_gqa_decode."""
+    _need(k_new, "k_new", dim=4)
+    _need(v_new, "v_new", dtype=k_new.dtype, dim=4)
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    _need(k_scale, "k_scale", torch.float32, 1)
+    _need(v_scale, "v_scale", torch.float32, 1)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(out, "out", dim=3)
+    _need(workspace, "workspace", torch.uint8)
+    if device_error is not None:
+        _need(device_error, "device_error", torch.int32)
+    B, Hq, D = q.shape
+    NP, Hkv, P, D2 = k_cache.shape
+    Bn, n_new, Hn, Dn = k_new.shape
+    if v_cache.shape != k_cache.shape or D2 != D or out.shape != q.shape:
+        raise ValueError("q / cache / out shapes disagree")
+    if v_new.shape != k_new.shape or Bn != B or Hn != Hkv or Dn != D:
+        raise ValueError("k_new / v_new must be [B, n_new, Hkv, head_dim]")
+    if block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_table / seq_lens shapes disagree with q")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    st = load().pkv_append_decode_fp8(_ptr(k_new), _ptr(v_new), _act_code(k_new), n_new, _ptr(q), _ptr(k_cache),
+                                      _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
+                                      block_table.shape[1], _ptr(seq_lens), B, Hq, Hkv, D, P, NP, float(sm_scale),
+                                      _ptr(out), _act_code(out), _ptr(workspace), workspace.numel(),
+                                      _ptr(device_error), int(max_ctas), _stream(stream))
+    if st != 0:
+        raise PkvError(st, "pkv_append_decode_fp8")
+
+
+def append_decode_fp8(k_new, v_new, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out=None,
+                      out_dtype=torch.bfloat16, workspace=None, sm_scale=None, device_error=None, max_ctas=0,
+                      stream=None) -> torch.Tensor:
+    if out is None:
+        out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    if workspace is None:
+        workspace = decode_workspace(q.shape[0], q.shape[1], k_cache.shape[1], k_cache.shape[2], q.device,
+                                     max_ctas)
+    pkv_append_decode_fp8(k_new, v_new, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out,
+                          workspace, sm_scale, device_error, max_ctas, stream)
+    return out
+
+
 def pkv_paged_gqa_decode_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out,
                                  sm_scale=None, device_error=None, max_ctas=0, stream=None) -> None:
     """pkv_paged_gqa_decode without a workspace, for callers that cannot
@@ -255,7 +310,8 @@ def paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_len
 
 
 __all__ = ["load", "lib_path", "pkv_kv_append_fp8", "pkv_paged_gqa_decode", "pkv_decode_workspace_size",
-           "pkv_paged_gqa_decode_noalloc", "pkv_decode_noalloc_scratch_bytes",
+           "pkv_paged_gqa_decode_noalloc", "pkv_decode_noalloc_scratch_bytes", "pkv_append_decode_fp8",
+           "append_decode_fp8",
            "pkv_status_string", "pkv_version", "kv_append_fp8", "paged_gqa_decode", "decode_workspace",
            "PkvError", "PKV_F32", "PKV_BF16", "DEVERR_SLOT", "DEVERR_PAGE", "DEVERR_SEQLEN",
            "DEVERR_TIMEOUT"]

@@ -156,6 +156,72 @@ size_t workspace_bytes_for(int batch, int hq, int hkv, int num_ctas)
     return decode_segment_bytes(batch, hkv) + ((bytes + 255) & ~size_t(255));
 }
 
+pkv_status decode_impl(const void *k_new, const void *v_new, int in_dtype, int n_new, const void *q, uint8_t *k_cache,
+                       uint8_t *v_cache, const float *k_scale, const float *v_scale, const int32_t *block_table,
+                       int max_pages_per_seq, const int32_t *seq_lens, int batch, int num_q_heads, int num_kv_heads,
+                       int head_dim, int page_size, int64_t num_pages, float sm_scale, void *out, int out_dtype,
+                       void *workspace, size_t workspace_bytes, int32_t *device_error, int max_ctas,
+                       cudaStream_t stream)
+{
+    pkv_status st = check_decode_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_seq,
+                                       num_pages);
+    if (st != PKV_OK)
+        return st;
+    if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
+        return PKV_ERR_DTYPE;
+    if (!(sm_scale == sm_scale) || isinf(sm_scale))
+        return PKV_ERR_SHAPE;
+    if (batch == 0)
+        return PKV_OK;
+    if (!q || !k_cache || !v_cache || !k_scale || !v_scale || !block_table || !seq_lens || !out)
+        return PKV_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4) ||
+        !aligned(device_error, 4))
+        return PKV_ERR_ALIGN;
+    if (!workspace || !aligned(workspace, 256))
+        return PKV_ERR_WORKSPACE;
+
+    const int ctas = decode_num_ctas(page_size, batch, max_ctas);
+    if (ctas <= 0)
+        return PKV_ERR_CUDA;
+    if (workspace_bytes < workspace_bytes_for(batch, num_q_heads, num_kv_heads, ctas))
+        return PKV_ERR_WORKSPACE;
+
+    alignas(64) CUtensorMap tm_k;
+    alignas(64) CUtensorMap tm_v;
+    if (!make_page_map(&tm_k, k_cache, num_pages, num_kv_heads, page_size) ||
+        !make_page_map(&tm_v, v_cache, num_pages, num_kv_heads, page_size))
+        return PKV_ERR_CUDA;
+
+    DecodeArgs a;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.block_table = block_table;
+    a.max_pages = max_pages_per_seq;
+    a.seq_lens = seq_lens;
+    a.batch = batch;
+    a.hq = num_q_heads;
+    a.hkv = num_kv_heads;
+    a.group = num_q_heads / num_kv_heads;
+    a.num_pages = num_pages;
+    a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+    a.out = out;
+    a.out_f32 = out_dtype == PKV_F32;
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.new_bf16 = in_dtype == PKV_BF16;
+    a.n_new = n_new;
+    a.k_pool = k_cache;
+    a.v_pool = v_cache;
+    a.seg_pieces = static_cast<int2 *>(workspace);
+    a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + decode_segment_bytes(batch, num_kv_heads));
+    a.err = device_error;
+    a.num_ctas = ctas;
+    return launch_paged_decode(a, tm_k, tm_v, page_size, stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -234,57 +300,33 @@ pkv_status pkv_paged_gqa_decode(const void *q, const uint8_t *k_cache, const uin
                                 int out_dtype, void *workspace, size_t workspace_bytes, int32_t *device_error,
                                 int max_ctas, cudaStream_t stream)
 {
-    pkv_status st = check_decode_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_seq,
-                                       num_pages);
-    if (st != PKV_OK)
-        return st;
-    if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
-        return PKV_ERR_DTYPE;
-    if (!(sm_scale == sm_scale) || isinf(sm_scale))
+    return decode_impl(nullptr, nullptr, PKV_F32, 0, q, const_cast<uint8_t *>(k_cache), const_cast<uint8_t *>(v_cache),
+                       k_scale, v_scale, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, num_kv_heads,
+                       head_dim, page_size, num_pages, sm_scale, out, out_dtype, workspace, workspace_bytes,
+                       device_error, max_ctas, stream);
+}
+
+pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dtype, int n_new, const void *q,
+                                 uint8_t *k_cache, uint8_t *v_cache, const float *k_scale, const float *v_scale,
+                                 const int32_t *block_table, int max_pages_per_seq, const int32_t *seq_lens,
+                                 int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                                 int64_t num_pages, float sm_scale, void *out, int out_dtype, void *workspace,
+                                 size_t workspace_bytes, int32_t *device_error, int max_ctas, cudaStream_t stream)
+{
+    if (n_new < 0)
         return PKV_ERR_SHAPE;
-    if (batch == 0)
-        return PKV_OK;
-    if (!q || !k_cache || !v_cache || !k_scale || !v_scale || !block_table || !seq_lens || !out)
-        return PKV_ERR_NULL;
-    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
-        !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4) ||
-        !aligned(device_error, 4))
-        return PKV_ERR_ALIGN;
-    if (!workspace || !aligned(workspace, 256))
-        return PKV_ERR_WORKSPACE;
-
-    const int ctas = decode_num_ctas(page_size, batch, max_ctas);
-    if (ctas <= 0)
-        return PKV_ERR_CUDA;
-    if (workspace_bytes < workspace_bytes_for(batch, num_q_heads, num_kv_heads, ctas))
-        return PKV_ERR_WORKSPACE;
-
-    alignas(64) CUtensorMap tm_k;
-    alignas(64) CUtensorMap tm_v;
-    if (!make_page_map(&tm_k, k_cache, num_pages, num_kv_heads, page_size) ||
-        !make_page_map(&tm_v, v_cache, num_pages, num_kv_heads, page_size))
-        return PKV_ERR_CUDA;
-
-    DecodeArgs a;
-    a.q = static_cast<const __nv_bfloat16 *>(q);
-    a.k_scale = k_scale;
-    a.v_scale = v_scale;
-    a.block_table = block_table;
-    a.max_pages = max_pages_per_seq;
-    a.seq_lens = seq_lens;
-    a.batch = batch;
-    a.hq = num_q_heads;
-    a.hkv = num_kv_heads;
-    a.group = num_q_heads / num_kv_heads;
-    a.num_pages = num_pages;
-    a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
-    a.out = out;
-    a.out_f32 = out_dtype == PKV_F32;
-    a.seg_pieces = static_cast<int2 *>(workspace);
-    a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + decode_segment_bytes(batch, num_kv_heads));
-    a.err = device_error;
-    a.num_ctas = ctas;
-    return launch_paged_decode(a, tm_k, tm_v, page_size, stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    if (in_dtype != PKV_F32 && in_dtype != PKV_BF16)
+        return PKV_ERR_DTYPE;
+    if (n_new > 0 && batch > 0) {
+        if (!k_new || !v_new)
+            return PKV_ERR_NULL;
+        if (!aligned(k_new, 16) || !aligned(v_new, 16))
+            return PKV_ERR_ALIGN;
+    }
+    return decode_impl(n_new > 0 ? k_new : nullptr, n_new > 0 ? v_new : nullptr, in_dtype, n_new, q, k_cache, v_cache,
+                       k_scale, v_scale, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, num_kv_heads,
+                       head_dim, page_size, num_pages, sm_scale, out, out_dtype, workspace, workspace_bytes,
+                       device_error, max_ctas, stream);
 }
 
 }  // extern "C"

@@ -43,18 +43,8 @@ __device__ __forceinline__ void load16(const void *base, int64_t elem, float (&x
 // 16 values / scale (IEEE division) -> 16 E4M3 bytes (RNE, saturating).
 __device__ __forceinline__ uint4 quantise16(const float (&x)[16], float scale)
 {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        uint32_t b[2];
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            float2 y = make_float2(__fdiv_rn(x[4 * i + 2 * k], scale), __fdiv_rn(x[4 * i + 2 * k + 1], scale));
-            b[k] = __nv_cvt_float2_to_fp8x2(y, __NV_SATFINITE, __NV_E4M3);
-        }
-        w[i] = (b[0] & 0xFFFFu) | (b[1] << 16);
-    }
-    return make_uint4(w[0], w[1], w[2], w[3]);
+    return make_uint4(quantise4(x[0], x[1], x[2], x[3], scale), quantise4(x[4], x[5], x[6], x[7], scale),
+                      quantise4(x[8], x[9], x[10], x[11], scale), quantise4(x[12], x[13], x[14], x[15], scale));
 }
 
 template <bool kBf16>

@@ -327,6 +327,64 @@ __device__ __forceinline__ void process_tile(TileFrags &fr, int nv, const uint32
     }
 }
 
+// Fused append: this worker quantises and stores the new tokens that fall in
+// the page-heads it owns (exactly one worker owns each page-head, so nobody
+// else reads or writes them in this call), then orders those generic-proxy
+// stores before its own TMA reads.  Lanes split the 128 dims, 4 each.
+template <int P>
+__device__ __noinline__ void append_own_tokens(const DecodeArgs &a, const int *pstart, int64_t lo, int64_t hi,
+                                               int cap, int lane)
+{
+    Loc l = locate(pstart, a.batch, a.hkv, lo);
+    int64_t cur = lo;
+    const int tail_pages = 1 + (a.n_new + P - 1) / P;    // new tokens live in a segment's last pages
+    while (cur < hi) {
+        const int np = pages_of(pstart, l.b);
+        const int n_piece = static_cast<int>(min(static_cast<int64_t>(np - l.pg), hi - cur));
+        if (l.pg + n_piece <= np - tail_pages) {           // this piece cannot hold a new token
+            cur += n_piece;
+            l = advance(pstart, a.batch, a.hkv, l, n_piece);
+            continue;
+        }
+        const int L = clamp_len(__ldg(a.seq_lens + l.b), cap);
+        const int first = max(0, L - a.n_new);            // positions [first, L) are new
+        for (int t = first; t < L; ++t) {
+            const int pg = t / P;
+            if (pg < l.pg || pg >= l.pg + n_piece)
+                continue;
+            const int phys = __ldg(a.block_table + static_cast<int64_t>(l.b) * a.max_pages + pg);
+            if (phys < 0 || phys >= a.num_pages) {
+                if (a.err && lane == 0)
+                    atomicOr(a.err, PKV_DEVERR_PAGE);
+                continue;
+            }
+            const int j = t - (L - a.n_new);
+            const int64_t src = ((static_cast<int64_t>(l.b) * a.n_new + j) * a.hkv + l.h) * kHeadDim + 4 * lane;
+            const int64_t dst = ((static_cast<int64_t>(phys) * a.hkv + l.h) * P + t % P) * kHeadDim + 4 * lane;
+            float k4[4], v4[4];
+            if (a.new_bf16) {
+                const uint2 kb = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(a.k_new) + src));
+                const uint2 vb = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(a.v_new) + src));
+                k4[0] = __uint_as_float(kb.x << 16); k4[1] = __uint_as_float(kb.x & 0xFFFF0000u);
+                k4[2] = __uint_as_float(kb.y << 16); k4[3] = __uint_as_float(kb.y & 0xFFFF0000u);
+                v4[0] = __uint_as_float(vb.x << 16); v4[1] = __uint_as_float(vb.x & 0xFFFF0000u);
+                v4[2] = __uint_as_float(vb.y << 16); v4[3] = __uint_as_float(vb.y & 0xFFFF0000u);
+            } else {
+                const float4 kf = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(a.k_new) + src));
+                const float4 vf = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(a.v_new) + src));
+                k4[0] = kf.x; k4[1] = kf.y; k4[2] = kf.z; k4[3] = kf.w;
+                v4[0] = vf.x; v4[1] = vf.y; v4[2] = vf.z; v4[3] = vf.w;
+            }
+            *reinterpret_cast<uint32_t *>(a.k_pool + dst) = quantise4(k4[0], k4[1], k4[2], k4[3], __ldg(a.k_scale + l.h));
+            *reinterpret_cast<uint32_t *>(a.v_pool + dst) = quantise4(v4[0], v4[1], v4[2], v4[3], __ldg(a.v_scale + l.h));
+        }
+        cur += n_piece;
+        l = advance(pstart, a.batch, a.hkv, l, n_piece);
+    }
+    asm volatile("fence.proxy.async;" ::: "memory");   // stores above -> this warp's TMA reads
+    __syncwarp();
+}
+
 template <int P>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
@@ -375,7 +433,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             const int L = __ldg(a.seq_lens + b);
             pstart[b] = run;
             run += (clamp_len(L, cap) + P - 1) / P;
-            if (blockIdx.x == 0 && a.err && (L < 0 || L > cap))
+            if (blockIdx.x == 0 && a.err && (L < 0 || L > cap || (a.k_new != nullptr && L < a.n_new)))
                 atomicOr(a.err, PKV_DEVERR_SEQLEN);
         }
         if (tid == kThreads - 1)
@@ -421,6 +479,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     if (lo >= hi)
         return;                                  // warp-level: no CTA barrier follows
     const int n_total = static_cast<int>(hi - lo);
+
+    if (a.k_new != nullptr)
+        append_own_tokens<P>(a, pstart, lo, hi, cap, lane);
 
     const uint32_t ring = smem_addr(smem) + warp * S::kWarpRing;
     const uint32_t bars = smem_addr(smem + S::kBar) + warp * kStages * 8;

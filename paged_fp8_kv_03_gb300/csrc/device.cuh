@@ -119,6 +119,17 @@ __device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t x, uint32_t &lo, uint32
         : "r"(x));
 }
 
+// Four fp32 values / scale (IEEE division) -> four E4M3 bytes (round to
+// nearest even, saturating to +-448; NaN -> NaN code), packed low to high.
+__device__ __forceinline__ uint32_t quantise4(float x0, float x1, float x2, float x3, float scale)
+{
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(x0, scale), __fdiv_rn(x1, scale)),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(x2, scale), __fdiv_rn(x3, scale)),
+                                                 __NV_SATFINITE, __NV_E4M3);
+    return (lo & 0xFFFFu) | (hi << 16);
+}
+
 // 2^x with the hardware approximation (relative error about 2^-22; -inf -> 0).
 __device__ __forceinline__ float ex2_approx(float x)
 {

@@ -42,6 +42,12 @@ struct DecodeArgs {
     float sm_scale_log2;        // sm_scale * log2(e): scores live in the exp2 domain
     void *out;
     int out_f32;
+    // Fused append (pkv_append_decode_fp8): n_new new tokens per sequence at
+    // positions seq_lens[b] - n_new .. seq_lens[b] - 1; k_new == nullptr: none.
+    const void *k_new, *v_new;      // [batch][n_new][hkv][128], fp32 or bf16
+    int new_bf16;
+    int n_new;
+    uint8_t *k_pool, *v_pool;       // the pools the tensor maps describe (for the stores)
     int2 *seg_pieces;               // [batch * hkv + 1] first/last worker of each segment (-1: nothing
                                     // to merge), then the list length split in two 31-bit halves
     float *partials;                // [num_ctas * kWarps + batch * hkv][group][kPartialStride]

@@ -19,9 +19,18 @@ class Filled:
     pass
 
 
-def fill_gpu(wl, layer: int, dev, chunk_tokens: int = 1 << 15, tail_fill: int = 0x7F) -> Filled:
-    """Prefill every sequence through kv_append_fp8 (chunked), then run the
-    decode step's own append (1 token per sequence) as one batched call."""
+def step_tokens(wl, layer: int, dev):
+    """The decode step's new K/V rows, [B, append, Hkv, D] each (fp32)."""
+    A = wl.append
+    k = torch.stack([wl.kv_rows(layer, 0, b, L, L + A, device=dev) for b, L in enumerate(wl.prefill_lens)])
+    v = torch.stack([wl.kv_rows(layer, 1, b, L, L + A, device=dev) for b, L in enumerate(wl.prefill_lens)])
+    return k.contiguous(), v.contiguous()
+
+
+def fill_gpu(wl, layer: int, dev, chunk_tokens: int = 1 << 15, tail_fill: int = 0x7F,
+             step_append: bool = True) -> Filled:
+    """Prefill every sequence through kv_append_fp8 (chunked), then (unless
+    step_append is False) run the decode step's own append as one batched call."""
     f = Filled()
     f.wl = wl
     f.layer = layer
@@ -36,7 +45,7 @@ def fill_gpu(wl, layer: int, dev, chunk_tokens: int = 1 << 15, tail_fill: int = 
             k = wl.kv_rows(layer, 0, b, t0, t1, device=dev)
             v = wl.kv_rows(layer, 1, b, t0, t1, device=dev)
             pkv.kv_append_fp8(k, v, wl.slots(b, t0, t1).to(dev), f.ks, f.vs, f.kc, f.vc, f.err)
-    if wl.append:
+    if wl.append and step_append:
         ks, vs, sl = [], [], []
         for b, L in enumerate(wl.prefill_lens):
             ks.append(wl.kv_rows(layer, 0, b, L, L + wl.append, device=dev))

@@ -122,3 +122,24 @@ def test_python_binding_rejects_cpu_tensors():
         pkv.pkv_kv_append_fp8(x, x, torch.zeros(1, dtype=torch.int64), torch.ones(1), torch.ones(1),
                               torch.zeros(1, 1, 16, 128, dtype=torch.uint8),
                               torch.zeros(1, 1, 16, 128, dtype=torch.uint8))
+
+
+def _fused(lib, **kw):
+    a = dict(kn=A16, vn=A16, dt=0, n=1, q=A16, kc=A16, vc=A16b, ks=A16, vs=A16, bt=A16, maxp=4, lens=A16, B=2,
+             Hq=16, Hkv=2, D=128, P=16, np_=8, sm=0.088, out=A16, odt=1, ws=A16, wsb=1 << 20, err=None, ctas=0)
+    a.update(kw)
+    return lib.pkv_append_decode_fp8(a["kn"], a["vn"], a["dt"], a["n"], a["q"], a["kc"], a["vc"], a["ks"], a["vs"],
+                                     a["bt"], a["maxp"], a["lens"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"],
+                                     a["np_"], a["sm"], a["out"], a["odt"], a["ws"], a["wsb"], a["err"], a["ctas"],
+                                     None)
+
+
+def test_fused_argument_errors(lib):
+    c = _status_codes()
+    assert _fused(lib, n=-1) == c["PKV_ERR_SHAPE"]
+    assert _fused(lib, dt=9) == c["PKV_ERR_DTYPE"]
+    assert _fused(lib, kn=None) == c["PKV_ERR_NULL"]
+    assert _fused(lib, vn=ctypes.c_void_p(0x10004)) == c["PKV_ERR_ALIGN"]
+    assert _fused(lib, Hq=12, Hkv=8) == c["PKV_ERR_SHAPE"]
+    assert _fused(lib, P=64) == c["PKV_ERR_UNSUPPORTED"]
+    assert _fused(lib, B=0, kn=None, vn=None, q=None, bt=None, lens=None, out=None) == c["PKV_OK"]
