@@ -207,6 +207,18 @@ def run_gpu(args, rank, world):
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
+    graphs = None
+    if args.graph:
+        # One graph per distinct layer-cache phase; each replays a whole step.
+        n_phase = n_layers // math.gcd(n_layers, per_step)
+        graphs = []
+        for ph in range(n_phase):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                step(ph)
+            graphs.append(g)
+        torch.cuda.synchronize()
+        stream = torch.cuda.current_stream(dev)
     clocks = ClockSampler(dev.index)
     if rank == 0:
         clocks.start()
@@ -219,14 +231,22 @@ def run_gpu(args, rank, world):
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record(stream)
     for i in range(args.steps):
-        step(i, evs[i])
+        if graphs is None:
+            step(i, evs[i])
+        else:
+            evs[i][0][0].record(stream)
+            graphs[i % len(graphs)].replay()
+            evs[i][-1][1].record(stream)
     t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop() if rank == 0 else None
     total_ms = t_start.elapsed_time(t_end)
-    decode_ms = [a.elapsed_time(b) for ev in evs for a, b in ev]
+    if graphs is None:
+        decode_ms = [a.elapsed_time(b) for ev in evs for a, b in ev]
+    else:   # per-call times are not separable inside a graph: whole step / layer passes
+        decode_ms = [ev[0][0].elapsed_time(ev[-1][1]) / per_step for ev in evs]
     if world > 1:
         t = torch.tensor([total_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -309,7 +329,8 @@ def run_gpu(args, rank, world):
                          f"{n_layers} distinct caches rotate layer pass by layer pass",
                    "parallelism": f"replicas x{world}"},
         "path": ("kv_append_fp8 + paged_gqa_decode (two calls)" if (wl.append and args.separate) else
-                 "append_decode_fp8 (append fused into the decode launch)" if wl.append else "paged_gqa_decode"),
+                 "append_decode_fp8 (append fused into the decode launch)" if wl.append else "paged_gqa_decode")
+                + (", CUDA-graph replay" if args.graph else ""),
         "roofline": {"bound": "hbm", "kernel": "decode call: paged_gqa_decode_kernel + splitk_merge_kernel",
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -355,14 +376,18 @@ class OracleRig:
         self.oracle.kv_append(wl.kv_rows(0, 1, b, 0, L).numpy(), sl, self.vs, self.vc)
         self.filled.add(b)
 
-    def step(self, seqs, threads):
+    def step(self, seqs, threads, n_kv_heads=None):
+        """Times the oracle on sequences `seqs`: append of their step tokens and
+        decode of the query heads of their first n_kv_heads kv heads (all by
+        default).  Returns (seconds, algorithmic KV bytes covered)."""
         wl = self.wl
+        hk = wl.hkv if n_kv_heads is None else max(1, min(wl.hkv, n_kv_heads))
         for b in seqs:
             self.fill(b)
         new = [(wl.kv_rows(0, 0, b, wl.prefill_lens[b], wl.seq_lens[b]).numpy(),
                 wl.kv_rows(0, 1, b, wl.prefill_lens[b], wl.seq_lens[b]).numpy(),
                 wl.slots(b, wl.prefill_lens[b], wl.seq_lens[b]).numpy()) for b in seqs]
-        sel = np.array([[b, i] for b in seqs for i in range(wl.hq)], np.int32)
+        sel = np.array([[b, i] for b in seqs for i in range(hk * wl.group)], np.int32)
         t0 = time.perf_counter()
         for kn, vn, sl in new:
             if len(sl):
@@ -371,7 +396,7 @@ class OracleRig:
         self.oracle.paged_decode(self.q, self.kc, self.vc, self.ks, self.vs, self.bt, self.lens, sel=sel,
                                  threads=threads)
         dt = time.perf_counter() - t0
-        return dt, sum(wl.seq_lens[b] for b in seqs) * wl.hkv * 2 * wl.head_dim
+        return dt, sum(wl.seq_lens[b] for b in seqs) * hk * 2 * wl.head_dim
 
 
 def cpu_baseline(wl, budget_s: float, scale_device="cpu") -> dict:
@@ -396,23 +421,28 @@ def run_reference(args, rank, world):
     wl = workloads.config(args.config, page_size=args.page)
     threads = len(os.sched_getaffinity(0))
     rig = OracleRig(wl)
-    per = []
-    nbytes = 0
+    # Size each step's sample (kv heads of one sequence) so that all warm-up
+    # and timed steps together take about args.ref_seconds of oracle time.
+    t_full, _ = rig.step([0], threads)
+    budget = args.ref_seconds / (args.warmup + args.steps)
+    n_kv = max(1, min(wl.hkv, int(wl.hkv * budget / max(t_full, 1e-9))))
+    per, nbytes = [], []
     for i in range(args.warmup + args.steps):
         b = i % wl.batch
-        dt, nb = rig.step([b], threads)
+        dt, nb = rig.step([b], threads, n_kv)
         if i >= args.warmup:
             per.append(dt)
-            nbytes = nb
+            nbytes.append(nb)
     ms = 1e3 * statistics.mean(per)
-    value = nbytes / (ms * 1e-3) / 1e9
+    value = sum(nbytes) / sum(per) / 1e9
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {**wl.describe(), "kv_bytes_per_step": wl.kv_bytes()},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-                             "sample": "each step: one sequence (all query heads) of the workload, "
-                                       "fp64 C oracle append + decode"},
+                             "sample": f"each step: the {n_kv * wl.group} query heads of {n_kv} of the {wl.hkv} "
+                                       "kv heads of one sequence (sequences in turn), fp64 C oracle append + "
+                                       "decode; value = algorithmic KV bytes covered / oracle time"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -428,7 +458,10 @@ def main():
     ap.add_argument("--rotate", type=int, default=0, help="distinct layer caches (0 = auto)")
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-seconds", type=float, default=90.0,
+                    help="oracle time budget of the whole --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--graph", action="store_true", help="replay each step from a captured CUDA graph")
     ap.add_argument("--separate", action="store_true",
                     help="time kv_append_fp8 and paged_gqa_decode as two calls instead of the fused step")
     args = ap.parse_args()

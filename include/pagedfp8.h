@@ -44,6 +44,12 @@
  *                        returned; outputs are undefined)
  * The word is sticky: clear it (e.g. cudaMemsetAsync) before a call whose
  * errors you want to attribute.
+ *
+ * Test facility: with the environment variable PKV_TEST_WITHHOLD_LOAD=<w>
+ * set, decode worker warp w never loads its first page, so its first
+ * pipeline wait runs out after about 2 s and the call sets
+ * PKV_DEVERR_TIMEOUT (outputs undefined) -- used to test the timeout path
+ * without faulting or hanging the GPU.  Unset, it has no effect.
  */
 #ifndef PAGEDFP8_H
 #define PAGEDFP8_H

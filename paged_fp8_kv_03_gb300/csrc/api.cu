@@ -1,6 +1,7 @@
 // C entry points: argument checks on the host, TMA tensor descriptions of the
 // page pools, grid sizing and launches.  Nothing here allocates device memory.
 #include <math.h>
+#include <stdlib.h>
 
 #include <map>
 #include <mutex>
@@ -219,6 +220,11 @@ pkv_status decode_impl(const void *k_new, const void *v_new, int in_dtype, int n
     a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + decode_segment_bytes(batch, num_kv_heads));
     a.err = device_error;
     a.num_ctas = ctas;
+    // Test facility for the timeout path: PKV_TEST_WITHHOLD_LOAD=<worker> makes
+    // that worker warp skip its first page's loads, so its first wait runs out
+    // (about 2 s) and the call reports PKV_DEVERR_TIMEOUT.  Unset: no effect.
+    const char *hold = getenv("PKV_TEST_WITHHOLD_LOAD");
+    a.withhold_worker = hold ? atoi(hold) : -1;
     return launch_paged_decode(a, tm_k, tm_v, page_size, stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 

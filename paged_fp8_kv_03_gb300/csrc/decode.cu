@@ -503,7 +503,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int zcur = lane < n_total ? tile_z(advance(pstart, a.batch, a.hkv, cons, lane)) : 0;
     int znext = 32 + lane < n_total ? tile_z(advance(pstart, a.batch, a.hkv, nbase, lane)) : 0;
     int fb = 0;
-    int issued_hi = 0;                           // pages [0, issued_hi) had their loads issued
+    // Warp-uniform bookkeeping of the ring: bit s of `pending` is set while
+    // stage s has a copy in flight that nobody has waited for yet, bit s of
+    // `pend_par` is the parity of that fill.  Used only to drain after an abort.
+    uint32_t pending = 0, pend_par = 0;
 
     auto issue = [&](int f) {                    // warp-uniform; page f goes to stage f % kStages
         if (f >= 32 * (fb + 1)) {
@@ -513,13 +516,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             znext = 32 * (fb + 1) + lane < n_total ? tile_z(advance(pstart, a.batch, a.hkv, nbase, lane)) : 0;
         }
         const int z = __shfl_sync(kFull, zcur, f & 31);
-        if (lane == 0 && !*abort_flag) {
+        // Test hook: the selected worker never loads its first page, so its
+        // first wait must run out (failure-detection test; -1 = off).
+        const bool withheld = worker == a.withhold_worker && f == 0;
+        const int go = __shfl_sync(kFull, (lane == 0 && !*abort_flag && !withheld) ? 1 : 0, 0);
+        if (go) {
             const int s = f % kStages;
-            const uint32_t dst = ring + s * S::kStageBytes;
-            mbar_arrive_expect_tx(bars + 8 * s, 2 * S::kTile);
-            tma_load_3d(dst, &tm_k, 0, 0, z, bars + 8 * s, policy);
-            tma_load_3d(dst + S::kTile, &tm_v, 0, 0, z, bars + 8 * s, policy);
-            issued_hi = f + 1;
+            if (lane == 0) {
+                const uint32_t dst = ring + s * S::kStageBytes;
+                mbar_arrive_expect_tx(bars + 8 * s, 2 * S::kTile);
+                tma_load_3d(dst, &tm_k, 0, 0, z, bars + 8 * s, policy);
+                tma_load_3d(dst + S::kTile, &tm_v, 0, 0, z, bars + 8 * s, policy);
+            }
+            pending |= 1u << s;
+            pend_par = (pend_par & ~(1u << s)) | ((static_cast<uint32_t>(f / kStages) & 1u) << s);
         }
     };
     for (int f = 0; f < kStages && f < n_total; ++f)
@@ -571,6 +581,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 ph ^= 1u;
             }
             const bool ready = wait_warp(bars + 8 * s, par, abort_flag, a.err, lane);
+            if (ready)
+                pending &= ~(1u << s);
             const uint32_t kt = ring + s * S::kStageBytes;
             // Copy the page into registers, then hand the stage straight back
             // to the TMA unit so every stage stays in flight during the math.
@@ -634,10 +646,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
 
     // Drain: never leave with a copy still writing this warp's ring (only
-    // possible after a timeout: normally every issued page was waited for).
-    if (*abort_flag && lane == 0) {
-        for (int f = max(0, issued_hi - kStages); f < issued_hi; ++f)
-            wait_thread(bars + 8 * (f % kStages), static_cast<uint32_t>(f / kStages) & 1u, abort_flag, a.err, false);
+    // possible after an abort: normally every issued page was waited for).
+    if (pending != 0 && lane == 0) {
+        for (int s = 0; s < kStages; ++s)
+            if (pending & (1u << s))
+                wait_thread(bars + 8 * s, (pend_par >> s) & 1u, abort_flag, a.err, false);
     }
 }
 

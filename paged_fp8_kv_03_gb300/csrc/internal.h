@@ -53,6 +53,7 @@ struct DecodeArgs {
     float *partials;                // [num_ctas * kWarps + batch * hkv][group][kPartialStride]
     int32_t *err;
     int num_ctas;
+    int withhold_worker;            // failure-detection test hook (-1 = off)
 };
 
 // Workspace = per-segment piece ranges + the list length (rounded to 256

@@ -1,0 +1,38 @@
+"""Failure detection on the GPU without a fault: a decode worker is told
+(test facility PKV_TEST_WITHHOLD_LOAD) never to load its first page, so its
+bounded pipeline wait runs out; the kernel must report PKV_DEVERR_TIMEOUT,
+drain, return within seconds, and leave the context usable."""
+import os
+import time
+
+import pytest
+import torch
+
+import workloads
+from tests.gpu_fill import assert_close, fill_gpu
+from tests.test_gpu_decode import _full_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+def test_withheld_load_times_out_and_context_survives(pkv, cuda_device):
+    wl = workloads.Workload(70, "timeout", [300, 77], 0, 8, 2, 16, seed=4)
+    f = fill_gpu(wl, 0, cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    os.environ["PKV_TEST_WITHHOLD_LOAD"] = "0"
+    try:
+        t0 = time.time()
+        pkv.paged_gqa_decode(f.q, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, out_dtype=torch.float32,
+                             device_error=err, max_ctas=4)
+        torch.cuda.synchronize()
+        dt = time.time() - t0
+    finally:
+        del os.environ["PKV_TEST_WITHHOLD_LOAD"]
+    assert int(err.item()) & pkv.DEVERR_TIMEOUT
+    assert 1.5 < dt < 20.0
+    err.zero_()
+    out = pkv.paged_gqa_decode(f.q, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, out_dtype=torch.float32,
+                               device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert_close(out.double().cpu().numpy(), _full_oracle(wl, f), "after timeout")
