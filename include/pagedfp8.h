@@ -122,6 +122,29 @@ pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, int in_dtype,
                              int32_t *device_error, cudaStream_t stream);
 
 /*
+ * kv_calibrate -- on-device KV-scale calibration ([G] §3.2: every attention
+ * layer keeps a running maximum of the KV values seen during prefill and
+ * quantises new KV with the scale derived from it; [G] §3.1: scale =
+ * absmax / 448 with a 1e-12 floor).
+ *
+ *   k_running_max[h] = max(k_running_max[h], |k_new[t][h][d]| over t, d)
+ *   (same for V; NaN values are ignored), then, if k_scale/v_scale are given,
+ *   k_scale[h] = max(k_running_max[h] / 448, 1e-12) (IEEE fp32 division).
+ *
+ *   k_new, v_new       device [num_tokens][num_kv_heads][head_dim], PKV_F32 or
+ *                      PKV_BF16, 16-byte aligned.
+ *   *_running_max      device fp32 [num_kv_heads], caller-owned state: zero it
+ *                      when a layer starts calibrating; updated in place.
+ *   k_scale, v_scale   device fp32 [num_kv_heads] outputs, or both NULL.
+ * Calls on one stream compose: the maxima of several prefill batches equal
+ * the maximum over their union.
+ */
+pkv_status pkv_kv_calibrate(const void *k_new, const void *v_new, int in_dtype,
+                            int64_t num_tokens, int num_kv_heads, int head_dim,
+                            float *k_running_max, float *v_running_max,
+                            float *k_scale, float *v_scale, cudaStream_t stream);
+
+/*
  * Workspace bytes pkv_paged_gqa_decode needs for these sizes on the current
  * device (partial softmax states of the split-K pass).  Returns 0 for sizes
  * the library rejects.  max_ctas as in pkv_paged_gqa_decode.

@@ -18,6 +18,9 @@ follows, is written at the top of ``oracle.c``:
   behind a block table: 0539edu.com Llama 3 notes §2.2, §5.2).
 * ``paged_decode`` -- fp64 softmax(q.K^T/sqrt(D)).V over the dequantised
   cache, reached through the block table, query head i reading KV head i // G.
+* ``kv_absmax_update`` / ``kv_scale_from_max`` -- the per-layer running
+  maximum of |K| (or |V|) per kv head over prefill batches, and the scale
+  max / 448 floored at 1e-12 (same guide §3.2 running max, §3.1 recipe).
 
 Parity status of every function is pinned by the ``-m "not gpu"`` tests in
 ``tests/test_oracle_*.py`` (no function here is unpinned).
@@ -76,6 +79,10 @@ def _load():
         lib.oracle_paged_decode.restype = i32
         lib.oracle_paged_decode.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32,
                                             i32, i64, dbl, P, i64, P, P, i64, i32]
+        lib.oracle_kv_absmax_update.restype = None
+        lib.oracle_kv_absmax_update.argtypes = [P, i32, i64, i32, i32, P]
+        lib.oracle_kv_scale_from_max.restype = None
+        lib.oracle_kv_scale_from_max.argtypes = [P, i32, P]
         _lib = lib
         return lib
 
@@ -172,3 +179,25 @@ def paged_decode(q_bits, k_cache, v_cache, k_scale, v_scale, block_table, seq_le
     if st != 0:
         raise ValueError(f"oracle_paged_decode failed with status {st}")
     return (out, weights[:, :w_stride]) if want_weights else out
+
+
+def kv_absmax_update(x, running_max: np.ndarray) -> None:
+    """Fold the rows x [T, Hkv, D] (fp32, or bf16 bits as uint16) into the
+    running per-head maximum of |x| (fp32 [Hkv], modified in place; NaN skipped)."""
+    x = np.asarray(x)
+    in_bf16 = 1 if x.dtype == np.uint16 else 0
+    x = _c(x, np.uint16 if in_bf16 else np.float32)
+    if not (running_max.flags.c_contiguous and running_max.dtype == np.float32):
+        raise TypeError("running_max must be a C-contiguous float32 array")
+    T, H, D = x.shape
+    if running_max.shape != (H,):
+        raise ValueError("shape mismatch")
+    _load().oracle_kv_absmax_update(_ptr(x), in_bf16, T, H, D, _ptr(running_max))
+
+
+def kv_scale_from_max(running_max) -> np.ndarray:
+    """fp32 scale per head: max(running_max / 448, 1e-12)."""
+    rm = _c(running_max, np.float32)
+    out = np.empty_like(rm)
+    _load().oracle_kv_scale_from_max(_ptr(rm), rm.size, _ptr(out))
+    return out

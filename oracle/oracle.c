@@ -23,11 +23,16 @@
  *     i / G ("FP8量化与长上下文实测", §1.2: 64 query heads over 8 KV heads).
  *   - Decode attention: for the one new query of every sequence,
  *     o = softmax(q . K^T / sqrt(D)) . V over every cached token.
+ *   - KV-scale calibration: every attention layer keeps a running maximum of
+ *     |K| and |V| over the prefill batches it has seen, per kv head, and the
+ *     scale is that maximum / 448, floored at 1e-12 ("FP8量化与长上下文实测",
+ *     §3.2 running max per layer, §3.1 absmax / 448 and the 1e-12 clamp).
  *
  * Readings where the pages are silent (all listed in the design notes):
  *   NaN input -> a NaN code (0x7F); |y| > 448 (and +-Inf) -> +-448; the sign of
  *   zero is kept; q widens exactly from bf16; sm_scale = 1/sqrt(D); tokens at
- *   t >= seq_len are never read; seq_len = 0 gives an all-zero output.
+ *   t >= seq_len are never read; seq_len = 0 gives an all-zero output; NaN
+ *   inputs do not enter the running maximum.
  */
 #include <math.h>
 #include <pthread.h>
@@ -326,4 +331,36 @@ int oracle_paged_decode(const uint16_t *q, const uint8_t *k_cache, const uint8_t
             status = job[k].status;
     }
     return status;
+}
+
+/* ---------------------------------------------------------------------- */
+/* KV-scale calibration: running |x| maximum per kv head, scale = max/448.  */
+/* ---------------------------------------------------------------------- */
+
+/* running_max[h] = max(running_max[h], |x[t][h][d]| for all t, d); NaN is
+ * skipped (a comparison with NaN is false). */
+void oracle_kv_absmax_update(const void *x, int in_bf16, int64_t T, int Hkv, int D, float *running_max)
+{
+    for (int h = 0; h < Hkv; ++h) {
+        float m = running_max[h];
+        for (int64_t t = 0; t < T; ++t) {
+            for (int d = 0; d < D; ++d) {
+                int64_t i = (t * Hkv + h) * (int64_t)D + d;
+                float v = in_bf16 ? bf16_bits_to_float(((const uint16_t *)x)[i]) : ((const float *)x)[i];
+                float a = fabsf(v);
+                if (a > m)
+                    m = a;
+            }
+        }
+        running_max[h] = m;
+    }
+}
+
+/* scale[h] = max(running_max[h] / 448, 1e-12), the division in IEEE fp32. */
+void oracle_kv_scale_from_max(const float *running_max, int Hkv, float *scale)
+{
+    for (int h = 0; h < Hkv; ++h) {
+        float s = running_max[h] / 448.0f;
+        scale[h] = s > 1e-12f ? s : 1e-12f;
+    }
 }

@@ -7,6 +7,7 @@ stream.  The entry points mirror the C ABI in ``include/pagedfp8.h``:
 * ``pkv_kv_append_fp8``       -- quantise new K/V rows into their pages
 * ``pkv_paged_gqa_decode``    -- grouped-query decode attention over the pages
 * ``pkv_append_decode_fp8``    -- both in one launch (one whole decode step)
+* ``pkv_kv_calibrate``         -- running |K|, |V| maxima per kv head and the scales
 * ``pkv_decode_workspace_size``, ``pkv_status_string``, ``pkv_version``
 
 ``kv_append_fp8`` / ``paged_gqa_decode`` are the same calls with the output
@@ -66,6 +67,8 @@ def load() -> ctypes.CDLL:
         lib.pkv_append_decode_fp8.restype = i32
         lib.pkv_append_decode_fp8.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
                                               i32, i64, f32, vp, i32, vp, sz, vp, i32, vp]
+        lib.pkv_kv_calibrate.restype = i32
+        lib.pkv_kv_calibrate.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp, vp, vp]
         lib.pkv_paged_gqa_decode_noalloc.restype = i32
         lib.pkv_paged_gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
                                                      i64, f32, vp, i32, vp, i32, vp]
@@ -144,6 +147,29 @@ def pkv_kv_append_fp8(k_new, v_new, slot_mapping, k_scale, v_scale, k_cache, v_c
                                   _ptr(device_error), _stream(stream))
     if st != 0:
         raise PkvError(st, "pkv_kv_append_fp8")
+
+
+def pkv_kv_calibrate(k_new, v_new, k_running_max, v_running_max, k_scale=None, v_scale=None,
+                     stream=None) -> None:
+    """Fold prefill rows k_new/v_new [T, Hkv, 128] (fp32|bf16) into the running
+    per-head maxima (fp32 [Hkv], in place) and, if given, write the scales
+    max(running_max / 448, 1e-12)."""
+    _need(k_new, "k_new", dim=3)
+    _need(v_new, "v_new", dtype=k_new.dtype, dim=3)
+    for t, n in ((k_running_max, "k_running_max"), (v_running_max, "v_running_max")):
+        _need(t, n, torch.float32, 1)
+    if (k_scale is None) != (v_scale is None):
+        raise ValueError("give both scales or neither")
+    if k_scale is not None:
+        _need(k_scale, "k_scale", torch.float32, 1)
+        _need(v_scale, "v_scale", torch.float32, 1)
+    T, H, D = k_new.shape
+    if v_new.shape != k_new.shape or k_running_max.shape[0] != H or v_running_max.shape[0] != H:
+        raise ValueError("shapes disagree")
+    st = load().pkv_kv_calibrate(_ptr(k_new), _ptr(v_new), _act_code(k_new), T, H, D, _ptr(k_running_max),
+                                 _ptr(v_running_max), _ptr(k_scale), _ptr(v_scale), _stream(stream))
+    if st != 0:
+        raise PkvError(st, "pkv_kv_calibrate")
 
 
 def pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim=HEAD_DIM, page_size=16,
@@ -311,7 +337,7 @@ def paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_len
 
 __all__ = ["load", "lib_path", "pkv_kv_append_fp8", "pkv_paged_gqa_decode", "pkv_decode_workspace_size",
            "pkv_paged_gqa_decode_noalloc", "pkv_decode_noalloc_scratch_bytes", "pkv_append_decode_fp8",
-           "append_decode_fp8",
+           "append_decode_fp8", "pkv_kv_calibrate",
            "pkv_status_string", "pkv_version", "kv_append_fp8", "paged_gqa_decode", "decode_workspace",
            "PkvError", "PKV_F32", "PKV_BF16", "DEVERR_SLOT", "DEVERR_PAGE", "DEVERR_SEQLEN",
            "DEVERR_TIMEOUT"]

@@ -327,6 +327,27 @@ __device__ __forceinline__ void process_tile(TileFrags &fr, int nv, const uint32
     }
 }
 
+// Index (within this worker's range) of the first page that may hold one of
+// the step's new tokens: they lie in a segment's last 1 + ceil(n_new / P)
+// pages.  Uses only the page offsets in shared memory.  n_total if none.
+template <int P>
+__device__ int first_tail_page(const DecodeArgs &a, const int *pstart, int64_t lo, int64_t hi)
+{
+    const int tail_pages = 1 + (a.n_new + P - 1) / P;
+    Loc l = locate(pstart, a.batch, a.hkv, lo);
+    int64_t cur = lo;
+    while (cur < hi) {
+        const int np = pages_of(pstart, l.b);
+        const int n_piece = static_cast<int>(min(static_cast<int64_t>(np - l.pg), hi - cur));
+        const int first = max(l.pg, np - tail_pages);
+        if (first < l.pg + n_piece)
+            return static_cast<int>(cur - lo) + (first - l.pg);
+        cur += n_piece;
+        l = advance(pstart, a.batch, a.hkv, l, n_piece);
+    }
+    return static_cast<int>(hi - lo);
+}
+
 // Fused append: this worker quantises and stores the new tokens that fall in
 // the page-heads it owns (exactly one worker owns each page-head, so nobody
 // else reads or writes them in this call), then orders those generic-proxy
@@ -480,7 +501,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         return;                                  // warp-level: no CTA barrier follows
     const int n_total = static_cast<int>(hi - lo);
 
-    if (a.k_new != nullptr)
+    // Fused append: if a page that may receive new tokens is among the first
+    // kStages pages of this worker, store the tokens before any load; otherwise
+    // start the loads first and store while they are in flight (those pages
+    // are issued later, after the stores and their proxy fence).
+    const bool append_early =
+        a.k_new != nullptr && first_tail_page<P>(a, pstart, lo, hi) < Smem<P>::kStages;
+    if (append_early)
         append_own_tokens<P>(a, pstart, lo, hi, cap, lane);
 
     const uint32_t ring = smem_addr(smem) + warp * S::kWarpRing;
@@ -534,6 +561,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     };
     for (int f = 0; f < kStages && f < n_total; ++f)
         issue(f);
+    if (a.k_new != nullptr && !append_early)
+        append_own_tokens<P>(a, pstart, lo, hi, cap, lane);
 
     const int gid = lane >> 2, t4 = lane & 3;
     const TileOffsets off = tile_offsets(lane);
@@ -677,54 +706,44 @@ __global__ void __launch_bounds__(kMergeThreads) splitk_merge_kernel(const Decod
     const int n_pieces = dense ? r.y - r.x + 1
                                : static_cast<int>(static_cast<int64_t>(r.y) * total / workers - x0 + 1);
     const int b = seg / a.hkv, h = seg % a.hkv;
-    const int lane = d & 31, warp = d >> 5;
-    __shared__ float f_sh[kMergeThreads];
-    __shared__ int w_sh[kMergeThreads];
-    __shared__ float red[kMergeThreads / 32];
     auto piece_worker = [&](int i) { return dense ? r.x + i : worker_of(x0 + i, total, workers); };
     auto slot = [&](int w) { return a.partials + (static_cast<int64_t>(w + seg) * a.group + g) * kPartialStride; };
 
-    float mloc = -INFINITY;
-    for (int i = d; i < n_pieces; i += kMergeThreads)
-        mloc = fmaxf(mloc, slot(piece_worker(i))[kHeadDim]);
+    // Pieces in groups of 8: all loads of a group are issued together, then
+    // folded into the running (M, L, A) with an exact rescale.  Every thread
+    // computes the same M and L; the order is fixed, so results are
+    // deterministic.
+    constexpr int kGroup = 8;
+    float M = -INFINITY, L = 0.f, A = 0.f;
+    for (int c0 = 0; c0 < n_pieces; c0 += kGroup) {
+        const int n = min(kGroup, n_pieces - c0);
+        float m[kGroup], l[kGroup], v[kGroup];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        mloc = fmaxf(mloc, __shfl_xor_sync(kFull, mloc, o));
-    if (lane == 0)
-        red[warp] = mloc;
-    __syncthreads();
-    float M = red[0];
-#pragma unroll
-    for (int w = 1; w < kMergeThreads / 32; ++w)
-        M = fmaxf(M, red[w]);
-    __syncthreads();
-
-    float L = 0.f, A = 0.f;
-    for (int c0 = 0; c0 < n_pieces; c0 += kMergeThreads) {
-        const int n = min(kMergeThreads, n_pieces - c0);
-        float f = 0.f, lw = 0.f;
-        int wk = 0;
-        if (d < n) {
-            wk = piece_worker(c0 + d);
-            const float *sl = slot(wk);
-            f = ex2_approx(sl[kHeadDim] - M);
-            lw = sl[kHeadDim + 1] * f;
+        for (int i = 0; i < kGroup; ++i) {
+            if (i < n) {
+                const float *sl = slot(piece_worker(c0 + i));
+                m[i] = sl[kHeadDim];
+                l[i] = sl[kHeadDim + 1];
+                v[i] = sl[d];
+            }
         }
-        f_sh[d] = f;
-        w_sh[d] = wk;
+        float mc = M;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1)
-            lw += __shfl_xor_sync(kFull, lw, o);
-        if (lane == 0)
-            red[warp] = lw;
-        __syncthreads();
+        for (int i = 0; i < kGroup; ++i)
+            if (i < n)
+                mc = fmaxf(mc, m[i]);
+        const float r0 = ex2_approx(M - mc);          // 0 on the first group (M = -inf)
+        L *= r0;
+        A *= r0;
 #pragma unroll
-        for (int w = 0; w < kMergeThreads / 32; ++w)
-            L += red[w];
-#pragma unroll 8
-        for (int i = 0; i < n; ++i)
-            A += slot(w_sh[i])[d] * f_sh[i];
-        __syncthreads();
+        for (int i = 0; i < kGroup; ++i) {
+            if (i < n) {
+                const float f = ex2_approx(m[i] - mc);
+                L += l[i] * f;
+                A += v[i] * f;
+            }
+        }
+        M = mc;
     }
     const float vsc = __ldg(a.v_scale + h);
     store_out(a, static_cast<int64_t>(b) * a.hq + static_cast<int64_t>(h) * a.group + g, d, A * (vsc / L));

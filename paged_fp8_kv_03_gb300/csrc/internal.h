@@ -68,6 +68,8 @@ int device_sm_count();
 
 // Launchers.
 cudaError_t launch_kv_append(const AppendArgs &a, cudaStream_t stream);
+cudaError_t launch_kv_calibrate(const void *k_new, const void *v_new, int in_bf16, int64_t T, int hkv,
+                                float *k_max, float *v_max, float *k_scale, float *v_scale, cudaStream_t stream);
 size_t decode_smem_bytes(int page_size, int batch);
 const void *decode_kernel_for(int page_size);
 int decode_num_ctas(int page_size, int batch, int max_ctas);

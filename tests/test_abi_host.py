@@ -143,3 +143,21 @@ def test_fused_argument_errors(lib):
     assert _fused(lib, Hq=12, Hkv=8) == c["PKV_ERR_SHAPE"]
     assert _fused(lib, P=64) == c["PKV_ERR_UNSUPPORTED"]
     assert _fused(lib, B=0, kn=None, vn=None, q=None, bt=None, lens=None, out=None) == c["PKV_OK"]
+
+
+def test_calibrate_argument_errors(lib):
+    c = _status_codes()
+
+    def cal(**kw):
+        a = dict(k=A16, v=A16, dt=0, T=4, H=8, D=128, rk=A16, rv=A16b, ks=A16, vs=A16b)
+        a.update(kw)
+        return lib.pkv_kv_calibrate(a["k"], a["v"], a["dt"], a["T"], a["H"], a["D"], a["rk"], a["rv"], a["ks"],
+                                    a["vs"], None)
+    assert cal(T=-1) == c["PKV_ERR_SHAPE"]
+    assert cal(H=0) == c["PKV_ERR_SHAPE"]
+    assert cal(dt=4) == c["PKV_ERR_DTYPE"]
+    assert cal(D=96) == c["PKV_ERR_UNSUPPORTED"]
+    assert cal(rk=None) == c["PKV_ERR_NULL"]
+    assert cal(ks=None) == c["PKV_ERR_NULL"]          # both scales or neither
+    assert cal(k=None) == c["PKV_ERR_NULL"]
+    assert cal(k=ctypes.c_void_p(0x10008)) == c["PKV_ERR_ALIGN"]
