@@ -16,6 +16,8 @@
  *        bound by memory bandwidth; §3.3 block_size 16, kv_cache_dtype fp8;
  *        §5.2 one block-table entry per 16 tokens (8000 for 128000 tokens).
  *   [S]  Llama 3 8B notes (mlqm.cn/news/162512), §3.3: block size 32 option.
+ *   [T]  Llama 3 technical notes (wmrh.cn/news/61679), §3.2: 256-token pages.
+ *        [N] §3.2 also proposes 64-token pages for long segments.
  *
  * Memory layout (part of the ABI, so page bytes compare bit for bit):
  *   k_cache, v_cache : uint8  [num_pages][num_kv_heads][page_size][head_dim]
@@ -111,7 +113,8 @@ enum {
  *   k_cache, v_cache device uint8 pools as laid out above, 16-byte aligned.
  *   device_error   device int32 or NULL; PKV_DEVERR_SLOT for slots outside
  *                  [0, num_pages * page_size) (the token is skipped).
- * num_tokens == 0 is a no-op.  Two tokens with the same slot race.
+ * page_size is 16, 32, 64, 128 or 256.  num_tokens == 0 is a no-op.  Two
+ * tokens with the same slot race.
  */
 pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, int in_dtype,
                              int64_t num_tokens, int num_kv_heads, int head_dim,
@@ -176,7 +179,7 @@ size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
  *   seq_lens       device int32 [batch]; must satisfy
  *                  0 <= seq_lens[b] <= max_pages_per_seq * page_size
  *                  (violations set PKV_DEVERR_SEQLEN and are clamped).
- *   head_dim       128.  page_size 16 or 32.  G in 1..8.
+ *   head_dim       128.  page_size 16, 32, 64, 128 or 256.  G in 1..8.
  *   sm_scale       softmax scale, normally 1/sqrt(head_dim).
  *   out            device [batch][num_q_heads][head_dim], out_dtype
  *                  PKV_BF16 (bf16, RNE of the fp32 result) or PKV_F32.

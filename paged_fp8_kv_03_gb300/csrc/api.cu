@@ -39,7 +39,8 @@ EncodeTiledFn encode_fn()
 }
 
 // A pool [num_pages][hkv][P][128] bytes seen as a 3-D tensor (128 bytes, P rows,
-// num_pages*hkv tiles); one box = one page of one kv head, 128-byte swizzled.
+// num_pages*hkv tiles); one box = 16 rows (one chunk) of one page of one kv
+// head, 128-byte swizzled.
 bool make_page_map(CUtensorMap *tm, const uint8_t *pool, int64_t num_pages, int hkv, int P)
 {
     EncodeTiledFn fn = encode_fn();
@@ -48,7 +49,7 @@ bool make_page_map(CUtensorMap *tm, const uint8_t *pool, int64_t num_pages, int 
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(P),
                                 static_cast<cuuint64_t>(num_pages) * static_cast<cuuint64_t>(hkv)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(P) * kHeadDim};
-    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(P), 1};
+    const cuuint32_t box[3] = {static_cast<cuuint32_t>(kHeadDim), 16u, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(pool), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -137,7 +138,7 @@ pkv_status check_decode_shape(int batch, int hq, int hkv, int head_dim, int page
         return PKV_ERR_SHAPE;
     if (hq % hkv != 0)
         return PKV_ERR_SHAPE;
-    if (head_dim != kHeadDim || (page_size != 16 && page_size != 32))
+    if (head_dim != kHeadDim || !page_size_ok(page_size))
         return PKV_ERR_UNSUPPORTED;
     if (hq / hkv > PKV_MAX_GROUP || batch > PKV_MAX_BATCH)
         return PKV_ERR_UNSUPPORTED;
@@ -206,6 +207,7 @@ pkv_status decode_impl(const void *k_new, const void *v_new, int in_dtype, int n
     a.hq = num_q_heads;
     a.hkv = num_kv_heads;
     a.group = num_q_heads / num_kv_heads;
+    a.page_size = page_size;
     a.num_pages = num_pages;
     a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
     a.out = out;
@@ -261,7 +263,7 @@ pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, int in_dtype,
         return PKV_ERR_SHAPE;
     if (in_dtype != PKV_F32 && in_dtype != PKV_BF16)
         return PKV_ERR_DTYPE;
-    if (head_dim != kHeadDim || (page_size != 16 && page_size != 32))
+    if (head_dim != kHeadDim || !page_size_ok(page_size))
         return PKV_ERR_UNSUPPORTED;
     if (num_tokens == 0)
         return PKV_OK;

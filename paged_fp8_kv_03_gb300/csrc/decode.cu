@@ -55,15 +55,17 @@ constexpr float kRescaleThreshold = 8.0f;   // log2 units
 constexpr unsigned kFull = 0xffffffffu;
 
 struct Loc {
-    int b, h, pg;   // sequence, kv head, page index within the sequence
+    int b, h, ck;   // sequence, kv head, 16-token chunk index within the sequence
 };
+
+constexpr int kChunk = 16;   // tokens per chunk: one TMA box, one mma tile
 
 __device__ __forceinline__ int clamp_len(int L, int cap)
 {
     return L < 0 ? 0 : (L > cap ? cap : L);
 }
 
-__device__ __forceinline__ int pages_of(const int *ps, int b)
+__device__ __forceinline__ int chunks_of(const int *ps, int b)
 {
     return ps[b + 1] - ps[b];
 }
@@ -80,19 +82,19 @@ __device__ Loc locate(const int *ps, int batch, int hkv, int64_t x)
             hi = mid - 1;
     }
     const int64_t rem = x - static_cast<int64_t>(ps[lo]) * hkv;
-    const int np = pages_of(ps, lo);
+    const int np = chunks_of(ps, lo);
     Loc l;
     l.b = lo;
     l.h = static_cast<int>(rem / np);
-    l.pg = static_cast<int>(rem % np);
+    l.ck = static_cast<int>(rem % np);
     return l;
 }
 
 __device__ Loc advance(const int *ps, int batch, int hkv, Loc l, int64_t n)
 {
-    int64_t pg = l.pg + n;
+    int64_t pg = l.ck + n;
     while (l.b < batch) {
-        const int np = pages_of(ps, l.b);
+        const int np = chunks_of(ps, l.b);
         if (pg < np)
             break;
         pg -= np;
@@ -101,7 +103,7 @@ __device__ Loc advance(const int *ps, int batch, int hkv, Loc l, int64_t n)
             ++l.b;
         }
     }
-    l.pg = static_cast<int>(pg);
+    l.ck = static_cast<int>(pg);
     return l;
 }
 
@@ -111,11 +113,10 @@ __device__ __forceinline__ int worker_of(int64_t x, int64_t total, int workers)
     return static_cast<int>(((x + 1) * workers - 1) / total);
 }
 
-template <int P>
 struct Smem {
-    static constexpr int kTile = P * kHeadDim;              // bytes of one K (or V) tile
+    static constexpr int kTile = kChunk * kHeadDim;         // bytes of one K (or V) chunk tile
     static constexpr int kStageBytes = 2 * kTile;
-    static constexpr int kStages = P == 16 ? 4 : 2;         // per warp: 16 KB ring
+    static constexpr int kStages = 4;                       // per warp: 16 KB ring
     static constexpr int kWarpRing = kStages * kStageBytes;
     static constexpr int kBar = kWarps * kWarpRing;         // full[kWarps][kStages]
     static constexpr int kFlag = kBar + kWarps * kStages * 8;   // abort flag
@@ -327,21 +328,20 @@ __device__ __forceinline__ void process_tile(TileFrags &fr, int nv, const uint32
     }
 }
 
-// Index (within this worker's range) of the first page that may hold one of
-// the step's new tokens: they lie in a segment's last 1 + ceil(n_new / P)
-// pages.  Uses only the page offsets in shared memory.  n_total if none.
-template <int P>
-__device__ int first_tail_page(const DecodeArgs &a, const int *pstart, int64_t lo, int64_t hi)
+// Index (within this worker's range) of the first chunk that may hold one of
+// the step's new tokens: they lie in a segment's last 1 + ceil(n_new / 16)
+// chunks.  Uses only the chunk offsets in shared memory.  n_total if none.
+__device__ int first_tail_chunk(const DecodeArgs &a, const int *pstart, int64_t lo, int64_t hi)
 {
-    const int tail_pages = 1 + (a.n_new + P - 1) / P;
+    const int tail_pages = 1 + (a.n_new + kChunk - 1) / kChunk;
     Loc l = locate(pstart, a.batch, a.hkv, lo);
     int64_t cur = lo;
     while (cur < hi) {
-        const int np = pages_of(pstart, l.b);
-        const int n_piece = static_cast<int>(min(static_cast<int64_t>(np - l.pg), hi - cur));
-        const int first = max(l.pg, np - tail_pages);
-        if (first < l.pg + n_piece)
-            return static_cast<int>(cur - lo) + (first - l.pg);
+        const int np = chunks_of(pstart, l.b);
+        const int n_piece = static_cast<int>(min(static_cast<int64_t>(np - l.ck), hi - cur));
+        const int first = max(l.ck, np - tail_pages);
+        if (first < l.ck + n_piece)
+            return static_cast<int>(cur - lo) + (first - l.ck);
         cur += n_piece;
         l = advance(pstart, a.batch, a.hkv, l, n_piece);
     }
@@ -352,17 +352,17 @@ __device__ int first_tail_page(const DecodeArgs &a, const int *pstart, int64_t l
 // the page-heads it owns (exactly one worker owns each page-head, so nobody
 // else reads or writes them in this call), then orders those generic-proxy
 // stores before its own TMA reads.  Lanes split the 128 dims, 4 each.
-template <int P>
 __device__ __noinline__ void append_own_tokens(const DecodeArgs &a, const int *pstart, int64_t lo, int64_t hi,
                                                int cap, int lane)
 {
+    const int P = a.page_size;
     Loc l = locate(pstart, a.batch, a.hkv, lo);
     int64_t cur = lo;
-    const int tail_pages = 1 + (a.n_new + P - 1) / P;    // new tokens live in a segment's last pages
+    const int tail_pages = 1 + (a.n_new + kChunk - 1) / kChunk;   // new tokens live in a segment's last chunks
     while (cur < hi) {
-        const int np = pages_of(pstart, l.b);
-        const int n_piece = static_cast<int>(min(static_cast<int64_t>(np - l.pg), hi - cur));
-        if (l.pg + n_piece <= np - tail_pages) {           // this piece cannot hold a new token
+        const int np = chunks_of(pstart, l.b);
+        const int n_piece = static_cast<int>(min(static_cast<int64_t>(np - l.ck), hi - cur));
+        if (l.ck + n_piece <= np - tail_pages) {           // this piece cannot hold a new token
             cur += n_piece;
             l = advance(pstart, a.batch, a.hkv, l, n_piece);
             continue;
@@ -370,10 +370,10 @@ __device__ __noinline__ void append_own_tokens(const DecodeArgs &a, const int *p
         const int L = clamp_len(__ldg(a.seq_lens + l.b), cap);
         const int first = max(0, L - a.n_new);            // positions [first, L) are new
         for (int t = first; t < L; ++t) {
-            const int pg = t / P;
-            if (pg < l.pg || pg >= l.pg + n_piece)
+            const int ck = t / kChunk;                     // the worker owning this chunk stores the token
+            if (ck < l.ck || ck >= l.ck + n_piece)
                 continue;
-            const int phys = __ldg(a.block_table + static_cast<int64_t>(l.b) * a.max_pages + pg);
+            const int phys = __ldg(a.block_table + static_cast<int64_t>(l.b) * a.max_pages + t / P);
             if (phys < 0 || phys >= a.num_pages) {
                 if (a.err && lane == 0)
                     atomicOr(a.err, PKV_DEVERR_PAGE);
@@ -406,13 +406,13 @@ __device__ __noinline__ void append_own_tokens(const DecodeArgs &a, const int *p
     __syncwarp();
 }
 
-template <int P>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                             const DecodeArgs a)
 {
-    using S = Smem<P>;
+    using S = Smem;
     constexpr int kStages = S::kStages;
+    const int P = a.page_size;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -428,7 +428,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int b0 = min(a.batch, tid * chunk), b1 = min(a.batch, b0 + chunk);
         int local = 0;
         for (int b = b0; b < b1; ++b)
-            local += (clamp_len(__ldg(a.seq_lens + b), cap) + P - 1) / P;
+            local += (clamp_len(__ldg(a.seq_lens + b), cap) + kChunk - 1) / kChunk;
         int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -453,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         for (int b = b0; b < b1; ++b) {
             const int L = __ldg(a.seq_lens + b);
             pstart[b] = run;
-            run += (clamp_len(L, cap) + P - 1) / P;
+            run += (clamp_len(L, cap) + kChunk - 1) / kChunk;
             if (blockIdx.x == 0 && a.err && (L < 0 || L > cap || (a.k_new != nullptr && L < a.n_new)))
                 atomicOr(a.err, PKV_DEVERR_SEQLEN);
         }
@@ -465,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // Sequences with no tokens: nobody streams them, so write their zero rows here.
     for (int sg = blockIdx.x; sg < a.batch * a.hkv; sg += a.num_ctas) {
         const int b = sg / a.hkv;
-        if (pages_of(pstart, b) == 0) {
+        if (chunks_of(pstart, b) == 0) {
             const int64_t row0 = static_cast<int64_t>(b) * a.hq + static_cast<int64_t>(sg % a.hkv) * a.group;
             for (int e = tid; e < a.group * kHeadDim; e += kThreads)
                 store_out(a, row0 + (e >> 7), e & (kHeadDim - 1), 0.f);
@@ -480,7 +480,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // segment that more than one worker touches (-1: nothing to merge).
     if (blockIdx.x == 0) {
         for (int sg = tid; sg < a.batch * a.hkv; sg += kThreads) {
-            const int b = sg / a.hkv, h = sg % a.hkv, np = pages_of(pstart, b);
+            const int b = sg / a.hkv, h = sg % a.hkv, np = chunks_of(pstart, b);
             int2 r = make_int2(-1, -1);
             if (np > 0) {
                 const int64_t start = static_cast<int64_t>(pstart[b]) * a.hkv + static_cast<int64_t>(h) * np;
@@ -506,43 +506,47 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // start the loads first and store while they are in flight (those pages
     // are issued later, after the stores and their proxy fence).
     const bool append_early =
-        a.k_new != nullptr && first_tail_page<P>(a, pstart, lo, hi) < Smem<P>::kStages;
+        a.k_new != nullptr && first_tail_chunk(a, pstart, lo, hi) < S::kStages;
     if (append_early)
-        append_own_tokens<P>(a, pstart, lo, hi, cap, lane);
+        append_own_tokens(a, pstart, lo, hi, cap, lane);
 
     const uint32_t ring = smem_addr(smem) + warp * S::kWarpRing;
     const uint32_t bars = smem_addr(smem + S::kBar) + warp * kStages * 8;
     const uint64_t policy = l2_policy_evict_first();
     const int zoob = static_cast<int>(a.num_pages * a.hkv);   // first out-of-pool tile: reads zeros
-    auto tile_z = [&](Loc l) -> int {
-        const int phys = __ldg(a.block_table + static_cast<int64_t>(l.b) * a.max_pages + l.pg);
+    const int cpp = P / kChunk;                                // chunks per page
+    // TMA coordinates of a chunk: tile z = page * hkv + head, row y = 16 * (chunk within page).
+    auto tile_zy = [&](Loc l) -> int2 {
+        const int phys = __ldg(a.block_table + static_cast<int64_t>(l.b) * a.max_pages + l.ck / cpp);
         if (phys < 0 || phys >= a.num_pages) {
             if (a.err)
                 atomicOr(a.err, PKV_DEVERR_PAGE);
-            return zoob;
+            return make_int2(zoob, 0);
         }
-        return phys * a.hkv + l.h;
+        return make_int2(phys * a.hkv + l.h, (l.ck % cpp) * kChunk);
     };
 
-    // ---- block-table batches: zcur holds pages [32*fb, 32*fb+32), znext the next 32
+    // ---- block-table batches: zcur holds chunks [32*fb, 32*fb+32), znext the next 32
     Loc cons = locate(pstart, a.batch, a.hkv, lo);
     Loc nbase = advance(pstart, a.batch, a.hkv, cons, 32);
-    int zcur = lane < n_total ? tile_z(advance(pstart, a.batch, a.hkv, cons, lane)) : 0;
-    int znext = 32 + lane < n_total ? tile_z(advance(pstart, a.batch, a.hkv, nbase, lane)) : 0;
+    int2 zcur = lane < n_total ? tile_zy(advance(pstart, a.batch, a.hkv, cons, lane)) : make_int2(0, 0);
+    int2 znext = 32 + lane < n_total ? tile_zy(advance(pstart, a.batch, a.hkv, nbase, lane)) : make_int2(0, 0);
     int fb = 0;
     // Warp-uniform bookkeeping of the ring: bit s of `pending` is set while
     // stage s has a copy in flight that nobody has waited for yet, bit s of
     // `pend_par` is the parity of that fill.  Used only to drain after an abort.
     uint32_t pending = 0, pend_par = 0;
 
-    auto issue = [&](int f) {                    // warp-uniform; page f goes to stage f % kStages
+    auto issue = [&](int f) {                    // warp-uniform; chunk f goes to stage f % kStages
         if (f >= 32 * (fb + 1)) {
             zcur = znext;
             ++fb;
             nbase = advance(pstart, a.batch, a.hkv, nbase, 32);
-            znext = 32 * (fb + 1) + lane < n_total ? tile_z(advance(pstart, a.batch, a.hkv, nbase, lane)) : 0;
+            znext = 32 * (fb + 1) + lane < n_total ? tile_zy(advance(pstart, a.batch, a.hkv, nbase, lane))
+                                                   : make_int2(0, 0);
         }
-        const int z = __shfl_sync(kFull, zcur, f & 31);
+        const int z = __shfl_sync(kFull, zcur.x, f & 31);
+        const int y = __shfl_sync(kFull, zcur.y, f & 31);
         // Test hook: the selected worker never loads its first page, so its
         // first wait must run out (failure-detection test; -1 = off).
         const bool withheld = worker == a.withhold_worker && f == 0;
@@ -552,8 +556,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (lane == 0) {
                 const uint32_t dst = ring + s * S::kStageBytes;
                 mbar_arrive_expect_tx(bars + 8 * s, 2 * S::kTile);
-                tma_load_3d(dst, &tm_k, 0, 0, z, bars + 8 * s, policy);
-                tma_load_3d(dst + S::kTile, &tm_v, 0, 0, z, bars + 8 * s, policy);
+                tma_load_3d(dst, &tm_k, 0, y, z, bars + 8 * s, policy);
+                tma_load_3d(dst + S::kTile, &tm_v, 0, y, z, bars + 8 * s, policy);
             }
             pending |= 1u << s;
             pend_par = (pend_par & ~(1u << s)) | ((static_cast<uint32_t>(f / kStages) & 1u) << s);
@@ -562,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int f = 0; f < kStages && f < n_total; ++f)
         issue(f);
     if (a.k_new != nullptr && !append_early)
-        append_own_tokens<P>(a, pstart, lo, hi, cap, lane);
+        append_own_tokens(a, pstart, lo, hi, cap, lane);
 
     const int gid = lane >> 2, t4 = lane & 3;
     const TileOffsets off = tile_offsets(lane);
@@ -570,10 +574,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint32_t ph = 0;                             // its fill parity
     int k = 0;
     while (k < n_total) {
-        const int np = pages_of(pstart, cons.b);
-        const int n_piece = min(np - cons.pg, n_total - k);
+        const int np = chunks_of(pstart, cons.b);
+        const int n_piece = min(np - cons.ck, n_total - k);
         const int L = clamp_len(__ldg(a.seq_lens + cons.b), cap);
-        const bool whole = (cons.pg == 0) && (n_piece == np);
+        const bool whole = (cons.ck == 0) && (n_piece == np);
         const int seg = cons.b * a.hkv + cons.h;
         const float scale2 = __ldg(a.k_scale + cons.h) * a.sm_scale_log2;
 
@@ -602,7 +606,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 acc[sg][c] = 0.f;
 
         for (int j = 0; j < n_piece; ++j, ++k) {
-            const int nv = min(P, L - (cons.pg + j) * P);
+            const int nv = min(kChunk, L - (cons.ck + j) * kChunk);
             const int s = st;
             const uint32_t par = ph;
             if (++st == kStages) {
@@ -613,28 +617,21 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (ready)
                 pending &= ~(1u << s);
             const uint32_t kt = ring + s * S::kStageBytes;
-            // Copy the page into registers, then hand the stage straight back
+            // Copy the chunk into registers, then hand the stage straight back
             // to the TMA unit so every stage stays in flight during the math.
-            TileFrags fr[P / 16];
-            if (ready) {
-#pragma unroll
-                for (int sub = 0; sub < P / 16; ++sub)
-                    load_tile(kt + sub * 16 * kHeadDim, kt + S::kTile + sub * 16 * kHeadDim, off, fr[sub]);
-            }
+            TileFrags fr;
+            if (ready)
+                load_tile(kt, kt + S::kTile, off, fr);
             if (k + kStages < n_total) {
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 issue(k + kStages);
             }
             if (ready) {
-#pragma unroll
-                for (int sub = 0; sub < P / 16; ++sub) {
-                    const int nvs = nv - sub * 16;
-                    if (nvs >= 16)
-                        process_tile<false>(fr[sub], 16, qa, scale2, m_ref, lsum, acc, lane);
-                    else if (nvs > 0)
-                        process_tile<true>(fr[sub], nvs, qa, scale2, m_ref, lsum, acc, lane);
-                }
+                if (nv >= kChunk)
+                    process_tile<false>(fr, kChunk, qa, scale2, m_ref, lsum, acc, lane);
+                else
+                    process_tile<true>(fr, nv, qa, scale2, m_ref, lsum, acc, lane);
             }
         }
 
@@ -749,32 +746,23 @@ __global__ void __launch_bounds__(kMergeThreads) splitk_merge_kernel(const Decod
     store_out(a, static_cast<int64_t>(b) * a.hq + static_cast<int64_t>(h) * a.group + g, d, A * (vsc / L));
 }
 
-template <int P>
-const void *decode_kernel_ptr()
-{
-    return reinterpret_cast<const void *>(&paged_gqa_decode_kernel<P>);
-}
-
 }  // namespace
 
-size_t decode_smem_bytes(int page_size, int batch)
+size_t decode_smem_bytes(int /*page_size*/, int batch)
 {
-    return page_size == 32 ? Smem<32>::bytes(batch) : Smem<16>::bytes(batch);
+    return Smem::bytes(batch);
 }
 
-const void *decode_kernel_for(int page_size)
+const void *decode_kernel_for(int /*page_size*/)
 {
-    return page_size == 32 ? decode_kernel_ptr<32>() : decode_kernel_ptr<16>();
+    return reinterpret_cast<const void *>(&paged_gqa_decode_kernel);
 }
 
 cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                 int page_size, cudaStream_t stream)
 {
     const size_t smem = decode_smem_bytes(page_size, a.batch);
-    if (page_size == 32)
-        paged_gqa_decode_kernel<32><<<a.num_ctas, kThreads, smem, stream>>>(tm_k, tm_v, a);
-    else
-        paged_gqa_decode_kernel<16><<<a.num_ctas, kThreads, smem, stream>>>(tm_k, tm_v, a);
+    paged_gqa_decode_kernel<<<a.num_ctas, kThreads, smem, stream>>>(tm_k, tm_v, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;

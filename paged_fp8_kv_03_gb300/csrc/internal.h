@@ -18,6 +18,12 @@ constexpr int kThreads = kWarps * 32;
 constexpr int kCtasPerSm = 3;                           // resident decode CTAs per SM
 constexpr int kPartialStride = kHeadDim + 4;            // floats per (slot, head): acc, m, l, pad
 
+// Page sizes the library accepts (tokens per page).
+inline bool page_size_ok(int p)
+{
+    return p == 16 || p == 32 || p == 64 || p == 128 || p == 256;
+}
+
 struct AppendArgs {
     const void *k_new, *v_new;
     int in_bf16;
@@ -38,6 +44,7 @@ struct DecodeArgs {
     int max_pages;
     const int32_t *seq_lens;
     int batch, hq, hkv, group;
+    int page_size;                  // tokens per page (16..256); the kernel works in 16-token chunks
     int64_t num_pages;
     float sm_scale_log2;        // sm_scale * log2(e): scores live in the exp2 domain
     void *out;

@@ -67,7 +67,8 @@ def test_append_argument_errors(lib):
     assert _append(lib, dtype=7) == c["PKV_ERR_DTYPE"]
     assert _append(lib, D=64) == c["PKV_ERR_UNSUPPORTED"]
     assert _append(lib, P=8) == c["PKV_ERR_UNSUPPORTED"]
-    assert _append(lib, P=64) == c["PKV_ERR_UNSUPPORTED"]
+    assert _append(lib, P=48) == c["PKV_ERR_UNSUPPORTED"]
+    assert _append(lib, P=512) == c["PKV_ERR_UNSUPPORTED"]
     assert _append(lib, k=None) == c["PKV_ERR_NULL"]
     assert _append(lib, slots=None) == c["PKV_ERR_NULL"]
     assert _append(lib, kc=ctypes.c_void_p(0x10008)) == c["PKV_ERR_ALIGN"]
@@ -93,7 +94,8 @@ def test_decode_argument_errors(lib):
     assert _decode(lib, np_=0) == c["PKV_ERR_SHAPE"]
     assert _decode(lib, Hq=32, Hkv=2) == c["PKV_ERR_UNSUPPORTED"]    # G = 16
     assert _decode(lib, D=64) == c["PKV_ERR_UNSUPPORTED"]
-    assert _decode(lib, P=64) == c["PKV_ERR_UNSUPPORTED"]
+    assert _decode(lib, P=48) == c["PKV_ERR_UNSUPPORTED"]
+    assert _decode(lib, P=512) == c["PKV_ERR_UNSUPPORTED"]
     assert _decode(lib, B=pkv.MAX_BATCH + 1) == c["PKV_ERR_UNSUPPORTED"]
     assert _decode(lib, np_=1 << 30, Hkv=2) == c["PKV_ERR_UNSUPPORTED"]   # tile index would overflow int32
     assert _decode(lib, odt=5) == c["PKV_ERR_DTYPE"]
@@ -141,7 +143,7 @@ def test_fused_argument_errors(lib):
     assert _fused(lib, kn=None) == c["PKV_ERR_NULL"]
     assert _fused(lib, vn=ctypes.c_void_p(0x10004)) == c["PKV_ERR_ALIGN"]
     assert _fused(lib, Hq=12, Hkv=8) == c["PKV_ERR_SHAPE"]
-    assert _fused(lib, P=64) == c["PKV_ERR_UNSUPPORTED"]
+    assert _fused(lib, P=24) == c["PKV_ERR_UNSUPPORTED"]
     assert _fused(lib, B=0, kn=None, vn=None, q=None, bt=None, lens=None, out=None) == c["PKV_OK"]
 
 

@@ -95,7 +95,7 @@ def test_empty_append_is_noop(pkv, cuda_device):
     assert int(kc.sum()) == 0
 
 
-@pytest.mark.parametrize("cfg,page", [(0, 16), (1, 16), (0, 32), (1, 32)])
+@pytest.mark.parametrize("cfg,page", [(0, 16), (1, 16), (0, 32), (1, 32), (0, 64), (0, 256)])
 def test_pages_bit_exact_small_configs(pkv, cuda_device, cfg, page):
     wl = workloads.config(cfg, page_size=page)
     f = fill_gpu(wl, 0, cuda_device, tail_fill=0)

@@ -46,7 +46,7 @@ def _full_oracle(wl, f):
     return ref.reshape(wl.batch, wl.hq, wl.head_dim)
 
 
-@pytest.mark.parametrize("page", [16, 32])
+@pytest.mark.parametrize("page", [16, 32, 64, 256])
 def test_tiny_config_all_rows(pkv, cuda_device, page):
     wl = workloads.config(0, page_size=page)
     f = fill_gpu(wl, 0, cuda_device)
@@ -70,6 +70,9 @@ def test_tiny_config_all_rows(pkv, cuda_device, page):
     ([513, 2049], 2, 2, 32),                  # G = 1
     ([77, 1], 16, 8, 16),                     # G = 2
     ([4097, 1, 999], 64, 8, 32),
+    ([1, 63, 64, 65, 200], 8, 2, 64),         # 64-token pages (chunks of 16 inside a page)
+    ([129, 1000, 5], 16, 2, 128),
+    ([255, 256, 257, 3000], 64, 8, 256),      # 256-token pages
 ])
 def test_ragged_shapes(pkv, cuda_device, lens, hq, hkv, page):
     wl = workloads.Workload(50, "ragged", lens, 0, hq, hkv, page, pool_factor=1.5, seed=21)
@@ -157,7 +160,8 @@ def test_device_errors_without_faults(pkv, cuda_device):
     assert not torch.isnan(out).any()
 
 
-@pytest.mark.parametrize("cfg,page,n_bh", [(1, 16, 6), (2, 16, 5), (3, 16, 3), (4, 16, 4), (4, 32, 4)])
+@pytest.mark.parametrize("cfg,page,n_bh", [(1, 16, 6), (2, 16, 5), (3, 16, 3), (4, 16, 4), (4, 32, 4),
+                                           (2, 64, 3), (4, 256, 3)])
 def test_full_size_configs_sampled(pkv, cuda_device, cfg, page, n_bh):
     """Full-size workloads in the benchmark's launch configuration; sampled
     (sequence, kv head) groups checked against the oracle."""

@@ -48,6 +48,8 @@ def _fused(pkv, wl, dev, dtype, max_ctas=0):
     ([100, 7, 64], 3, 16, 4, 32),
     ([4096] * 4, 1, 32, 8, 16),
     ([0, 5], 1, 4, 1, 16),              # a sequence made of its new token only
+    ([63, 100, 17], 2, 16, 2, 64),      # 64-token pages: new tokens in chunks inside a page
+    ([255, 30], 1, 8, 8, 256),
 ])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_fused_equals_separate(pkv, cuda_device, lens, append, hq, hkv, page, dtype):
