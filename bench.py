@@ -128,6 +128,15 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": n}
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest value any rank holds (the slowest rank's time decides)."""
+    if world <= 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
 # ----------------------------------------------------------------------------- GPU arm
 def _fill_layer(pkv, wl, layer, dev):
     P, H, D = wl.page_size, wl.hkv, wl.head_dim
@@ -247,10 +256,7 @@ def run_gpu(args, rank, world):
         decode_ms = [a.elapsed_time(b) for ev in evs for a, b in ev]
     else:   # per-call times are not separable inside a graph: whole step / layer passes
         decode_ms = [ev[0][0].elapsed_time(ev[-1][1]) / per_step for ev in evs]
-    if world > 1:
-        t = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
     assert int(err.item()) == 0, f"device error word {int(err.item())}"
 
     # ---- end to end through the public API with host buffers
@@ -294,10 +300,7 @@ def run_gpu(args, rank, world):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
 
     ms_per_step = total_ms / args.steps
     step_bytes = per_step * kv_bytes
