@@ -18,6 +18,9 @@ follows, is written at the top of ``oracle.c``:
   behind a block table: 0539edu.com Llama 3 notes §2.2, §5.2).
 * ``paged_decode`` -- fp64 softmax(q.K^T/sqrt(D)).V over the dequantised
   cache, reached through the block table, query head i reading KV head i // G.
+* ``paged_prefill`` -- chunked prefill: the n queries of a sequence's chunk
+  sit at positions L - n .. L - 1 and each attends causally to cached tokens
+  0 .. its position (0539edu.com Llama 3 notes §2.2).
 * ``kv_absmax_update`` / ``kv_scale_from_max`` -- the per-layer running
   maximum of |K| (or |V|) per kv head over prefill batches, and the scale
   max / 448 floored at 1e-12 (same guide §3.2 running max, §3.1 recipe).
@@ -79,6 +82,9 @@ def _load():
         lib.oracle_paged_decode.restype = i32
         lib.oracle_paged_decode.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32,
                                             i32, i64, dbl, P, i64, P, P, i64, i32]
+        lib.oracle_paged_prefill.restype = i32
+        lib.oracle_paged_prefill.argtypes = [P, P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i64, dbl, P,
+                                             i32]
         lib.oracle_kv_absmax_update.restype = None
         lib.oracle_kv_absmax_update.argtypes = [P, i32, i64, i32, i32, P]
         lib.oracle_kv_scale_from_max.restype = None
@@ -200,4 +206,34 @@ def kv_scale_from_max(running_max) -> np.ndarray:
     rm = _c(running_max, np.float32)
     out = np.empty_like(rm)
     _load().oracle_kv_scale_from_max(_ptr(rm), rm.size, _ptr(out))
+    return out
+
+
+def paged_prefill(q_bits, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
+                  sm_scale: float | None = None, threads: int = 1) -> np.ndarray:
+    """fp64 chunked-prefill attention.  q_bits: [T, Hq, D] bf16 bit patterns,
+    the chunks of all sequences back to back; cu_q: [B + 1] row offsets;
+    seq_lens[b] includes the chunk.  Returns out [T, Hq, D] (fp64)."""
+    q_bits = _c(q_bits, np.uint16)
+    cu_q = _c(cu_q, np.int32)
+    k_cache = _c(k_cache, np.uint8)
+    v_cache = _c(v_cache, np.uint8)
+    k_scale = _c(k_scale, np.float32)
+    v_scale = _c(v_scale, np.float32)
+    block_table = _c(block_table, np.int32)
+    seq_lens = _c(seq_lens, np.int32)
+    T, Hq, D = q_bits.shape
+    NP, Hkv, P, D2 = k_cache.shape
+    B = seq_lens.shape[0]
+    if (v_cache.shape != k_cache.shape or D2 != D or cu_q.shape != (B + 1,) or block_table.shape[0] != B
+            or cu_q[0] != 0 or cu_q[-1] != T):
+        raise ValueError("shape mismatch")
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(D)
+    out = np.zeros((T, Hq, D), np.float64)
+    st = _load().oracle_paged_prefill(_ptr(q_bits), _ptr(cu_q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                      _ptr(v_scale), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                      B, Hq, Hkv, D, P, NP, float(sm_scale), _ptr(out), int(threads))
+    if st != 0:
+        raise ValueError(f"oracle_paged_prefill failed with status {st}")
     return out

@@ -23,6 +23,11 @@
  *     i / G ("FP8量化与长上下文实测", §1.2: 64 query heads over 8 KV heads).
  *   - Decode attention: for the one new query of every sequence,
  *     o = softmax(q . K^T / sqrt(D)) . V over every cached token.
+ *   - Chunked prefill (0539edu.com Llama 3 notes, §2.2: a 128K prompt is
+ *     prefilled as 8 chunks of 16K, each chunk's KV joined to the cache): the
+ *     chunk's K/V are appended to the pages first, then the query at position
+ *     p attends to every cached token t <= p (causal, the earlier chunks
+ *     included).
  *   - KV-scale calibration: every attention layer keeps a running maximum of
  *     |K| and |V| over the prefill batches it has seen, per kv head, and the
  *     scale is that maximum / 448, floored at 1e-12 ("FP8量化与长上下文实测",
@@ -363,4 +368,51 @@ void oracle_kv_scale_from_max(const float *running_max, int Hkv, float *scale)
         float s = running_max[h] / 448.0f;
         scale[h] = s > 1e-12f ? s : 1e-12f;
     }
+}
+
+/* ---------------------------------------------------------------------- */
+/* Chunked-prefill attention: a chunk of queries per sequence, causal.     */
+/* ---------------------------------------------------------------------- */
+
+/* q: [T][Hq][D] bf16 bits, the queries of all sequences back to back;
+ * cu_q[B + 1]: sequence b owns query rows cu_q[b] .. cu_q[b+1] - 1.  seq_lens[b]
+ * counts the chunk, so with n = cu_q[b+1] - cu_q[b] its queries sit at
+ * positions L - n .. L - 1.  The query at position p attends to cached tokens
+ * 0 .. p, exactly as oracle_paged_decode does for a sequence of length p + 1.
+ * out: [T][Hq][D] fp64.  A sequence with L < n is an error (status 3); its
+ * rows are left untouched.  `threads` workers split each row's heads.
+ * Returns 0 or the first non-zero status. */
+int oracle_paged_prefill(const uint16_t *q, const int32_t *cu_q, const uint8_t *k_cache, const uint8_t *v_cache,
+                         const float *k_scale, const float *v_scale,
+                         const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                         int B, int Hq, int Hkv, int D, int P, int64_t num_pages,
+                         double sm_scale, double *out, int threads)
+{
+    int status = 0;
+    int32_t *sel = (int32_t *)malloc(sizeof(int32_t) * 2 * (size_t)(Hq > 0 ? Hq : 1));
+    if (!sel)
+        return 2;
+    for (int i = 0; i < Hq; ++i) {                       /* every query head of the row */
+        sel[2 * i] = 0;
+        sel[2 * i + 1] = i;
+    }
+    for (int b = 0; b < B; ++b) {
+        int32_t n = cu_q[b + 1] - cu_q[b];
+        if (n < 0 || seq_lens[b] < n) {
+            if (!status)
+                status = 3;
+            continue;
+        }
+        for (int32_t c = 0; c < n; ++c) {
+            int32_t len = seq_lens[b] - n + c + 1;       /* keys 0 .. position */
+            int64_t row = (int64_t)cu_q[b] + c;
+            int st = oracle_paged_decode(q + row * Hq * D, k_cache, v_cache, k_scale, v_scale,
+                                         block_table + (int64_t)b * max_pages, max_pages, &len, 1, Hq, Hkv, D, P,
+                                         num_pages, sm_scale, sel, Hq, out + row * Hq * D, NULL, 0, threads);
+            if (st && !status)
+                status = st;
+        }
+    }
+    free(sel);
+    return status;
 }

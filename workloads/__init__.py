@@ -206,6 +206,14 @@ class Workload:
         z = unit_normal(stream_key(self.seed, self.index, layer, 5, step), idx)
         return z.to(torch.bfloat16).view(B, Hq, D)
 
+    def q_rows(self, layer: int, rows: int, step: int = 0, device="cpu") -> torch.Tensor:
+        """bf16 [rows, Hq, D] queries of a prefill chunk (the chunks of all
+        sequences back to back), drawn like q() from their own stream."""
+        Hq, D = self.hq, self.head_dim
+        idx = torch.arange(rows * Hq * D, dtype=torch.int64, device=device)
+        z = unit_normal(stream_key(self.seed, self.index, layer, 6, step), idx)
+        return z.to(torch.bfloat16).view(rows, Hq, D)
+
     def scales(self, layer: int = 0, device="cpu") -> tuple:
         """(k_scale, v_scale), fp32 [Hkv] each: max(absmax/448, 1e-12) per kv
         head over the prefill tokens of every sequence."""
