@@ -274,6 +274,54 @@ pkv_status pkv_paged_gqa_decode_noalloc(const void *q,
 /* Size in bytes of the fixed scratch array pkv_paged_gqa_decode_noalloc uses. */
 size_t pkv_decode_noalloc_scratch_bytes(void);
 
+/*
+ * paged_prefill -- chunked-prefill attention over the paged FP8 cache ([N]
+ * §2.2: a long prompt is prefilled in chunks, 8 x 16K for a 128K prompt, and
+ * each chunk's KV joins the cache; [G] §1.2 GQA).  Call it after
+ * pkv_kv_append_fp8 has written the chunk's own K/V into the pages.
+ *
+ * Sequence b owns query rows cu_q[b] .. cu_q[b+1] - 1 (n_b rows) of q; with
+ * L = seq_lens[b] (the length INCLUDING the chunk), row c sits at position
+ * p = L - n_b + c, and for every query head i (h = i / G, G = num_q_heads /
+ * num_kv_heads):
+ *     s_t = sm_scale * sum_d q[cu_q[b]+c][i][d] * E4M3(k_cache[pg(t)][h][t % P][d]) * k_scale[h]
+ *     w_t = softmax_t(s_t)                              for t <= p (causal)
+ *     out[cu_q[b]+c][i][d] = sum_t w_t * E4M3(v_cache[pg(t)][h][t % P][d]) * v_scale[h]
+ * with pg(t) = block_table[b][t / P].  A chunk of one query is exactly one
+ * decode step.  Runs on the tcgen05 tensor cores (f16 operands: E4M3 widens
+ * exactly, q is widened from bf16, softmax weights enter as two f16 parts);
+ * one launch, no workspace, deterministic.
+ *
+ *   q              device bf16 [total_q][num_q_heads][head_dim] (|q| < 65504),
+ *                  16-byte aligned.
+ *   cu_q           device int32 [batch + 1], non-decreasing, cu_q[0] = 0,
+ *                  cu_q[batch] <= total_q.
+ *   total_q        rows of q and out.
+ *   max_q_len      an upper bound of the chunk lengths n_b (sizes the grid).
+ *   seq_lens       device int32 [batch]; a sequence with n_b > max_q_len,
+ *                  seq_lens[b] < n_b or seq_lens[b] > max_pages_per_seq *
+ *                  page_size, or inconsistent cu_q, sets PKV_DEVERR_SEQLEN and
+ *                  its rows are not written.
+ *   block_table    entries of pages the chunk's positions need must lie in
+ *                  [0, num_pages); others set PKV_DEVERR_PAGE and the page
+ *                  reads as zeros.
+ *   out            device [total_q][num_q_heads][head_dim], PKV_BF16 or
+ *                  PKV_F32, 16-byte aligned.  Rows outside every chunk are
+ *                  not written.
+ *   Caches, scales, head_dim (128), page sizes, G (1..8), sm_scale and
+ *   device_error as in pkv_paged_gqa_decode.  batch * num_kv_heads *
+ *   ceil(max_q_len / (128 / G)) must be below 2^31.
+ */
+pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, int max_q_len,
+                             const uint8_t *k_cache, const uint8_t *v_cache,
+                             const float *k_scale, const float *v_scale,
+                             const int32_t *block_table, int max_pages_per_seq,
+                             const int32_t *seq_lens,
+                             int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                             int page_size, int64_t num_pages, float sm_scale,
+                             void *out, int out_dtype,
+                             int32_t *device_error, cudaStream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char *pkv_status_string(pkv_status status);
 

@@ -18,7 +18,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB_DIR = os.path.join(PKG, "lib")
 LIB = os.path.join(LIB_DIR, "libpagedfp8.so")
 
-SOURCES = ["append.cu", "decode.cu", "api.cu", "noalloc.cu", "calibrate.cu"]
+SOURCES = ["append.cu", "decode.cu", "api.cu", "noalloc.cu", "calibrate.cu", "prefill.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
          "--expt-relaxed-constexpr"]

@@ -56,6 +56,25 @@ bool make_page_map(CUtensorMap *tm, const uint8_t *pool, int64_t num_pages, int 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Queries [total_q][hq][128] bf16 as a 3-D tensor (128 dims, hq heads, total_q
+// rows); one box = 64 dims of the G heads of one kv head for tpt rows, 128-byte
+// swizzled, which is the layout the tensor cores read as a K-major operand.
+bool make_q_map(CUtensorMap *tm, const void *q, int total_q, int hq, int group, int tpt)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(hq),
+                                static_cast<cuuint64_t>(total_q)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
+                                   static_cast<cuuint64_t>(hq) * kHeadDim * 2};
+    const cuuint32_t box[3] = {64u, static_cast<cuuint32_t>(group), static_cast<cuuint32_t>(tpt)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void *p, uintptr_t a)
 {
     return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
@@ -335,6 +354,68 @@ pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dt
                        k_scale, v_scale, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, num_kv_heads,
                        head_dim, page_size, num_pages, sm_scale, out, out_dtype, workspace, workspace_bytes,
                        device_error, max_ctas, stream);
+}
+
+pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, int max_q_len, const uint8_t *k_cache,
+                             const uint8_t *v_cache, const float *k_scale, const float *v_scale,
+                             const int32_t *block_table, int max_pages_per_seq, const int32_t *seq_lens, int batch,
+                             int num_q_heads, int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
+                             float sm_scale, void *out, int out_dtype, int32_t *device_error, cudaStream_t stream)
+{
+    pkv_status st = check_decode_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_seq,
+                                       num_pages);
+    if (st != PKV_OK)
+        return st;
+    if (total_q < 0 || max_q_len < 0)
+        return PKV_ERR_SHAPE;
+    if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
+        return PKV_ERR_DTYPE;
+    if (!(sm_scale == sm_scale) || isinf(sm_scale))
+        return PKV_ERR_SHAPE;
+    if (batch == 0 || total_q == 0 || max_q_len == 0)
+        return PKV_OK;
+    if (!q || !cu_q || !k_cache || !v_cache || !k_scale || !v_scale || !block_table || !seq_lens || !out)
+        return PKV_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(cu_q, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(k_scale, 4) ||
+        !aligned(v_scale, 4) || !aligned(device_error, 4))
+        return PKV_ERR_ALIGN;
+    const int group = num_q_heads / num_kv_heads;
+    const int tpt = 128 / group;
+    const int64_t max_tiles = (static_cast<int64_t>(max_q_len) + tpt - 1) / tpt;
+    if (static_cast<int64_t>(batch) * num_kv_heads * max_tiles >= (int64_t(1) << 31))
+        return PKV_ERR_UNSUPPORTED;
+
+    alignas(64) CUtensorMap tm_q;
+    alignas(64) CUtensorMap tm_k;
+    alignas(64) CUtensorMap tm_v;
+    if (!make_q_map(&tm_q, q, total_q, num_q_heads, group, tpt) ||
+        !make_page_map(&tm_k, k_cache, num_pages, num_kv_heads, page_size) ||
+        !make_page_map(&tm_v, v_cache, num_pages, num_kv_heads, page_size))
+        return PKV_ERR_CUDA;
+
+    PrefillArgs a;
+    a.cu_q = cu_q;
+    a.total_q = total_q;
+    a.max_q_len = max_q_len;
+    a.tokens_per_tile = tpt;
+    a.max_tiles = static_cast<int>(max_tiles);
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
+    a.block_table = block_table;
+    a.max_pages = max_pages_per_seq;
+    a.seq_lens = seq_lens;
+    a.batch = batch;
+    a.hq = num_q_heads;
+    a.hkv = num_kv_heads;
+    a.group = group;
+    a.page_size = page_size;
+    a.num_pages = num_pages;
+    a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
+    a.out = out;
+    a.out_f32 = out_dtype == PKV_F32;
+    a.err = device_error;
+    return launch_paged_prefill(a, tm_q, tm_k, tm_v, stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -67,6 +67,15 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
     return p;
 }
 
+// Data that many CTAs read again (a sequence's KV prefix under prefill): keep
+// it in L2 ahead of streaming data.
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // 3-D tiled bulk tensor copy global -> shared, completing on an mbarrier.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int x, int y, int z,
                                             uint32_t bar, uint64_t policy)

@@ -63,6 +63,27 @@ struct DecodeArgs {
     int withhold_worker;            // failure-detection test hook (-1 = off)
 };
 
+// Chunked prefill (csrc/prefill.cu).  The queries of all sequences are rows
+// of q [total_q][hq][128]; sequence b owns rows cu_q[b] .. cu_q[b+1]-1, which
+// sit at positions seq_lens[b] - n_b .. seq_lens[b] - 1.
+struct PrefillArgs {
+    const int32_t *cu_q;
+    int total_q, max_q_len;
+    int tokens_per_tile;            // 128 / group query tokens per CTA tile
+    int max_tiles;                  // ceil(max_q_len / tokens_per_tile)
+    const float *k_scale, *v_scale;
+    const int32_t *block_table;
+    int max_pages;
+    const int32_t *seq_lens;
+    int batch, hq, hkv, group;
+    int page_size;
+    int64_t num_pages;
+    float sm_scale_log2;
+    void *out;
+    int out_f32;
+    int32_t *err;
+};
+
 // Workspace = per-segment piece ranges + the list length (rounded to 256
 // bytes), then the partial slots.
 inline size_t decode_segment_bytes(int batch, int hkv)
@@ -80,6 +101,9 @@ cudaError_t launch_kv_calibrate(const void *k_new, const void *v_new, int in_bf1
 size_t decode_smem_bytes(int page_size, int batch);
 const void *decode_kernel_for(int page_size);
 int decode_num_ctas(int page_size, int batch, int max_ctas);
+size_t prefill_smem_bytes();
+cudaError_t launch_paged_prefill(const PrefillArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                 const CUtensorMap &tm_v, cudaStream_t stream);
 cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                 int page_size, cudaStream_t stream);
 

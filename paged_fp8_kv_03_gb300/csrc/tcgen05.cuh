@@ -1,0 +1,160 @@
+// Inline-PTX wrappers for the 5th-generation tensor cores (tcgen05) on
+// sm_103a: tensor-memory (TMEM) allocation, MMA issue with shared-memory
+// operand descriptors, commit to an mbarrier, and TMEM <-> register moves.
+//
+// Conventions used by every caller in this library:
+//   * one CTA (cta_group::1), M = 128: accumulator row i lives in TMEM lane i,
+//     fp32 column j in TMEM column (base + j);
+//   * operands in shared memory use the 128-byte swizzle: a tile is stored as
+//     blocks of 64 16-bit elements (128 bytes) per row, 8-row atoms of 1024
+//     bytes, and the 16-byte chunk c of row r sits at chunk position c ^ (r & 7)
+//     inside its atom (the pattern the TMA unit writes for SWIZZLE_128B);
+//   * a warp may touch only its quarter of TMEM lanes: warp w reaches lanes
+//     32 * (w % 4) .. 32 * (w % 4) + 31.
+#pragma once
+
+#include <cstdint>
+
+namespace pkv {
+namespace tc {
+
+// ---------------------------------------------------------------- allocation
+// Executed by one whole warp.  Writes the TMEM base address to *slot (shared).
+__device__ __forceinline__ void tmem_alloc(uint32_t *slot, uint32_t ncols)
+{
+    const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(slot));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(s), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// Ordering of tcgen05 operations across a thread synchronisation (mbarrier or
+// bar.sync): "before" on the signalling side, "after" on the waiting side.
+__device__ __forceinline__ void fence_before()
+{
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_after()
+{
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- descriptors
+// Shared-memory matrix descriptor, 128-byte swizzle.  `lbo` / `sbo` in bytes:
+// for a K-major operand sbo is the distance between 8-row atoms (1024 for a
+// dense tile) and lbo is unused; for an MN-major operand lbo is the distance
+// between 64-element column blocks and sbo the distance between 8-row atoms
+// along K.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;   // descriptor version of the tcgen05 family
+    d |= static_cast<uint64_t>(2) << 61;   // swizzle mode: 128 bytes
+    return d;
+}
+
+// Instruction descriptor for kind::f16 with f16 A and B and an fp32
+// accumulator.  b_mn_major: B is stored with N contiguous instead of K.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n, bool b_mn_major)
+{
+    return (1u << 4)                                        // D: fp32
+           | (0u << 7) | (0u << 10)                         // A, B: f16
+           | ((b_mn_major ? 1u : 0u) << 16)                 // B major-ness
+           | (static_cast<uint32_t>(n >> 3) << 17)          // N / 8
+           | (static_cast<uint32_t>(m >> 4) << 24);         // M / 16
+}
+
+// ---------------------------------------------------------------- MMA issue
+// D[tmem] (+)= A[smem desc] * B[smem desc]^T ; accumulate = 0 overwrites D.
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// A from TMEM: lane i holds row i of A, each 32-bit column two consecutive K
+// elements (f16x2); one K = 16 step consumes 8 columns.
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                       uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive (once) on an mbarrier when every tcgen05 operation this thread has
+// issued so far has completed.
+__device__ __forceinline__ void commit(uint64_t *bar)
+{
+    const uint32_t b = static_cast<uint32_t>(__cvta_generic_to_shared(bar));
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(b)
+                 : "memory");
+}
+
+// ---------------------------------------------------------------- TMEM <-> registers
+// 32 consecutive columns of the calling thread's lane (shape 32x32b, x32).
+__device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+          "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+          "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+          "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void st32(uint32_t taddr, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
+        "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
+        "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void wait_ld()
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void wait_st()
+{
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// TMEM address of (lane, column).
+__device__ __forceinline__ uint32_t taddr_at(uint32_t base, uint32_t lane, uint32_t col)
+{
+    return base + (lane << 16) + col;
+}
+
+}  // namespace tc
+}  // namespace pkv

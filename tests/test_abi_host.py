@@ -163,3 +163,32 @@ def test_calibrate_argument_errors(lib):
     assert cal(ks=None) == c["PKV_ERR_NULL"]          # both scales or neither
     assert cal(k=None) == c["PKV_ERR_NULL"]
     assert cal(k=ctypes.c_void_p(0x10008)) == c["PKV_ERR_ALIGN"]
+
+
+def test_prefill_argument_errors(lib):
+    c = _status_codes()
+
+    def pre(**kw):
+        a = dict(q=A16, cu=A16, T=64, mq=32, kc=A16, vc=A16b, ks=A16, vs=A16, bt=A16, maxp=4, lens=A16, B=2,
+                 Hq=16, Hkv=2, D=128, P=16, np_=8, sm=0.088, out=A16, odt=1, err=None)
+        a.update(kw)
+        return lib.pkv_paged_prefill(a["q"], a["cu"], a["T"], a["mq"], a["kc"], a["vc"], a["ks"], a["vs"],
+                                     a["bt"], a["maxp"], a["lens"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"],
+                                     a["np_"], a["sm"], a["out"], a["odt"], a["err"], None)
+    assert pre(T=-1) == c["PKV_ERR_SHAPE"]
+    assert pre(mq=-1) == c["PKV_ERR_SHAPE"]
+    assert pre(Hq=12, Hkv=8) == c["PKV_ERR_SHAPE"]
+    assert pre(maxp=0) == c["PKV_ERR_SHAPE"]
+    assert pre(sm=float("nan")) == c["PKV_ERR_SHAPE"]
+    assert pre(odt=3) == c["PKV_ERR_DTYPE"]
+    assert pre(D=64) == c["PKV_ERR_UNSUPPORTED"]
+    assert pre(P=48) == c["PKV_ERR_UNSUPPORTED"]
+    assert pre(Hq=32, Hkv=2) == c["PKV_ERR_UNSUPPORTED"]             # G = 16
+    assert pre(B=8192, Hkv=2, Hq=16, mq=1 << 30) == c["PKV_ERR_UNSUPPORTED"]   # grid above 2^31
+    assert pre(cu=None) == c["PKV_ERR_NULL"]
+    assert pre(q=None) == c["PKV_ERR_NULL"]
+    assert pre(q=ctypes.c_void_p(0x10008)) == c["PKV_ERR_ALIGN"]
+    assert pre(cu=ctypes.c_void_p(0x10002)) == c["PKV_ERR_ALIGN"]
+    assert pre(out=ctypes.c_void_p(0x10004)) == c["PKV_ERR_ALIGN"]
+    assert pre(T=0, q=None, cu=None, out=None) == c["PKV_OK"]          # nothing to compute
+    assert pre(mq=0, q=None, cu=None, out=None) == c["PKV_OK"]
