@@ -17,6 +17,9 @@ with --separate kv_append_fp8 followed by paged_gqa_decode.  Prints ONE JSON lin
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1] [--page 16]
     python bench.py --impl reference ...      # the oracle as the reference arm
+    python bench.py --workload prefill        # chunked prefill: a 128K prompt as 8 x 16K
+                                              # chunks (append + causal attention each),
+                                              # TFLOP/s against the tensor roofline
 
 With N > 1 (torchrun) every rank runs an independent replica: the path has no
 exchange step, so there is no collective beyond the timing barrier.
@@ -53,6 +56,18 @@ def _peaks():
             p = json.load(fh)
         return float(p["hbm_gbs"]), "measured"
     return 6800.0, "fallback"
+
+
+def _tensor_peak():
+    """Dense f16/bf16 tensor peak for a kernel timed inside a long step: the
+    measured sustained cuBLAS bf16 rate (f16 has the same nominal rate)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        if "bf16_tflops_sustained" in p:
+            return float(p["bf16_tflops_sustained"]), "measured (cuBLAS bf16, sustained; f16 same nominal rate)"
+    return 1700.0, "fallback (sustained bf16; f16 same nominal rate)"
 
 
 def _kernel_sha() -> str:
@@ -350,6 +365,253 @@ def run_gpu(args, rank, world):
         print(json.dumps(line), flush=True)
 
 
+# ----------------------------------------------------------------------------- chunked prefill
+PREFILL_METRIC = ("chunked-prefill attention over the paged FP8 cache: causal TFLOP/s "
+                  "(append + attention of every chunk of one 128K prompt layer)")
+
+
+def _prefill_flops(first: int, n: int, hq: int, d: int = 128) -> float:
+    """Algorithmic FLOPs of n causal queries at positions first .. first+n-1:
+    QK^T and PV, 2 * 2 * d per (query head, visible key)."""
+    keys = n * first + n * (n + 1) // 2
+    return 4.0 * d * hq * keys
+
+
+def _prefill_setup(wl, chunk, dev):
+    """Everything one chunked-prefill step needs, resident on the device: the
+    fp32 K/V rows and slots of every chunk, the bf16 queries, per-chunk
+    lengths and row offsets, an empty layer cache."""
+    B, L = wl.batch, wl.seq_lens[0]
+    n_chunks = L // chunk
+    ks, vs = wl.scales(0, device=dev)
+    kc = torch.zeros((wl.num_pages, wl.hkv, wl.page_size, wl.head_dim), dtype=torch.uint8, device=dev)
+    chunks = []
+    for c in range(n_chunks):
+        t0, t1 = c * chunk, (c + 1) * chunk
+        k = torch.cat([wl.kv_rows(0, 0, b, t0, t1, device=dev) for b in range(B)])
+        v = torch.cat([wl.kv_rows(0, 1, b, t0, t1, device=dev) for b in range(B)])
+        sl = torch.cat([wl.slots(b, t0, t1) for b in range(B)]).to(dev)
+        q = wl.q_rows(0, B * chunk, step=c, device=dev)
+        chunks.append({"k": k, "v": v, "slots": sl, "q": q,
+                       "lens": torch.full((B,), t1, dtype=torch.int32, device=dev),
+                       "cu": torch.arange(0, (B + 1) * chunk, chunk, dtype=torch.int32, device=dev),
+                       "flops": B * _prefill_flops(t0, chunk, wl.hq, wl.head_dim)})
+    return {"kc": kc, "vc": torch.zeros_like(kc), "ks": ks, "vs": vs, "chunks": chunks,
+            "bt": wl.block_table().to(dev)}
+
+
+def run_prefill_gpu(args, rank, world):
+    import paged_fp8_kv_03_gb300 as pkv
+    from paged_fp8_kv_03_gb300 import build as pbuild
+
+    if rank == 0 or not os.path.exists(pbuild.LIB):
+        pbuild.build()
+    if world > 1:
+        torch.distributed.barrier()
+    pkv.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    wl, chunk = workloads.prefill_config(page_size=args.page, prompt=args.prompt, chunk=args.chunk)
+    st = _prefill_setup(wl, chunk, dev)
+    B = wl.batch
+    out = torch.empty((B * chunk, wl.hq, wl.head_dim), dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n_chunks = len(st["chunks"])
+
+    def step(evs=None):
+        for c, ch in enumerate(st["chunks"]):
+            pkv.pkv_kv_append_fp8(ch["k"], ch["v"], ch["slots"], st["ks"], st["vs"], st["kc"], st["vc"], err)
+            if evs is not None:
+                evs[c][0].record(stream)
+            pkv.pkv_paged_prefill(ch["q"], ch["cu"], st["kc"], st["vc"], st["ks"], st["vs"], st["bt"], ch["lens"],
+                                  out, chunk, device_error=err)
+            if evs is not None:
+                evs[c][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(dev.index)
+    if rank == 0:
+        clocks.start()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_chunks)]
+           for _ in range(args.steps)]
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if rank == 0 else None
+    total_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    assert int(err.item()) == 0, f"device error word {int(err.item())}"
+    launch_ms = [[a.elapsed_time(b) for a, b in ev] for ev in evs]
+    per_chunk_ms = [statistics.mean(launch_ms[i][c] for i in range(args.steps)) for c in range(n_chunks)]
+    step_flops = sum(ch["flops"] for ch in st["chunks"])
+
+    # ---- end to end through the public API: each chunk's q and K/V rows come
+    # from pinned host memory and its output goes back
+    host = [{"k": ch["k"].cpu().pin_memory(), "v": ch["v"].cpu().pin_memory(), "q": ch["q"].cpu().pin_memory(),
+             "slots": ch["slots"].cpu().pin_memory(), "lens": ch["lens"].cpu().pin_memory(),
+             "cu": ch["cu"].cpu().pin_memory()} for ch in st["chunks"]]
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for h in host for t in h.values())
+    d2h = n_chunks * out.numel() * out.element_size()
+
+    def e2e_step():
+        for h in host:
+            d = {k: v.to(dev, non_blocking=True) for k, v in h.items()}
+            pkv.kv_append_fp8(d["k"], d["v"], d["slots"], st["ks"], st["vs"], st["kc"], st["vc"])
+            o = pkv.paged_prefill(d["q"], d["cu"], st["kc"], st["vc"], st["ks"], st["vs"], st["bt"], d["lens"],
+                                  chunk)
+            out_host.copy_(o, non_blocking=True)
+
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    e2e_step()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+
+    ms_per_step = total_ms / args.steps
+    peak, peak_kind = _tensor_peak()
+    prefill_ms = sum(per_chunk_ms)
+    achieved = step_flops / (prefill_ms * 1e-3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC,
+        "value": round(world * step_flops / (ms_per_step * 1e-3) / 1e12, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f16 tensor-core operands, f32 accumulate",
+        "kv_dtype": "e4m3",
+        "data": "synthetic",
+        "config": {**wl.describe(), "chunk": chunk, "chunks": n_chunks,
+                   "flops_per_step": step_flops,
+                   "l2": f"inputs larger than L2 ({wl.kv_bytes() / 1e6:.0f} MB of FP8 KV and "
+                         f"{wl.seq_lens[0] * wl.batch * wl.hq * 256 / 1e6:.0f} MB of queries per step)",
+                   "parallelism": f"replicas x{world}"},
+        "path": "per chunk: kv_append_fp8 of its K/V, then paged_prefill over the cache",
+        "per_chunk_ms": [round(x, 3) for x in per_chunk_ms],
+        "roofline": {"bound": "tensor", "kernel": "paged_prefill_kernel",
+                     "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "algorithmic_flops_per_launch": step_flops / n_chunks,
+                     "avg_launch_us": round(1e3 * prefill_ms / n_chunks, 1)},
+        "e2e": {"value": round(world * step_flops / (e2e_ms * 1e-3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": 2 * n_chunks * args.steps,
+        "clocks": clk,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = prefill_cpu_baseline(wl, chunk, args.cpu_seconds, scale_device=dev)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+class OraclePrefillRig:
+    """The CPU oracle on the chunked-prefill workload: pools of the whole
+    prompt prepared once (untimed); sample() times the oracle on single query
+    rows of the last chunk (all query heads of one kv head each)."""
+
+    def __init__(self, wl, chunk, gen_device="cpu"):
+        import oracle
+        self.oracle, self.wl, self.chunk = oracle, wl, chunk
+        L = wl.seq_lens[0]
+        ks, vs = wl.scales(0, device=gen_device)
+        self.ks, self.vs = ks.cpu().numpy(), vs.cpu().numpy()
+        shape = (wl.num_pages, wl.hkv, wl.page_size, wl.head_dim)
+        self.kc = np.zeros(shape, np.uint8)
+        self.vc = np.zeros(shape, np.uint8)
+        sl = wl.slots(0, 0, L).numpy()
+        step = 1 << 15
+        for t0 in range(0, L, step):
+            t1 = min(L, t0 + step)
+            oracle.kv_append(wl.kv_rows(0, 0, 0, t0, t1, device=gen_device).cpu().numpy(), sl[t0:t1], self.ks, self.kc)
+            oracle.kv_append(wl.kv_rows(0, 1, 0, t0, t1, device=gen_device).cpu().numpy(), sl[t0:t1], self.vs, self.vc)
+        last = L // chunk - 1
+        self.q = wl.q_rows(0, chunk, step=last).view(torch.uint16).numpy()     # the last chunk's queries
+        self.first = L - chunk
+        self.bt = wl.block_table().numpy()[:1]
+
+    def sample(self, row, h, threads):
+        """Oracle time for query row `row` of the last chunk, the G heads of kv
+        head h.  Returns (seconds, algorithmic FLOPs)."""
+        wl = self.wl
+        G = wl.group
+        pos = self.first + row
+        sel = np.array([[0, h * G + g] for g in range(G)], np.int32)
+        t0 = time.perf_counter()
+        self.oracle.paged_decode(self.q[row:row + 1], self.kc, self.vc, self.ks, self.vs, self.bt,
+                                 np.array([pos + 1], np.int32), sel=sel, threads=threads)
+        return time.perf_counter() - t0, 4.0 * wl.head_dim * G * (pos + 1)
+
+
+def prefill_cpu_baseline(wl, chunk, budget_s, scale_device="cpu") -> dict:
+    threads = len(os.sched_getaffinity(0))
+    rig = OraclePrefillRig(wl, chunk, scale_device)
+    rng = np.random.default_rng(0)
+    secs, flops, n = 0.0, 0.0, 0
+    while secs < budget_s and n < 4096:
+        dt, f = rig.sample(int(rng.integers(chunk)), n % wl.hkv, threads)
+        secs += dt
+        flops += f
+        n += 1
+    return {"value": round(flops / secs / 1e12, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+            "sample": f"{n} (query row, kv head) pairs of the last {chunk}-token chunk (positions from "
+                      f"{rig.first}), the "
+                      f"{wl.group} query heads of the kv head each, fp64 C oracle, {secs:.1f} s timed"}
+
+
+def run_prefill_reference(args, rank, world):
+    if rank != 0:
+        return
+    wl, chunk = workloads.prefill_config(page_size=args.page, prompt=args.prompt, chunk=args.chunk)
+    threads = len(os.sched_getaffinity(0))
+    rig = OraclePrefillRig(wl, chunk)
+    dt1, _ = rig.sample(chunk - 1, 0, threads)
+    per_step = max(1, int(args.ref_seconds / (args.warmup + args.steps) / max(dt1, 1e-9)))
+    rng = np.random.default_rng(1)
+    per, fl = [], []
+    for i in range(args.warmup + args.steps):
+        s, f = 0.0, 0.0
+        for k in range(per_step):
+            dt, ff = rig.sample(int(rng.integers(chunk)), k % wl.hkv, threads)
+            s += dt
+            f += ff
+        if i >= args.warmup:
+            per.append(s)
+            fl.append(f)
+    value = sum(fl) / sum(per) / 1e12
+    line = {"impl": "reference", "metric": PREFILL_METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1e3 * statistics.mean(per), 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {**wl.describe(), "chunk": chunk},
+            "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                             "sample": f"each step: {per_step} (query row, kv head) pairs of the last chunk, the "
+                                       f"{wl.group} query heads of the kv head each, fp64 C oracle"},
+            "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 class OracleRig:
     """The CPU oracle on this workload.  Pools, scales and prefill pages are
@@ -453,8 +715,12 @@ def run_reference(args, rank, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=3000)
-    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", choices=["decode", "prefill"], default="decode",
+                    help="decode: the decode-step line (default); prefill: chunked prefill of a 128K prompt")
+    ap.add_argument("--prompt", type=int, default=131072, help="prefill: prompt tokens")
+    ap.add_argument("--chunk", type=int, default=16384, help="prefill: tokens per chunk")
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (decode 3000, prefill 10)")
+    ap.add_argument("--warmup", type=int, default=None, help="warm-up steps (decode 50, prefill 3)")
     ap.add_argument("--config", type=int, default=1)
     ap.add_argument("--page", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
@@ -468,6 +734,10 @@ def main():
     ap.add_argument("--separate", action="store_true",
                     help="time kv_append_fp8 and paged_gqa_decode as two calls instead of the fused step")
     args = ap.parse_args()
+    if args.steps is None:
+        args.steps = 3000 if args.workload == "decode" else 10
+    if args.warmup is None:
+        args.warmup = 50 if args.workload == "decode" else 3
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -477,7 +747,9 @@ def main():
             torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", 0)))
         torch.distributed.init_process_group(backend)
     try:
-        if args.impl == "reference":
+        if args.workload == "prefill":
+            (run_prefill_reference if args.impl == "reference" else run_prefill_gpu)(args, rank, world)
+        elif args.impl == "reference":
             run_reference(args, rank, world)
         else:
             run_gpu(args, rank, world)

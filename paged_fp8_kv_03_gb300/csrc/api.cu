@@ -411,6 +411,8 @@ pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, in
     a.group = group;
     a.page_size = page_size;
     a.num_pages = num_pages;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
     a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
     a.out = out;
     a.out_f32 = out_dtype == PKV_F32;

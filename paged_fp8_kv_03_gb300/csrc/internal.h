@@ -78,6 +78,7 @@ struct PrefillArgs {
     int batch, hq, hkv, group;
     int page_size;
     int64_t num_pages;
+    const uint8_t *k_cache, *v_cache;
     float sm_scale_log2;
     void *out;
     int out_f32;

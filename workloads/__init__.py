@@ -276,3 +276,18 @@ def config(i: int, page_size: int | None = None, seed: int = 0) -> Workload:
         return Workload(4, f"mixed_b64_loguniform_512_131072_p{P}", lens, 1, 64, 8, P, layers=80,
                         seed=seed, notes="log-uniform lengths, 80 layers per step")
     raise ValueError(f"no workload {i}")
+
+
+def prefill_config(page_size: int | None = None, seed: int = 0, prompt: int = 131072, chunk: int = 16384,
+                   batch: int = 1):
+    """The chunked-prefill workload: `batch` prompts of `prompt` tokens on the
+    Llama-3-70B attention geometry (64 query heads, 8 kv heads), prefilled in
+    chunks of `chunk` tokens (128K as 8 x 16K by default).  Returns
+    (workload, chunk); workload.seq_lens are the full prompt lengths."""
+    if prompt % chunk:
+        raise ValueError("the prompt must be a whole number of chunks")
+    return (Workload(10, f"prefill_llama3_70b_b{batch}_{prompt // 1024}k_as_{prompt // chunk}x{chunk // 1024}k",
+                     [prompt] * batch, 0, 64, 8, page_size or 16, seed=seed,
+                     notes="chunked prefill: each chunk is appended, then its queries attend causally"),
+            chunk)
+
