@@ -74,6 +74,22 @@ __device__ __forceinline__ uint64_t global_timer_ns()
 }
 
 // ---------------------------------------------------------------- TMA
+// 3-D tiled bulk tensor copy global -> shared without a cache policy.
+__device__ __forceinline__ void tma_load_3d_plain(uint32_t dst, const void *tmap, int x, int y, int z, uint32_t bar)
+{
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
+// Brings a tensor map into the copy engine's descriptor cache.
+__device__ __forceinline__ void prefetch_tensormap(const void *tmap)
+{
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
+}
+
 // KV pages are read once per decode step: mark them first to leave L2.
 __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {

@@ -180,22 +180,28 @@ __device__ __forceinline__ PieceMap piece_map(int lane)
 
 // FP8 rows of 32 keys (TMA 128B swizzle, rows ring_row0.. of a ring stage) ->
 // f16 operand rows kk0.. (exact).  Keys past `last` or in a piece that was not
-// loaded (mask bit of its 16-key piece clear) become zeros.
+// loaded (mask bit of its 16-key piece clear) become zeros.  All eight reads
+// are issued before any conversion, and the zeroing is a select, so the eight
+// read -> convert -> store chains overlap.
 __device__ __forceinline__ void widen32(const uint8_t *ring, uint8_t *tile, const PieceMap &pm, int ring_row0,
                                         int kk0, int key0, int last, uint32_t mask)
 {
+    uint4 v[8];
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+        const int rr = ring_row0 + pm.kr[it];
+        v[it] = *reinterpret_cast<const uint4 *>(ring + rr * 128 + ((pm.e ^ (rr & 7)) << 4));
+    }
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
         const int rr = ring_row0 + pm.kr[it];
         const int kk = kk0 + pm.kr[it];
-        uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
-        if (((mask >> (rr >> 4)) & 1u) && key0 + kk <= last) {
-            const uint4 v = *reinterpret_cast<const uint4 *>(ring + rr * 128 + ((pm.e ^ (rr & 7)) << 4));
-            e4m3x4_to_f16x4(v.x, lo.x, lo.y);
-            e4m3x4_to_f16x4(v.y, lo.z, lo.w);
-            e4m3x4_to_f16x4(v.z, hi.x, hi.y);
-            e4m3x4_to_f16x4(v.w, hi.z, hi.w);
-        }
+        const bool keep = ((mask >> (rr >> 4)) & 1u) && key0 + kk <= last;
+        uint4 lo, hi;
+        e4m3x4_to_f16x4(keep ? v[it].x : 0u, lo.x, lo.y);
+        e4m3x4_to_f16x4(keep ? v[it].y : 0u, lo.z, lo.w);
+        e4m3x4_to_f16x4(keep ? v[it].z : 0u, hi.x, hi.y);
+        e4m3x4_to_f16x4(keep ? v[it].w : 0u, hi.z, hi.w);
         uint8_t *row = tile + (pm.e >> 2) * 16384 + kk * 128;
         const int c0 = (pm.e & 3) * 2;
         *reinterpret_cast<uint4 *>(row + ((c0 ^ (kk & 7)) << 4)) = lo;
@@ -364,26 +370,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
         const int tile_off = is_v ? PS::kV16 : PS::kK16;
         const uint32_t ring = sb + PS::kF8 + cw * kStages * PS::kRing;
         const uint8_t *ring_p = smem + PS::kF8 + cw * kStages * PS::kRing;
-        const uint64_t pol = l2_policy_evict_last();     // every query tile of the sequence reads these keys
         const PieceMap pm = piece_map(lane);
 
-        // Lanes 0-3 look up the page of piece `lane` (16 keys) of a tile; -1: nothing to load.
+        // Lanes 0-3 look up the page of piece `lane` (16 keys) of a tile; -1:
+        // nothing to load.  The entry is only checked where it is used (issue),
+        // so the lookup's latency overlaps a whole tile of work.
         auto fetch_page = [&](int tile) -> int {
             int pg = -1;
             const int k = tile * kKeys + kb0 + 16 * lane;
-            if (lane < 4 && tile < nt && k <= last) {
+            if (lane < 4 && tile < nt && k <= last)
                 pg = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + k / P);
-                if (pg < 0 || pg >= a.num_pages) {
-                    if (a.err)
-                        atomicOr(a.err, PKV_DEVERR_PAGE);
-                    pg = -1;
-                }
-            }
             return pg;
         };
         // Issues the copies of a tile's pieces into its ring stage; returns the
-        // mask of pieces loaded (warp-uniform).
+        // mask of pieces loaded (warp-uniform).  An entry outside the pool sets
+        // PKV_DEVERR_PAGE and its piece reads as zeros.
         auto issue = [&](int tile, int pg) -> uint32_t {
+            const int k = tile * kKeys + kb0 + 16 * lane;
+            if (lane < 4 && tile < nt && k <= last && (pg < 0 || pg >= a.num_pages)) {
+                if (a.err)
+                    atomicOr(a.err, PKV_DEVERR_PAGE);
+                pg = -1;
+            }
             const uint32_t mask = __ballot_sync(kAll, pg >= 0) & 0xFu;
             int pgs[4];
 #pragma unroll
@@ -396,12 +404,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     if ((mask >> i) & 1u)
-                        tma_load_3d(ring + st * PS::kRing + i * 2048, tmap, 0, (tile * kKeys + kb0 + 16 * i) % P,
-                                    pgs[i] * a.hkv + h, fb8, pol);
+                        tma_load_3d_plain(ring + st * PS::kRing + i * 2048, tmap, 0,
+                                          (tile * kKeys + kb0 + 16 * i) % P, pgs[i] * a.hkv + h, fb8);
             }
             return mask;
         };
 
+        if (lane == 0)
+            prefetch_tensormap(tmap);
         uint32_t masks[kStages] = {0, 0, 0};
         int issued = 0;                                  // tiles whose copies were issued
         int pg_next = fetch_page(0);
