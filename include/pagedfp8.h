@@ -288,9 +288,11 @@ size_t pkv_decode_noalloc_scratch_bytes(void);
  *     w_t = softmax_t(s_t)                              for t <= p (causal)
  *     out[cu_q[b]+c][i][d] = sum_t w_t * E4M3(v_cache[pg(t)][h][t % P][d]) * v_scale[h]
  * with pg(t) = block_table[b][t / P].  A chunk of one query is exactly one
- * decode step.  Runs on the tcgen05 tensor cores (f16 operands: E4M3 widens
- * exactly, q is widened from bf16, softmax weights enter as two f16 parts);
- * one launch, no workspace, deterministic.
+ * decode step.  Two launches: the visible K/V of every sequence with a
+ * non-empty chunk are first widened once from the pages to f16 (exact) in the
+ * workspace, then the attention runs on the tcgen05 tensor cores (f16
+ * operands, q widened from bf16, softmax weights as two f16 parts, fp32
+ * accumulation).  Deterministic.
  *
  *   q              device bf16 [total_q][num_q_heads][head_dim] (|q| < 65504),
  *                  16-byte aligned.
@@ -298,28 +300,36 @@ size_t pkv_decode_noalloc_scratch_bytes(void);
  *                  cu_q[batch] <= total_q.
  *   total_q        rows of q and out.
  *   max_q_len      an upper bound of the chunk lengths n_b (sizes the grid).
+ *   max_kv_len     an upper bound of seq_lens (sizes the workspace).
  *   seq_lens       device int32 [batch]; a sequence with n_b > max_q_len,
- *                  seq_lens[b] < n_b or seq_lens[b] > max_pages_per_seq *
- *                  page_size, or inconsistent cu_q, sets PKV_DEVERR_SEQLEN and
- *                  its rows are not written.
+ *                  seq_lens[b] < n_b, seq_lens[b] > max_kv_len or >
+ *                  max_pages_per_seq * page_size, or inconsistent cu_q, sets
+ *                  PKV_DEVERR_SEQLEN and its rows are not written.
  *   block_table    entries of pages the chunk's positions need must lie in
  *                  [0, num_pages); others set PKV_DEVERR_PAGE and the page
  *                  reads as zeros.
  *   out            device [total_q][num_q_heads][head_dim], PKV_BF16 or
  *                  PKV_F32, 16-byte aligned.  Rows outside every chunk are
  *                  not written.
+ *   workspace      device, >= pkv_prefill_workspace_size(batch, num_kv_heads,
+ *                  max_kv_len) bytes, 256-byte aligned: the f16 copies of K
+ *                  and V (overwritten every call; must not be shared by calls
+ *                  that overlap on the GPU).
  *   Caches, scales, head_dim (128), page sizes, G (1..8), sm_scale and
  *   device_error as in pkv_paged_gqa_decode.  batch * num_kv_heads *
  *   ceil(max_q_len / (128 / G)) must be below 2^31.
  */
+size_t pkv_prefill_workspace_size(int batch, int num_kv_heads, int max_kv_len);
+
 pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, int max_q_len,
                              const uint8_t *k_cache, const uint8_t *v_cache,
                              const float *k_scale, const float *v_scale,
                              const int32_t *block_table, int max_pages_per_seq,
-                             const int32_t *seq_lens,
-                             int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                             const int32_t *seq_lens, int batch, int max_kv_len,
+                             int num_q_heads, int num_kv_heads, int head_dim,
                              int page_size, int64_t num_pages, float sm_scale,
                              void *out, int out_dtype,
+                             void *workspace, size_t workspace_bytes,
                              int32_t *device_error, cudaStream_t stream);
 
 /* Human-readable name of a status code (static string). */

@@ -74,9 +74,11 @@ def load() -> ctypes.CDLL:
                                                      i64, f32, vp, i32, vp, i32, vp]
         lib.pkv_decode_noalloc_scratch_bytes.restype = sz
         lib.pkv_decode_noalloc_scratch_bytes.argtypes = []
+        lib.pkv_prefill_workspace_size.restype = sz
+        lib.pkv_prefill_workspace_size.argtypes = [i32, i32, i32]
         lib.pkv_paged_prefill.restype = i32
         lib.pkv_paged_prefill.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
-                                          i64, ctypes.c_float, vp, i32, vp, vp]
+                                          i32, i64, ctypes.c_float, vp, i32, vp, sz, vp, vp]
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_status_string.argtypes = [i32]
         lib.pkv_version.restype = i32
@@ -338,12 +340,17 @@ def paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_len
     return out
 
 
+def pkv_prefill_workspace_size(batch, num_kv_heads, max_kv_len) -> int:
+    return int(load().pkv_prefill_workspace_size(int(batch), int(num_kv_heads), int(max_kv_len)))
+
+
 def pkv_paged_prefill(q, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, max_q_len,
-                      sm_scale=None, device_error=None, stream=None) -> None:
+                      max_kv_len, workspace, sm_scale=None, device_error=None, stream=None) -> None:
     """q bf16 [total_q, Hq, 128] (the chunks of all sequences back to back);
     cu_q int32 [B + 1] row offsets; seq_lens int32 [B] (lengths including the
     chunk); caches, scales and block_table as for decode; out [total_q, Hq,
-    128] bf16 or fp32; max_q_len an upper bound of the chunk lengths."""
+    128] bf16 or fp32; max_q_len / max_kv_len bounds of the chunk lengths and
+    of seq_lens; workspace uint8 (pkv_prefill_workspace_size bytes)."""
     _need(q, "q", torch.bfloat16, 3)
     _need(cu_q, "cu_q", torch.int32, 1)
     _need(k_cache, "k_cache", torch.uint8, 4)
@@ -353,6 +360,7 @@ def pkv_paged_prefill(q, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, 
     _need(block_table, "block_table", torch.int32, 2)
     _need(seq_lens, "seq_lens", torch.int32, 1)
     _need(out, "out", dim=3)
+    _need(workspace, "workspace", torch.uint8)
     if device_error is not None:
         _need(device_error, "device_error", torch.int32)
     T, Hq, D = q.shape
@@ -366,24 +374,33 @@ def pkv_paged_prefill(q, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, 
         sm_scale = 1.0 / math.sqrt(D)
     st = load().pkv_paged_prefill(_ptr(q), _ptr(cu_q), T, int(max_q_len), _ptr(k_cache), _ptr(v_cache),
                                   _ptr(k_scale), _ptr(v_scale), _ptr(block_table), block_table.shape[1],
-                                  _ptr(seq_lens), B, Hq, Hkv, D, P, NP, float(sm_scale), _ptr(out), _act_code(out),
-                                  _ptr(device_error), _stream(stream))
+                                  _ptr(seq_lens), B, int(max_kv_len), Hq, Hkv, D, P, NP, float(sm_scale), _ptr(out),
+                                  _act_code(out), _ptr(workspace), workspace.numel(), _ptr(device_error),
+                                  _stream(stream))
     if st != 0:
         raise PkvError(st, "pkv_paged_prefill")
 
 
 def paged_prefill(q, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, max_q_len, out=None,
-                  out_dtype=torch.bfloat16, sm_scale=None, device_error=None, stream=None) -> torch.Tensor:
+                  out_dtype=torch.bfloat16, max_kv_len=None, workspace=None, sm_scale=None, device_error=None,
+                  stream=None) -> torch.Tensor:
+    """Allocating convenience form: max_kv_len defaults to the block table's
+    capacity (max_pages x page size), the workspace to a fresh buffer."""
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    if max_kv_len is None:
+        max_kv_len = block_table.shape[1] * k_cache.shape[2]
+    if workspace is None:
+        workspace = torch.empty(pkv_prefill_workspace_size(seq_lens.shape[0], k_cache.shape[1], max_kv_len),
+                                dtype=torch.uint8, device=q.device)
     pkv_paged_prefill(q, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, max_q_len,
-                      sm_scale, device_error, stream)
+                      max_kv_len, workspace, sm_scale, device_error, stream)
     return out
 
 
 __all__ = ["load", "lib_path", "pkv_kv_append_fp8", "pkv_paged_gqa_decode", "pkv_decode_workspace_size",
            "pkv_paged_gqa_decode_noalloc", "pkv_decode_noalloc_scratch_bytes", "pkv_append_decode_fp8",
-           "append_decode_fp8", "pkv_kv_calibrate", "pkv_paged_prefill", "paged_prefill",
+           "append_decode_fp8", "pkv_kv_calibrate", "pkv_paged_prefill", "paged_prefill", "pkv_prefill_workspace_size",
            "pkv_status_string", "pkv_version", "kv_append_fp8", "paged_gqa_decode", "decode_workspace",
            "PkvError", "PKV_F32", "PKV_BF16", "DEVERR_SLOT", "DEVERR_PAGE", "DEVERR_SEQLEN",
            "DEVERR_TIMEOUT"]

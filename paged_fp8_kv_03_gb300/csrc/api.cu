@@ -75,6 +75,25 @@ bool make_q_map(CUtensorMap *tm, const void *q, int total_q, int hq, int group, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The f16 copies of K or V, [rows][kv_pad][128], as a 3-D tensor (128 dims,
+// kv_pad keys, rows = sequences x kv heads); one box = 64 dims of 128 keys,
+// 128-byte swizzled: one column block of an MMA operand tile.
+bool make_f16_kv_map(CUtensorMap *tm, const void *base, int rows, int kv_pad)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return false;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(kv_pad),
+                                static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
+                                   static_cast<cuuint64_t>(kv_pad) * kHeadDim * 2};
+    const cuuint32_t box[3] = {64u, 128u, 1u};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void *p, uintptr_t a)
 {
     return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
@@ -356,17 +375,25 @@ pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dt
                        device_error, max_ctas, stream);
 }
 
+size_t pkv_prefill_workspace_size(int batch, int num_kv_heads, int max_kv_len)
+{
+    if (batch < 0 || num_kv_heads <= 0 || max_kv_len < 0)
+        return 0;
+    return prefill_workspace_bytes(batch, num_kv_heads, max_kv_len);
+}
+
 pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, int max_q_len, const uint8_t *k_cache,
                              const uint8_t *v_cache, const float *k_scale, const float *v_scale,
                              const int32_t *block_table, int max_pages_per_seq, const int32_t *seq_lens, int batch,
-                             int num_q_heads, int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
-                             float sm_scale, void *out, int out_dtype, int32_t *device_error, cudaStream_t stream)
+                             int max_kv_len, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+                             int64_t num_pages, float sm_scale, void *out, int out_dtype, void *workspace,
+                             size_t workspace_bytes, int32_t *device_error, cudaStream_t stream)
 {
     pkv_status st = check_decode_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_seq,
                                        num_pages);
     if (st != PKV_OK)
         return st;
-    if (total_q < 0 || max_q_len < 0)
+    if (total_q < 0 || max_q_len < 0 || max_kv_len < 0)
         return PKV_ERR_SHAPE;
     if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
         return PKV_ERR_DTYPE;
@@ -385,13 +412,21 @@ pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, in
     const int64_t max_tiles = (static_cast<int64_t>(max_q_len) + tpt - 1) / tpt;
     if (static_cast<int64_t>(batch) * num_kv_heads * max_tiles >= (int64_t(1) << 31))
         return PKV_ERR_UNSUPPORTED;
+    const int64_t kv_pad = (static_cast<int64_t>(max_kv_len) + 127) / 128 * 128;
+    if (kv_pad == 0 || kv_pad >= (int64_t(1) << 31) || static_cast<int64_t>(batch) * num_kv_heads >= (int64_t(1) << 31))
+        return max_kv_len == 0 ? PKV_OK : PKV_ERR_UNSUPPORTED;
+    if (!workspace || !aligned(workspace, 256) ||
+        workspace_bytes < prefill_workspace_bytes(batch, num_kv_heads, max_kv_len))
+        return PKV_ERR_WORKSPACE;
+    __half *k16 = static_cast<__half *>(workspace);
+    __half *v16 = k16 + static_cast<size_t>(batch) * num_kv_heads * kv_pad * kHeadDim;
 
     alignas(64) CUtensorMap tm_q;
     alignas(64) CUtensorMap tm_k;
     alignas(64) CUtensorMap tm_v;
     if (!make_q_map(&tm_q, q, total_q, num_q_heads, group, tpt) ||
-        !make_page_map(&tm_k, k_cache, num_pages, num_kv_heads, page_size) ||
-        !make_page_map(&tm_v, v_cache, num_pages, num_kv_heads, page_size))
+        !make_f16_kv_map(&tm_k, k16, batch * num_kv_heads, static_cast<int>(kv_pad)) ||
+        !make_f16_kv_map(&tm_v, v16, batch * num_kv_heads, static_cast<int>(kv_pad)))
         return PKV_ERR_CUDA;
 
     PrefillArgs a;
@@ -413,6 +448,10 @@ pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, in
     a.num_pages = num_pages;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
+    a.max_kv_len = max_kv_len;
+    a.kv_pad = static_cast<int>(kv_pad);
+    a.k16 = k16;
+    a.v16 = v16;
     a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
     a.out = out;
     a.out_f32 = out_dtype == PKV_F32;

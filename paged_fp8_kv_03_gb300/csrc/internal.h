@@ -79,11 +79,21 @@ struct PrefillArgs {
     int page_size;
     int64_t num_pages;
     const uint8_t *k_cache, *v_cache;
+    int max_kv_len;                 // bound of seq_lens; the f16 copy holds kv_pad rows per (sequence, kv head)
+    int kv_pad;                     // max_kv_len rounded up to a key tile (128)
+    __half *k16, *v16;              // f16 copies [batch * hkv][kv_pad][128] (caller workspace)
     float sm_scale_log2;
     void *out;
     int out_f32;
     int32_t *err;
 };
+
+// Workspace of pkv_paged_prefill: the f16 copies of K and V.
+inline size_t prefill_workspace_bytes(int batch, int hkv, int max_kv_len)
+{
+    const size_t pad = (static_cast<size_t>(max_kv_len) + 127) / 128 * 128;
+    return 2 * static_cast<size_t>(batch) * hkv * pad * 128 * sizeof(__half);
+}
 
 // Workspace = per-segment piece ranges + the list length (rounded to 256
 // bytes), then the partial slots.
@@ -103,8 +113,8 @@ size_t decode_smem_bytes(int page_size, int batch);
 const void *decode_kernel_for(int page_size);
 int decode_num_ctas(int page_size, int batch, int max_ctas);
 size_t prefill_smem_bytes();
-cudaError_t launch_paged_prefill(const PrefillArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                                 const CUtensorMap &tm_v, cudaStream_t stream);
+cudaError_t launch_paged_prefill(const PrefillArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k16,
+                                 const CUtensorMap &tm_v16, cudaStream_t stream);
 cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                 int page_size, cudaStream_t stream);
 

@@ -10,34 +10,39 @@
 // E4M3 value x per-(kv head) scale (same guide, §3.1-§3.2).  The chunk's own
 // K/V are already in the pages (kv_append_fp8 ran first).
 //
-// Design.  One CTA per (sequence, kv head, tile of 128 / G query tokens).  The
-// tile's 128 rows are (token, query head of the group) pairs, so each K/V tile
-// brought on chip serves all G heads.  Keys are visited in tiles of 128.  One
-// role per warp:
-//   warp 0      TMA of the bf16 query tile (once, into V buffer 1 for staging);
+// Two launches.
+//   kv_widen_kernel    reads every cached token the chunk can see once from
+//                      the pages (block-table lookup) and writes it as f16
+//                      (exact) to a dense per-(sequence, kv head) copy in the
+//                      caller's workspace, zero rows up to the next 128-key
+//                      tile.  HBM-bound, about 1/1000 of the attention time.
+//   paged_prefill_kernel  one CTA per (sequence, kv head, tile of 128 / G query
+//                      tokens).  The tile's 128 rows are (token, query head of
+//                      the group) pairs, so each K/V tile brought on chip
+//                      serves all G heads.  Keys are visited in tiles of 128.
+// Widening once, instead of in every CTA that reads a tile (a key tile of a
+// 16K chunk is read by about a thousand CTAs), takes the FP8 -> f16
+// conversions off the attention kernel's critical resources (the conversion
+// pipe it shares with exp2 and the f32 -> f16 packing of P, and shared-memory
+// bandwidth), and turns 16 page-sized copies per tile into 4 tile-sized ones.
+//
+// Attention kernel roles (one per warp):
+//   warp 0      TMA: the bf16 query tile (once, into a staging slot), then per
+//               key tile two 16 KB boxes of K and two of V, already in the
+//               128B-swizzled operand layout, into 3-stage rings;
 //   warp 1      owns the 512 TMEM columns and issues tcgen05.mma (one thread):
 //                 S_j  = Q K_j^T  M 128 rows, N 128 keys, K 128 dims; A = Q held
 //                                 in TMEM, S in TMEM (2 buffers, so S_{j+1}
 //                                 overlaps softmax j)
 //                 O   += P_j V_j  A = P_j read from TMEM (f16 hi + lo parts),
 //                                 B = V_j stored N(=dim)-major
-//   warps 2-5   warps 2-3 build K tiles, warps 4-5 V tiles, 64 keys of every
-//               tile each.  A warp issues its own TMA copies of its 16-token
-//               page pieces into its own 3-stage FP8 ring (block-table entries
-//               fetched a tile ahead), then widens E4M3 -> f16 (exact) into the
-//               128B-swizzled operand tiles (one K buffer: the QK^T MMAs free
-//               it while the previous PV runs; two V buffers).
-//               Copies are issued by four warps because each issue costs the
-//               issuing thread about as long as a 2 KB copy takes to stream;
-//               K and V have their own warps so that K tiles, which the short
-//               QK^T MMAs release early, never wait behind V tiles.  These warps
-//               also widen the query rows into TMEM at the start;
-//   warps 6-13  online softmax, two warps per TMEM lane quarter: one row per
+//   warps 2-9   online softmax, two warps per TMEM lane quarter: one row per
 //               thread, each warp one half (64 keys) of the tile.  The row
 //               maximum is exchanged through shared memory; exp2 domain, lazy
 //               rescaling of O (only when the maximum grows by more than 2^8);
 //               P is written over S in TMEM; at the end each warp stores its
-//               half of O / l x v_scale.
+//               half of O / l x v_scale.  They also widen the query rows into
+//               TMEM at the start.
 // Every wait is bounded (2 s): on expiry the CTA sets PKV_DEVERR_TIMEOUT,
 // drains its own copies and MMAs, frees TMEM and exits.
 #include <mutex>
@@ -51,33 +56,32 @@ namespace {
 
 constexpr int kRows = 128;                       // M: rows of a query tile
 constexpr int kKeys = 128;                       // keys per tile
-constexpr int kConvWarps = 4;                    // warps 2 .. 5: two for K, two for V
-constexpr int kStages = 3;                       // FP8 ring depth of a widening warp
-constexpr int kSmWarp0 = 2 + kConvWarps;         // first softmax warp
+constexpr int kKStages = 3, kVStages = 3;        // f16 operand rings
+constexpr int kSmWarp0 = 2;                      // first softmax warp
 constexpr int kSmWarps = 8;
 constexpr int kPThreads = 32 * (kSmWarp0 + kSmWarps);
 constexpr uint32_t kColO = 256, kColQ = 384;     // TMEM columns: S/P 0-255, O 256-383, Q 384-447
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr unsigned kAll = 0xffffffffu;
+static_assert(kSmWarps == 8, "two softmax warps per TMEM lane quarter");
 
 // Shared memory, offsets from a 1024-byte aligned base.  Operand tiles are
 // [2 column blocks][128 rows][128 bytes] with the 128-byte swizzle.
 struct PS {
     static constexpr int kTile = 32768;
-    static constexpr int kK16 = 0;                    // 1 buffer
-    static constexpr int kV16 = kK16 + kTile;         // 2 buffers; buffer 1 first stages the bf16 query tile
-    static constexpr int kRing = 4 * 2048;            // one stage of one widening warp: 4 page pieces
-    static constexpr int kF8 = kV16 + 2 * kTile;      // [4 warps][kStages][4 pieces][16 rows][128 B]
-    static constexpr int kRedMax = kF8 + kConvWarps * kStages * kRing;   // float [2 parities][2 halves][128]
-    static constexpr int kRedL = kRedMax + 2048;      // float [2 halves][128 rows]
+    static constexpr int kK16 = 0;                    // kKStages tiles
+    static constexpr int kV16 = kK16 + kKStages * kTile;   // kVStages tiles; the last one first stages the query
+    static constexpr int kQStage = kV16 + (kVStages - 1) * kTile;
+    static constexpr int kRedMax = kV16 + kVStages * kTile;   // float [2 parities][2 halves][128 rows]
+    static constexpr int kRedL = kRedMax + 2048;              // float [2 halves][128 rows]
     static constexpr int kBars = kRedL + 1024;
     enum {
-        Q_FULL, Q_READY, K16_FULL, K16_EMPTY, V16_FULL, V16_EMPTY = V16_FULL + 2,
-        S_FULL = V16_EMPTY + 2, P_FULL = S_FULL + 2, PV_DONE = P_FULL + 2, O_FINAL, DRAIN,
+        Q_FULL, Q_READY, K_FULL, K_EMPTY = K_FULL + kKStages, V_FULL = K_EMPTY + kKStages,
+        V_EMPTY = V_FULL + kVStages, S_FULL = V_EMPTY + kVStages, P_FULL = S_FULL + 2, PV_DONE = P_FULL + 2,
+        O_FINAL, DRAIN,
         MX = DRAIN + 1,                                  // [2 tile parities][4 lane quarters]: row-max exchange
         LX = MX + 8,                                     // [4 lane quarters]: final row-sum exchange
-        F8 = LX + 4,                                     // [4 widening warps][kStages]: FP8 pieces landed
-        kNumBars = F8 + kConvWarps * kStages
+        kNumBars = LX + 4
     };
     static constexpr int kTmem = kBars + kNumBars * 8;
     static constexpr int kFlag = kTmem + 4;
@@ -85,6 +89,7 @@ struct PS {
     static constexpr size_t bytes() { return static_cast<size_t>(kEnd) + 1024; }
 };
 static_assert(PS::bytes() <= 232448, "prefill tile buffers exceed the shared memory of one CTA");
+static_assert(kVStages >= 3, "the query staging slot is V stage kVStages-1, first filled for key tile kVStages-1");
 
 // Bounded wait, one thread.  honour_abort = false for drains.
 __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int32_t *err,
@@ -137,11 +142,6 @@ __device__ __forceinline__ bool wwait(uint32_t bar, uint32_t parity, volatile in
     }
 }
 
-__device__ __forceinline__ void fence_proxy_async_smem()
-{
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
 // K-major B operand (128 keys x 128 dims, 128B swizzle), K step s of 16 dims.
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int s)
 {
@@ -153,60 +153,6 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int s)
 __device__ __forceinline__ uint64_t vmn_desc(uint32_t tile, int s)
 {
     return tc::smem_desc_sw128(tile + s * 2048, 16384, 1024);
-}
-
-// The pieces (16 FP8 bytes each) a widening lane converts for 32 keys: piece
-// `it` covers dims 16 e .. 16 e + 15 of local key row kr[it].  Each 8-lane
-// phase takes pieces 0-3 of one row and 4-7 of the next (or the other way
-// round), so its eight 16-byte reads of the TMA-swizzled FP8 rows and its
-// eight pairs of 16-byte stores into the f16 tile land on eight different bank
-// groups.
-struct PieceMap {
-    int kr[8];
-    int e;
-};
-
-__device__ __forceinline__ PieceMap piece_map(int lane)
-{
-    PieceMap pm;
-    pm.e = lane & 7;
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int c = lane + 32 * it;
-        pm.kr[it] = 2 * (c >> 4) + ((pm.e >> 2) ^ ((c >> 3) & 1));
-    }
-    return pm;
-}
-
-// FP8 rows of 32 keys (TMA 128B swizzle, rows ring_row0.. of a ring stage) ->
-// f16 operand rows kk0.. (exact).  Keys past `last` or in a piece that was not
-// loaded (mask bit of its 16-key piece clear) become zeros.  All eight reads
-// are issued before any conversion, and the zeroing is a select, so the eight
-// read -> convert -> store chains overlap.
-__device__ __forceinline__ void widen32(const uint8_t *ring, uint8_t *tile, const PieceMap &pm, int ring_row0,
-                                        int kk0, int key0, int last, uint32_t mask)
-{
-    uint4 v[8];
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int rr = ring_row0 + pm.kr[it];
-        v[it] = *reinterpret_cast<const uint4 *>(ring + rr * 128 + ((pm.e ^ (rr & 7)) << 4));
-    }
-#pragma unroll
-    for (int it = 0; it < 8; ++it) {
-        const int rr = ring_row0 + pm.kr[it];
-        const int kk = kk0 + pm.kr[it];
-        const bool keep = ((mask >> (rr >> 4)) & 1u) && key0 + kk <= last;
-        uint4 lo, hi;
-        e4m3x4_to_f16x4(keep ? v[it].x : 0u, lo.x, lo.y);
-        e4m3x4_to_f16x4(keep ? v[it].y : 0u, lo.z, lo.w);
-        e4m3x4_to_f16x4(keep ? v[it].z : 0u, hi.x, hi.y);
-        e4m3x4_to_f16x4(keep ? v[it].w : 0u, hi.z, hi.w);
-        uint8_t *row = tile + (pm.e >> 2) * 16384 + kk * 128;
-        const int c0 = (pm.e & 3) * 2;
-        *reinterpret_cast<uint4 *>(row + ((c0 ^ (kk & 7)) << 4)) = lo;
-        *reinterpret_cast<uint4 *>(row + (((c0 + 1) ^ (kk & 7)) << 4)) = hi;
-    }
 }
 
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w)
@@ -226,6 +172,70 @@ __device__ __forceinline__ void split_pair(float p0, float p1, uint32_t &hi, uin
     lo = f32x2_to_f16x2(p0 - h0, p1 - h1);
 }
 
+// Checks a sequence's sizes; false (and PKV_DEVERR_SEQLEN when `report`) when
+// the chunk or its length are inconsistent.
+__device__ __forceinline__ bool sequence_ok(const PrefillArgs &a, int q0, int q1, int L, bool report)
+{
+    const int n = q1 - q0;
+    const bool ok = q0 >= 0 && n >= 0 && q1 <= a.total_q && n <= a.max_q_len && L >= n && L <= a.max_kv_len &&
+                    static_cast<int64_t>(L) <= static_cast<int64_t>(a.max_pages) * a.page_size;
+    if (!ok && report && a.err)
+        atomicOr(a.err, PKV_DEVERR_SEQLEN);
+    return ok;
+}
+
+// ---------------------------------------------------------------------- widening
+// One thread per 16 FP8 bytes (16 dims of one key row of one kv head) of K and
+// of V: reads them through the block table and writes 32 bytes of f16 to the
+// dense copies.  Rows from L up to the next multiple of 128 are zeros.
+// Sequences with an empty or inconsistent chunk are skipped.
+__global__ void __launch_bounds__(256) kv_widen_kernel(const PrefillArgs a)
+{
+    const int64_t per_head = static_cast<int64_t>(a.kv_pad) * 8;   // pieces of one (sequence, kv head)
+    const int64_t total = static_cast<int64_t>(a.batch) * a.hkv * per_head;
+    for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < total;
+         u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t bh = u / per_head;
+        const int r = static_cast<int>((u - bh * per_head) >> 3);  // key row
+        const int e = static_cast<int>(u & 7);                      // dims 16 e .. 16 e + 15
+        const int b = static_cast<int>(bh / a.hkv);
+        const int h = static_cast<int>(bh - static_cast<int64_t>(b) * a.hkv);
+        const int q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1);
+        const int L = __ldg(a.seq_lens + b);
+        if (q1 - q0 <= 0 || !sequence_ok(a, q0, q1, L, false))
+            continue;
+        if (r >= ((L + kKeys - 1) / kKeys) * kKeys)
+            continue;
+        uint4 k = make_uint4(0, 0, 0, 0), v = make_uint4(0, 0, 0, 0);
+        if (r < L) {
+            const int pg = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + r / a.page_size);
+            if (pg >= 0 && pg < a.num_pages) {
+                const int64_t src = ((static_cast<int64_t>(pg) * a.hkv + h) * a.page_size + r % a.page_size) * kHeadDim
+                                    + 16 * e;
+                k = __ldg(reinterpret_cast<const uint4 *>(a.k_cache + src));
+                v = __ldg(reinterpret_cast<const uint4 *>(a.v_cache + src));
+            } else if (e == 0 && a.err) {
+                atomicOr(a.err, PKV_DEVERR_PAGE);
+            }
+        }
+        const int64_t dst = (bh * a.kv_pad + r) * kHeadDim + 16 * e;   // in f16 elements
+        uint4 lo, hi;
+        e4m3x4_to_f16x4(k.x, lo.x, lo.y);
+        e4m3x4_to_f16x4(k.y, lo.z, lo.w);
+        e4m3x4_to_f16x4(k.z, hi.x, hi.y);
+        e4m3x4_to_f16x4(k.w, hi.z, hi.w);
+        reinterpret_cast<uint4 *>(a.k16 + dst)[0] = lo;
+        reinterpret_cast<uint4 *>(a.k16 + dst)[1] = hi;
+        e4m3x4_to_f16x4(v.x, lo.x, lo.y);
+        e4m3x4_to_f16x4(v.y, lo.z, lo.w);
+        e4m3x4_to_f16x4(v.z, hi.x, hi.y);
+        e4m3x4_to_f16x4(v.w, hi.z, hi.w);
+        reinterpret_cast<uint4 *>(a.v16 + dst)[0] = lo;
+        reinterpret_cast<uint4 *>(a.v16 + dst)[1] = hi;
+    }
+}
+
+// ---------------------------------------------------------------------- attention
 __global__ void __launch_bounds__(kPThreads, 1)
     paged_prefill_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a)
@@ -237,16 +247,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int qt = a.max_tiles - 1 - rank;
     const int b = bh / a.hkv;
     const int h = bh - b * a.hkv;
-    const int G = a.group, tpt = a.tokens_per_tile, P = a.page_size;
+    const int G = a.group, tpt = a.tokens_per_tile;
     const int q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1);
     const int n = q1 - q0;
     const int L = __ldg(a.seq_lens + b);
-    if (q0 < 0 || n < 0 || q1 > a.total_q || n > a.max_q_len || L < n ||
-        static_cast<int64_t>(L) > static_cast<int64_t>(a.max_pages) * P) {
-        if (qt == 0 && h == 0 && threadIdx.x == 0 && a.err)
-            atomicOr(a.err, PKV_DEVERR_SEQLEN);
+    if (!sequence_ok(a, q0, q1, L, qt == 0 && h == 0 && threadIdx.x == 0))
         return;
-    }
     const int t0 = qt * tpt;                             // first token of the tile in the chunk
     if (t0 >= n)
         return;
@@ -266,12 +272,16 @@ __global__ void __launch_bounds__(kPThreads, 1)
 
     if (threadIdx.x == 0) {
         mbar_init(bar(PS::Q_FULL), 1);
-        mbar_init(bar(PS::Q_READY), kConvWarps);
-        mbar_init(bar(PS::K16_FULL), kConvWarps / 2);
-        mbar_init(bar(PS::K16_EMPTY), 1);
+        mbar_init(bar(PS::Q_READY), kSmWarps);
+        for (int i = 0; i < kKStages; ++i) {
+            mbar_init(bar(PS::K_FULL + i), 1);
+            mbar_init(bar(PS::K_EMPTY + i), 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
+            mbar_init(bar(PS::V_FULL + i), 1);
+            mbar_init(bar(PS::V_EMPTY + i), 1);
+        }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(bar(PS::V16_FULL + i), kConvWarps / 2);
-            mbar_init(bar(PS::V16_EMPTY + i), 1);
             mbar_init(bar(PS::S_FULL + i), 1);
             mbar_init(bar(PS::P_FULL + i), 32 * kSmWarps);
         }
@@ -282,8 +292,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
             mbar_init(bar(PS::MX + i), 64);
         for (int i = 0; i < 4; ++i)
             mbar_init(bar(PS::LX + i), 64);
-        for (int i = 0; i < kConvWarps * kStages; ++i)
-            mbar_init(bar(PS::F8 + i), 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -297,15 +305,53 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const uint32_t tm = *tslot;
 
     if (warp == 0) {
-        // ------------------------------------------------------------ query tile -> staging
+        // ------------------------------------------------------------ TMA: query tile, f16 K/V tiles
         if (lane == 0) {
-            const uint64_t pol = l2_policy_evict_first();
-            const uint32_t stage = sb + PS::kV16 + PS::kTile;
+            prefetch_tensormap(&tm_k);
+            prefetch_tensormap(&tm_v);
             mbar_arrive_expect_tx(bar(PS::Q_FULL), 2u * 128u * G * tpt);
-            tma_load_3d(stage, &tm_q, 0, h * G, q0 + t0, bar(PS::Q_FULL), pol);
-            tma_load_3d(stage + 16384, &tm_q, 64, h * G, q0 + t0, bar(PS::Q_FULL), pol);
-            // The copy must have landed before the CTA may leave.
+            const uint64_t pol = l2_policy_evict_first();
+            tma_load_3d(sb + PS::kQStage, &tm_q, 0, h * G, q0 + t0, bar(PS::Q_FULL), pol);
+            tma_load_3d(sb + PS::kQStage + 16384, &tm_q, 64, h * G, q0 + t0, bar(PS::Q_FULL), pol);
+            const int z = b * a.hkv + h;
+            uint32_t karmed[kKStages] = {}, varmed[kVStages] = {};
+            bool ok = true;
+            for (int t = 0; ok && t < nt; ++t) {
+                const int ks = t % kKStages, vs = t % kVStages;
+                if (t >= kKStages &&
+                    !pwait(bar(PS::K_EMPTY + ks), ((t / kKStages) - 1) & 1, abort_flag, a.err)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(PS::K_FULL + ks), PS::kTile);
+                karmed[ks] = static_cast<uint32_t>(t / kKStages) + 1;
+                tma_load_3d_plain(sb + PS::kK16 + ks * PS::kTile, &tm_k, 0, t * kKeys, z, bar(PS::K_FULL + ks));
+                tma_load_3d_plain(sb + PS::kK16 + ks * PS::kTile + 16384, &tm_k, 64, t * kKeys, z,
+                                  bar(PS::K_FULL + ks));
+                if (t >= kVStages &&
+                    !pwait(bar(PS::V_EMPTY + vs), ((t / kVStages) - 1) & 1, abort_flag, a.err)) {
+                    ok = false;
+                    break;
+                }
+                // the last V stage staged the query: the softmax warps must have widened it
+                if (t == kVStages - 1 && !pwait(bar(PS::Q_READY), 0, abort_flag, a.err)) {
+                    ok = false;
+                    break;
+                }
+                mbar_arrive_expect_tx(bar(PS::V_FULL + vs), PS::kTile);
+                varmed[vs] = static_cast<uint32_t>(t / kVStages) + 1;
+                tma_load_3d_plain(sb + PS::kV16 + vs * PS::kTile, &tm_v, 0, t * kKeys, z, bar(PS::V_FULL + vs));
+                tma_load_3d_plain(sb + PS::kV16 + vs * PS::kTile + 16384, &tm_v, 64, t * kKeys, z,
+                                  bar(PS::V_FULL + vs));
+            }
+            // No copy may still be landing when the CTA leaves.
             pwait(bar(PS::Q_FULL), 0, abort_flag, a.err, false);
+            for (int s = 0; s < kKStages; ++s)
+                if (karmed[s])
+                    pwait(bar(PS::K_FULL + s), (karmed[s] - 1) & 1, abort_flag, a.err, false);
+            for (int s = 0; s < kVStages; ++s)
+                if (varmed[s])
+                    pwait(bar(PS::V_FULL + s), (varmed[s] - 1) & 1, abort_flag, a.err, false);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
@@ -317,28 +363,28 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tc::fence_after();
             for (int j = 0; ok && j <= nt; ++j) {
                 if (j < nt) {
-                    const int fb = j & 1;
-                    if (!pwait(bar(PS::K16_FULL), j & 1, abort_flag, a.err)) {
+                    const int fb = j & 1, ks = j % kKStages;
+                    if (!pwait(bar(PS::K_FULL + ks), (j / kKStages) & 1, abort_flag, a.err)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after();
-                    const uint32_t kb = sb + PS::kK16;
+                    const uint32_t kb = sb + PS::kK16 + ks * PS::kTile;
 #pragma unroll
                     for (int s = 0; s < 8; ++s)         // Q dims 16s..16s+15: TMEM columns kColQ + 8s ..
                         tc::mma_ts(tm + fb * 128, tm + kColQ + 8 * s, kmajor_desc(kb, s), id_qk, s > 0);
                     tc::commit(bar_ptr + PS::S_FULL + fb);
-                    tc::commit(bar_ptr + PS::K16_EMPTY);
+                    tc::commit(bar_ptr + PS::K_EMPTY + ks);
                 }
                 if (j > 0) {
-                    const int i = j - 1, fb = i & 1;
+                    const int i = j - 1, fb = i & 1, vs = i % kVStages;
                     if (!pwait(bar(PS::P_FULL + fb), (i >> 1) & 1, abort_flag, a.err) ||
-                        !pwait(bar(PS::V16_FULL + fb), (i >> 1) & 1, abort_flag, a.err)) {
+                        !pwait(bar(PS::V_FULL + vs), (i / kVStages) & 1, abort_flag, a.err)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after();
-                    const uint32_t vb = sb + PS::kV16 + fb * PS::kTile;
+                    const uint32_t vb = sb + PS::kV16 + vs * PS::kTile;
                     const uint32_t p_tm = tm + fb * 128;
                     // keys 16s..16s+15: hi parts in columns 32(s/2) + 8(s%2) .. +7, lo 16 further
 #pragma unroll
@@ -349,7 +395,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     for (int s = 0; s < 8; ++s)
                         tc::mma_ts(o_tm, p_tm + 32 * (s >> 1) + 8 * (s & 1) + 16, vmn_desc(vb, s), id_pv, 1u);
                     tc::commit(bar_ptr + PS::PV_DONE);
-                    tc::commit(bar_ptr + PS::V16_EMPTY + fb);
+                    tc::commit(bar_ptr + PS::V_EMPTY + vs);
                     if (i == nt - 1)
                         tc::commit(bar_ptr + PS::O_FINAL);
                 }
@@ -358,127 +404,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tc::commit(bar_ptr + PS::DRAIN);
             pwait(bar(PS::DRAIN), 0, abort_flag, a.err, false);
         }
-    } else if (warp < kSmWarp0) {
-        // ------------------------------------------------------------ pages -> f16 operands
-        const int cw = warp - 2;
-        const bool is_v = cw >= 2;                       // warps 2-3: K, warps 4-5: V
-        const CUtensorMap *tmap = is_v ? &tm_v : &tm_k;
-        const int kb0 = 64 * (cw & 1);                   // this warp's keys kb0 .. kb0 + 63 of every tile
-        const int nbuf = is_v ? 2 : 1;                   // f16 buffers of this tensor
-        const int full_bar = is_v ? PS::V16_FULL : PS::K16_FULL;
-        const int empty_bar = is_v ? PS::V16_EMPTY : PS::K16_EMPTY;
-        const int tile_off = is_v ? PS::kV16 : PS::kK16;
-        const uint32_t ring = sb + PS::kF8 + cw * kStages * PS::kRing;
-        const uint8_t *ring_p = smem + PS::kF8 + cw * kStages * PS::kRing;
-        const PieceMap pm = piece_map(lane);
-
-        // Lanes 0-3 look up the page of piece `lane` (16 keys) of a tile; -1:
-        // nothing to load.  The entry is only checked where it is used (issue),
-        // so the lookup's latency overlaps a whole tile of work.
-        auto fetch_page = [&](int tile) -> int {
-            int pg = -1;
-            const int k = tile * kKeys + kb0 + 16 * lane;
-            if (lane < 4 && tile < nt && k <= last)
-                pg = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + k / P);
-            return pg;
-        };
-        // Issues the copies of a tile's pieces into its ring stage; returns the
-        // mask of pieces loaded (warp-uniform).  An entry outside the pool sets
-        // PKV_DEVERR_PAGE and its piece reads as zeros.
-        auto issue = [&](int tile, int pg) -> uint32_t {
-            const int k = tile * kKeys + kb0 + 16 * lane;
-            if (lane < 4 && tile < nt && k <= last && (pg < 0 || pg >= a.num_pages)) {
-                if (a.err)
-                    atomicOr(a.err, PKV_DEVERR_PAGE);
-                pg = -1;
-            }
-            const uint32_t mask = __ballot_sync(kAll, pg >= 0) & 0xFu;
-            int pgs[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                pgs[i] = __shfl_sync(kAll, pg, i);
-            if (lane == 0) {
-                const int st = tile % kStages;
-                const uint32_t fb8 = bar(PS::F8 + cw * kStages + st);
-                mbar_arrive_expect_tx(fb8, __popc(mask) * 2048u);
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if ((mask >> i) & 1u)
-                        tma_load_3d_plain(ring + st * PS::kRing + i * 2048, tmap, 0,
-                                          (tile * kKeys + kb0 + 16 * i) % P, pgs[i] * a.hkv + h, fb8);
-            }
-            return mask;
-        };
-
-        if (lane == 0)
-            prefetch_tensormap(tmap);
-        uint32_t masks[kStages] = {0, 0, 0};
-        int issued = 0;                                  // tiles whose copies were issued
-        int pg_next = fetch_page(0);
-        for (; issued < kStages - 1 && issued < nt; ++issued) {
-            masks[issued] = issue(issued, pg_next);
-            pg_next = fetch_page(issued + 1);
-        }
-
-        // The query rows: bf16 (staged by TMA, 128B-swizzled) -> f16 in TMEM
-        // columns kColQ.. (two dims per column).  Warp w reaches lanes of quarter
-        // w % 4, so warps 2-5 cover the 128 rows.
-        bool ok = wwait(bar(PS::Q_FULL), 0, abort_flag, a.err, lane);
-        if (ok) {
-            const int qrow = (warp & 3) * 32 + lane;
-            const uint8_t *stage = smem + PS::kV16 + PS::kTile;
-            const bool used = qrow < G * tpt;
-#pragma unroll
-            for (int hb = 0; hb < 2; ++hb) {            // dims 64 hb .. 64 hb + 63
-                uint32_t w[32];
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    uint4 v = make_uint4(0, 0, 0, 0);
-                    if (used)
-                        v = *reinterpret_cast<const uint4 *>(stage + hb * 16384 + qrow * 128 + ((c ^ (qrow & 7)) << 4));
-                    w[4 * c] = bf16x2_to_f16x2(v.x);
-                    w[4 * c + 1] = bf16x2_to_f16x2(v.y);
-                    w[4 * c + 2] = bf16x2_to_f16x2(v.z);
-                    w[4 * c + 3] = bf16x2_to_f16x2(v.w);
-                }
-                tc::st32(tm + (static_cast<uint32_t>((warp & 3) * 32) << 16) + kColQ + 32 * hb, w);
-            }
-            tc::wait_st();
-            tc::fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(bar(PS::Q_READY));
-        }
-        int j = 0;
-        for (; ok && j < nt; ++j) {
-            const int fb = j % nbuf, use = j / nbuf, st = j % kStages;
-            if (issued < nt) {                           // keep kStages - 1 tiles in flight
-                masks[issued % kStages] = issue(issued, pg_next);
-                ++issued;
-                pg_next = fetch_page(issued);
-            }
-            if (!wwait(bar(PS::F8 + cw * kStages + st), (j / kStages) & 1, abort_flag, a.err, lane))
-                break;
-            if (j >= nbuf && !wwait(bar(empty_bar + fb), (use - 1) & 1, abort_flag, a.err, lane))
-                break;
-            // V buffer 1 first held the staged query: all four widening warps
-            // must be done with it before it is overwritten
-            if (is_v && j == 1 && !wwait(bar(PS::Q_READY), 0, abort_flag, a.err, lane))
-                break;
-#pragma unroll
-            for (int gi = 0; gi < 2; ++gi)
-                widen32(ring_p + st * PS::kRing, smem + tile_off + fb * PS::kTile, pm, 32 * gi, kb0 + 32 * gi,
-                        j * kKeys, last, masks[st]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(bar(full_bar + fb));
-        }
-        // No copy may still be landing when the CTA leaves.
-        if (lane == 0)
-            for (int t = j; t < issued; ++t)
-                pwait(bar(PS::F8 + cw * kStages + t % kStages), (t / kStages) & 1, abort_flag, a.err, false);
-        __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + output
         const int qtr = warp & 3;                        // TMEM lane quarter of this warp
@@ -493,8 +418,32 @@ __global__ void __launch_bounds__(kPThreads, 1)
         float *red_max = reinterpret_cast<float *>(smem + PS::kRedMax);
         float *red_l = reinterpret_cast<float *>(smem + PS::kRedL);
         float m = -INFINITY, l = 0.f;
-        bool ok = true;
-        for (int j = 0; j < nt; ++j) {
+        // The query rows: bf16 (staged by TMA, 128B-swizzled) -> f16 in TMEM
+        // columns kColQ.. (two dims per column); this warp takes dims
+        // 64 half .. 64 half + 63 of its quarter's rows.
+        bool ok = wwait(bar(PS::Q_FULL), 0, abort_flag, a.err, lane);
+        if (ok) {
+            const uint8_t *stage = smem + PS::kQStage + half * 16384;
+            const bool used = row < G * tpt;
+            uint32_t w[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint4 v = make_uint4(0, 0, 0, 0);
+                if (used)
+                    v = *reinterpret_cast<const uint4 *>(stage + row * 128 + ((c ^ (row & 7)) << 4));
+                w[4 * c] = bf16x2_to_f16x2(v.x);
+                w[4 * c + 1] = bf16x2_to_f16x2(v.y);
+                w[4 * c + 2] = bf16x2_to_f16x2(v.z);
+                w[4 * c + 3] = bf16x2_to_f16x2(v.w);
+            }
+            tc::st32(lanes + kColQ + 32 * half, w);
+            tc::wait_st();
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(bar(PS::Q_READY));
+        }
+        for (int j = 0; ok && j < nt; ++j) {
             const int fb = j & 1;
             if (!wwait(bar(PS::S_FULL + fb), (j >> 1) & 1, abort_flag, a.err, lane)) {
                 ok = false;
@@ -656,8 +605,8 @@ size_t prefill_smem_bytes()
     return PS::bytes();
 }
 
-cudaError_t launch_paged_prefill(const PrefillArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k,
-                                 const CUtensorMap &tm_v, cudaStream_t stream)
+cudaError_t launch_paged_prefill(const PrefillArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k16,
+                                 const CUtensorMap &tm_v16, cudaStream_t stream)
 {
     const int64_t grid = static_cast<int64_t>(a.batch) * a.hkv * a.max_tiles;
     if (grid <= 0)
@@ -678,7 +627,14 @@ cudaError_t launch_paged_prefill(const PrefillArgs &a, const CUtensorMap &tm_q, 
             g_prefill_attr[dev] = true;
         }
     }
-    paged_prefill_kernel<<<static_cast<unsigned>(grid), kPThreads, PS::bytes(), stream>>>(tm_q, tm_k, tm_v, a);
+    const int64_t pieces = static_cast<int64_t>(a.batch) * a.hkv * a.kv_pad * 8;
+    int64_t wblocks = (pieces + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
+    if (wblocks > cap)
+        wblocks = cap;
+    if (wblocks > 0)
+        kv_widen_kernel<<<static_cast<unsigned>(wblocks), 256, 0, stream>>>(a);
+    paged_prefill_kernel<<<static_cast<unsigned>(grid), kPThreads, PS::bytes(), stream>>>(tm_q, tm_k16, tm_v16, a);
     return cudaGetLastError();
 }
 

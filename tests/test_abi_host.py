@@ -170,13 +170,14 @@ def test_prefill_argument_errors(lib):
 
     def pre(**kw):
         a = dict(q=A16, cu=A16, T=64, mq=32, kc=A16, vc=A16b, ks=A16, vs=A16, bt=A16, maxp=4, lens=A16, B=2,
-                 Hq=16, Hkv=2, D=128, P=16, np_=8, sm=0.088, out=A16, odt=1, err=None)
+                 mkv=64, Hq=16, Hkv=2, D=128, P=16, np_=8, sm=0.088, out=A16, odt=1, ws=A16, wsb=1 << 24, err=None)
         a.update(kw)
         return lib.pkv_paged_prefill(a["q"], a["cu"], a["T"], a["mq"], a["kc"], a["vc"], a["ks"], a["vs"],
-                                     a["bt"], a["maxp"], a["lens"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"],
-                                     a["np_"], a["sm"], a["out"], a["odt"], a["err"], None)
+                                     a["bt"], a["maxp"], a["lens"], a["B"], a["mkv"], a["Hq"], a["Hkv"], a["D"],
+                                     a["P"], a["np_"], a["sm"], a["out"], a["odt"], a["ws"], a["wsb"], a["err"], None)
     assert pre(T=-1) == c["PKV_ERR_SHAPE"]
     assert pre(mq=-1) == c["PKV_ERR_SHAPE"]
+    assert pre(mkv=-1) == c["PKV_ERR_SHAPE"]
     assert pre(Hq=12, Hkv=8) == c["PKV_ERR_SHAPE"]
     assert pre(maxp=0) == c["PKV_ERR_SHAPE"]
     assert pre(sm=float("nan")) == c["PKV_ERR_SHAPE"]
@@ -190,5 +191,11 @@ def test_prefill_argument_errors(lib):
     assert pre(q=ctypes.c_void_p(0x10008)) == c["PKV_ERR_ALIGN"]
     assert pre(cu=ctypes.c_void_p(0x10002)) == c["PKV_ERR_ALIGN"]
     assert pre(out=ctypes.c_void_p(0x10004)) == c["PKV_ERR_ALIGN"]
+    assert pre(ws=None) == c["PKV_ERR_WORKSPACE"]
+    assert pre(ws=ctypes.c_void_p(0x10010)) == c["PKV_ERR_WORKSPACE"]          # not 256-byte aligned
+    need = pkv.pkv_prefill_workspace_size(2, 2, 64)
+    assert need == 2 * 2 * 2 * 128 * 128 * 2                                    # K and V, kv rows padded to 128
+    assert pre(wsb=need - 1) == c["PKV_ERR_WORKSPACE"]
     assert pre(T=0, q=None, cu=None, out=None) == c["PKV_OK"]          # nothing to compute
     assert pre(mq=0, q=None, cu=None, out=None) == c["PKV_OK"]
+    assert pkv.pkv_prefill_workspace_size(-1, 2, 64) == 0

@@ -104,6 +104,28 @@ def test_one_query_chunks_equal_decode(pkv, cuda_device):
     assert d <= 2e-3, d
 
 
+def test_explicit_bounds_and_workspace(pkv, cuda_device):
+    """max_kv_len as the real bound (a tight workspace) gives the same rows
+    as the default bound; a sequence above max_kv_len is reported, not read."""
+    wl = workloads.Workload(65, "prefill", [300, 129], 0, 32, 8, 16, seed=6)
+    f = fill_gpu(wl, 0, cuda_device)
+    q = wl.q_rows(0, 100).to(cuda_device)
+    cu = torch.tensor([0, 60, 100], dtype=torch.int32, device=cuda_device)
+    ref = _prefill(pkv, f, q, cu, 60)
+    ws = torch.full((pkv.pkv_prefill_workspace_size(2, 8, 300),), 0xFF, dtype=torch.uint8, device=cuda_device)
+    out = torch.full(q.shape, float("nan"), dtype=torch.float32, device=cuda_device)
+    pkv.pkv_paged_prefill(q, cu, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, out, 60, 300, ws, device_error=f.err)
+    torch.cuda.synchronize()
+    assert int(f.err.item()) == 0
+    assert torch.equal(out, ref)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    pkv.pkv_paged_prefill(q, cu, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, out, 60, 299,
+                          torch.empty(pkv.pkv_prefill_workspace_size(2, 8, 299), dtype=torch.uint8,
+                                      device=cuda_device), device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & pkv.DEVERR_SEQLEN
+
+
 def test_error_bits(pkv, cuda_device):
     wl = workloads.Workload(63, "prefill", [50, 40], 0, 16, 2, 16, seed=4)
     f = fill_gpu(wl, 0, cuda_device)
