@@ -142,17 +142,30 @@ __device__ __forceinline__ bool wwait(uint32_t bar, uint32_t parity, volatile in
     }
 }
 
-// K-major B operand (128 keys x 128 dims, 128B swizzle), K step s of 16 dims.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int s)
+// Descriptors are built once per ring stage; a K step then only advances the
+// start-address field (bytes / 16, the low bits of the descriptor), so the
+// issuing thread spends its time issuing, not rebuilding 64-bit descriptors.
+// K-major B operand (128 keys x 128 dims, 128B swizzle): K step s of 16 dims
+// starts (s / 4) * 16 KB + (s % 4) * 32 B into the tile.
+__device__ __forceinline__ uint64_t kmajor_base(uint32_t tile)
 {
-    return tc::smem_desc_sw128(tile + (s >> 2) * 16384 + (s & 3) * 32, 16, 1024);
+    return tc::smem_desc_sw128(tile, 16, 1024);
+}
+__device__ __forceinline__ uint64_t kmajor_step(uint64_t base, int s)
+{
+    return base + static_cast<uint64_t>(((s >> 2) * 16384 + (s & 3) * 32) >> 4);
 }
 
 // V as the B operand of O += P V: rows = keys (the K dimension), 128 dims (N)
-// contiguous in two 64-dim column blocks 16 KB apart; K step s = keys 16s..16s+15.
-__device__ __forceinline__ uint64_t vmn_desc(uint32_t tile, int s)
+// contiguous in two 64-dim column blocks 16 KB apart; K step s = keys 16s..16s+15
+// starts s * 2 KB into the tile.
+__device__ __forceinline__ uint64_t vmn_base(uint32_t tile)
 {
-    return tc::smem_desc_sw128(tile + s * 2048, 16384, 1024);
+    return tc::smem_desc_sw128(tile, 16384, 1024);
+}
+__device__ __forceinline__ uint64_t vmn_step(uint64_t base, int s)
+{
+    return base + static_cast<uint64_t>((s * 2048) >> 4);
 }
 
 __device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w)
@@ -359,6 +372,13 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const uint32_t id_qk = tc::idesc_f16_f32(kRows, kKeys, false);
             const uint32_t id_pv = tc::idesc_f16_f32(kRows, kHeadDim, true);
             const uint32_t o_tm = tm + kColO;
+            uint64_t kdesc[kKStages], vdesc[kVStages];
+#pragma unroll
+            for (int i = 0; i < kKStages; ++i)
+                kdesc[i] = kmajor_base(sb + PS::kK16 + i * PS::kTile);
+#pragma unroll
+            for (int i = 0; i < kVStages; ++i)
+                vdesc[i] = vmn_base(sb + PS::kV16 + i * PS::kTile);
             bool ok = pwait(bar(PS::Q_READY), 0, abort_flag, a.err);
             tc::fence_after();
             for (int j = 0; ok && j <= nt; ++j) {
@@ -369,10 +389,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         break;
                     }
                     tc::fence_after();
-                    const uint32_t kb = sb + PS::kK16 + ks * PS::kTile;
+                    const uint64_t kd = kdesc[ks];
+                    const uint32_t s_tm = tm + fb * 128;
 #pragma unroll
                     for (int s = 0; s < 8; ++s)         // Q dims 16s..16s+15: TMEM columns kColQ + 8s ..
-                        tc::mma_ts(tm + fb * 128, tm + kColQ + 8 * s, kmajor_desc(kb, s), id_qk, s > 0);
+                        tc::mma_ts(s_tm, tm + kColQ + 8 * s, kmajor_step(kd, s), id_qk, s > 0);
                     tc::commit(bar_ptr + PS::S_FULL + fb);
                     tc::commit(bar_ptr + PS::K_EMPTY + ks);
                 }
@@ -384,16 +405,17 @@ __global__ void __launch_bounds__(kPThreads, 1)
                         break;
                     }
                     tc::fence_after();
-                    const uint32_t vb = sb + PS::kV16 + vs * PS::kTile;
+                    const uint64_t vd = vdesc[vs];
                     const uint32_t p_tm = tm + fb * 128;
+                    const uint32_t acc0 = i > 0 ? 1u : 0u;
                     // keys 16s..16s+15: hi parts in columns 32(s/2) + 8(s%2) .. +7, lo 16 further
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
-                        tc::mma_ts(o_tm, p_tm + 32 * (s >> 1) + 8 * (s & 1), vmn_desc(vb, s), id_pv,
-                                   (i > 0 || s > 0) ? 1u : 0u);
+                        tc::mma_ts(o_tm, p_tm + 32 * (s >> 1) + 8 * (s & 1), vmn_step(vd, s), id_pv,
+                                   s > 0 ? 1u : acc0);
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
-                        tc::mma_ts(o_tm, p_tm + 32 * (s >> 1) + 8 * (s & 1) + 16, vmn_desc(vb, s), id_pv, 1u);
+                        tc::mma_ts(o_tm, p_tm + 32 * (s >> 1) + 8 * (s & 1) + 16, vmn_step(vd, s), id_pv, 1u);
                     tc::commit(bar_ptr + PS::PV_DONE);
                     tc::commit(bar_ptr + PS::V_EMPTY + vs);
                     if (i == nt - 1)
