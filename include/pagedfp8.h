@@ -48,8 +48,9 @@
  * errors you want to attribute.
  *
  * Test facility: with the environment variable PKV_TEST_WITHHOLD_LOAD=<w>
- * set, decode worker warp w never loads its first page, so its first
- * pipeline wait runs out after about 2 s and the call sets
+ * set, decode worker warp w never loads its first page, and in
+ * pkv_paged_prefill the CTA of grid block w never loads its first K tile,
+ * so a pipeline wait runs out after about 2 s and the call sets
  * PKV_DEVERR_TIMEOUT (outputs undefined) -- used to test the timeout path
  * without faulting or hanging the GPU.  Unset, it has no effect.
  */

@@ -452,6 +452,10 @@ pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, in
     a.kv_pad = static_cast<int>(kv_pad);
     a.k16 = k16;
     a.v16 = v16;
+    // Test facility for the timeout path (PKV_TEST_WITHHOLD_LOAD=<block>): that
+    // CTA never loads its first K tile, so its MMA warp's wait runs out.
+    const char *hold = getenv("PKV_TEST_WITHHOLD_LOAD");
+    a.withhold_block = hold ? atoi(hold) : -1;
     a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
     a.out = out;
     a.out_f32 = out_dtype == PKV_F32;

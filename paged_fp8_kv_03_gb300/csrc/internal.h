@@ -82,6 +82,7 @@ struct PrefillArgs {
     int max_kv_len;                 // bound of seq_lens; the f16 copy holds kv_pad rows per (sequence, kv head)
     int kv_pad;                     // max_kv_len rounded up to a key tile (128)
     __half *k16, *v16;              // f16 copies [batch * hkv][kv_pad][128] (caller workspace)
+    int withhold_block;             // failure-detection test hook (-1 = off)
     float sm_scale_log2;
     void *out;
     int out_f32;

@@ -336,11 +336,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     ok = false;
                     break;
                 }
-                mbar_arrive_expect_tx(bar(PS::K_FULL + ks), PS::kTile);
-                karmed[ks] = static_cast<uint32_t>(t / kKStages) + 1;
-                tma_load_3d_plain(sb + PS::kK16 + ks * PS::kTile, &tm_k, 0, t * kKeys, z, bar(PS::K_FULL + ks));
-                tma_load_3d_plain(sb + PS::kK16 + ks * PS::kTile + 16384, &tm_k, 64, t * kKeys, z,
-                                  bar(PS::K_FULL + ks));
+                // (test facility: the withheld CTA never arms or loads its first K tile)
+                if (t > 0 || static_cast<int>(blockIdx.x) != a.withhold_block) {
+                    mbar_arrive_expect_tx(bar(PS::K_FULL + ks), PS::kTile);
+                    karmed[ks] = static_cast<uint32_t>(t / kKStages) + 1;
+                    tma_load_3d_plain(sb + PS::kK16 + ks * PS::kTile, &tm_k, 0, t * kKeys, z, bar(PS::K_FULL + ks));
+                    tma_load_3d_plain(sb + PS::kK16 + ks * PS::kTile + 16384, &tm_k, 64, t * kKeys, z,
+                                      bar(PS::K_FULL + ks));
+                }
                 if (t >= kVStages &&
                     !pwait(bar(PS::V_EMPTY + vs), ((t / kVStages) - 1) & 1, abort_flag, a.err)) {
                     ok = false;

@@ -36,3 +36,37 @@ def test_withheld_load_times_out_and_context_survives(pkv, cuda_device):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert_close(out.double().cpu().numpy(), _full_oracle(wl, f), "after timeout")
+
+
+def test_prefill_withheld_tile_times_out_and_context_survives(pkv, cuda_device):
+    """Prefill CTA 0 (the heaviest query tile) never gets its first K tile: its
+    MMA warp's wait runs out, every role drains its own copies and MMAs, TMEM
+    is freed, the call reports PKV_DEVERR_TIMEOUT, and the next call is exact."""
+    from tests.test_gpu_prefill import _oracle_pools
+    import numpy as np
+    import oracle
+    wl = workloads.Workload(71, "prefill-timeout", [400], 0, 8, 1, 16, seed=5)
+    f = fill_gpu(wl, 0, cuda_device)
+    q = wl.q_rows(0, 40)
+    cu = torch.tensor([0, 40], dtype=torch.int32, device=cuda_device)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    os.environ["PKV_TEST_WITHHOLD_LOAD"] = "0"
+    try:
+        t0 = time.time()
+        pkv.paged_prefill(q.to(cuda_device), cu, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, 40,
+                          out_dtype=torch.float32, device_error=err)
+        torch.cuda.synchronize()
+        dt = time.time() - t0
+    finally:
+        del os.environ["PKV_TEST_WITHHOLD_LOAD"]
+    assert int(err.item()) & pkv.DEVERR_TIMEOUT
+    assert 1.5 < dt < 20.0
+    err.zero_()
+    out = pkv.paged_prefill(q.to(cuda_device), cu, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, 40,
+                            out_dtype=torch.float32, device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    kco, vco, ks, vs = _oracle_pools(wl)
+    ref = oracle.paged_prefill(q.view(torch.uint16).numpy(), np.array([0, 40], np.int32), kco, vco, ks, vs,
+                               wl.block_table().numpy(), np.array(wl.seq_lens, np.int32), threads=8)
+    assert_close(out.double().cpu().numpy(), ref, "prefill after timeout")
