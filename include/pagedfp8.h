@@ -316,9 +316,12 @@ size_t pkv_decode_noalloc_scratch_bytes(void);
  *                  max_kv_len) bytes, 256-byte aligned: the f16 copies of K
  *                  and V (overwritten every call; must not be shared by calls
  *                  that overlap on the GPU).
- *   Caches, scales, head_dim (128), page sizes, G (1..8), sm_scale and
- *   device_error as in pkv_paged_gqa_decode.  batch * num_kv_heads *
- *   ceil(max_q_len / (128 / G)) must be below 2^31.
+ *   sm_scale       softmax scale, > 0 (normally 1/sqrt(head_dim)); k_scale
+ *                  entries must be positive (calibration gives absmax/448,
+ *                  floored at 1e-12).
+ *   Caches, scales, head_dim (128), page sizes, G (1..8) and device_error as
+ *   in pkv_paged_gqa_decode.  batch * num_kv_heads * ceil(max_q_len /
+ *   (128 / G)) must be below 2^31.
  */
 size_t pkv_prefill_workspace_size(int batch, int num_kv_heads, int max_kv_len);
 

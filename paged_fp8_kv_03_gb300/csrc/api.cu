@@ -397,7 +397,7 @@ pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, in
         return PKV_ERR_SHAPE;
     if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
         return PKV_ERR_DTYPE;
-    if (!(sm_scale == sm_scale) || isinf(sm_scale))
+    if (!(sm_scale > 0.f) || isinf(sm_scale))            // the kernel scales raw scores after their maximum
         return PKV_ERR_SHAPE;
     if (batch == 0 || total_q == 0 || max_q_len == 0)
         return PKV_OK;

@@ -480,42 +480,69 @@ __global__ void __launch_bounds__(kPThreads, 1)
             tc::ld32(s_tm, x[0]);
             tc::ld32(s_tm + 32, x[1]);
             tc::wait_ld();
-            // pass 1: maximum of the visible scaled logits of this half (hidden
-            // keys become -inf here, so pass 2 needs no mask), then of the row
+            // pass 1 on the raw scores (sl2 > 0): the maximum of the visible scaled
+            // logits of this half is sl2 x the maximum raw score.  Hidden keys
+            // become -inf, so pass 2 needs no mask.
             const int vis = p_row - j * kKeys - 64 * half;
             float mx[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k)
                 mx[k] = -INFINITY;
-            if (vis >= 63) {
+            if (vis < 63) {
 #pragma unroll
                 for (int c = 0; c < 2; ++c)
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const float v = __uint_as_float(x[c][k]) * sl2;
-                        x[c][k] = __float_as_uint(v);
-                        mx[k & 7] = fmaxf(mx[k & 7], v);
-                    }
-            } else {
-#pragma unroll
-                for (int c = 0; c < 2; ++c)
-#pragma unroll
-                    for (int k = 0; k < 32; ++k) {
-                        const float v = 32 * c + k <= vis ? __uint_as_float(x[c][k]) * sl2 : -INFINITY;
-                        x[c][k] = __float_as_uint(v);
-                        mx[k & 7] = fmaxf(mx[k & 7], v);
-                    }
+                    for (int k = 0; k < 32; ++k)
+                        if (32 * c + k > vis)
+                            x[c][k] = __float_as_uint(-INFINITY);
             }
+#pragma unroll
+            for (int c = 0; c < 2; ++c)
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                    mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(x[c][k]));
             const float mh = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            // exchange with the other half's warp (same lane quarter)
+                                   fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
+            // P = 2^(x sl2 - mm) <= 2^8 as f16 hi + lo, written over each 32-column
+            // piece of S (hi in its first 16 columns, lo in the last 16); returns
+            // the half row's sum of P.
+            auto emit = [&](float mm) -> float {
+                float ls[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    ls[k] = 0.f;
+#pragma unroll
+                for (int c = 0; c < 2; ++c) {
+                    uint32_t ph[16], pl[16];
+#pragma unroll
+                    for (int q = 0; q < 16; ++q) {
+                        const float p0 = ex2_approx(fmaf(__uint_as_float(x[c][2 * q]), sl2, -mm));
+                        const float p1 = ex2_approx(fmaf(__uint_as_float(x[c][2 * q + 1]), sl2, -mm));
+                        ls[(2 * q) & 7] += p0;
+                        ls[(2 * q + 1) & 7] += p1;
+                        split_pair(p0, p1, ph[q], pl[q]);
+                    }
+                    tc::st16(s_tm + 32 * c, ph);
+                    tc::st16(s_tm + 32 * c + 16, pl);
+                }
+                return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+            };
+            // Publish this half's maximum to the other half's warp (same lane
+            // quarter).  While it is in flight, compute P with the running
+            // maximum: that is the final P unless a row's maximum grows by more
+            // than 2^8 in this tile (then both warps redo it with the new one).
             red_max[(fb * 2 + half) * kRows + row] = mh;
             mbar_arrive(bar(PS::MX + fb * 4 + qtr));
+            const bool spec = j > 0 && !__any_sync(kAll, mh > m + 8.f);
+            float psum = 0.f;
+            if (spec)
+                psum = emit(m);
             if (!wwait(bar(PS::MX + fb * 4 + qtr), (j >> 1) & 1, abort_flag, a.err, lane)) {
                 ok = false;
                 break;
             }
             const float mloc = fmaxf(mh, red_max[(fb * 2 + (half ^ 1)) * kRows + row]);
+            bool redo = !spec;
             if (j == 0) {
                 m = mloc;                                  // key 0 is visible to every row
             } else {
@@ -542,29 +569,12 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     tc::wait_st();
                     l *= f;
                     m = mn;
+                    redo = true;
                 }
             }
-            // pass 2: P = 2^(x - m) <= 2^8 as f16 hi + lo, written over each
-            // 32-column piece of S (hi in its first 16 columns, lo in the last 16)
-            float ls[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                ls[k] = 0.f;
-#pragma unroll
-            for (int c = 0; c < 2; ++c) {
-                uint32_t ph[16], pl[16];
-#pragma unroll
-                for (int q = 0; q < 16; ++q) {
-                    const float p0 = ex2_approx(__uint_as_float(x[c][2 * q]) - m);
-                    const float p1 = ex2_approx(__uint_as_float(x[c][2 * q + 1]) - m);
-                    ls[(2 * q) & 7] += p0;
-                    ls[(2 * q + 1) & 7] += p1;
-                    split_pair(p0, p1, ph[q], pl[q]);
-                }
-                tc::st16(s_tm + 32 * c, ph);
-                tc::st16(s_tm + 32 * c + 16, pl);
-            }
-            l += ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+            if (redo)
+                psum = emit(m);
+            l += psum;
             tc::wait_st();
             tc::fence_before();
             mbar_arrive(bar(PS::P_FULL + fb));

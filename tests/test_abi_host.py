@@ -181,6 +181,8 @@ def test_prefill_argument_errors(lib):
     assert pre(Hq=12, Hkv=8) == c["PKV_ERR_SHAPE"]
     assert pre(maxp=0) == c["PKV_ERR_SHAPE"]
     assert pre(sm=float("nan")) == c["PKV_ERR_SHAPE"]
+    assert pre(sm=0.0) == c["PKV_ERR_SHAPE"]
+    assert pre(sm=-0.088) == c["PKV_ERR_SHAPE"]
     assert pre(odt=3) == c["PKV_ERR_DTYPE"]
     assert pre(D=64) == c["PKV_ERR_UNSUPPORTED"]
     assert pre(P=48) == c["PKV_ERR_UNSUPPORTED"]
