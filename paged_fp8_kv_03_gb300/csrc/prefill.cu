@@ -30,7 +30,10 @@
 //   warp 0      TMA: the bf16 query tile (once, into a staging slot), then per
 //               key tile two 16 KB boxes of K and two of V, already in the
 //               128B-swizzled operand layout, into 3-stage rings;
-//   warp 1      owns the 512 TMEM columns and issues tcgen05.mma (one thread):
+//   warp 1      owns the 512 TMEM columns and issues tcgen05.mma (the warp
+//               runs the loop converged, one elected lane issues; a loop run
+//               by a lone lane made every MMA issue compete with the softmax
+//               warps of its SMSP and left the tensor pipe half idle):
 //                 S_j  = Q K_j^T  M 128 rows, N 128 keys, K 128 dims; A = Q held
 //                                 in TMEM, S in TMEM (2 buffers, so S_{j+1}
 //                                 overlaps softmax j)
@@ -183,6 +186,18 @@ __device__ __forceinline__ void split_pair(float p0, float p1, uint32_t &hi, uin
     const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFFE000u);
     hi = f32x2_to_f16x2(h0, h1);
     lo = f32x2_to_f16x2(p0 - h0, p1 - h1);
+}
+
+// True in exactly one lane of the (converged) warp.
+__device__ __forceinline__ bool elect_one()
+{
+    uint32_t p;
+    asm volatile(
+        "{\n\t.reg .pred e;\n\t"
+        "elect.sync _|e, 0xffffffff;\n\t"
+        "selp.u32 %0, 1, 0, e;\n\t}"
+        : "=r"(p));
+    return p != 0;
 }
 
 // Checks a sequence's sizes; false (and PKV_DEVERR_SEQLEN when `report`) when
@@ -371,46 +386,52 @@ __global__ void __launch_bounds__(kPThreads, 1)
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issue
-        if (lane == 0) {
-            const uint32_t id_qk = tc::idesc_f16_f32(kRows, kKeys, false);
-            const uint32_t id_pv = tc::idesc_f16_f32(kRows, kHeadDim, true);
-            const uint32_t o_tm = tm + kColO;
-            uint64_t kdesc[kKStages], vdesc[kVStages];
+        // The whole warp runs this loop converged (descriptors stay warp-uniform);
+        // one elected lane issues the MMAs and the commits that track them.
+        const uint32_t id_qk = tc::idesc_f16_f32(kRows, kKeys, false);
+        const uint32_t id_pv = tc::idesc_f16_f32(kRows, kHeadDim, true);
+        const uint32_t o_tm = tm + kColO;
+        uint64_t kdesc[kKStages], vdesc[kVStages];
 #pragma unroll
-            for (int i = 0; i < kKStages; ++i)
-                kdesc[i] = kmajor_base(sb + PS::kK16 + i * PS::kTile);
+        for (int i = 0; i < kKStages; ++i)
+            kdesc[i] = kmajor_base(sb + PS::kK16 + i * PS::kTile);
 #pragma unroll
-            for (int i = 0; i < kVStages; ++i)
-                vdesc[i] = vmn_base(sb + PS::kV16 + i * PS::kTile);
-            bool ok = pwait(bar(PS::Q_READY), 0, abort_flag, a.err);
-            tc::fence_after();
-            for (int j = 0; ok && j <= nt; ++j) {
-                if (j < nt) {
-                    const int fb = j & 1, ks = j % kKStages;
-                    if (!pwait(bar(PS::K_FULL + ks), (j / kKStages) & 1, abort_flag, a.err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after();
-                    const uint64_t kd = kdesc[ks];
-                    const uint32_t s_tm = tm + fb * 128;
+        for (int i = 0; i < kVStages; ++i)
+            vdesc[i] = vmn_base(sb + PS::kV16 + i * PS::kTile);
+        const bool leader = elect_one();
+        bool ok = wwait(bar(PS::Q_READY), 0, abort_flag, a.err, lane);
+        tc::fence_after();
+        for (int j = 0; ok && j <= nt; ++j) {
+            if (j < nt) {
+                const int fb = j & 1, ks = j % kKStages;
+                if (!wwait(bar(PS::K_FULL + ks), (j / kKStages) & 1, abort_flag, a.err, lane)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after();
+                const uint64_t kd = kdesc[ks];
+                const uint32_t s_tm = tm + fb * 128;
+                if (leader) {
 #pragma unroll
                     for (int s = 0; s < 8; ++s)         // Q dims 16s..16s+15: TMEM columns kColQ + 8s ..
                         tc::mma_ts(s_tm, tm + kColQ + 8 * s, kmajor_step(kd, s), id_qk, s > 0);
                     tc::commit(bar_ptr + PS::S_FULL + fb);
                     tc::commit(bar_ptr + PS::K_EMPTY + ks);
                 }
-                if (j > 0) {
-                    const int i = j - 1, fb = i & 1, vs = i % kVStages;
-                    if (!pwait(bar(PS::P_FULL + fb), (i >> 1) & 1, abort_flag, a.err) ||
-                        !pwait(bar(PS::V_FULL + vs), (i / kVStages) & 1, abort_flag, a.err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc::fence_after();
-                    const uint64_t vd = vdesc[vs];
-                    const uint32_t p_tm = tm + fb * 128;
-                    const uint32_t acc0 = i > 0 ? 1u : 0u;
+                __syncwarp();
+            }
+            if (j > 0) {
+                const int i = j - 1, fb = i & 1, vs = i % kVStages;
+                if (!wwait(bar(PS::P_FULL + fb), (i >> 1) & 1, abort_flag, a.err, lane) ||
+                    !wwait(bar(PS::V_FULL + vs), (i / kVStages) & 1, abort_flag, a.err, lane)) {
+                    ok = false;
+                    break;
+                }
+                tc::fence_after();
+                const uint64_t vd = vdesc[vs];
+                const uint32_t p_tm = tm + fb * 128;
+                const uint32_t acc0 = i > 0 ? 1u : 0u;
+                if (leader) {
                     // keys 16s..16s+15: hi parts in columns 32(s/2) + 8(s%2) .. +7, lo 16 further
 #pragma unroll
                     for (int s = 0; s < 8; ++s)
@@ -424,11 +445,15 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     if (i == nt - 1)
                         tc::commit(bar_ptr + PS::O_FINAL);
                 }
+                __syncwarp();
             }
-            // Every MMA issued has finished before TMEM is released.
+        }
+        // Every MMA issued has finished before TMEM is released.
+        if (leader) {
             tc::commit(bar_ptr + PS::DRAIN);
             pwait(bar(PS::DRAIN), 0, abort_flag, a.err, false);
         }
+        __syncwarp();
     } else {
         // ------------------------------------------------------------ softmax + output
         const int qtr = warp & 3;                        // TMEM lane quarter of this warp
