@@ -290,13 +290,14 @@ size_t pkv_decode_noalloc_scratch_bytes(void);
  *     out[cu_q[b]+c][i][d] = sum_t w_t * E4M3(v_cache[pg(t)][h][t % P][d]) * v_scale[h]
  * with pg(t) = block_table[b][t / P].  A chunk of one query is exactly one
  * decode step.  Two launches: the visible K/V of every sequence with a
- * non-empty chunk are first widened once from the pages to f16 (exact) in the
- * workspace, then the attention runs on the tcgen05 tensor cores (f16
- * operands, q widened from bf16, softmax weights as two f16 parts, fp32
- * accumulation).  Deterministic.
+ * non-empty chunk are first widened once from the pages to 16 bits (exact: K
+ * as bf16, V as f16) in the workspace, then the attention runs on the tcgen05
+ * tensor cores (q K^T on bf16 operands; the softmax weights as two f16 parts
+ * against f16 V; fp32 accumulation, the PV accumulator added into a second
+ * fp32 accumulator every 16 key tiles).  Deterministic.
  *
- *   q              device bf16 [total_q][num_q_heads][head_dim] (|q| < 65504),
- *                  16-byte aligned.
+ *   q              device bf16 [total_q][num_q_heads][head_dim], 16-byte
+ *                  aligned.
  *   cu_q           device int32 [batch + 1], non-decreasing, cu_q[0] = 0,
  *                  cu_q[batch] <= total_q.
  *   total_q        rows of q and out.
@@ -313,9 +314,9 @@ size_t pkv_decode_noalloc_scratch_bytes(void);
  *                  PKV_F32, 16-byte aligned.  Rows outside every chunk are
  *                  not written.
  *   workspace      device, >= pkv_prefill_workspace_size(batch, num_kv_heads,
- *                  max_kv_len) bytes, 256-byte aligned: the f16 copies of K
- *                  and V (overwritten every call; must not be shared by calls
- *                  that overlap on the GPU).
+ *                  max_kv_len) bytes, 256-byte aligned: the 16-bit copies
+ *                  of K and V (overwritten every call; must not be shared by
+ *                  calls that overlap on the GPU).
  *   sm_scale       softmax scale, > 0 (normally 1/sqrt(head_dim)); k_scale
  *                  entries must be positive (calibration gives absmax/448,
  *                  floored at 1e-12).

@@ -75,10 +75,10 @@ bool make_q_map(CUtensorMap *tm, const void *q, int total_q, int hq, int group, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The f16 copies of K or V, [rows][kv_pad][128], as a 3-D tensor (128 dims,
-// kv_pad keys, rows = sequences x kv heads); one box = 64 dims of 128 keys,
-// 128-byte swizzled: one column block of an MMA operand tile.
-bool make_f16_kv_map(CUtensorMap *tm, const void *base, int rows, int kv_pad)
+// The 16-bit copies of K (bf16) or V (f16), [rows][kv_pad][128], as a 3-D
+// tensor (128 dims, kv_pad keys, rows = sequences x kv heads); one box = 64
+// dims of 128 keys, 128-byte swizzled: one column block of an MMA operand tile.
+bool make_kv16_map(CUtensorMap *tm, const void *base, int rows, int kv_pad, CUtensorMapDataType dtype)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
@@ -89,7 +89,7 @@ bool make_f16_kv_map(CUtensorMap *tm, const void *base, int rows, int kv_pad)
                                    static_cast<cuuint64_t>(kv_pad) * kHeadDim * 2};
     const cuuint32_t box[3] = {64u, 128u, 1u};
     const cuuint32_t estr[3] = {1, 1, 1};
-    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+    return fn(tm, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -425,8 +425,8 @@ pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, in
     alignas(64) CUtensorMap tm_k;
     alignas(64) CUtensorMap tm_v;
     if (!make_q_map(&tm_q, q, total_q, num_q_heads, group, tpt) ||
-        !make_f16_kv_map(&tm_k, k16, batch * num_kv_heads, static_cast<int>(kv_pad)) ||
-        !make_f16_kv_map(&tm_v, v16, batch * num_kv_heads, static_cast<int>(kv_pad)))
+        !make_kv16_map(&tm_k, k16, batch * num_kv_heads, static_cast<int>(kv_pad), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) ||
+        !make_kv16_map(&tm_v, v16, batch * num_kv_heads, static_cast<int>(kv_pad), CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
         return PKV_ERR_CUDA;
 
     PrefillArgs a;

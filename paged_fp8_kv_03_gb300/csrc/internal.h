@@ -81,7 +81,8 @@ struct PrefillArgs {
     const uint8_t *k_cache, *v_cache;
     int max_kv_len;                 // bound of seq_lens; the f16 copy holds kv_pad rows per (sequence, kv head)
     int kv_pad;                     // max_kv_len rounded up to a key tile (128)
-    __half *k16, *v16;              // f16 copies [batch * hkv][kv_pad][128] (caller workspace)
+    __half *k16, *v16;              // 16-bit copies [batch * hkv][kv_pad][128] (caller workspace):
+                                    // K as bf16 bits, V as f16, both exact widenings of E4M3
     int withhold_block;             // failure-detection test hook (-1 = off)
     float sm_scale_log2;
     void *out;

@@ -12,40 +12,44 @@
 //
 // Two launches.
 //   kv_widen_kernel    reads every cached token the chunk can see once from
-//                      the pages (block-table lookup) and writes it as f16
-//                      (exact) to a dense per-(sequence, kv head) copy in the
-//                      caller's workspace, zero rows up to the next 128-key
-//                      tile.  HBM-bound, about 1/1000 of the attention time.
+//                      the pages (block-table lookup) and writes it widened
+//                      (exactly: E4M3 has 3 mantissa bits) to dense
+//                      per-(sequence, kv head) copies in the caller's
+//                      workspace, K as bf16 and V as f16, zero rows up to the
+//                      next 128-key tile.  HBM-bound, about 1/1000 of the
+//                      attention time.
 //   paged_prefill_kernel  one CTA per (sequence, kv head, tile of 128 / G query
 //                      tokens).  The tile's 128 rows are (token, query head of
 //                      the group) pairs, so each K/V tile brought on chip
 //                      serves all G heads.  Keys are visited in tiles of 128.
 // Widening once, instead of in every CTA that reads a tile (a key tile of a
-// 16K chunk is read by about a thousand CTAs), takes the FP8 -> f16
-// conversions off the attention kernel's critical resources (the conversion
-// pipe it shares with exp2 and the f32 -> f16 packing of P, and shared-memory
-// bandwidth), and turns 16 page-sized copies per tile into 4 tile-sized ones.
+// 16K chunk is read by about a thousand CTAs), takes the FP8 conversions off
+// the attention kernel's critical resources and turns 16 page-sized copies
+// per tile into 4 tile-sized ones.
 //
 // Attention kernel roles (one per warp):
-//   warp 0      TMA: the bf16 query tile (once, into a staging slot), then per
-//               key tile two 16 KB boxes of K and two of V, already in the
-//               128B-swizzled operand layout, into 3-stage rings;
+//   warp 0      TMA: the bf16 query tile (once; it stays in shared memory as
+//               the A operand of S = Q K^T), then per key tile two 16 KB boxes
+//               of K and two of V, already in the 128B-swizzled operand
+//               layout, into 2- and 3-stage rings;
 //   warp 1      owns the 512 TMEM columns and issues tcgen05.mma (the warp
 //               runs the loop converged, one elected lane issues; a loop run
 //               by a lone lane made every MMA issue compete with the softmax
 //               warps of its SMSP and left the tensor pipe half idle):
-//                 S_j  = Q K_j^T  M 128 rows, N 128 keys, K 128 dims; A = Q held
-//                                 in TMEM, S in TMEM (2 buffers, so S_{j+1}
-//                                 overlaps softmax j)
-//                 O   += P_j V_j  A = P_j read from TMEM (f16 hi + lo parts),
-//                                 B = V_j stored N(=dim)-major
+//                 S_j   = Q K_j^T  M 128 rows, N 128 keys, K 128 dims, bf16;
+//                                  S in TMEM (2 buffers, so S_{j+1} overlaps
+//                                  softmax j)
+//                 O_seg += P_j V_j A = P_j read from TMEM (f16 hi + lo parts),
+//                                  B = V_j stored N(=dim)-major
 //   warps 2-9   online softmax, two warps per TMEM lane quarter: one row per
 //               thread, each warp one half (64 keys) of the tile.  The row
 //               maximum is exchanged through shared memory; exp2 domain, lazy
-//               rescaling of O (only when the maximum grows by more than 2^8);
-//               P is written over S in TMEM; at the end each warp stores its
-//               half of O / l x v_scale.  They also widen the query rows into
-//               TMEM at the start.
+//               rescaling (only when the maximum grows by more than 2^8);
+//               P is written over S in TMEM.  Every kFold key tiles they add
+//               O_seg into O (a second TMEM accumulator) in fp32 and the next
+//               PV starts O_seg afresh, so no chain of accumulating MMAs is
+//               longer than 16 kFold; at the end each warp stores its half of
+//               (O + O_seg) / l x v_scale.
 // Every wait is bounded (2 s): on expiry the CTA sets PKV_DEVERR_TIMEOUT,
 // drains its own copies and MMAs, frees TMEM and exits.
 #include <mutex>
@@ -59,11 +63,12 @@ namespace {
 
 constexpr int kRows = 128;                       // M: rows of a query tile
 constexpr int kKeys = 128;                       // keys per tile
-constexpr int kKStages = 3, kVStages = 3;        // f16 operand rings
+constexpr int kKStages = 2, kVStages = 3;        // operand rings: K bf16, V f16
+constexpr int kFold = 16;                        // key tiles per tensor-core accumulation segment of O
 constexpr int kSmWarp0 = 2;                      // first softmax warp
 constexpr int kSmWarps = 8;
 constexpr int kPThreads = 32 * (kSmWarp0 + kSmWarps);
-constexpr uint32_t kColO = 256, kColQ = 384;     // TMEM columns: S/P 0-255, O 256-383, Q 384-447
+constexpr uint32_t kColO = 256, kColM = 384;     // TMEM columns: S/P 0-255, O of the segment 256-383, O 384-511
 constexpr uint64_t kWaitNs = 2000000000ull;
 constexpr unsigned kAll = 0xffffffffu;
 static_assert(kSmWarps == 8, "two softmax warps per TMEM lane quarter");
@@ -72,9 +77,9 @@ static_assert(kSmWarps == 8, "two softmax warps per TMEM lane quarter");
 // [2 column blocks][128 rows][128 bytes] with the 128-byte swizzle.
 struct PS {
     static constexpr int kTile = 32768;
-    static constexpr int kK16 = 0;                    // kKStages tiles
-    static constexpr int kV16 = kK16 + kKStages * kTile;   // kVStages tiles; the last one first stages the query
-    static constexpr int kQStage = kV16 + (kVStages - 1) * kTile;
+    static constexpr int kQ = 0;                           // the query tile (bf16)
+    static constexpr int kK16 = kQ + kTile;                // kKStages tiles (bf16)
+    static constexpr int kV16 = kK16 + kKStages * kTile;   // kVStages tiles (f16)
     static constexpr int kRedMax = kV16 + kVStages * kTile;   // float [2 parities][2 halves][128 rows]
     static constexpr int kRedL = kRedMax + 2048;              // float [2 halves][128 rows]
     static constexpr int kBars = kRedL + 1024;
@@ -92,7 +97,6 @@ struct PS {
     static constexpr size_t bytes() { return static_cast<size_t>(kEnd) + 1024; }
 };
 static_assert(PS::bytes() <= 232448, "prefill tile buffers exceed the shared memory of one CTA");
-static_assert(kVStages >= 3, "the query staging slot is V stage kVStages-1, first filled for key tile kVStages-1");
 
 // Bounded wait, one thread.  honour_abort = false for drains.
 __device__ __forceinline__ bool pwait(uint32_t bar, uint32_t parity, volatile int *abort_flag, int32_t *err,
@@ -171,9 +175,12 @@ __device__ __forceinline__ uint64_t vmn_step(uint64_t base, int s)
     return base + static_cast<uint64_t>((s * 2048) >> 4);
 }
 
-__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w)
+// f16 pair -> bf16 pair (exact for widened E4M3 values: 3 mantissa bits).
+__device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h)
 {
-    return f32x2_to_f16x2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    const float2 f = f16x2_to_f32x2(h);
+    __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+    return *reinterpret_cast<uint32_t *>(&b);
 }
 
 // P = 2^(x - m) as two f16 parts: hi = x with its low 13 mantissa bits cleared
@@ -252,8 +259,10 @@ __global__ void __launch_bounds__(256) kv_widen_kernel(const PrefillArgs a)
         e4m3x4_to_f16x4(k.y, lo.z, lo.w);
         e4m3x4_to_f16x4(k.z, hi.x, hi.y);
         e4m3x4_to_f16x4(k.w, hi.z, hi.w);
-        reinterpret_cast<uint4 *>(a.k16 + dst)[0] = lo;
-        reinterpret_cast<uint4 *>(a.k16 + dst)[1] = hi;
+        reinterpret_cast<uint4 *>(a.k16 + dst)[0] =
+            make_uint4(f16x2_to_bf16x2(lo.x), f16x2_to_bf16x2(lo.y), f16x2_to_bf16x2(lo.z), f16x2_to_bf16x2(lo.w));
+        reinterpret_cast<uint4 *>(a.k16 + dst)[1] =
+            make_uint4(f16x2_to_bf16x2(hi.x), f16x2_to_bf16x2(hi.y), f16x2_to_bf16x2(hi.z), f16x2_to_bf16x2(hi.w));
         e4m3x4_to_f16x4(v.x, lo.x, lo.y);
         e4m3x4_to_f16x4(v.y, lo.z, lo.w);
         e4m3x4_to_f16x4(v.z, hi.x, hi.y);
@@ -339,8 +348,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
             prefetch_tensormap(&tm_v);
             mbar_arrive_expect_tx(bar(PS::Q_FULL), 2u * 128u * G * tpt);
             const uint64_t pol = l2_policy_evict_first();
-            tma_load_3d(sb + PS::kQStage, &tm_q, 0, h * G, q0 + t0, bar(PS::Q_FULL), pol);
-            tma_load_3d(sb + PS::kQStage + 16384, &tm_q, 64, h * G, q0 + t0, bar(PS::Q_FULL), pol);
+            tma_load_3d(sb + PS::kQ, &tm_q, 0, h * G, q0 + t0, bar(PS::Q_FULL), pol);
+            tma_load_3d(sb + PS::kQ + 16384, &tm_q, 64, h * G, q0 + t0, bar(PS::Q_FULL), pol);
             const int z = b * a.hkv + h;
             uint32_t karmed[kKStages] = {}, varmed[kVStages] = {};
             bool ok = true;
@@ -364,11 +373,6 @@ __global__ void __launch_bounds__(kPThreads, 1)
                     ok = false;
                     break;
                 }
-                // the last V stage staged the query: the softmax warps must have widened it
-                if (t == kVStages - 1 && !pwait(bar(PS::Q_READY), 0, abort_flag, a.err)) {
-                    ok = false;
-                    break;
-                }
                 mbar_arrive_expect_tx(bar(PS::V_FULL + vs), PS::kTile);
                 varmed[vs] = static_cast<uint32_t>(t / kVStages) + 1;
                 tma_load_3d_plain(sb + PS::kV16 + vs * PS::kTile, &tm_v, 0, t * kKeys, z, bar(PS::V_FULL + vs));
@@ -388,9 +392,10 @@ __global__ void __launch_bounds__(kPThreads, 1)
         // ------------------------------------------------------------ MMA issue
         // The whole warp runs this loop converged (descriptors stay warp-uniform);
         // one elected lane issues the MMAs and the commits that track them.
-        const uint32_t id_qk = tc::idesc_f16_f32(kRows, kKeys, false);
+        const uint32_t id_qk = tc::idesc_bf16_f32(kRows, kKeys, false);
         const uint32_t id_pv = tc::idesc_f16_f32(kRows, kHeadDim, true);
         const uint32_t o_tm = tm + kColO;
+        const uint64_t qdesc = kmajor_base(sb + PS::kQ);
         uint64_t kdesc[kKStages], vdesc[kVStages];
 #pragma unroll
         for (int i = 0; i < kKStages; ++i)
@@ -413,8 +418,8 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 const uint32_t s_tm = tm + fb * 128;
                 if (leader) {
 #pragma unroll
-                    for (int s = 0; s < 8; ++s)         // Q dims 16s..16s+15: TMEM columns kColQ + 8s ..
-                        tc::mma_ts(s_tm, tm + kColQ + 8 * s, kmajor_step(kd, s), id_qk, s > 0);
+                    for (int s = 0; s < 8; ++s)         // dims 16s..16s+15
+                        tc::mma_ss(s_tm, kmajor_step(qdesc, s), kmajor_step(kd, s), id_qk, s > 0);
                     tc::commit(bar_ptr + PS::S_FULL + fb);
                     tc::commit(bar_ptr + PS::K_EMPTY + ks);
                 }
@@ -430,7 +435,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 tc::fence_after();
                 const uint64_t vd = vdesc[vs];
                 const uint32_t p_tm = tm + fb * 128;
-                const uint32_t acc0 = i > 0 ? 1u : 0u;
+                const uint32_t acc0 = (i % kFold) != 0 ? 1u : 0u;   // a new segment starts from zero
                 if (leader) {
                     // keys 16s..16s+15: hi parts in columns 32(s/2) + 8(s%2) .. +7, lo 16 further
 #pragma unroll
@@ -468,27 +473,18 @@ __global__ void __launch_bounds__(kPThreads, 1)
         float *red_max = reinterpret_cast<float *>(smem + PS::kRedMax);
         float *red_l = reinterpret_cast<float *>(smem + PS::kRedL);
         float m = -INFINITY, l = 0.f;
-        // The query rows: bf16 (staged by TMA, 128B-swizzled) -> f16 in TMEM
-        // columns kColQ.. (two dims per column); this warp takes dims
-        // 64 half .. 64 half + 63 of its quarter's rows.
+        // The query tile is the A operand of S = Q K^T as TMA wrote it (bf16,
+        // 128B-swizzled, row = token x G + head).  Rows past the G x tpt the
+        // copy fills are zeroed here (this warp: its row, dims 64 half ..).
         bool ok = wwait(bar(PS::Q_FULL), 0, abort_flag, a.err, lane);
         if (ok) {
-            const uint8_t *stage = smem + PS::kQStage + half * 16384;
-            const bool used = row < G * tpt;
-            uint32_t w[32];
+            if (row >= G * tpt) {
+                uint4 *qrow = reinterpret_cast<uint4 *>(smem + PS::kQ + half * 16384 + row * 128);
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 v = make_uint4(0, 0, 0, 0);
-                if (used)
-                    v = *reinterpret_cast<const uint4 *>(stage + row * 128 + ((c ^ (row & 7)) << 4));
-                w[4 * c] = bf16x2_to_f16x2(v.x);
-                w[4 * c + 1] = bf16x2_to_f16x2(v.y);
-                w[4 * c + 2] = bf16x2_to_f16x2(v.z);
-                w[4 * c + 3] = bf16x2_to_f16x2(v.w);
+                for (int c = 0; c < 8; ++c)
+                    qrow[c] = make_uint4(0, 0, 0, 0);
             }
-            tc::st32(lanes + kColQ + 32 * half, w);
-            tc::wait_st();
-            tc::fence_before();
+            fence_proxy_async_smem();     // generic-proxy writes -> visible to the tensor cores
             __syncwarp();
             if (lane == 0)
                 mbar_arrive(bar(PS::Q_READY));
@@ -571,30 +567,57 @@ __global__ void __launch_bounds__(kPThreads, 1)
             if (j == 0) {
                 m = mloc;                                  // key 0 is visible to every row
             } else {
+                // Every kFold tiles the segment accumulator (O_seg, TMEM columns
+                // kColO..) is added into O (kColM..) in fp32 and PV_j starts a new
+                // segment: the tensor cores' accumulation rounds toward zero, and
+                // a chain of thousands of accumulating MMAs (a 128K context is
+                // 16K of them) would bias O by ~1e-3 relative.
+                const bool fold = (j % kFold) == 0;
+                const bool have_o = j > kFold;             // O holds earlier segments
                 const bool need = mloc > m + 8.f;
-                if (__any_sync(kAll, need)) {
-                    // O holds the sum up to tile j-1: wait for that PV, then rescale this half of O.
+                const bool rescale = __any_sync(kAll, need);
+                if (fold || rescale) {
+                    // O_seg holds the segment up to tile j-1: wait for that PV.
                     if (!wwait(bar(PS::PV_DONE), (j - 1) & 1, abort_flag, a.err, lane)) {
                         ok = false;
                         break;
                     }
                     tc::fence_after();
                     const float mn = need ? mloc : m;
-                    const float f = ex2_approx(m - mn);
+                    const float f = rescale ? ex2_approx(m - mn) : 1.f;
 #pragma unroll 1
-                    for (int c = 0; c < 2; ++c) {
-                        uint32_t o[32];
-                        tc::ld32(lanes + kColO + 64 * half + 32 * c, o);
+                    for (int c = 0; c < 4; ++c) {
+                        const uint32_t cs = lanes + kColO + 64 * half + 16 * c;
+                        const uint32_t cm = lanes + kColM + 64 * half + 16 * c;
+                        uint32_t o[16], t[16];
+                        tc::ld16(cs, o);
+                        if (have_o)
+                            tc::ld16(cm, t);
                         tc::wait_ld();
+                        if (fold) {                        // O = (O + O_seg) f
 #pragma unroll
-                        for (int k = 0; k < 32; ++k)
-                            o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
-                        tc::st32(lanes + kColO + 64 * half + 32 * c, o);
+                            for (int k = 0; k < 16; ++k)
+                                t[k] = __float_as_uint(((have_o ? __uint_as_float(t[k]) : 0.f) + __uint_as_float(o[k])) * f);
+                            tc::st16(cm, t);
+                        } else {                           // both in units of the old maximum
+#pragma unroll
+                            for (int k = 0; k < 16; ++k)
+                                o[k] = __float_as_uint(__uint_as_float(o[k]) * f);
+                            tc::st16(cs, o);
+                            if (have_o) {
+#pragma unroll
+                                for (int k = 0; k < 16; ++k)
+                                    t[k] = __float_as_uint(__uint_as_float(t[k]) * f);
+                                tc::st16(cm, t);
+                            }
+                        }
                     }
                     tc::wait_st();
-                    l *= f;
-                    m = mn;
-                    redo = true;
+                    if (rescale) {
+                        l *= f;
+                        m = mn;
+                        redo = true;
+                    }
                 }
             }
             if (redo)
@@ -615,30 +638,35 @@ __global__ void __launch_bounds__(kPThreads, 1)
         if (ok) {
             const float inv = __ldg(a.v_scale + h) / (l + red_l[(half ^ 1) * kRows + row]);
             const int64_t orow = (static_cast<int64_t>(q0) + t0 + tl) * a.hq + h * G + g;
+            const bool have_o = nt > kFold;                // at least one segment was folded into O
 #pragma unroll 1
-            for (int c = 0; c < 2; ++c) {
-                uint32_t o[32];
-                tc::ld32(lanes + kColO + 64 * half + 32 * c, o);
+            for (int c = 0; c < 4; ++c) {
+                uint32_t o[16], t[16];
+                tc::ld16(lanes + kColO + 64 * half + 16 * c, o);
+                if (have_o)
+                    tc::ld16(lanes + kColM + 64 * half + 16 * c, t);
                 tc::wait_ld();
                 if (!valid)
                     continue;
-                const int d0 = 64 * half + 32 * c;
+                float v[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+                    v[k] = ((have_o ? __uint_as_float(t[k]) : 0.f) + __uint_as_float(o[k])) * inv;
+                const int d0 = 64 * half + 16 * c;
                 if (a.out_f32) {
                     float4 *dst = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + orow * kHeadDim + d0);
 #pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        dst[k] = make_float4(__uint_as_float(o[4 * k]) * inv, __uint_as_float(o[4 * k + 1]) * inv,
-                                             __uint_as_float(o[4 * k + 2]) * inv, __uint_as_float(o[4 * k + 3]) * inv);
+                    for (int k = 0; k < 4; ++k)
+                        dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
                 } else {
                     uint4 *dst = reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(a.out) + orow * kHeadDim + d0);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
+                    for (int k = 0; k < 2; ++k) {
                         uint32_t w[4];
 #pragma unroll
                         for (int e = 0; e < 4; ++e) {
-                            __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(o[8 * k + 2 * e]) * inv,
-                                                                     __uint_as_float(o[8 * k + 2 * e + 1]) * inv);
-                            w[e] = *reinterpret_cast<uint32_t *>(&v);
+                            __nv_bfloat162 b2 = __floats2bfloat162_rn(v[8 * k + 2 * e], v[8 * k + 2 * e + 1]);
+                            w[e] = *reinterpret_cast<uint32_t *>(&b2);
                         }
                         dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
                     }

@@ -76,6 +76,12 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n, bool b_mn_maj
            | (static_cast<uint32_t>(m >> 4) << 24);         // M / 16
 }
 
+// The same with bf16 A and B (format code 1 in both operand fields).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, bool b_mn_major)
+{
+    return idesc_f16_f32(m, n, b_mn_major) | (1u << 7) | (1u << 10);
+}
+
 // ---------------------------------------------------------------- MMA issue
 // D[tmem] (+)= A[smem desc] * B[smem desc]^T ; accumulate = 0 overwrites D.
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
@@ -124,6 +130,17 @@ __device__ __forceinline__ void ld32(uint32_t taddr, uint32_t (&r)[32])
           "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
           "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
           "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+}
+
+// 16 consecutive columns (shape 32x32b, x16).
+__device__ __forceinline__ void ld16(uint32_t taddr, uint32_t (&r)[16])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
 }
 
