@@ -502,7 +502,7 @@ def run_prefill_gpu(args, rank, world):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "f16 tensor-core operands, f32 accumulate",
+        "dtype": "bf16 (QK^T) and f16 (PV) tensor-core operands, f32 accumulate",
         "kv_dtype": "e4m3",
         "data": "synthetic",
         "config": {**wl.describe(), "chunk": chunk, "chunks": n_chunks,
@@ -510,8 +510,8 @@ def run_prefill_gpu(args, rank, world):
                    "l2": f"inputs larger than L2 ({wl.kv_bytes() / 1e6:.0f} MB of FP8 KV and "
                          f"{wl.seq_lens[0] * wl.batch * wl.hq * 256 / 1e6:.0f} MB of queries per step)",
                    "parallelism": f"replicas x{world}"},
-        "path": "per chunk: kv_append_fp8 of its K/V, then paged_prefill (widen the visible FP8 K/V to f16 once, "
-                "then the tcgen05 attention)",
+        "path": "per chunk: kv_append_fp8 of its K/V, then paged_prefill (widen the visible FP8 K/V once, K to "
+                "bf16 and V to f16, then the tcgen05 attention)",
         "per_chunk_ms": [round(x, 3) for x in per_chunk_ms],
         "roofline": {"bound": "tensor", "kernel": "paged_prefill_kernel",
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind, "unit": "TFLOP/s",

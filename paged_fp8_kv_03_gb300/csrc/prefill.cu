@@ -278,9 +278,11 @@ __global__ void __launch_bounds__(kPThreads, 1)
                          const __grid_constant__ CUtensorMap tm_v, const PrefillArgs a)
 {
     // ---------------------------------------------------------------- the tile
-    const int bh_count = a.batch * a.hkv;
-    const int rank = blockIdx.x / bh_count;             // heaviest tiles (largest positions) first
-    const int bh = blockIdx.x - rank * bh_count;
+    // (sequence, kv head)-major order, heaviest query tiles (largest positions)
+    // first within each: the CTAs resident at one time mostly read the K/V of
+    // one kv head, so the tiles they share stay in L2.
+    const int bh = blockIdx.x / a.max_tiles;
+    const int rank = blockIdx.x - bh * a.max_tiles;
     const int qt = a.max_tiles - 1 - rank;
     const int b = bh / a.hkv;
     const int h = bh - b * a.hkv;
