@@ -100,16 +100,18 @@ class _HostStage:
 
     def __init__(self, parts):
         self.layout = []
+        host = []
         off = 0
         for name, t in parts.items():
             t = t.detach().cpu().contiguous()
             n = t.numel() * t.element_size()
             self.layout.append((name, off, t.dtype, tuple(t.shape), n))
+            host.append(t)
             off = (off + n + 255) // 256 * 256
         self.nbytes = off
         self.buf = torch.empty(off, dtype=torch.uint8).pin_memory()
-        for (name, o, dt, shape, n), t in zip(self.layout, parts.values()):
-            self.buf[o:o + n].copy_(t.detach().cpu().contiguous().view(-1).view(torch.uint8))
+        for (name, o, dt, shape, n), t in zip(self.layout, host):
+            self.buf[o:o + n].copy_(t.view(-1).view(torch.uint8))
 
         self.dbuf = None
         self.views = None
@@ -491,21 +493,44 @@ def run_prefill_gpu(args, rank, world):
     step_flops = sum(ch["flops"] for ch in st["chunks"])
 
     # ---- end to end through the public API: each chunk's q and K/V rows come
-    # from pinned host memory and its output goes back
-    host = [{"k": ch["k"].cpu().pin_memory(), "v": ch["v"].cpu().pin_memory(), "q": ch["q"].cpu().pin_memory(),
-             "slots": ch["slots"].cpu().pin_memory(), "lens": ch["lens"].cpu().pin_memory(),
-             "cu": ch["cu"].cpu().pin_memory()} for ch in st["chunks"]]
-    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for h in host for t in h.values())
+    # from pinned host memory and its output goes back.  As a serving loop
+    # would, the copies run on their own streams: chunk c+1's inputs cross
+    # while chunk c computes, chunk c-1's output while chunk c computes.
+    stage = [_HostStage({"k": ch["k"], "v": ch["v"], "q": ch["q"], "slots": ch["slots"], "lens": ch["lens"],
+                         "cu": ch["cu"]}) for ch in st["chunks"]]
+    out_host = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(n_chunks)]
+    outs = [out, torch.empty_like(out)]
+    h2d = sum(sg.nbytes for sg in stage)
     d2h = n_chunks * out.numel() * out.element_size()
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    read_done = [None] * n_chunks      # compute finished with chunk c's staged inputs
+    out_free = [None, None]            # output buffer's copy to the host finished
 
     def e2e_step():
-        for h in host:
-            d = {k: v.to(dev, non_blocking=True) for k, v in h.items()}
-            pkv.kv_append_fp8(d["k"], d["v"], d["slots"], st["ks"], st["vs"], st["kc"], st["vc"])
-            o = pkv.paged_prefill(d["q"], d["cu"], st["kc"], st["vc"], st["ks"], st["vs"], st["bt"], d["lens"],
-                                  chunk, max_kv_len=max_kv, workspace=ws)
-            out_host.copy_(o, non_blocking=True)
+        for c in range(n_chunks):
+            with torch.cuda.stream(s_in):
+                if read_done[c] is not None:
+                    s_in.wait_event(read_done[c])
+                d = stage[c].upload(dev)
+                ready = torch.cuda.Event()
+                ready.record(s_in)
+            stream.wait_event(ready)
+            ob = outs[c % 2]
+            if out_free[c % 2] is not None:
+                stream.wait_event(out_free[c % 2])
+            pkv.pkv_kv_append_fp8(d["k"], d["v"], d["slots"], st["ks"], st["vs"], st["kc"], st["vc"], err)
+            pkv.pkv_paged_prefill(d["q"], d["cu"], st["kc"], st["vc"], st["ks"], st["vs"], st["bt"], d["lens"],
+                                  ob, chunk, max_kv, ws, device_error=err)
+            done = torch.cuda.Event()
+            done.record(stream)
+            read_done[c] = done
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done)
+                out_host[c].copy_(ob, non_blocking=True)
+                freed = torch.cuda.Event()
+                freed.record(s_out)
+            out_free[c % 2] = freed
 
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
     e2e_step()
@@ -513,11 +538,14 @@ def run_prefill_gpu(args, rank, world):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    s_in.wait_event(e0)                                # no copy starts before the timed region
     for _ in range(e2e_steps):
         e2e_step()
+    stream.wait_event(out_free[(n_chunks - 1) % 2])    # the last output is on the host
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    assert int(err.item()) == 0, f"device error word {int(err.item())} (end-to-end steps)"
 
     ms_per_step = total_ms / args.steps
     peak, peak_kind = _tensor_peak()
