@@ -204,3 +204,79 @@ def test_full_size_last_16k_chunk_of_128k_sampled(pkv, cuda_device):
     max_abs, _ = errors(np.stack([got[r, i] for (r, i) in ref]), np.stack(list(ref.values())))
     assert max_abs <= 3e-4, max_abs
     assert torch.isfinite(out).all()
+
+
+def test_maximum_jumps_at_fold_tiles(pkv, cuda_device):
+    """The running maximum of every row jumps by more than 2^8 (log2 units) at
+    key tiles 16 and 32, where the segment accumulator is also folded into O
+    (fold and rescale in one step), and at tile 40, between folds (both
+    accumulators rescaled).  Only 8 keys carry each jump, so the earlier keys
+    keep a visible share of the softmax and a wrong factor on either
+    accumulator would show.  Rows of the chunk sit before, between and after
+    the jumps; a second, short sequence makes the batch ragged."""
+    Hq, Hkv, D, P = 16, 2, 128, 16
+    lens, chunks = [6221, 300], [3200, 40]
+    g = torch.Generator().manual_seed(77)
+    K = [torch.randn(L, Hkv, D, generator=g) for L in lens]
+    V = [torch.randn(L, Hkv, D, generator=g) for L in lens]
+    # q . k / sqrt(D) is ~ K[t, h, 0] / sqrt(D): 0 for every key but the jumps
+    # (E4M3 codes 144, 288, 448 of the scale absmax/448: about 9.8, 19.7 and
+    # 30.6 in log2 units)
+    K[0][:, :, 0] = 0.0
+    for t0, val in [(2048, 80.0), (4096, 160.0), (5120, 240.0)]:
+        K[0][t0:t0 + 8, :, 0] = val
+    ks = torch.clamp(torch.stack([k.abs().amax(dim=(0, 2)) for k in K]).amax(0) / 448.0, min=1e-12).float()
+    vs = torch.clamp(torch.stack([v.abs().amax(dim=(0, 2)) for v in V]).amax(0) / 448.0, min=1e-12).float()
+    pages = [(L + P - 1) // P for L in lens]
+    num_pages = sum(pages) + 3
+    perm = torch.randperm(num_pages, generator=g).to(torch.int32)
+    bt = torch.zeros(len(lens), max(pages), dtype=torch.int32)
+    o = 0
+    for b, n in enumerate(pages):
+        bt[b, :n] = perm[o:o + n]
+        o += n
+    slots = [bt[b].to(torch.int64)[torch.arange(L) // P] * P + torch.arange(L) % P for b, L in enumerate(lens)]
+    T = sum(chunks)
+    q = torch.zeros(T, Hq, D)
+    q[:, :, 0] = 1.0
+    q[:, :, 1:] = 0.01 * torch.randn(T, Hq, D - 1, generator=g)
+    q = q.to(torch.bfloat16)
+    cu = np.array([0, chunks[0], T], np.int32)
+
+    dev = cuda_device
+    kc = torch.zeros(num_pages, Hkv, P, D, dtype=torch.uint8, device=dev)
+    vc = torch.zeros_like(kc)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    for b in range(len(lens)):
+        pkv.kv_append_fp8(K[b].to(dev), V[b].to(dev), slots[b].to(dev), ks.to(dev), vs.to(dev), kc, vc, err)
+    lens_d = torch.tensor(lens, dtype=torch.int32, device=dev)
+    out = torch.full((T, Hq, D), float("nan"), dtype=torch.float32, device=dev)
+    pkv.paged_prefill(q.to(dev), torch.from_numpy(cu).to(dev), kc, vc, ks.to(dev), vs.to(dev), bt.to(dev), lens_d,
+                      max(chunks), out=out, device_error=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+
+    kco = np.zeros((num_pages, Hkv, P, D), np.uint8)
+    vco = np.zeros_like(kco)
+    for b in range(len(lens)):
+        oracle.kv_append(K[b].numpy(), slots[b].numpy(), ks.numpy(), kco)
+        oracle.kv_append(V[b].numpy(), slots[b].numpy(), vs.numpy(), vco)
+    assert np.array_equal(kc.cpu().numpy(), kco) and np.array_equal(vc.cpu().numpy(), vco)
+    got = out.double().cpu().numpy()
+    assert np.isfinite(got).all()
+    # Sampled rows, each through the decode oracle at its own causal length:
+    # the long chunk covers positions 3021 .. 6220, so rows sit before, on
+    # and after the jumps at 4096 and 5120; every row of the short sequence.
+    q_bits = q.view(torch.uint16).numpy()
+    rng = np.random.default_rng(3)
+    pos = [3021, 3500, 4095, 4096, 4103, 4104, 4500, 5119, 5120, 5127, 5128, 6000, 6220]
+    rows = [(0, p_ - (lens[0] - chunks[0])) for p_ in pos] + [(0, int(r)) for r in rng.integers(0, chunks[0], 8)]
+    rows += [(1, chunks[0] + c) for c in range(chunks[1])]
+    exp, act = [], []
+    for b, r in rows:
+        p_ = lens[b] - chunks[b] + (r - int(cu[b]))
+        ref = oracle.paged_decode(np.ascontiguousarray(q_bits[r:r + 1]), kco, vco, ks.numpy(), vs.numpy(),
+                                  bt[b:b + 1].numpy(), np.array([p_ + 1], np.int32), threads=8)
+        exp.append(ref.reshape(Hq, D))         # rows (0, head 0 .. Hq-1)
+        act.append(got[r])
+    assert_close(np.stack(act), np.stack(exp), "maximum jumps at fold tiles")
