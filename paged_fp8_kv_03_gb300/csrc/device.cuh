@@ -58,21 +58,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
-// As mbar_try_wait, but the thread may sleep up to `ns` nanoseconds waiting for
-// the phase instead of returning at once (it wakes when the phase completes).
-__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t ns)
-{
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity), "r"(ns)
-        : "memory");
-    return ok != 0;
-}
-
 __device__ __forceinline__ uint64_t global_timer_ns()
 {
     uint64_t t;
@@ -102,15 +87,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first()
 {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-
-// Data that many CTAs read again (a sequence's KV prefix under prefill): keep
-// it in L2 ahead of streaming data.
-__device__ __forceinline__ uint64_t l2_policy_evict_last()
-{
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 
@@ -194,12 +170,6 @@ __device__ __forceinline__ uint32_t f32x2_to_f16x2(float lo, float hi)
 __device__ __forceinline__ float2 f16x2_to_f32x2(uint32_t v)
 {
     return __half22float2(*reinterpret_cast<__half2 *>(&v));
-}
-
-// ---------------------------------------------------------------- barriers
-__device__ __forceinline__ void named_barrier(int id, int threads)
-{
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 }  // namespace pkv

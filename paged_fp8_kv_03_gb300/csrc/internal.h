@@ -79,7 +79,7 @@ struct PrefillArgs {
     int page_size;
     int64_t num_pages;
     const uint8_t *k_cache, *v_cache;
-    int max_kv_len;                 // bound of seq_lens; the f16 copy holds kv_pad rows per (sequence, kv head)
+    int max_kv_len;                 // bound of seq_lens; the 16-bit copies hold kv_pad rows per (sequence, kv head)
     int kv_pad;                     // max_kv_len rounded up to a key tile (128)
     __half *k16, *v16;              // 16-bit copies [batch * hkv][kv_pad][128] (caller workspace):
                                     // K as bf16 bits, V as f16, both exact widenings of E4M3
@@ -90,7 +90,7 @@ struct PrefillArgs {
     int32_t *err;
 };
 
-// Workspace of pkv_paged_prefill: the f16 copies of K and V.
+// Workspace of pkv_paged_prefill: the 16-bit copies of K (bf16) and V (f16).
 inline size_t prefill_workspace_bytes(int batch, int hkv, int max_kv_len)
 {
     const size_t pad = (static_cast<size_t>(max_kv_len) + 127) / 128 * 128;
