@@ -731,7 +731,7 @@ def cpu_baseline(wl, budget_s: float, scale_device="cpu") -> dict:
     threads = len(os.sched_getaffinity(0))
     rig = OracleRig(wl, scale_device)
     done, secs, nbytes, i = 0, 0.0, 0, 0
-    while secs < budget_s and (i < 4 * wl.batch):
+    while secs < budget_s and i < 256 * wl.batch:       # the time budget decides; the count only bounds it
         b = i % wl.batch
         dt, nb = rig.step([b], threads)
         done += 1
