@@ -152,8 +152,9 @@ __device__ __forceinline__ bool wwait(uint32_t bar, uint32_t parity, volatile in
 // Descriptors are built once per ring stage; a K step then only advances the
 // start-address field (bytes / 16, the low bits of the descriptor), so the
 // issuing thread spends its time issuing, not rebuilding 64-bit descriptors.
-// K-major B operand (128 keys x 128 dims, 128B swizzle): K step s of 16 dims
-// starts (s / 4) * 16 KB + (s % 4) * 32 B into the tile.
+// K-major operand (128 rows x 128 dims, 128B swizzle; the query tile as A and
+// a K tile as B of S = Q K^T): K step s of 16 dims starts (s / 4) * 16 KB +
+// (s % 4) * 32 B into the tile.
 __device__ __forceinline__ uint64_t kmajor_base(uint32_t tile)
 {
     return tc::smem_desc_sw128(tile, 16, 1024);
@@ -183,7 +184,7 @@ __device__ __forceinline__ uint32_t f16x2_to_bf16x2(uint32_t h)
     return *reinterpret_cast<uint32_t *>(&b);
 }
 
-// P = 2^(x - m) as two f16 parts: hi = x with its low 13 mantissa bits cleared
+// P = 2^(x - m) as two f16 parts: hi = P with its low 13 mantissa bits cleared
 // (exact in f16 for P >= 2^-14), lo = the rest (exact in fp32, rounded to f16).
 // hi + lo equals P to about 2^-22 relative; below 2^-14 the parts keep an
 // absolute error under 2^-24.
