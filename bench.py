@@ -15,7 +15,7 @@ with --separate kv_append_fp8 followed by paged_gqa_decode.  Prints ONE JSON lin
              HBM copy bandwidth
   cpu_baseline  the CPU oracle on a bounded sample of the same workload
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 1] [--page 16]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 4] [--page 16]
     python bench.py --impl reference ...      # the oracle as the reference arm
     python bench.py --workload prefill        # chunked prefill: a 128K prompt as 8 x 16K
                                               # chunks (append + causal attention each),
@@ -227,7 +227,7 @@ def run_gpu(args, rank, world):
     kv_bytes = wl.kv_bytes()
     # distinct layer caches rotated step by step so a step never finds the
     # previous step's KV in L2 (each cache alone is already larger than L2)
-    n_layers = max(1, args.rotate or int(math.ceil(3 * L2_BYTES / kv_bytes)))
+    n_layers = max(1, args.rotate or max(2, int(math.ceil(3 * L2_BYTES / kv_bytes))))
     free, _ = torch.cuda.mem_get_info(dev)
     n_layers = max(1, min(n_layers, int(0.8 * free // (kv_bytes + (1 << 20)))))
     layers = [_fill_layer(pkv, wl, l, dev) for l in range(n_layers)]
@@ -260,11 +260,15 @@ def run_gpu(args, rank, world):
             if evs is not None:
                 evs[l][1].record(stream)
 
-    for i in range(args.warmup):
-        step(i)
-    torch.cuda.synchronize()
+    # nvidia-smi starts sampling before the warm-up, so no pause separates the
+    # warm-up from the timed steps
+    clocks = ClockSampler(dev.index)
+    if rank == 0:
+        clocks.start()
     graphs = None
     if args.graph:
+        step(0)                 # first calls (library set-up) happen outside the capture
+        torch.cuda.synchronize()
         # One graph per distinct layer-cache phase; each replays a whole step.
         n_phase = n_layers // math.gcd(n_layers, per_step)
         graphs = []
@@ -275,16 +279,22 @@ def run_gpu(args, rank, world):
             graphs.append(g)
         torch.cuda.synchronize()
         stream = torch.cuda.current_stream(dev)
-    clocks = ClockSampler(dev.index)
-    if rank == 0:
-        clocks.start()
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
     evs = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(per_step)]
            for _ in range(args.steps)]
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    for i in range(args.warmup):
+        if graphs is None:
+            step(i)
+        else:
+            graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    h0 = time.perf_counter()
     t_start.record(stream)
     for i in range(args.steps):
         if graphs is None:
@@ -294,6 +304,7 @@ def run_gpu(args, rank, world):
             graphs[i % len(graphs)].replay()
             evs[i][-1][1].record(stream)
     t_end.record(stream)
+    host_s = time.perf_counter() - h0        # host time to enqueue the timed steps
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -308,24 +319,28 @@ def run_gpu(args, rank, world):
 
     # ---- end to end through the public API with host buffers
     e2e_steps = min(args.steps, args.e2e_steps)
-    # A layer pass's inputs are staged back to back (256-byte aligned) in one
-    # pinned buffer and cross with one copy, as a serving loop would stage them.
+    # The step's block table and lengths cross once per step; each layer
+    # pass's own inputs (q and the new K/V rows) are staged back to back
+    # (256-byte aligned) in one pinned buffer and cross with one copy, as a
+    # serving loop would stage them.
+    seq_stage = _HostStage({"bt": bt, "lens": lens})
     host = []
     for l in range(n_layers):
         s = steps_in[l]
-        parts = {"q": s["q"], "bt": bt, "lens": lens}
+        parts = {"q": s["q"]}
         if s["k_new"] is not None:
             parts.update(k_new=s["k_new"], v_new=s["v_new"], slots=s["slots"])
         host.append(_HostStage(parts))
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    h2d = per_step * host[0].nbytes
+    h2d = seq_stage.nbytes + per_step * host[0].nbytes
     d2h = per_step * out.numel() * out.element_size()
 
     def e2e_step(i):
+        sq = seq_stage.upload(dev)
         for l in range(per_step):
             g = i * per_step + l
             c = layers[g % n_layers]
-            d = host[g % n_layers].upload(dev)
+            d = dict(host[g % n_layers].upload(dev), **sq)
             if "k_new" in d and args.separate:
                 pkv.pkv_kv_append_fp8(d["k_new"].flatten(0, 1), d["v_new"].flatten(0, 1), d["slots"], c["ks"],
                                       c["vs"], c["kc"], c["vc"], err)
@@ -391,10 +406,11 @@ def run_gpu(args, rank, world):
         "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
+        "host_us_per_call": round(1e6 * host_s / (args.steps * (1 if graphs is not None else per_step)), 2),
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, scale_device=dev)
+        line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, gen_device=dev)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
@@ -465,12 +481,12 @@ def run_prefill_gpu(args, rank, world):
             if evs is not None:
                 evs[c][1].record(stream)
 
-    for _ in range(args.warmup):
-        step()
-    torch.cuda.synchronize()
     clocks = ClockSampler(dev.index)
     if rank == 0:
         clocks.start()
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -676,16 +692,31 @@ def run_prefill_reference(args, rank, world):
 
 
 # ----------------------------------------------------------------------------- CPU oracle
+def sample_sequences(wl, max_tokens: int = 131072) -> list:
+    """The sequences the CPU oracle samples: the first ones in index order
+    while their lengths add up to at most max_tokens (at least one), so that
+    preparing their pages stays bounded on the mixed 512..128K batch."""
+    seqs, tot = [], 0
+    for b, L in enumerate(wl.seq_lens):
+        if seqs and tot + L > max_tokens:
+            break
+        seqs.append(b)
+        tot += L
+    return seqs
+
+
 class OracleRig:
     """The CPU oracle on this workload.  Pools, scales and prefill pages are
-    prepared once from host-generated inputs (untimed); step() times the
-    oracle's append of the step's tokens and its decode of whole sequences."""
+    prepared once from generated inputs (untimed; generation on gen_device,
+    whose values are bit-identical to the host's); step() times the oracle's
+    append of the step's tokens and its decode of whole sequences."""
 
-    def __init__(self, wl, scale_device="cpu"):
+    def __init__(self, wl, gen_device="cpu"):
         import oracle
         self.oracle = oracle
         self.wl = wl
-        ks, vs = wl.scales(0, device=scale_device)
+        self.gen = gen_device
+        ks, vs = wl.scales(0, device=gen_device)
         self.ks, self.vs = ks.cpu().numpy(), vs.cpu().numpy()
         shape = (wl.num_pages, wl.hkv, wl.page_size, wl.head_dim)
         self.kc = np.zeros(shape, np.uint8)
@@ -695,13 +726,19 @@ class OracleRig:
         self.lens = np.array(wl.seq_lens, np.int32)
         self.filled = set()
 
+    def _rows(self, which, b, t0, t1):
+        return self.wl.kv_rows(0, which, b, t0, t1, device=self.gen).cpu().numpy()
+
     def fill(self, b):
         if b in self.filled:
             return
         wl, L = self.wl, self.wl.prefill_lens[b]
         sl = wl.slots(b, 0, L).numpy()
-        self.oracle.kv_append(wl.kv_rows(0, 0, b, 0, L).numpy(), sl, self.ks, self.kc)
-        self.oracle.kv_append(wl.kv_rows(0, 1, b, 0, L).numpy(), sl, self.vs, self.vc)
+        step = 1 << 15
+        for t0 in range(0, L, step):
+            t1 = min(L, t0 + step)
+            self.oracle.kv_append(self._rows(0, b, t0, t1), sl[t0:t1], self.ks, self.kc)
+            self.oracle.kv_append(self._rows(1, b, t0, t1), sl[t0:t1], self.vs, self.vc)
         self.filled.add(b)
 
     def step(self, seqs, threads, n_kv_heads=None):
@@ -712,8 +749,7 @@ class OracleRig:
         hk = wl.hkv if n_kv_heads is None else max(1, min(wl.hkv, n_kv_heads))
         for b in seqs:
             self.fill(b)
-        new = [(wl.kv_rows(0, 0, b, wl.prefill_lens[b], wl.seq_lens[b]).numpy(),
-                wl.kv_rows(0, 1, b, wl.prefill_lens[b], wl.seq_lens[b]).numpy(),
+        new = [(self._rows(0, b, wl.prefill_lens[b], wl.seq_lens[b]), self._rows(1, b, wl.prefill_lens[b], wl.seq_lens[b]),
                 wl.slots(b, wl.prefill_lens[b], wl.seq_lens[b]).numpy()) for b in seqs]
         sel = np.array([[b, i] for b in seqs for i in range(hk * wl.group)], np.int32)
         t0 = time.perf_counter()
@@ -727,20 +763,22 @@ class OracleRig:
         return dt, sum(wl.seq_lens[b] for b in seqs) * hk * 2 * wl.head_dim
 
 
-def cpu_baseline(wl, budget_s: float, scale_device="cpu") -> dict:
+def cpu_baseline(wl, budget_s: float, gen_device="cpu") -> dict:
     threads = len(os.sched_getaffinity(0))
-    rig = OracleRig(wl, scale_device)
+    rig = OracleRig(wl, gen_device)
+    seqs = sample_sequences(wl)
     done, secs, nbytes, i = 0, 0.0, 0, 0
-    while secs < budget_s and i < 256 * wl.batch:       # the time budget decides; the count only bounds it
-        b = i % wl.batch
+    while secs < budget_s and i < 256 * len(seqs):      # the time budget decides; the count only bounds it
+        b = seqs[i % len(seqs)]
         dt, nb = rig.step([b], threads)
         done += 1
         secs += dt
         nbytes += nb
         i += 1
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
-            "sample": f"{done} sequence decode steps ({min(done, wl.batch)} distinct of {wl.batch}), "
-                      f"all {wl.hq} query heads each, fp64 C oracle append+decode, {secs:.1f} s timed"}
+            "sample": f"{done} sequence decode steps over sequences {seqs[0]}..{seqs[-1]} "
+                      f"({sum(wl.seq_lens[b] for b in seqs)} tokens) of {wl.batch}, all {wl.hq} query heads "
+                      f"each, one layer, fp64 C oracle append+decode, {secs:.1f} s timed"}
 
 
 def run_reference(args, rank, world):
@@ -749,14 +787,15 @@ def run_reference(args, rank, world):
     wl = workloads.config(args.config, page_size=args.page)
     threads = len(os.sched_getaffinity(0))
     rig = OracleRig(wl)
+    seqs = sample_sequences(wl)
     # Size each step's sample (kv heads of one sequence) so that all warm-up
     # and timed steps together take about args.ref_seconds of oracle time.
-    t_full, _ = rig.step([0], threads)
+    t_full, _ = rig.step([seqs[-1]], threads)
     budget = args.ref_seconds / (args.warmup + args.steps)
     n_kv = max(1, min(wl.hkv, int(wl.hkv * budget / max(t_full, 1e-9))))
     per, nbytes = [], []
     for i in range(args.warmup + args.steps):
-        b = i % wl.batch
+        b = seqs[i % len(seqs)]
         dt, nb = rig.step([b], threads, n_kv)
         if i >= args.warmup:
             per.append(dt)
@@ -769,8 +808,9 @@ def run_reference(args, rank, world):
             "config": {**wl.describe(), "kv_bytes_per_step": wl.kv_bytes()},
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": f"each step: the {n_kv * wl.group} query heads of {n_kv} of the {wl.hkv} "
-                                       "kv heads of one sequence (sequences in turn), fp64 C oracle append + "
-                                       "decode; value = algorithmic KV bytes covered / oracle time"},
+                                       f"kv heads of one sequence (sequences {seqs[0]}..{seqs[-1]} in turn, one "
+                                       "layer), fp64 C oracle append + decode; value = algorithmic KV bytes "
+                                       "covered / oracle time"},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -784,7 +824,8 @@ def main():
     ap.add_argument("--chunk", type=int, default=16384, help="prefill: tokens per chunk")
     ap.add_argument("--steps", type=int, default=None, help="timed steps (decode 3000, prefill 10)")
     ap.add_argument("--warmup", type=int, default=None, help="warm-up steps (decode 50, prefill 3)")
-    ap.add_argument("--config", type=int, default=1)
+    ap.add_argument("--config", type=int, default=4,
+                    help="decode workload (default 4: the mixed 64-sequence 512..128K batch, 80 layers)")
     ap.add_argument("--page", type=int, default=None)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--rotate", type=int, default=0, help="distinct layer caches (0 = auto)")
@@ -798,9 +839,10 @@ def main():
                     help="time kv_append_fp8 and paged_gqa_decode as two calls instead of the fused step")
     args = ap.parse_args()
     if args.steps is None:
-        args.steps = 3000 if args.workload == "decode" else 10
+        args.steps = (3000 if args.config in (0, 1, 2) else 300 if args.config == 3 else 50) \
+            if args.workload == "decode" else 10
     if args.warmup is None:
-        args.warmup = 50 if args.workload == "decode" else 3
+        args.warmup = (50 if args.config in (0, 1, 2, 3) else 5) if args.workload == "decode" else 3
     args.warmup = max(3, args.warmup)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))

@@ -44,15 +44,8 @@
  *   PKV_DEVERR_TIMEOUT   a pipeline wait exceeded its time limit (the kernel
  *                        stopped issuing work, drained its copies and
  *                        returned; outputs are undefined)
- * The word is sticky: clear it (e.g. cudaMemsetAsync) before a call whose
- * errors you want to attribute.
- *
- * Test facility: with the environment variable PKV_TEST_WITHHOLD_LOAD=<w>
- * set, decode worker warp w never loads its first page, and in
- * pkv_paged_prefill the CTA of grid block w never loads its first K tile,
- * so a pipeline wait runs out after about 2 s and the call sets
- * PKV_DEVERR_TIMEOUT (outputs undefined) -- used to test the timeout path
- * without faulting or hanging the GPU.  Unset, it has no effect.
+ * The word is sticky: clear it (pkv_read_device_error with clear = 1, or
+ * cudaMemsetAsync) before a call whose errors you want to attribute.
  */
 #ifndef PAGEDFP8_H
 #define PAGEDFP8_H
@@ -248,19 +241,22 @@ pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dt
  *
  * Same arguments and results as pkv_paged_gqa_decode minus the workspace.
  * The split-K scratch lives in a fixed array inside the library image,
- * pkv_decode_noalloc_scratch_bytes() bytes (16 MiB), which every GPU that
- * loads the library keeps until the process exits.  The call allocates
- * nothing.  Sizes whose scratch would not fit return PKV_ERR_WORKSPACE (the
- * scratch holds 8 bytes per (sequence, kv head) plus G * 528 bytes per
- * partial slot, one slot per worker warp (1824 on a 152-SM GPU) plus one per
- * (sequence, kv head); at G = 8 that allows batch * num_kv_heads up to about
- * 2100).
+ * pkv_decode_noalloc_scratch_bytes() bytes (16 MiB).  Under CUDA's default
+ * lazy module loading a GPU holds the array from the first call on it (the
+ * first launch of any of this library's kernels there) until the process
+ * exits; with eager loading, from library load.  The call allocates nothing.
+ * It accepts exactly the sizes for which pkv_decode_workspace_size(...) with
+ * the same arguments is at most pkv_decode_noalloc_scratch_bytes(), and
+ * returns PKV_ERR_WORKSPACE for larger ones; that bound depends on the GPU in
+ * use (its SM count sets the number of split-K workers), so query it rather
+ * than assume a batch limit.
  * All calls share the array: calls that overlap on the GPU (two streams, or
  * unordered host threads) race and corrupt each other's results; calls
  * ordered on one stream are safe.  The array keeps the previous call's
  * contents, which the decode never reads before writing.  The first call on
- * each device looks up the array's device address (with that device
- * current) and caches it: make that first call before any stream capture.
+ * each device looks up the array's device address (with that device current)
+ * and caches it: make that first call before any stream capture.  After
+ * cudaDeviceReset the next call looks the address up again.
  */
 pkv_status pkv_paged_gqa_decode_noalloc(const void *q,
                                         const uint8_t *k_cache, const uint8_t *v_cache,
@@ -336,6 +332,33 @@ pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, in
                              void *out, int out_dtype,
                              void *workspace, size_t workspace_bytes,
                              int32_t *device_error, cudaStream_t stream);
+
+/*
+ * read_device_error -- read (and optionally clear) a device error word after
+ * the work already enqueued on `stream`.
+ *
+ *   device_error   device int32, the word passed to the calls above.
+ *   clear          non-zero: reset the word to 0 after reading it (enqueued
+ *                  on `stream`, so it is ordered before later work there).
+ *   code           host int32 out: the word's bits (PKV_DEVERR_*).
+ * Unlike every other call this one synchronises `stream` (it waits for the
+ * word).  Returns PKV_ERR_NULL / PKV_ERR_ALIGN for bad pointers and
+ * PKV_ERR_CUDA if the copy or the wait fails (for example after a sticky
+ * CUDA error of an earlier launch).
+ */
+pkv_status pkv_read_device_error(const int32_t *device_error, int clear, int32_t *code,
+                                 cudaStream_t stream);
+
+/*
+ * Test facility for the failure-detection tests, not for production use.
+ * After pkv_test_withhold_load(w) with w >= 0, decode worker warp w never
+ * loads its first page, and in pkv_paged_prefill the CTA of grid block w
+ * never loads its first K tile: a pipeline wait runs out after about 2 s and
+ * the call sets PKV_DEVERR_TIMEOUT (outputs undefined), without faulting or
+ * hanging the GPU.  w < 0 (the state at load) turns it off.  Process-wide;
+ * applies to calls made after it returns.
+ */
+void pkv_test_withhold_load(int index);
 
 /* Human-readable name of a status code (static string). */
 const char *pkv_status_string(pkv_status status);

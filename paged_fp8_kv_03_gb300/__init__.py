@@ -16,6 +16,7 @@ if the library is not built, loading raises.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import math
 import os
@@ -79,12 +80,35 @@ def load() -> ctypes.CDLL:
         lib.pkv_paged_prefill.restype = i32
         lib.pkv_paged_prefill.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
                                           i32, i64, ctypes.c_float, vp, i32, vp, sz, vp, vp]
+        lib.pkv_read_device_error.restype = i32
+        lib.pkv_read_device_error.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int32), vp]
+        lib.pkv_test_withhold_load.restype = None
+        lib.pkv_test_withhold_load.argtypes = [i32]
         lib.pkv_status_string.restype = ctypes.c_char_p
         lib.pkv_status_string.argtypes = [i32]
         lib.pkv_version.restype = i32
         lib.pkv_version.argtypes = []
         _lib = lib
         return lib
+
+
+def pkv_read_device_error(device_error, clear: bool = False, stream=None) -> int:
+    """The bits of a device error word (waits for the work enqueued on the
+    stream); with clear=True the word is reset to 0 afterwards."""
+    _need(device_error, "device_error", torch.int32)
+    code = ctypes.c_int32(0)
+    with _device_of(device_error):
+        st = load().pkv_read_device_error(_ptr(device_error), 1 if clear else 0, ctypes.byref(code), _stream(stream))
+    if st != 0:
+        raise PkvError(st, "pkv_read_device_error")
+    return int(code.value)
+
+
+def pkv_test_withhold_load(index: int) -> None:
+    """Test facility (failure-detection tests only): decode worker warp /
+    prefill CTA `index` skips its first load so its bounded wait runs out;
+    a negative index turns it off."""
+    load().pkv_test_withhold_load(int(index))
 
 
 def pkv_status_string(status: int) -> str:
@@ -105,6 +129,20 @@ def _stream(stream):
     if isinstance(stream, torch.cuda.Stream):
         return ctypes.c_void_p(stream.cuda_stream)
     return ctypes.c_void_p(int(stream))
+
+
+def _device_of(t):
+    """Runs a call with the tensors' device current: the library launches on
+    the current device and takes the current stream of that device."""
+    if t.device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(t.device)
+
+
+def _same_device(ref, *ts):
+    for t in ts:
+        if t is not None and t.device != ref.device:
+            raise ValueError(f"all tensors must be on {ref.device}, got one on {t.device}")
 
 
 def _need(t, name, dtype=None, dim=None, cuda=True):
@@ -147,9 +185,11 @@ def pkv_kv_append_fp8(k_new, v_new, slot_mapping, k_scale, v_scale, k_cache, v_c
         raise ValueError("k/v shapes disagree")
     if slot_mapping.shape[0] != T or k_scale.shape[0] != H or v_scale.shape[0] != H:
         raise ValueError("slot_mapping / scale shapes disagree")
-    st = load().pkv_kv_append_fp8(_ptr(k_new), _ptr(v_new), _act_code(k_new), T, H, D, _ptr(slot_mapping),
-                                  _ptr(k_scale), _ptr(v_scale), _ptr(k_cache), _ptr(v_cache), NP, P,
-                                  _ptr(device_error), _stream(stream))
+    _same_device(k_new, v_new, slot_mapping, k_scale, v_scale, k_cache, v_cache, device_error)
+    with _device_of(k_new):
+        st = load().pkv_kv_append_fp8(_ptr(k_new), _ptr(v_new), _act_code(k_new), T, H, D, _ptr(slot_mapping),
+                                      _ptr(k_scale), _ptr(v_scale), _ptr(k_cache), _ptr(v_cache), NP, P,
+                                      _ptr(device_error), _stream(stream))
     if st != 0:
         raise PkvError(st, "pkv_kv_append_fp8")
 
@@ -171,8 +211,10 @@ def pkv_kv_calibrate(k_new, v_new, k_running_max, v_running_max, k_scale=None, v
     T, H, D = k_new.shape
     if v_new.shape != k_new.shape or k_running_max.shape[0] != H or v_running_max.shape[0] != H:
         raise ValueError("shapes disagree")
-    st = load().pkv_kv_calibrate(_ptr(k_new), _ptr(v_new), _act_code(k_new), T, H, D, _ptr(k_running_max),
-                                 _ptr(v_running_max), _ptr(k_scale), _ptr(v_scale), _stream(stream))
+    _same_device(k_new, v_new, k_running_max, v_running_max, k_scale, v_scale)
+    with _device_of(k_new):
+        st = load().pkv_kv_calibrate(_ptr(k_new), _ptr(v_new), _act_code(k_new), T, H, D, _ptr(k_running_max),
+                                     _ptr(v_running_max), _ptr(k_scale), _ptr(v_scale), _stream(stream))
     if st != 0:
         raise PkvError(st, "pkv_kv_calibrate")
 
@@ -205,12 +247,14 @@ def pkv_paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq
         raise ValueError("q / cache / out shapes disagree")
     if block_table.shape[0] != B or seq_lens.shape[0] != B:
         raise ValueError("block_table / seq_lens shapes disagree with q")
+    _same_device(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace, device_error)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
-    st = load().pkv_paged_gqa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-                                     _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, Hq, Hkv, D, P,
-                                     NP, float(sm_scale), _ptr(out), _act_code(out), _ptr(workspace),
-                                     workspace.numel(), _ptr(device_error), int(max_ctas), _stream(stream))
+    with _device_of(q):
+        st = load().pkv_paged_gqa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                         _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, Hq, Hkv, D, P,
+                                         NP, float(sm_scale), _ptr(out), _act_code(out), _ptr(workspace),
+                                         workspace.numel(), _ptr(device_error), int(max_ctas), _stream(stream))
     if st != 0:
         raise PkvError(st, "pkv_paged_gqa_decode")
 
@@ -242,13 +286,15 @@ def pkv_append_decode_fp8(k_new, v_new, q, k_cache, v_cache, k_scale, v_scale, b
         raise ValueError("k_new / v_new must be [B, n_new, Hkv, head_dim]")
     if block_table.shape[0] != B or seq_lens.shape[0] != B:
         raise ValueError("block_table / seq_lens shapes disagree with q")
+    _same_device(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace, k_new, v_new, device_error)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
-    st = load().pkv_append_decode_fp8(_ptr(k_new), _ptr(v_new), _act_code(k_new), n_new, _ptr(q), _ptr(k_cache),
-                                      _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
-                                      block_table.shape[1], _ptr(seq_lens), B, Hq, Hkv, D, P, NP, float(sm_scale),
-                                      _ptr(out), _act_code(out), _ptr(workspace), workspace.numel(),
-                                      _ptr(device_error), int(max_ctas), _stream(stream))
+    with _device_of(k_new):
+        st = load().pkv_append_decode_fp8(_ptr(k_new), _ptr(v_new), _act_code(k_new), n_new, _ptr(q), _ptr(k_cache),
+                                          _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
+                                          block_table.shape[1], _ptr(seq_lens), B, Hq, Hkv, D, P, NP, float(sm_scale),
+                                          _ptr(out), _act_code(out), _ptr(workspace), workspace.numel(),
+                                          _ptr(device_error), int(max_ctas), _stream(stream))
     if st != 0:
         raise PkvError(st, "pkv_append_decode_fp8")
 
@@ -288,12 +334,14 @@ def pkv_paged_gqa_decode_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_ta
         raise ValueError("q / cache / out shapes disagree")
     if block_table.shape[0] != B or seq_lens.shape[0] != B:
         raise ValueError("block_table / seq_lens shapes disagree with q")
+    _same_device(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, device_error)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
-    st = load().pkv_paged_gqa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
-                                             _ptr(v_scale), _ptr(block_table), block_table.shape[1],
-                                             _ptr(seq_lens), B, Hq, Hkv, D, P, NP, float(sm_scale), _ptr(out),
-                                             _act_code(out), _ptr(device_error), int(max_ctas), _stream(stream))
+    with _device_of(q):
+        st = load().pkv_paged_gqa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
+                                                 _ptr(v_scale), _ptr(block_table), block_table.shape[1],
+                                                 _ptr(seq_lens), B, Hq, Hkv, D, P, NP, float(sm_scale), _ptr(out),
+                                                 _act_code(out), _ptr(device_error), int(max_ctas), _stream(stream))
     if st != 0:
         raise PkvError(st, "pkv_paged_gqa_decode_noalloc")
 
@@ -370,13 +418,15 @@ def pkv_paged_prefill(q, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, 
         raise ValueError("q / cache / out shapes disagree")
     if block_table.shape[0] != B or cu_q.shape[0] != B + 1:
         raise ValueError("block_table / cu_q shapes disagree with seq_lens")
+    _same_device(q, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace, device_error)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
-    st = load().pkv_paged_prefill(_ptr(q), _ptr(cu_q), T, int(max_q_len), _ptr(k_cache), _ptr(v_cache),
-                                  _ptr(k_scale), _ptr(v_scale), _ptr(block_table), block_table.shape[1],
-                                  _ptr(seq_lens), B, int(max_kv_len), Hq, Hkv, D, P, NP, float(sm_scale), _ptr(out),
-                                  _act_code(out), _ptr(workspace), workspace.numel(), _ptr(device_error),
-                                  _stream(stream))
+    with _device_of(q):
+        st = load().pkv_paged_prefill(_ptr(q), _ptr(cu_q), T, int(max_q_len), _ptr(k_cache), _ptr(v_cache),
+                                      _ptr(k_scale), _ptr(v_scale), _ptr(block_table), block_table.shape[1],
+                                      _ptr(seq_lens), B, int(max_kv_len), Hq, Hkv, D, P, NP, float(sm_scale), _ptr(out),
+                                      _act_code(out), _ptr(workspace), workspace.numel(), _ptr(device_error),
+                                      _stream(stream))
     if st != 0:
         raise PkvError(st, "pkv_paged_prefill")
 
@@ -401,6 +451,6 @@ def paged_prefill(q, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, seq_
 __all__ = ["load", "lib_path", "pkv_kv_append_fp8", "pkv_paged_gqa_decode", "pkv_decode_workspace_size",
            "pkv_paged_gqa_decode_noalloc", "pkv_decode_noalloc_scratch_bytes", "pkv_append_decode_fp8",
            "append_decode_fp8", "pkv_kv_calibrate", "pkv_paged_prefill", "paged_prefill", "pkv_prefill_workspace_size",
-           "pkv_status_string", "pkv_version", "kv_append_fp8", "paged_gqa_decode", "decode_workspace",
+           "pkv_status_string", "pkv_version", "pkv_read_device_error", "pkv_test_withhold_load", "kv_append_fp8", "paged_gqa_decode", "decode_workspace",
            "PkvError", "PKV_F32", "PKV_BF16", "DEVERR_SLOT", "DEVERR_PAGE", "DEVERR_SEQLEN",
            "DEVERR_TIMEOUT"]

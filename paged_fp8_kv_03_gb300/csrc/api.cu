@@ -1,8 +1,8 @@
 // C entry points: argument checks on the host, TMA tensor descriptions of the
 // page pools, grid sizing and launches.  Nothing here allocates device memory.
 #include <math.h>
-#include <stdlib.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -17,6 +17,7 @@ std::mutex g_mu;
 std::map<int, int> g_sm_count;                              // device -> SMs
 std::map<std::tuple<int, int, size_t>, int> g_occupancy;     // (device, P, smem) -> CTAs per SM
 std::map<std::tuple<int, int>, size_t> g_smem_attr;          // (device, P) -> max dynamic smem set
+std::atomic<int> g_withhold{-1};                            // failure-detection test facility (-1 = off)
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
@@ -260,11 +261,10 @@ pkv_status decode_impl(const void *k_new, const void *v_new, int in_dtype, int n
     a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + decode_segment_bytes(batch, num_kv_heads));
     a.err = device_error;
     a.num_ctas = ctas;
-    // Test facility for the timeout path: PKV_TEST_WITHHOLD_LOAD=<worker> makes
-    // that worker warp skip its first page's loads, so its first wait runs out
-    // (about 2 s) and the call reports PKV_DEVERR_TIMEOUT.  Unset: no effect.
-    const char *hold = getenv("PKV_TEST_WITHHOLD_LOAD");
-    a.withhold_worker = hold ? atoi(hold) : -1;
+    // Test facility for the timeout path (pkv_test_withhold_load): that worker
+    // warp skips its first page's loads, so its first wait runs out (about
+    // 2 s) and the call reports PKV_DEVERR_TIMEOUT.  -1: no effect.
+    a.withhold_worker = g_withhold.load(std::memory_order_relaxed);
     return launch_paged_decode(a, tm_k, tm_v, page_size, stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
@@ -275,6 +275,28 @@ extern "C" {
 int pkv_version(void)
 {
     return (1 << 16) | 0;
+}
+
+void pkv_test_withhold_load(int index)
+{
+    g_withhold.store(index < 0 ? -1 : index, std::memory_order_relaxed);
+}
+
+pkv_status pkv_read_device_error(const int32_t *device_error, int clear, int32_t *code, cudaStream_t stream)
+{
+    if (!device_error || !code)
+        return PKV_ERR_NULL;
+    if (!aligned(device_error, 4))
+        return PKV_ERR_ALIGN;
+    int32_t word = 0;
+    if (cudaMemcpyAsync(&word, device_error, sizeof(word), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    *code = word;
+    if (clear && cudaMemsetAsync(const_cast<int32_t *>(device_error), 0, sizeof(word), stream) != cudaSuccess)
+        return PKV_ERR_CUDA;
+    return PKV_OK;
 }
 
 const char *pkv_status_string(pkv_status s)
@@ -452,10 +474,9 @@ pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, in
     a.kv_pad = static_cast<int>(kv_pad);
     a.k16 = k16;
     a.v16 = v16;
-    // Test facility for the timeout path (PKV_TEST_WITHHOLD_LOAD=<block>): that
-    // CTA never loads its first K tile, so its MMA warp's wait runs out.
-    const char *hold = getenv("PKV_TEST_WITHHOLD_LOAD");
-    a.withhold_block = hold ? atoi(hold) : -1;
+    // Test facility for the timeout path (pkv_test_withhold_load): that CTA
+    // never loads its first K tile, so its MMA warp's wait runs out.
+    a.withhold_block = g_withhold.load(std::memory_order_relaxed);
     a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
     a.out = out;
     a.out_f32 = out_dtype == PKV_F32;

@@ -24,7 +24,10 @@
 //
 // The first call on each device looks up the array's device address
 // (cudaGetSymbolAddress, with that device current) and caches it; make that
-// first call before any stream capture begins.
+// first call before any stream capture begins.  The cache is keyed by the
+// device's current context, so after cudaDeviceReset (which destroys the
+// context and unloads the library's device image) the next call on that
+// device looks the address up again instead of using a stale one.
 #include <mutex>
 
 #include "internal.h"
@@ -38,8 +41,41 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+struct ScratchEntry {
+    unsigned long long ctx_id = 0;   // context the address belongs to (0: none yet)
+    void *ptr = nullptr;
+};
+
 std::mutex g_noalloc_mu;
-void *g_noalloc_ptr[64] = {nullptr};
+ScratchEntry g_noalloc[64];
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+template <typename Fn>
+Fn driver_fn(const char *name)
+{
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion(name, &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<Fn>(fn);
+}
+
+// Unique id (for the life of the process) of the current device's context.
+bool current_context_id(unsigned long long *id)
+{
+    if (!g_ctx_get_current)
+        g_ctx_get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    if (!g_ctx_get_id)
+        g_ctx_get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    CUcontext ctx = nullptr;
+    return g_ctx_get_current && g_ctx_get_id && g_ctx_get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+           g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 void *scratch_for_current_device()
 {
@@ -47,13 +83,18 @@ void *scratch_for_current_device()
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
         return nullptr;
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (!g_noalloc_ptr[dev]) {
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess)
-            return nullptr;
-        g_noalloc_ptr[dev] = p;
-    }
-    return g_noalloc_ptr[dev];
+    ScratchEntry &e = g_noalloc[dev];
+    unsigned long long id = 0;
+    if (e.ptr != nullptr && current_context_id(&id) && id == e.ctx_id)
+        return e.ptr;
+    // Set-up for this device (or its new context): the lookup also makes the
+    // device's primary context current if it was not yet.
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !current_context_id(&id))
+        return nullptr;
+    e.ptr = p;
+    e.ctx_id = id;
+    return p;
 }
 
 }  // namespace

@@ -201,3 +201,16 @@ def test_prefill_argument_errors(lib):
     assert pre(T=0, q=None, cu=None, out=None) == c["PKV_OK"]          # nothing to compute
     assert pre(mq=0, q=None, cu=None, out=None) == c["PKV_OK"]
     assert pkv.pkv_prefill_workspace_size(-1, 2, 64) == 0
+
+
+def test_read_device_error_argument_errors(lib):
+    c = _status_codes()
+    code = ctypes.c_int32(0)
+    assert lib.pkv_read_device_error(None, 0, ctypes.byref(code), None) == c["PKV_ERR_NULL"]
+    assert lib.pkv_read_device_error(A16, 0, None, None) == c["PKV_ERR_NULL"]
+    assert lib.pkv_read_device_error(ctypes.c_void_p(0x10002), 1, ctypes.byref(code), None) == c["PKV_ERR_ALIGN"]
+
+
+def test_withhold_facility_is_off_at_load_and_settable(lib):
+    lib.pkv_test_withhold_load(-5)          # any negative index turns it off
+    lib.pkv_test_withhold_load(-1)

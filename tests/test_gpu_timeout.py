@@ -1,8 +1,7 @@
 """Failure detection on the GPU without a fault: a decode worker is told
-(test facility PKV_TEST_WITHHOLD_LOAD) never to load its first page, so its
+(test facility pkv_test_withhold_load) never to load its first page, so its
 bounded pipeline wait runs out; the kernel must report PKV_DEVERR_TIMEOUT,
 drain, return within seconds, and leave the context usable."""
-import os
 import time
 
 import pytest
@@ -19,7 +18,7 @@ def test_withheld_load_times_out_and_context_survives(pkv, cuda_device):
     wl = workloads.Workload(70, "timeout", [300, 77], 0, 8, 2, 16, seed=4)
     f = fill_gpu(wl, 0, cuda_device)
     err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
-    os.environ["PKV_TEST_WITHHOLD_LOAD"] = "0"
+    pkv.pkv_test_withhold_load(0)
     try:
         t0 = time.time()
         pkv.paged_gqa_decode(f.q, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, out_dtype=torch.float32,
@@ -27,7 +26,7 @@ def test_withheld_load_times_out_and_context_survives(pkv, cuda_device):
         torch.cuda.synchronize()
         dt = time.time() - t0
     finally:
-        del os.environ["PKV_TEST_WITHHOLD_LOAD"]
+        pkv.pkv_test_withhold_load(-1)
     assert int(err.item()) & pkv.DEVERR_TIMEOUT
     assert 1.5 < dt < 20.0
     err.zero_()
@@ -50,7 +49,7 @@ def test_prefill_withheld_tile_times_out_and_context_survives(pkv, cuda_device):
     q = wl.q_rows(0, 40)
     cu = torch.tensor([0, 40], dtype=torch.int32, device=cuda_device)
     err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
-    os.environ["PKV_TEST_WITHHOLD_LOAD"] = "0"
+    pkv.pkv_test_withhold_load(0)
     try:
         t0 = time.time()
         pkv.paged_prefill(q.to(cuda_device), cu, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, 40,
@@ -58,7 +57,7 @@ def test_prefill_withheld_tile_times_out_and_context_survives(pkv, cuda_device):
         torch.cuda.synchronize()
         dt = time.time() - t0
     finally:
-        del os.environ["PKV_TEST_WITHHOLD_LOAD"]
+        pkv.pkv_test_withhold_load(-1)
     assert int(err.item()) & pkv.DEVERR_TIMEOUT
     assert 1.5 < dt < 20.0
     err.zero_()
