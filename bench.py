@@ -235,7 +235,7 @@ def run_gpu(args, rank, world):
     bt = wl.block_table().to(dev)
     lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev)
     out = torch.empty((wl.batch, wl.hq, wl.head_dim), dtype=torch.bfloat16, device=dev)
-    ws = pkv.decode_workspace(wl.batch, wl.hq, wl.hkv, wl.page_size, dev)
+    ws = pkv.decode_workspace(wl.batch, wl.hq, wl.hkv, wl.page_size, dev, max_seq_len=wl.max_pages * wl.page_size)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 

@@ -39,11 +39,14 @@
  *   PKV_DEVERR_SLOT      a slot outside the pool (token skipped)
  *   PKV_DEVERR_PAGE      a block-table entry outside [0, num_pages) (its
  *                        page is read as zeros)
- *   PKV_DEVERR_SEQLEN    seq_lens[b] < 0 or beyond max_pages_per_seq pages
- *                        (clamped)
+ *   PKV_DEVERR_SEQLEN    seq_lens[b] < 0, beyond max_seq_len or beyond
+ *                        max_pages_per_seq pages (clamped)
  *   PKV_DEVERR_TIMEOUT   a pipeline wait exceeded its time limit (the kernel
  *                        stopped issuing work, drained its copies and
  *                        returned; outputs are undefined)
+ *   PKV_DEVERR_PAGESIZE  a per-sequence page size that is not a power of two
+ *                        in [page_size, 256] (the sequence is treated as
+ *                        empty: zero output rows)
  * The word is sticky: clear it (pkv_read_device_error with clear = 1, or
  * cudaMemsetAsync) before a call whose errors you want to attribute.
  */
@@ -80,7 +83,8 @@ enum {
     PKV_DEVERR_SLOT = 1,
     PKV_DEVERR_PAGE = 2,
     PKV_DEVERR_SEQLEN = 4,
-    PKV_DEVERR_TIMEOUT = 8
+    PKV_DEVERR_TIMEOUT = 8,
+    PKV_DEVERR_PAGESIZE = 16
 };
 
 /* Build limits. */
@@ -142,12 +146,17 @@ pkv_status pkv_kv_calibrate(const void *k_new, const void *v_new, int in_dtype,
                             float *k_scale, float *v_scale, cudaStream_t stream);
 
 /*
- * Workspace bytes pkv_paged_gqa_decode needs for these sizes on the current
- * device (partial softmax states of the split-K pass).  Returns 0 for sizes
- * the library rejects.  max_ctas as in pkv_paged_gqa_decode.
+ * Workspace bytes pkv_paged_gqa_decode needs on the current device for a
+ * call with these sizes whose seq_lens are all <= max_seq_len (partial
+ * softmax states of the split-K pass: one slot per split-K worker and
+ * sub-piece of its range, plus one per (sequence, kv head)).  Returns 0 for
+ * sizes the library rejects.  max_ctas as in pkv_paged_gqa_decode.  Grows
+ * with batch * max_seq_len only once the list is longer than 512 chunks of
+ * 16 tokens per worker (for example about 38 MB at batch 64, 8 kv heads,
+ * G = 8 and 128K tokens on a 152-SM GPU).
  */
 size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
-                                 int head_dim, int page_size, int max_ctas);
+                                 int head_dim, int max_seq_len, int page_size, int max_ctas);
 
 /*
  * paged_gqa_decode -- one decode step of grouped-query attention over the
@@ -156,32 +165,45 @@ size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
  *
  * For every sequence b < batch and query head i < num_q_heads, with
  * G = num_q_heads / num_kv_heads, h = i / G and L = seq_lens[b]:
- *     s_t = sm_scale * sum_d q[b][i][d] * E4M3(k_cache[pg(t)][h][t % P][d]) * k_scale[h]
+ *     s_t = sm_scale * sum_d q[b][i][d] * E4M3(k_cache[pg(t)][h][row(t)][d]) * k_scale[h]
  *     w_t = softmax_t(s_t)                              for t < L
- *     out[b][i][d] = sum_t w_t * E4M3(v_cache[pg(t)][h][t % P][d]) * v_scale[h]
- * where pg(t) = block_table[b][t / P].  L == 0 gives a zero row.  Long
- * contexts are split across warps (split-K / flash-decoding) and a second
- * kernel merges the partial softmax states exactly (log-sum-exp) in a fixed
- * order: results are deterministic run to run and independent of where the
- * pages sit in the pool.  Two kernel launches (the second is a programmatic
- * dependent launch that overlaps the first one's tail).
+ *     out[b][i][d] = sum_t w_t * E4M3(v_cache[pg(t)][h][row(t)][d]) * v_scale[h]
+ * where, with P = page_size and P_b the sequence's page size (P unless
+ * seq_page_sizes is given), pg(t) = block_table[b][t / P_b] + (t % P_b) / P
+ * and row(t) = t % P: a page of P_b tokens is a run of P_b / P consecutive
+ * pool pages, and its table entry is the first of them ([N] §3.2: 16-token
+ * pages for short sequences, 64-token pages for long ones).  L == 0 gives a
+ * zero row.  Long contexts are split across warps (split-K /
+ * flash-decoding); no warp accumulates more than 512 chunks of 16 tokens
+ * into one partial state, and a second kernel merges the partial softmax
+ * states exactly (log-sum-exp) in a fixed order: results are deterministic
+ * run to run and independent of where the pages sit in the pool.  Two kernel
+ * launches (the second is a programmatic dependent launch that overlaps the
+ * first one's tail).
  *
  *   q              device bf16 [batch][num_q_heads][head_dim] (|q| < 65504).
  *   k_cache, v_cache device uint8 pools (layout above), 16-byte aligned.
  *   k_scale, v_scale device fp32 [num_kv_heads].
  *   block_table    device int32 [batch][max_pages_per_seq].
  *   seq_lens       device int32 [batch]; must satisfy
- *                  0 <= seq_lens[b] <= max_pages_per_seq * page_size
+ *                  0 <= seq_lens[b] <= min(max_seq_len, max_pages_per_seq * P_b)
  *                  (violations set PKV_DEVERR_SEQLEN and are clamped).
+ *   max_seq_len    host bound of seq_lens (sizes the workspace); 0 means
+ *                  max_pages_per_seq * page_size (pass the real bound when
+ *                  seq_page_sizes is given).
+ *   seq_page_sizes device int32 [batch] or NULL: tokens per page of each
+ *                  sequence, a power of two in [page_size, 256] (others set
+ *                  PKV_DEVERR_PAGESIZE and the sequence reads as empty).
  *   head_dim       128.  page_size 16, 32, 64, 128 or 256.  G in 1..8.
  *   sm_scale       softmax scale, normally 1/sqrt(head_dim).
  *   out            device [batch][num_q_heads][head_dim], out_dtype
  *                  PKV_BF16 (bf16, RNE of the fp32 result) or PKV_F32.
- *   workspace      device, >= pkv_decode_workspace_size(...) bytes, 256-byte
- *                  aligned: per-(sequence, kv head) piece ranges, then the
- *                  partial states.  Contents need no initialisation; one
- *                  workspace must not be shared by calls that overlap on the
- *                  GPU.
+ *   workspace      device, >= pkv_decode_workspace_size(batch, num_q_heads,
+ *                  num_kv_heads, head_dim, max_seq_len, page_size, max_ctas)
+ *                  bytes, 256-byte aligned: a header, per-(sequence, kv
+ *                  head) records, then the partial states.  Contents need no
+ *                  initialisation; one workspace must not be shared by calls
+ *                  that overlap on the GPU.
  *   device_error   device int32 or NULL (bits above).
  *   max_ctas       0 = one persistent CTA per resident slot on the device;
  *                  > 0 caps the CTA count (changes the split, not the math).
@@ -190,7 +212,8 @@ pkv_status pkv_paged_gqa_decode(const void *q,
                                 const uint8_t *k_cache, const uint8_t *v_cache,
                                 const float *k_scale, const float *v_scale,
                                 const int32_t *block_table, int max_pages_per_seq,
-                                const int32_t *seq_lens,
+                                const int32_t *seq_lens, int max_seq_len,
+                                const int32_t *seq_page_sizes,
                                 int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                 int page_size, int64_t num_pages, float sm_scale,
                                 void *out, int out_dtype,
@@ -204,10 +227,11 @@ pkv_status pkv_paged_gqa_decode(const void *q,
  *
  * For every sequence b with L = seq_lens[b] (the length AFTER this step's
  * tokens) and j < n_new, token position t = L - n_new + j:
- *     k_cache[pg(t)][h][t % P][d] = E4M3(k_new[b][j][h][d] / k_scale[h])
- * (same for V, same rounding as pkv_kv_append_fp8), then exactly the
- * attention of pkv_paged_gqa_decode over t < L.  Page bytes and outputs are
- * bit-identical to calling pkv_kv_append_fp8 with slot = pg(t) * P + t % P
+ *     k_cache[pg(t)][h][row(t)][d] = E4M3(k_new[b][j][h][d] / k_scale[h])
+ * (same for V, same rounding as pkv_kv_append_fp8; pg and row as in
+ * pkv_paged_gqa_decode), then exactly the attention of pkv_paged_gqa_decode
+ * over t < L.  Page bytes and outputs are bit-identical to calling
+ * pkv_kv_append_fp8 with slot = block_table[b][t / P_b] * P + t % P_b
  * followed by pkv_paged_gqa_decode.  Each new token is written by the warp
  * that later reads its page, so no extra launch or grid-wide ordering is
  * needed.
@@ -224,7 +248,8 @@ pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dt
                                  const void *q, uint8_t *k_cache, uint8_t *v_cache,
                                  const float *k_scale, const float *v_scale,
                                  const int32_t *block_table, int max_pages_per_seq,
-                                 const int32_t *seq_lens,
+                                 const int32_t *seq_lens, int max_seq_len,
+                                 const int32_t *seq_page_sizes,
                                  int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                  int page_size, int64_t num_pages, float sm_scale,
                                  void *out, int out_dtype,
@@ -262,7 +287,8 @@ pkv_status pkv_paged_gqa_decode_noalloc(const void *q,
                                         const uint8_t *k_cache, const uint8_t *v_cache,
                                         const float *k_scale, const float *v_scale,
                                         const int32_t *block_table, int max_pages_per_seq,
-                                        const int32_t *seq_lens,
+                                        const int32_t *seq_lens, int max_seq_len,
+                                        const int32_t *seq_page_sizes,
                                         int batch, int num_q_heads, int num_kv_heads, int head_dim,
                                         int page_size, int64_t num_pages, float sm_scale,
                                         void *out, int out_dtype,

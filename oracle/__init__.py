@@ -80,7 +80,7 @@ def _load():
         lib.oracle_kv_append.restype = i64
         lib.oracle_kv_append.argtypes = [P, i32, i64, i32, i32, P, P, P, i64, i32]
         lib.oracle_paged_decode.restype = i32
-        lib.oracle_paged_decode.argtypes = [P, P, P, P, P, P, i32, P, i32, i32, i32, i32,
+        lib.oracle_paged_decode.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32, i32,
                                             i32, i64, dbl, P, i64, P, P, i64, i32]
         lib.oracle_paged_prefill.restype = i32
         lib.oracle_paged_prefill.argtypes = [P, P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i64, dbl, P,
@@ -144,13 +144,16 @@ def kv_append(x, slots, scale, cache: np.ndarray) -> int:
 
 def paged_decode(q_bits, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
                  sm_scale: float | None = None, sel=None, threads: int = 1,
-                 want_weights: bool = False):
+                 want_weights: bool = False, seq_page_sizes=None):
     """fp64 decode attention.
 
     q_bits: [B, Hq, D] bf16 bit patterns (uint16).  k_cache/v_cache: uint8
     [num_pages, Hkv, P, D].  k_scale/v_scale: fp32 [Hkv].  block_table: int32
     [B, max_pages].  seq_lens: int32 [B].  sel: optional int32 [n, 2] list of
     (b, q_head) rows to compute (default: all, in row-major order).
+    seq_page_sizes: optional int32 [B], tokens per page of each sequence (a
+    page of P_b tokens is P_b / P consecutive pool pages starting at its table
+    entry; default P for every sequence).
     Returns out [n, D] (fp64), and the softmax weights [n, max(seq_lens)] if
     `want_weights`.
     """
@@ -167,6 +170,10 @@ def paged_decode(q_bits, k_cache, v_cache, k_scale, v_scale, block_table, seq_le
         raise ValueError("cache shape mismatch")
     if block_table.ndim != 2 or block_table.shape[0] != B or seq_lens.shape != (B,):
         raise ValueError("block_table / seq_lens shape mismatch")
+    if seq_page_sizes is not None:
+        seq_page_sizes = _c(seq_page_sizes, np.int32)
+        if seq_page_sizes.shape != (B,):
+            raise ValueError("seq_page_sizes shape mismatch")
     if sm_scale is None:
         sm_scale = 1.0 / np.sqrt(D)
     if sel is None:
@@ -179,7 +186,8 @@ def paged_decode(q_bits, k_cache, v_cache, k_scale, v_scale, block_table, seq_le
     weights = np.zeros((n, max(w_stride, 1)), np.float64) if want_weights else None
     st = _load().oracle_paged_decode(
         _ptr(q_bits), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-        _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, Hq, Hkv, D, P, NP,
+        _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+        _ptr(seq_page_sizes) if seq_page_sizes is not None else None, B, Hq, Hkv, D, P, NP,
         float(sm_scale), _ptr(sel), n, _ptr(out),
         _ptr(weights) if want_weights else None, w_stride, int(threads))
     if st != 0:

@@ -205,6 +205,7 @@ struct decode_args {
     const int32_t *bt;                 /* [B][max_pages] */
     int max_pages;
     const int32_t *lens;               /* [B] */
+    const int32_t *page_sizes;         /* [B] tokens per page of each sequence, or NULL (all P) */
     int B, Hq, Hkv, D, P;
     int64_t num_pages;
     double sm_scale;
@@ -216,10 +217,31 @@ struct decode_args {
     int status;                        /* 0 ok, 1 bad block-table entry */
 };
 
+/* Where token t of sequence b lives.  A page of P_b tokens (P_b = P unless
+ * per-sequence page sizes are given: 0539edu.com Llama 3 notes, §3.2, 16-token
+ * pages for short sequences and 64-token pages for long ones) is a run of
+ * P_b / P consecutive pool pages whose first page is the table entry
+ * block_table[b][t / P_b]; offset o = t % P_b of the logical page lies in pool
+ * page entry + o / P at row o % P.  Returns the pool page, or -1 if the table
+ * runs out or the page lies outside the pool. */
+static int64_t token_pool_page(const struct decode_args *a, int b, int t)
+{
+    int Pb = a->page_sizes ? a->page_sizes[b] : a->P;
+    int32_t entry;
+    int64_t page;
+    if (Pb <= 0 || t / Pb >= a->max_pages)
+        return -1;
+    entry = a->bt[(int64_t)b * a->max_pages + t / Pb];
+    page = (int64_t)entry + (t % Pb) / a->P;
+    if (entry < 0 || page >= a->num_pages)
+        return -1;
+    return page;
+}
+
 /* One (sequence b, query head i) output row.
  *   K^_td = value(k byte) * k_scale[h], V^_td likewise, h = i / G;
  *   s_t   = (sum_d q_id K^_td) * sm_scale,  t < L_b, token t found at
- *           page block_table[b][t / P], row t % P;
+ *           pool page token_pool_page(b, t), row t % P;
  *   w_t   = exp(s_t - max s) / sum_u exp(s_u - max s);
  *   o_id  = sum_t w_t V^_td.                                               */
 static int decode_one(const struct decode_args *a, int64_t k)
@@ -244,17 +266,12 @@ static int decode_one(const struct decode_args *a, int64_t k)
     if (!s)
         return 2;
     for (int t = 0; t < L; ++t) {
-        int32_t phys;
-        if (t / P >= a->max_pages) {
+        int64_t phys = token_pool_page(a, b, t);
+        if (phys < 0) {
             free(s);
             return 1;
         }
-        phys = a->bt[(int64_t)b * a->max_pages + t / P];
-        if (phys < 0 || phys >= a->num_pages) {
-            free(s);
-            return 1;
-        }
-        const uint8_t *krow = a->kc + (((int64_t)phys * a->Hkv + h) * P + t % P) * D;
+        const uint8_t *krow = a->kc + ((phys * a->Hkv + h) * P + t % P) * D;
         double acc = 0.0;
         for (int d = 0; d < D; ++d)
             acc += q[d] * (oracle_e4m3_value(krow[d]) * (double)a->ks[h]);
@@ -271,8 +288,8 @@ static int decode_one(const struct decode_args *a, int64_t k)
     }
     for (int t = 0; t < L; ++t) {
         double w = s[t] / denom;
-        int32_t phys = a->bt[(int64_t)b * a->max_pages + t / P];
-        const uint8_t *vrow = a->vc + (((int64_t)phys * a->Hkv + h) * P + t % P) * D;
+        int64_t phys = token_pool_page(a, b, t);
+        const uint8_t *vrow = a->vc + ((phys * a->Hkv + h) * P + t % P) * D;
         for (int d = 0; d < D; ++d)
             o[d] += w * (oracle_e4m3_value(vrow[d]) * (double)a->vs[h]);
         if (a->weights && t < a->w_stride)
@@ -302,6 +319,7 @@ static void *decode_worker(void *arg)
 int oracle_paged_decode(const uint16_t *q, const uint8_t *k_cache, const uint8_t *v_cache,
                         const float *k_scale, const float *v_scale,
                         const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                        const int32_t *page_sizes,
                         int B, int Hq, int Hkv, int D, int P, int64_t num_pages,
                         double sm_scale, const int32_t *sel, int64_t n_sel,
                         double *out, double *weights, int64_t w_stride, int threads)
@@ -314,7 +332,7 @@ int oracle_paged_decode(const uint16_t *q, const uint8_t *k_cache, const uint8_t
     if (D > 1024 || Hkv <= 0 || Hq % Hkv != 0)
         return 3;
     a.q = q; a.kc = k_cache; a.vc = v_cache; a.ks = k_scale; a.vs = v_scale;
-    a.bt = block_table; a.max_pages = max_pages; a.lens = seq_lens;
+    a.bt = block_table; a.max_pages = max_pages; a.lens = seq_lens; a.page_sizes = page_sizes;
     a.B = B; a.Hq = Hq; a.Hkv = Hkv; a.D = D; a.P = P; a.num_pages = num_pages;
     a.sm_scale = sm_scale; a.sel = sel; a.n_sel = n_sel; a.out = out;
     a.weights = weights; a.w_stride = w_stride; a.status = 0;
@@ -407,7 +425,7 @@ int oracle_paged_prefill(const uint16_t *q, const int32_t *cu_q, const uint8_t *
             int32_t len = seq_lens[b] - n + c + 1;       /* keys 0 .. position */
             int64_t row = (int64_t)cu_q[b] + c;
             int st = oracle_paged_decode(q + row * Hq * D, k_cache, v_cache, k_scale, v_scale,
-                                         block_table + (int64_t)b * max_pages, max_pages, &len, 1, Hq, Hkv, D, P,
+                                         block_table + (int64_t)b * max_pages, max_pages, &len, NULL, 1, Hq, Hkv, D, P,
                                          num_pages, sm_scale, sel, Hq, out + row * Hq * D, NULL, 0, threads);
             if (st && !status)
                 status = st;

@@ -61,18 +61,18 @@ def load() -> ctypes.CDLL:
         lib.pkv_kv_append_fp8.restype = i32
         lib.pkv_kv_append_fp8.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp, vp, vp, i64, i32, vp, vp]
         lib.pkv_decode_workspace_size.restype = sz
-        lib.pkv_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.pkv_decode_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
         lib.pkv_paged_gqa_decode.restype = i32
-        lib.pkv_paged_gqa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32, i64,
-                                             f32, vp, i32, vp, sz, vp, i32, vp]
+        lib.pkv_paged_gqa_decode.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32,
+                                             i64, f32, vp, i32, vp, sz, vp, i32, vp]
         lib.pkv_append_decode_fp8.restype = i32
-        lib.pkv_append_decode_fp8.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32,
-                                              i32, i64, f32, vp, i32, vp, sz, vp, i32, vp]
+        lib.pkv_append_decode_fp8.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32,
+                                              i32, i32, i32, i64, f32, vp, i32, vp, sz, vp, i32, vp]
         lib.pkv_kv_calibrate.restype = i32
         lib.pkv_kv_calibrate.argtypes = [vp, vp, i32, i64, i32, i32, vp, vp, vp, vp, vp]
         lib.pkv_paged_gqa_decode_noalloc.restype = i32
-        lib.pkv_paged_gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
-                                                     i64, f32, vp, i32, vp, i32, vp]
+        lib.pkv_paged_gqa_decode_noalloc.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32,
+                                                     i32, i64, f32, vp, i32, vp, i32, vp]
         lib.pkv_decode_noalloc_scratch_bytes.restype = sz
         lib.pkv_decode_noalloc_scratch_bytes.argtypes = []
         lib.pkv_prefill_workspace_size.restype = sz
@@ -143,6 +143,13 @@ def _same_device(ref, *ts):
     for t in ts:
         if t is not None and t.device != ref.device:
             raise ValueError(f"all tensors must be on {ref.device}, got one on {t.device}")
+
+
+def _check_page_sizes(seq_page_sizes, batch):
+    if seq_page_sizes is not None:
+        _need(seq_page_sizes, "seq_page_sizes", torch.int32, 1)
+        if seq_page_sizes.shape[0] != batch:
+            raise ValueError("seq_page_sizes must have one entry per sequence")
 
 
 def _need(t, name, dtype=None, dim=None, cuda=True):
@@ -219,17 +226,21 @@ def pkv_kv_calibrate(k_new, v_new, k_running_max, v_running_max, k_scale=None, v
         raise PkvError(st, "pkv_kv_calibrate")
 
 
-def pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim=HEAD_DIM, page_size=16,
+def pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim=HEAD_DIM, max_seq_len=0, page_size=16,
                               max_ctas=0) -> int:
-    return int(load().pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, page_size,
-                                                max_ctas))
+    """Workspace bytes of a decode call whose seq_lens are all <= max_seq_len."""
+    return int(load().pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, int(max_seq_len),
+                                                page_size, max_ctas))
 
 
 def pkv_paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace,
-                         sm_scale=None, device_error=None, max_ctas=0, stream=None) -> None:
+                         sm_scale=None, device_error=None, max_ctas=0, stream=None, max_seq_len=0,
+                         seq_page_sizes=None) -> None:
     """q bf16 [B, Hq, 128]; caches uint8 [num_pages, Hkv, P, 128]; scales fp32
     [Hkv]; block_table int32 [B, max_pages]; seq_lens int32 [B]; out
-    [B, Hq, 128] bf16 or fp32; workspace uint8 (pkv_decode_workspace_size bytes)."""
+    [B, Hq, 128] bf16 or fp32; workspace uint8 (pkv_decode_workspace_size
+    bytes for max_seq_len); seq_page_sizes int32 [B] or None (tokens per page
+    of each sequence, a power-of-two multiple of P: runs of pool pages)."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_cache, "k_cache", torch.uint8, 4)
     _need(v_cache, "v_cache", torch.uint8, 4)
@@ -247,20 +258,24 @@ def pkv_paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq
         raise ValueError("q / cache / out shapes disagree")
     if block_table.shape[0] != B or seq_lens.shape[0] != B:
         raise ValueError("block_table / seq_lens shapes disagree with q")
-    _same_device(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace, device_error)
+    _check_page_sizes(seq_page_sizes, B)
+    _same_device(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace, device_error,
+                 seq_page_sizes)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     with _device_of(q):
         st = load().pkv_paged_gqa_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
-                                         _ptr(block_table), block_table.shape[1], _ptr(seq_lens), B, Hq, Hkv, D, P,
-                                         NP, float(sm_scale), _ptr(out), _act_code(out), _ptr(workspace),
-                                         workspace.numel(), _ptr(device_error), int(max_ctas), _stream(stream))
+                                         _ptr(block_table), block_table.shape[1], _ptr(seq_lens), int(max_seq_len),
+                                         _ptr(seq_page_sizes), B, Hq, Hkv, D, P, NP, float(sm_scale), _ptr(out),
+                                         _act_code(out), _ptr(workspace), workspace.numel(), _ptr(device_error),
+                                         int(max_ctas), _stream(stream))
     if st != 0:
         raise PkvError(st, "pkv_paged_gqa_decode")
 
 
 def pkv_append_decode_fp8(k_new, v_new, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out,
-                          workspace, sm_scale=None, device_error=None, max_ctas=0, stream=None) -> None:
+                          workspace, sm_scale=None, device_error=None, max_ctas=0, stream=None, max_seq_len=0,
+                          seq_page_sizes=None) -> None:
     """One fused decode step: k_new/v_new [B, n_new, Hkv, 128] (fp32|bf16) are
     quantised into the cache at positions seq_lens[b] - n_new .. seq_lens[b] - 1
     (seq_lens counts them), then attention as pkv_paged_gqa_decode."""
@@ -286,34 +301,50 @@ def pkv_append_decode_fp8(k_new, v_new, q, k_cache, v_cache, k_scale, v_scale, b
         raise ValueError("k_new / v_new must be [B, n_new, Hkv, head_dim]")
     if block_table.shape[0] != B or seq_lens.shape[0] != B:
         raise ValueError("block_table / seq_lens shapes disagree with q")
-    _same_device(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace, k_new, v_new, device_error)
+    _check_page_sizes(seq_page_sizes, B)
+    _same_device(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace, k_new, v_new,
+                 device_error, seq_page_sizes)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     with _device_of(k_new):
         st = load().pkv_append_decode_fp8(_ptr(k_new), _ptr(v_new), _act_code(k_new), n_new, _ptr(q), _ptr(k_cache),
                                           _ptr(v_cache), _ptr(k_scale), _ptr(v_scale), _ptr(block_table),
-                                          block_table.shape[1], _ptr(seq_lens), B, Hq, Hkv, D, P, NP, float(sm_scale),
-                                          _ptr(out), _act_code(out), _ptr(workspace), workspace.numel(),
-                                          _ptr(device_error), int(max_ctas), _stream(stream))
+                                          block_table.shape[1], _ptr(seq_lens), int(max_seq_len),
+                                          _ptr(seq_page_sizes), B, Hq, Hkv, D, P, NP, float(sm_scale), _ptr(out),
+                                          _act_code(out), _ptr(workspace), workspace.numel(), _ptr(device_error),
+                                          int(max_ctas), _stream(stream))
     if st != 0:
         raise PkvError(st, "pkv_append_decode_fp8")
 
 
 def append_decode_fp8(k_new, v_new, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out=None,
                       out_dtype=torch.bfloat16, workspace=None, sm_scale=None, device_error=None, max_ctas=0,
-                      stream=None) -> torch.Tensor:
+                      stream=None, max_seq_len=0, seq_page_sizes=None) -> torch.Tensor:
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    max_seq_len = _default_max_len(block_table, k_cache, max_seq_len, seq_page_sizes)
     if workspace is None:
         workspace = decode_workspace(q.shape[0], q.shape[1], k_cache.shape[1], k_cache.shape[2], q.device,
-                                     max_ctas)
+                                     max_ctas, max_seq_len)
     pkv_append_decode_fp8(k_new, v_new, q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out,
-                          workspace, sm_scale, device_error, max_ctas, stream)
+                          workspace, sm_scale, device_error, max_ctas, stream, max_seq_len, seq_page_sizes)
     return out
 
 
+def _default_max_len(block_table, k_cache, max_seq_len, seq_page_sizes):
+    """The allocating forms bound seq_lens by the table's capacity at the pool
+    page size unless told otherwise; with per-sequence page sizes the bound
+    must be given."""
+    if max_seq_len:
+        return int(max_seq_len)
+    if seq_page_sizes is not None:
+        raise ValueError("give max_seq_len when seq_page_sizes is given")
+    return int(block_table.shape[1] * k_cache.shape[2])
+
+
 def pkv_paged_gqa_decode_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out,
-                                 sm_scale=None, device_error=None, max_ctas=0, stream=None) -> None:
+                                 sm_scale=None, device_error=None, max_ctas=0, stream=None, max_seq_len=0,
+                                 seq_page_sizes=None) -> None:
     """pkv_paged_gqa_decode without a workspace, for callers that cannot
     allocate device memory: the split-K scratch is a fixed array inside the
     library (see pkv_decode_noalloc_scratch_bytes).  Calls that overlap on the
@@ -334,14 +365,16 @@ def pkv_paged_gqa_decode_noalloc(q, k_cache, v_cache, k_scale, v_scale, block_ta
         raise ValueError("q / cache / out shapes disagree")
     if block_table.shape[0] != B or seq_lens.shape[0] != B:
         raise ValueError("block_table / seq_lens shapes disagree with q")
-    _same_device(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, device_error)
+    _check_page_sizes(seq_page_sizes, B)
+    _same_device(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, device_error, seq_page_sizes)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     with _device_of(q):
         st = load().pkv_paged_gqa_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                                  _ptr(v_scale), _ptr(block_table), block_table.shape[1],
-                                                 _ptr(seq_lens), B, Hq, Hkv, D, P, NP, float(sm_scale), _ptr(out),
-                                                 _act_code(out), _ptr(device_error), int(max_ctas), _stream(stream))
+                                                 _ptr(seq_lens), int(max_seq_len), _ptr(seq_page_sizes), B, Hq, Hkv,
+                                                 D, P, NP, float(sm_scale), _ptr(out), _act_code(out),
+                                                 _ptr(device_error), int(max_ctas), _stream(stream))
     if st != 0:
         raise PkvError(st, "pkv_paged_gqa_decode_noalloc")
 
@@ -353,16 +386,18 @@ def pkv_decode_noalloc_scratch_bytes() -> int:
 _ws_cache: dict = {}
 
 
-def decode_workspace(batch, num_q_heads, num_kv_heads, page_size, device=None, max_ctas=0) -> torch.Tensor:
+def decode_workspace(batch, num_q_heads, num_kv_heads, page_size, device=None, max_ctas=0,
+                     max_seq_len=0) -> torch.Tensor:
     """A workspace tensor for these sizes, cached per (device, stream, sizes).
     Calls that use it must not overlap on the GPU (same stream is fine)."""
     device = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
     stream = torch.cuda.current_stream(device).cuda_stream
-    key = (device.index, stream, batch, num_q_heads, num_kv_heads, page_size, max_ctas)
+    key = (device.index, stream, batch, num_q_heads, num_kv_heads, page_size, max_ctas, max_seq_len)
     ws = _ws_cache.get(key)
     if ws is None:
         with torch.cuda.device(device):
-            n = pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, HEAD_DIM, page_size, max_ctas)
+            n = pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, HEAD_DIM, max_seq_len, page_size,
+                                          max_ctas)
         if n == 0:
             raise PkvError(4, "pkv_decode_workspace_size")
         ws = torch.empty(n, dtype=torch.uint8, device=device)
@@ -377,14 +412,15 @@ def kv_append_fp8(k_new, v_new, slot_mapping, k_scale, v_scale, k_cache, v_cache
 
 def paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out=None,
                      out_dtype=torch.bfloat16, workspace=None, sm_scale=None, device_error=None, max_ctas=0,
-                     stream=None) -> torch.Tensor:
+                     stream=None, max_seq_len=0, seq_page_sizes=None) -> torch.Tensor:
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
+    max_seq_len = _default_max_len(block_table, k_cache, max_seq_len, seq_page_sizes)
     if workspace is None:
         workspace = decode_workspace(q.shape[0], q.shape[1], k_cache.shape[1], k_cache.shape[2], q.device,
-                                     max_ctas)
+                                     max_ctas, max_seq_len)
     pkv_paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace,
-                         sm_scale, device_error, max_ctas, stream)
+                         sm_scale, device_error, max_ctas, stream, max_seq_len, seq_page_sizes)
     return out
 
 

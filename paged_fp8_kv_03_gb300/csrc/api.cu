@@ -164,6 +164,19 @@ int decode_num_ctas(int page_size, int batch, int max_ctas)
     return c;
 }
 
+// Workspace for a call whose sequences are at most max_len tokens: header and
+// segment records, then one partial slot per (worker, sub-piece) plus one per
+// segment.  The sub-pieces per worker follow from the largest possible list.
+size_t decode_workspace_bytes(int batch, int hq, int hkv, long long max_len, int num_ctas)
+{
+    const long long workers = static_cast<long long>(num_ctas) * kWarps;
+    const long long total_max = static_cast<long long>(batch) * hkv * ((max_len + 15) / 16);
+    const long long subs = decode_subs(total_max, workers);
+    const size_t slots = static_cast<size_t>(workers * subs) + static_cast<size_t>(batch) * hkv;
+    const size_t bytes = slots * static_cast<size_t>(hq / hkv) * kPartialStride * sizeof(float);
+    return decode_segment_bytes(batch, hkv) + ((bytes + 255) & ~size_t(255));
+}
+
 }  // namespace pkv
 
 using namespace pkv;
@@ -190,24 +203,28 @@ pkv_status check_decode_shape(int batch, int hq, int hkv, int head_dim, int page
     return PKV_OK;
 }
 
-size_t workspace_bytes_for(int batch, int hq, int hkv, int num_ctas)
+// Effective bound of seq_lens: max_seq_len, or the table's capacity at the
+// pool page size when max_seq_len is 0.
+long long effective_max_len(int max_seq_len, int max_pages, int page_size)
 {
-    const size_t slots = static_cast<size_t>(num_ctas) * kWarps + static_cast<size_t>(batch) * hkv;
-    const size_t bytes = slots * static_cast<size_t>(hq / hkv) * kPartialStride * sizeof(float);
-    return decode_segment_bytes(batch, hkv) + ((bytes + 255) & ~size_t(255));
+    return max_seq_len > 0 ? max_seq_len : static_cast<long long>(max_pages) * page_size;
 }
 
 pkv_status decode_impl(const void *k_new, const void *v_new, int in_dtype, int n_new, const void *q, uint8_t *k_cache,
                        uint8_t *v_cache, const float *k_scale, const float *v_scale, const int32_t *block_table,
-                       int max_pages_per_seq, const int32_t *seq_lens, int batch, int num_q_heads, int num_kv_heads,
-                       int head_dim, int page_size, int64_t num_pages, float sm_scale, void *out, int out_dtype,
-                       void *workspace, size_t workspace_bytes, int32_t *device_error, int max_ctas,
-                       cudaStream_t stream)
+                       int max_pages_per_seq, const int32_t *seq_lens, int max_seq_len, const int32_t *seq_page_sizes,
+                       int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
+                       float sm_scale, void *out, int out_dtype, void *workspace, size_t workspace_bytes,
+                       int32_t *device_error, int max_ctas, cudaStream_t stream)
 {
     pkv_status st = check_decode_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_seq,
                                        num_pages);
     if (st != PKV_OK)
         return st;
+    if (max_seq_len < 0)
+        return PKV_ERR_SHAPE;
+    if (seq_page_sizes && static_cast<int64_t>(max_pages_per_seq) * 256 >= (int64_t(1) << 31))
+        return PKV_ERR_UNSUPPORTED;
     if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
         return PKV_ERR_DTYPE;
     if (!(sm_scale == sm_scale) || isinf(sm_scale))
@@ -218,15 +235,18 @@ pkv_status decode_impl(const void *k_new, const void *v_new, int in_dtype, int n
         return PKV_ERR_NULL;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4) ||
-        !aligned(device_error, 4))
+        !aligned(device_error, 4) || !aligned(seq_page_sizes, 4))
         return PKV_ERR_ALIGN;
     if (!workspace || !aligned(workspace, 256))
         return PKV_ERR_WORKSPACE;
 
+    const long long max_len = effective_max_len(max_seq_len, max_pages_per_seq, page_size);
+    if (max_len >= (int64_t(1) << 31))
+        return PKV_ERR_UNSUPPORTED;
     const int ctas = decode_num_ctas(page_size, batch, max_ctas);
     if (ctas <= 0)
         return PKV_ERR_CUDA;
-    if (workspace_bytes < workspace_bytes_for(batch, num_q_heads, num_kv_heads, ctas))
+    if (workspace_bytes < decode_workspace_bytes(batch, num_q_heads, num_kv_heads, max_len, ctas))
         return PKV_ERR_WORKSPACE;
 
     alignas(64) CUtensorMap tm_k;
@@ -242,11 +262,14 @@ pkv_status decode_impl(const void *k_new, const void *v_new, int in_dtype, int n
     a.block_table = block_table;
     a.max_pages = max_pages_per_seq;
     a.seq_lens = seq_lens;
+    a.max_len = static_cast<int>(max_len);
+    a.page_sizes = seq_page_sizes;
     a.batch = batch;
     a.hq = num_q_heads;
     a.hkv = num_kv_heads;
     a.group = num_q_heads / num_kv_heads;
     a.page_size = page_size;
+    a.pool_log2 = 31 - __builtin_clz(static_cast<unsigned>(page_size));
     a.num_pages = num_pages;
     a.sm_scale_log2 = sm_scale * 1.4426950408889634f;
     a.out = out;
@@ -257,7 +280,8 @@ pkv_status decode_impl(const void *k_new, const void *v_new, int in_dtype, int n
     a.n_new = n_new;
     a.k_pool = k_cache;
     a.v_pool = v_cache;
-    a.seg_pieces = static_cast<int2 *>(workspace);
+    a.header = static_cast<DecodeHeader *>(workspace);
+    a.segs = reinterpret_cast<SegRecord *>(static_cast<uint8_t *>(workspace) + sizeof(DecodeHeader));
     a.partials = reinterpret_cast<float *>(static_cast<uint8_t *>(workspace) + decode_segment_bytes(batch, num_kv_heads));
     a.err = device_error;
     a.num_ctas = ctas;
@@ -350,36 +374,38 @@ pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, int in_dtype,
     return launch_kv_append(a, stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
 }
 
-size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
-                                 int max_ctas)
+size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim, int max_seq_len,
+                                 int page_size, int max_ctas)
 {
-    if (check_decode_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, 1, 1) != PKV_OK)
+    if (check_decode_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, 1, 1) != PKV_OK ||
+        max_seq_len < 0)
         return 0;
     const int ctas = decode_num_ctas(page_size, batch, max_ctas);
     if (ctas <= 0)
         return 0;
-    return workspace_bytes_for(batch, num_q_heads, num_kv_heads, ctas);
+    return decode_workspace_bytes(batch, num_q_heads, num_kv_heads, max_seq_len, ctas);
 }
 
 pkv_status pkv_paged_gqa_decode(const void *q, const uint8_t *k_cache, const uint8_t *v_cache, const float *k_scale,
                                 const float *v_scale, const int32_t *block_table, int max_pages_per_seq,
-                                const int32_t *seq_lens, int batch, int num_q_heads, int num_kv_heads,
-                                int head_dim, int page_size, int64_t num_pages, float sm_scale, void *out,
-                                int out_dtype, void *workspace, size_t workspace_bytes, int32_t *device_error,
-                                int max_ctas, cudaStream_t stream)
+                                const int32_t *seq_lens, int max_seq_len, const int32_t *seq_page_sizes, int batch,
+                                int num_q_heads, int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
+                                float sm_scale, void *out, int out_dtype, void *workspace, size_t workspace_bytes,
+                                int32_t *device_error, int max_ctas, cudaStream_t stream)
 {
     return decode_impl(nullptr, nullptr, PKV_F32, 0, q, const_cast<uint8_t *>(k_cache), const_cast<uint8_t *>(v_cache),
-                       k_scale, v_scale, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, num_kv_heads,
-                       head_dim, page_size, num_pages, sm_scale, out, out_dtype, workspace, workspace_bytes,
-                       device_error, max_ctas, stream);
+                       k_scale, v_scale, block_table, max_pages_per_seq, seq_lens, max_seq_len, seq_page_sizes, batch,
+                       num_q_heads, num_kv_heads, head_dim, page_size, num_pages, sm_scale, out, out_dtype, workspace,
+                       workspace_bytes, device_error, max_ctas, stream);
 }
 
 pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dtype, int n_new, const void *q,
                                  uint8_t *k_cache, uint8_t *v_cache, const float *k_scale, const float *v_scale,
                                  const int32_t *block_table, int max_pages_per_seq, const int32_t *seq_lens,
-                                 int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
-                                 int64_t num_pages, float sm_scale, void *out, int out_dtype, void *workspace,
-                                 size_t workspace_bytes, int32_t *device_error, int max_ctas, cudaStream_t stream)
+                                 int max_seq_len, const int32_t *seq_page_sizes, int batch, int num_q_heads,
+                                 int num_kv_heads, int head_dim, int page_size, int64_t num_pages, float sm_scale,
+                                 void *out, int out_dtype, void *workspace, size_t workspace_bytes,
+                                 int32_t *device_error, int max_ctas, cudaStream_t stream)
 {
     if (n_new < 0)
         return PKV_ERR_SHAPE;
@@ -392,9 +418,9 @@ pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dt
             return PKV_ERR_ALIGN;
     }
     return decode_impl(n_new > 0 ? k_new : nullptr, n_new > 0 ? v_new : nullptr, in_dtype, n_new, q, k_cache, v_cache,
-                       k_scale, v_scale, block_table, max_pages_per_seq, seq_lens, batch, num_q_heads, num_kv_heads,
-                       head_dim, page_size, num_pages, sm_scale, out, out_dtype, workspace, workspace_bytes,
-                       device_error, max_ctas, stream);
+                       k_scale, v_scale, block_table, max_pages_per_seq, seq_lens, max_seq_len, seq_page_sizes, batch,
+                       num_q_heads, num_kv_heads, head_dim, page_size, num_pages, sm_scale, out, out_dtype, workspace,
+                       workspace_bytes, device_error, max_ctas, stream);
 }
 
 size_t pkv_prefill_workspace_size(int batch, int num_kv_heads, int max_kv_len)

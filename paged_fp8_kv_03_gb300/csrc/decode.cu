@@ -65,6 +65,46 @@ __device__ __forceinline__ int clamp_len(int L, int cap)
     return L < 0 ? 0 : (L > cap ? cap : L);
 }
 
+// log2 of sequence b's page size in tokens (its pages are runs of
+// P_b / page_size consecutive pool pages), or -1 if P_b is not a power of two
+// in [page_size, 256].
+__device__ __forceinline__ int page_log2_of(const DecodeArgs &a, int b)
+{
+    if (a.page_sizes == nullptr)
+        return a.pool_log2;
+    const int pb = __ldg(a.page_sizes + b);
+    if (pb < a.page_size || pb > 256 || (pb & (pb - 1)) != 0)
+        return -1;
+    return 31 - __clz(pb);
+}
+
+// Tokens of sequence b the call attends: seq_lens[b] clamped to [0, min(max_len,
+// max_pages * P_b)]; 0 for an invalid page size.
+__device__ __forceinline__ int seq_len_of(const DecodeArgs &a, int b)
+{
+    const int lp = page_log2_of(a, b);
+    if (lp < 0)
+        return 0;
+    const long long cap_pages = static_cast<long long>(a.max_pages) << lp;
+    const int cap = cap_pages < a.max_len ? static_cast<int>(cap_pages) : a.max_len;
+    return clamp_len(__ldg(a.seq_lens + b), cap);
+}
+
+// Pool page and row of token t of sequence b (lp = page_log2_of): entry
+// bt[b][t / P_b] is the first pool page of the run holding the logical page,
+// offset o = t % P_b lies in pool page entry + o / P, row o % P.  Returns
+// false for an entry outside the pool.
+__device__ __forceinline__ bool token_page(const DecodeArgs &a, int b, int lp, int t, int &phys, int &row)
+{
+    const int entry = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + (t >> lp));
+    const int o = t & ((1 << lp) - 1);
+    if (entry < 0 || entry >= a.num_pages)
+        return false;
+    phys = entry + (o >> a.pool_log2);
+    row = o & (a.page_size - 1);
+    return phys < a.num_pages;
+}
+
 __device__ __forceinline__ int chunks_of(const int *ps, int b)
 {
     return ps[b + 1] - ps[b];
@@ -353,9 +393,8 @@ __device__ int first_tail_chunk(const DecodeArgs &a, const int *pstart, int64_t 
 // else reads or writes them in this call), then orders those generic-proxy
 // stores before its own TMA reads.  Lanes split the 128 dims, 4 each.
 __device__ __noinline__ void append_own_tokens(const DecodeArgs &a, const int *pstart, int64_t lo, int64_t hi,
-                                               int cap, int lane)
+                                               int lane)
 {
-    const int P = a.page_size;
     Loc l = locate(pstart, a.batch, a.hkv, lo);
     int64_t cur = lo;
     const int tail_pages = 1 + (a.n_new + kChunk - 1) / kChunk;   // new tokens live in a segment's last chunks
@@ -367,21 +406,22 @@ __device__ __noinline__ void append_own_tokens(const DecodeArgs &a, const int *p
             l = advance(pstart, a.batch, a.hkv, l, n_piece);
             continue;
         }
-        const int L = clamp_len(__ldg(a.seq_lens + l.b), cap);
+        const int L = seq_len_of(a, l.b);
+        const int lp = page_log2_of(a, l.b);
         const int first = max(0, L - a.n_new);            // positions [first, L) are new
         for (int t = first; t < L; ++t) {
             const int ck = t / kChunk;                     // the worker owning this chunk stores the token
             if (ck < l.ck || ck >= l.ck + n_piece)
                 continue;
-            const int phys = __ldg(a.block_table + static_cast<int64_t>(l.b) * a.max_pages + t / P);
-            if (phys < 0 || phys >= a.num_pages) {
+            int phys, row;
+            if (!token_page(a, l.b, lp, t, phys, row)) {
                 if (a.err && lane == 0)
                     atomicOr(a.err, PKV_DEVERR_PAGE);
                 continue;
             }
             const int j = t - (L - a.n_new);
             const int64_t src = ((static_cast<int64_t>(l.b) * a.n_new + j) * a.hkv + l.h) * kHeadDim + 4 * lane;
-            const int64_t dst = ((static_cast<int64_t>(phys) * a.hkv + l.h) * P + t % P) * kHeadDim + 4 * lane;
+            const int64_t dst = ((static_cast<int64_t>(phys) * a.hkv + l.h) * a.page_size + row) * kHeadDim + 4 * lane;
             float k4[4], v4[4];
             if (a.new_bf16) {
                 const uint2 kb = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(a.k_new) + src));
@@ -412,7 +452,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 {
     using S = Smem;
     constexpr int kStages = S::kStages;
-    const int P = a.page_size;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -420,7 +459,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int *pstart = reinterpret_cast<int *>(smem + S::kPstart);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kFlag);
     int *warp_sum = reinterpret_cast<int *>(smem + S::kWarpSum);
-    const int cap = a.max_pages * P;
 
     // ---- per-sequence page offsets (every CTA computes them; B ints from L2)
     {
@@ -428,7 +466,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int b0 = min(a.batch, tid * chunk), b1 = min(a.batch, b0 + chunk);
         int local = 0;
         for (int b = b0; b < b1; ++b)
-            local += (clamp_len(__ldg(a.seq_lens + b), cap) + kChunk - 1) / kChunk;
+            local += (seq_len_of(a, b) + kChunk - 1) / kChunk;
         int incl = local;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -451,11 +489,16 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             base += warp_sum[w];
         int run = base + incl - local;
         for (int b = b0; b < b1; ++b) {
-            const int L = __ldg(a.seq_lens + b);
+            const int L = seq_len_of(a, b);
             pstart[b] = run;
-            run += (clamp_len(L, cap) + kChunk - 1) / kChunk;
-            if (blockIdx.x == 0 && a.err && (L < 0 || L > cap || (a.k_new != nullptr && L < a.n_new)))
-                atomicOr(a.err, PKV_DEVERR_SEQLEN);
+            run += (L + kChunk - 1) / kChunk;
+            if (blockIdx.x == 0 && a.err) {
+                const int raw = __ldg(a.seq_lens + b);
+                if (page_log2_of(a, b) < 0)
+                    atomicOr(a.err, PKV_DEVERR_PAGESIZE);
+                else if (raw != L || (a.k_new != nullptr && L < a.n_new))
+                    atomicOr(a.err, PKV_DEVERR_SEQLEN);
+            }
         }
         if (tid == kThreads - 1)
             pstart[a.batch] = base + incl;
@@ -475,23 +518,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int workers = a.num_ctas * kWarps;
     const int worker = blockIdx.x * kWarps + warp;
     const int64_t total = static_cast<int64_t>(pstart[a.batch]) * a.hkv;
+    const int subs = static_cast<int>(decode_subs(total, workers));
 
-    // Piece table for the merge kernel: first and last worker of every
-    // segment that more than one worker touches (-1: nothing to merge).
+    // Segment records for the merge kernel: where each segment lies in the
+    // list and whether its pieces need merging (it spans several workers, or
+    // a sub-piece cut of its worker falls inside it).
     if (blockIdx.x == 0) {
         for (int sg = tid; sg < a.batch * a.hkv; sg += kThreads) {
             const int b = sg / a.hkv, h = sg % a.hkv, np = chunks_of(pstart, b);
-            int2 r = make_int2(-1, -1);
+            SegRecord r;
+            r.start = static_cast<long long>(pstart[b]) * a.hkv + static_cast<long long>(h) * np;
+            r.n = np;
+            r.w0 = -1;
             if (np > 0) {
-                const int64_t start = static_cast<int64_t>(pstart[b]) * a.hkv + static_cast<int64_t>(h) * np;
-                const int w0 = worker_of(start, total, workers), w1 = worker_of(start + np - 1, total, workers);
-                if (w0 != w1)
-                    r = make_int2(w0, w1);
+                const int w0 = worker_of(r.start, total, workers), w1 = worker_of(r.start + np - 1, total, workers);
+                const int64_t lo0 = static_cast<int64_t>(w0) * total / workers;
+                if (w0 != w1 || (r.start - lo0) / kChainChunks != (r.start + np - 1 - lo0) / kChainChunks)
+                    r.w0 = w0;
             }
-            a.seg_pieces[sg] = r;
+            a.segs[sg] = r;
         }
-        if (tid == 0)
-            a.seg_pieces[a.batch * a.hkv] = make_int2(static_cast<int>(total & 0x7FFFFFFF), static_cast<int>(total >> 31));
+        if (tid == 0) {
+            DecodeHeader hd;
+            hd.total = total;
+            hd.subs = subs;
+            hd.pad = 0;
+            *a.header = hd;
+        }
     }
     // Let the merge kernel get scheduled now; it waits for this grid to finish.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -508,22 +561,22 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const bool append_early =
         a.k_new != nullptr && first_tail_chunk(a, pstart, lo, hi) < S::kStages;
     if (append_early)
-        append_own_tokens(a, pstart, lo, hi, cap, lane);
+        append_own_tokens(a, pstart, lo, hi, lane);
 
     const uint32_t ring = smem_addr(smem) + warp * S::kWarpRing;
     const uint32_t bars = smem_addr(smem + S::kBar) + warp * kStages * 8;
     const uint64_t policy = l2_policy_evict_first();
     const int zoob = static_cast<int>(a.num_pages * a.hkv);   // first out-of-pool tile: reads zeros
-    const int cpp = P / kChunk;                                // chunks per page
-    // TMA coordinates of a chunk: tile z = page * hkv + head, row y = 16 * (chunk within page).
+    // TMA coordinates of a chunk: tile z = pool page * hkv + head, row y = the
+    // chunk's first row within that pool page.
     auto tile_zy = [&](Loc l) -> int2 {
-        const int phys = __ldg(a.block_table + static_cast<int64_t>(l.b) * a.max_pages + l.ck / cpp);
-        if (phys < 0 || phys >= a.num_pages) {
+        int phys, row;
+        if (!token_page(a, l.b, page_log2_of(a, l.b), l.ck * kChunk, phys, row)) {
             if (a.err)
                 atomicOr(a.err, PKV_DEVERR_PAGE);
             return make_int2(zoob, 0);
         }
-        return make_int2(phys * a.hkv + l.h, (l.ck % cpp) * kChunk);
+        return make_int2(phys * a.hkv + l.h, row);
     };
 
     // ---- block-table batches: zcur holds chunks [32*fb, 32*fb+32), znext the next 32
@@ -566,7 +619,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     for (int f = 0; f < kStages && f < n_total; ++f)
         issue(f);
     if (a.k_new != nullptr && !append_early)
-        append_own_tokens(a, pstart, lo, hi, cap, lane);
+        append_own_tokens(a, pstart, lo, hi, lane);
 
     const int gid = lane >> 2, t4 = lane & 3;
     const TileOffsets off = tile_offsets(lane);
@@ -575,8 +628,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int k = 0;
     while (k < n_total) {
         const int np = chunks_of(pstart, cons.b);
-        const int n_piece = min(np - cons.ck, n_total - k);
-        const int L = clamp_len(__ldg(a.seq_lens + cons.b), cap);
+        // a piece ends at its segment's end, the worker's range end, or the
+        // next sub-piece cut (every kChainChunks chunks of the range)
+        const int n_piece = min(min(np - cons.ck, n_total - k), kChainChunks - (k & (kChainChunks - 1)));
+        const int slot_index = worker * subs + k / kChainChunks;
+        const int L = seq_len_of(a, cons.b);
         const bool whole = (cons.ck == 0) && (n_piece == np);
         const int seg = cons.b * a.hkv + cons.h;
         const float scale2 = __ldg(a.k_scale + cons.h) * a.sm_scale_log2;
@@ -653,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     store_pair(a, row0 + 2 * t4 + 1, d, acc[sg][1] * s1, acc[sg][3] * s1);
             }
         } else {
-            float *slot = a.partials + static_cast<int64_t>(worker + seg) * a.group * kPartialStride;
+            float *slot = a.partials + static_cast<int64_t>(slot_index + seg) * a.group * kPartialStride;
 #pragma unroll
             for (int sg = 0; sg < 8; ++sg) {
                 const int d = 16 * sg + 2 * gid;
@@ -683,45 +739,42 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 constexpr int kMergeThreads = kHeadDim;   // one thread per dimension
 
 // One CTA per (segment, head g): merges the partial states that the workers
-// covering the segment wrote for that head, in worker order, and writes the
-// output row.  When the list has at least as many page-heads as workers, the
-// pieces come from the contiguous workers w0..w1; otherwise every worker owns
-// at most one page-head and piece i comes from the worker owning position
-// x0 + i.
+// covering the segment wrote for that head, in list order, and writes the
+// output row.  With one sub-piece per worker range (subs == 1) the pieces
+// come from the consecutive workers w0..w1 when the list has at least as many
+// chunk-heads as workers, and otherwise (every worker owns at most one
+// chunk-head) piece i comes from the worker owning position start + i.  With
+// subs > 1 a worker's range is also cut every kChainChunks chunks, and the
+// pieces are walked worker by worker.
 __global__ void __launch_bounds__(kMergeThreads) splitk_merge_kernel(const DecodeArgs a)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid has finished
     const int seg = blockIdx.x, g = blockIdx.y, d = threadIdx.x;
-    const int2 r = a.seg_pieces[seg];
-    if (r.x < 0)
+    const SegRecord r = a.segs[seg];
+    if (r.w0 < 0)
         return;
-    const int2 tw = a.seg_pieces[a.batch * a.hkv];
-    const int64_t total = static_cast<int64_t>(tw.x) | (static_cast<int64_t>(tw.y) << 31);
+    const DecodeHeader hd = *a.header;
+    const int64_t total = hd.total;
+    const int subs = hd.subs;
     const int workers = a.num_ctas * kWarps;
-    const bool dense = total >= workers;
-    const int64_t x0 = dense ? 0 : static_cast<int64_t>(r.x) * total / workers;
-    const int n_pieces = dense ? r.y - r.x + 1
-                               : static_cast<int>(static_cast<int64_t>(r.y) * total / workers - x0 + 1);
     const int b = seg / a.hkv, h = seg % a.hkv;
-    auto piece_worker = [&](int i) { return dense ? r.x + i : worker_of(x0 + i, total, workers); };
-    auto slot = [&](int w) { return a.partials + (static_cast<int64_t>(w + seg) * a.group + g) * kPartialStride; };
+    auto slot = [&](int s) { return a.partials + (static_cast<int64_t>(s + seg) * a.group + g) * kPartialStride; };
 
-    // Pieces in groups of 8: all loads of a group are issued together, then
-    // folded into the running (M, L, A) with an exact rescale.  Every thread
-    // computes the same M and L; the order is fixed, so results are
-    // deterministic.
     constexpr int kGroup = 8;
     float M = -INFINITY, L = 0.f, A = 0.f;
-    for (int c0 = 0; c0 < n_pieces; c0 += kGroup) {
-        const int n = min(kGroup, n_pieces - c0);
+    // Folds up to kGroup pieces (slot indices in sl[0..n)): all loads issued
+    // together, then an exact rescale into the running (M, L, A).  Every
+    // thread computes the same M and L; the order is fixed, so results are
+    // deterministic.
+    auto fold = [&](const int (&sl)[kGroup], int n) {
         float m[kGroup], l[kGroup], v[kGroup];
 #pragma unroll
         for (int i = 0; i < kGroup; ++i) {
             if (i < n) {
-                const float *sl = slot(piece_worker(c0 + i));
-                m[i] = sl[kHeadDim];
-                l[i] = sl[kHeadDim + 1];
-                v[i] = sl[d];
+                const float *p = slot(sl[i]);
+                m[i] = p[kHeadDim];
+                l[i] = p[kHeadDim + 1];
+                v[i] = p[d];
             }
         }
         float mc = M;
@@ -741,7 +794,42 @@ __global__ void __launch_bounds__(kMergeThreads) splitk_merge_kernel(const Decod
             }
         }
         M = mc;
+    };
+
+    int sl[kGroup];
+    int n = 0;
+    if (subs == 1) {
+        const int w1 = worker_of(r.start + r.n - 1, total, workers);
+        const bool dense = total >= workers;
+        const int n_pieces = dense ? w1 - r.w0 + 1 : r.n;
+        for (int i = 0; i < n_pieces; ++i) {
+            sl[n++] = dense ? r.w0 + i : worker_of(r.start + i, total, workers);
+            if (n == kGroup) {
+                fold(sl, n);
+                n = 0;
+            }
+        }
+    } else {
+        const int64_t end = r.start + r.n;
+        int64_t x = r.start;
+        int w = r.w0;
+        while (x < end) {
+            const int64_t lo_w = static_cast<int64_t>(w) * total / workers;
+            const int64_t hi_w = static_cast<int64_t>(w + 1) * total / workers;
+            const int64_t e = end < hi_w ? end : hi_w;
+            for (int64_t k = x - lo_w; lo_w + k < e; k = (k / kChainChunks + 1) * kChainChunks) {
+                sl[n++] = w * subs + static_cast<int>(k / kChainChunks);
+                if (n == kGroup) {
+                    fold(sl, n);
+                    n = 0;
+                }
+            }
+            x = e;
+            ++w;
+        }
     }
+    if (n > 0)
+        fold(sl, n);
     const float vsc = __ldg(a.v_scale + h);
     store_out(a, static_cast<int64_t>(b) * a.hq + static_cast<int64_t>(h) * a.group + g, d, A * (vsc / L));
 }

@@ -37,14 +37,36 @@ struct AppendArgs {
     int32_t *err;
 };
 
+// Longest chain of 16-token chunks one decode worker accumulates into one
+// partial state: a worker whose range is longer cuts it into sub-pieces at
+// every kChainChunks chunks of its range (the tensor cores' fp32 accumulation
+// rounds toward zero, so error would otherwise grow with the chain).
+constexpr int kChainChunks = 512;
+
+// Decode workspace: a header, one record per (sequence, kv head) segment,
+// then the partial-state slots.
+struct DecodeHeader {
+    long long total;                // chunk-heads in the list (all segments)
+    int subs;                       // sub-pieces per worker range: ceil(ceil(total / workers) / kChainChunks)
+    int pad;
+};
+struct SegRecord {
+    long long start;                // list position of the segment's first chunk-head
+    int n;                          // its chunks (0: empty sequence)
+    int w0;                         // worker of its first chunk; -1: one piece, nothing to merge
+};
+
 struct DecodeArgs {
     const __nv_bfloat16 *q;
     const float *k_scale, *v_scale;
     const int32_t *block_table;
     int max_pages;
     const int32_t *seq_lens;
+    int max_len;                    // bound of seq_lens (entries above are clamped and flagged)
+    const int32_t *page_sizes;      // [batch] tokens per page of each sequence, or nullptr: all page_size
     int batch, hq, hkv, group;
-    int page_size;                  // tokens per page (16..256); the kernel works in 16-token chunks
+    int page_size;                  // tokens per pool page (16..256); the kernel works in 16-token chunks
+    int pool_log2;                  // log2(page_size)
     int64_t num_pages;
     float sm_scale_log2;        // sm_scale * log2(e): scores live in the exp2 domain
     void *out;
@@ -55,9 +77,9 @@ struct DecodeArgs {
     int new_bf16;
     int n_new;
     uint8_t *k_pool, *v_pool;       // the pools the tensor maps describe (for the stores)
-    int2 *seg_pieces;               // [batch * hkv + 1] first/last worker of each segment (-1: nothing
-                                    // to merge), then the list length split in two 31-bit halves
-    float *partials;                // [num_ctas * kWarps + batch * hkv][group][kPartialStride]
+    DecodeHeader *header;           // workspace header (written by CTA 0)
+    SegRecord *segs;                // [batch * hkv] segment records (written by CTA 0)
+    float *partials;                // [num_ctas * kWarps * subs + batch * hkv][group][kPartialStride]
     int32_t *err;
     int num_ctas;
     int withhold_worker;            // failure-detection test hook (-1 = off)
@@ -97,11 +119,20 @@ inline size_t prefill_workspace_bytes(int batch, int hkv, int max_kv_len)
     return 2 * static_cast<size_t>(batch) * hkv * pad * 128 * sizeof(__half);
 }
 
-// Workspace = per-segment piece ranges + the list length (rounded to 256
-// bytes), then the partial slots.
+// Workspace = header + segment records (rounded to 256 bytes), then the
+// partial slots.
 inline size_t decode_segment_bytes(int batch, int hkv)
 {
-    return ((static_cast<size_t>(batch) * hkv + 1) * sizeof(int2) + 255) & ~size_t(255);
+    return (sizeof(DecodeHeader) + static_cast<size_t>(batch) * hkv * sizeof(SegRecord) + 255) & ~size_t(255);
+}
+
+// Sub-pieces per worker range for a list of `total` chunk-heads over
+// `workers` workers (at least 1).
+inline __host__ __device__ long long decode_subs(long long total, long long workers)
+{
+    const long long per = (total + workers - 1) / workers;
+    const long long s = (per + kChainChunks - 1) / kChainChunks;
+    return s < 1 ? 1 : s;
 }
 
 // Host helpers (api.cu).
@@ -114,6 +145,7 @@ cudaError_t launch_kv_calibrate(const void *k_new, const void *v_new, int in_bf1
 size_t decode_smem_bytes(int page_size, int batch);
 const void *decode_kernel_for(int page_size);
 int decode_num_ctas(int page_size, int batch, int max_ctas);
+size_t decode_workspace_bytes(int batch, int hq, int hkv, long long max_len, int num_ctas);
 size_t prefill_smem_bytes();
 cudaError_t launch_paged_prefill(const PrefillArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k16,
                                  const CUtensorMap &tm_v16, cudaStream_t stream);

@@ -28,6 +28,7 @@
 // device's current context, so after cudaDeviceReset (which destroys the
 // context and unloads the library's device image) the next call on that
 // device looks the address up again instead of using a stale one.
+#include <algorithm>
 #include <mutex>
 
 #include "internal.h"
@@ -106,25 +107,33 @@ extern "C" size_t pkv_decode_noalloc_scratch_bytes(void)
 
 extern "C" pkv_status pkv_paged_gqa_decode_noalloc(
     const void *q, const uint8_t *k_cache, const uint8_t *v_cache, const float *k_scale, const float *v_scale,
-    const int32_t *block_table, int max_pages_per_seq, const int32_t *seq_lens, int batch, int num_q_heads,
-    int num_kv_heads, int head_dim, int page_size, int64_t num_pages, float sm_scale, void *out, int out_dtype,
-    int32_t *device_error, int max_ctas, cudaStream_t stream)
+    const int32_t *block_table, int max_pages_per_seq, const int32_t *seq_lens, int max_seq_len,
+    const int32_t *seq_page_sizes, int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
+    int64_t num_pages, float sm_scale, void *out, int out_dtype, int32_t *device_error, int max_ctas,
+    cudaStream_t stream)
 {
-    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0)
-        return pkv_paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, max_pages_per_seq,
-                                    seq_lens, batch, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
-                                    sm_scale, out, out_dtype, nullptr, 0, device_error, max_ctas, stream);
-    const size_t need = pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_ctas);
-    if (need == 0)   // sizes the library rejects: let the full check report the reason
-        return pkv_paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, max_pages_per_seq,
-                                    seq_lens, batch, num_q_heads, num_kv_heads, head_dim, page_size, num_pages,
-                                    sm_scale, out, out_dtype, nullptr, 0, device_error, max_ctas, stream);
+    auto full_check = [&]() {   // sizes the library rejects anyway: let the full check report the reason
+        return pkv_paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, max_pages_per_seq, seq_lens,
+                                    max_seq_len, seq_page_sizes, batch, num_q_heads, num_kv_heads, head_dim, page_size,
+                                    num_pages, sm_scale, out, out_dtype, nullptr, 0, device_error, max_ctas, stream);
+    };
+    if (batch <= 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+        max_pages_per_seq <= 0 || max_seq_len < 0)
+        return full_check();
+    const int bound = max_seq_len > 0 ? max_seq_len
+                      : static_cast<int>(std::min<int64_t>(static_cast<int64_t>(max_pages_per_seq) * page_size,
+                                                           INT32_MAX));
+    const size_t need =
+        pkv_decode_workspace_size(batch, num_q_heads, num_kv_heads, head_dim, bound, page_size, max_ctas);
+    if (need == 0)
+        return full_check();
     if (need > kNoAllocScratchBytes)
         return PKV_ERR_WORKSPACE;
     void *scratch = scratch_for_current_device();
     if (!scratch)
         return PKV_ERR_CUDA;
     return pkv_paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, max_pages_per_seq, seq_lens,
-                                batch, num_q_heads, num_kv_heads, head_dim, page_size, num_pages, sm_scale, out,
-                                out_dtype, scratch, kNoAllocScratchBytes, device_error, max_ctas, stream);
+                                bound, seq_page_sizes, batch, num_q_heads, num_kv_heads, head_dim, page_size,
+                                num_pages, sm_scale, out, out_dtype, scratch, kNoAllocScratchBytes, device_error,
+                                max_ctas, stream);
 }

@@ -55,6 +55,9 @@ def fill_gpu(wl, layer: int, dev, chunk_tokens: int = 1 << 15, tail_fill: int = 
     f.bt = wl.block_table().to(dev)
     f.lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev)
     f.q = wl.q(layer, 0, device=dev)
+    # per-sequence page sizes (None: the pool page size) and the bound of seq_lens
+    f.psz = torch.tensor(wl.page_sizes, dtype=torch.int32, device=dev) if wl.page_sizes is not None else None
+    f.max_len = wl.max_len
     torch.cuda.synchronize()
     return f
 
@@ -86,8 +89,10 @@ def oracle_rows(wl, layer: int, pairs, ks: np.ndarray, vs: np.ndarray, threads: 
         kc, vc = oracle_pages(wl, layer, b, h, float(ks[h]), float(vs[h]))
         qg = np.ascontiguousarray(q_bits[b:b + 1, h * G:(h + 1) * G])
         sel = np.array([[0, i - h * G] for i in heads], np.int32)
+        psz = np.array([wl.page_sizes[b]], np.int32) if wl.page_sizes is not None else None
         rows = oracle.paged_decode(qg, kc, vc, ks[h:h + 1], vs[h:h + 1], bt[b:b + 1],
-                                   np.array([wl.seq_lens[b]], np.int32), sel=sel, threads=threads)
+                                   np.array([wl.seq_lens[b]], np.int32), sel=sel, threads=threads,
+                                   seq_page_sizes=psz)
         for i, r in zip(heads, rows):
             out[(b, i)] = r
     return out

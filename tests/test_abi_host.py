@@ -78,12 +78,12 @@ def test_append_argument_errors(lib):
 
 
 def _decode(lib, **kw):
-    a = dict(q=A16, kc=A16, vc=A16b, ks=A16, vs=A16, bt=A16, maxp=4, lens=A16, B=2, Hq=16, Hkv=2, D=128,
-             P=16, np_=8, sm=0.088, out=A16, odt=1, ws=A16, wsb=1 << 20, err=None, ctas=0)
+    a = dict(q=A16, kc=A16, vc=A16b, ks=A16, vs=A16, bt=A16, maxp=4, lens=A16, maxl=0, psz=None, B=2, Hq=16,
+             Hkv=2, D=128, P=16, np_=8, sm=0.088, out=A16, odt=1, ws=A16, wsb=1 << 20, err=None, ctas=0)
     a.update(kw)
     return lib.pkv_paged_gqa_decode(a["q"], a["kc"], a["vc"], a["ks"], a["vs"], a["bt"], a["maxp"], a["lens"],
-                                    a["B"], a["Hq"], a["Hkv"], a["D"], a["P"], a["np_"], a["sm"], a["out"],
-                                    a["odt"], a["ws"], a["wsb"], a["err"], a["ctas"], None)
+                                    a["maxl"], a["psz"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"], a["np_"],
+                                    a["sm"], a["out"], a["odt"], a["ws"], a["wsb"], a["err"], a["ctas"], None)
 
 
 def test_decode_argument_errors(lib):
@@ -109,12 +109,16 @@ def test_decode_argument_errors(lib):
     assert _decode(lib, ws=None) == c["PKV_ERR_WORKSPACE"]
     assert _decode(lib, ws=ctypes.c_void_p(0x10010)) == c["PKV_ERR_WORKSPACE"]
     assert _decode(lib, B=0, q=None, bt=None, lens=None, out=None) == c["PKV_OK"]
+    assert _decode(lib, maxl=-1) == c["PKV_ERR_SHAPE"]
+    assert _decode(lib, psz=ctypes.c_void_p(0x10002)) == c["PKV_ERR_ALIGN"]
+    assert _decode(lib, psz=A16, maxp=1 << 24) == c["PKV_ERR_UNSUPPORTED"]   # max_pages * 256 overflows int32
 
 
 def test_workspace_size_rejects_unsupported(lib):
     assert pkv.pkv_decode_workspace_size(2, 12, 8) == 0
     assert pkv.pkv_decode_workspace_size(2, 16, 8, head_dim=64) == 0
     assert pkv.pkv_decode_workspace_size(2, 16, 8, page_size=8) == 0
+    assert pkv.pkv_decode_workspace_size(2, 16, 8, max_seq_len=-1) == 0
 
 
 def test_python_binding_rejects_cpu_tensors():
@@ -127,13 +131,14 @@ def test_python_binding_rejects_cpu_tensors():
 
 
 def _fused(lib, **kw):
-    a = dict(kn=A16, vn=A16, dt=0, n=1, q=A16, kc=A16, vc=A16b, ks=A16, vs=A16, bt=A16, maxp=4, lens=A16, B=2,
-             Hq=16, Hkv=2, D=128, P=16, np_=8, sm=0.088, out=A16, odt=1, ws=A16, wsb=1 << 20, err=None, ctas=0)
+    a = dict(kn=A16, vn=A16, dt=0, n=1, q=A16, kc=A16, vc=A16b, ks=A16, vs=A16, bt=A16, maxp=4, lens=A16, maxl=0,
+             psz=None, B=2, Hq=16, Hkv=2, D=128, P=16, np_=8, sm=0.088, out=A16, odt=1, ws=A16, wsb=1 << 20,
+             err=None, ctas=0)
     a.update(kw)
     return lib.pkv_append_decode_fp8(a["kn"], a["vn"], a["dt"], a["n"], a["q"], a["kc"], a["vc"], a["ks"], a["vs"],
-                                     a["bt"], a["maxp"], a["lens"], a["B"], a["Hq"], a["Hkv"], a["D"], a["P"],
-                                     a["np_"], a["sm"], a["out"], a["odt"], a["ws"], a["wsb"], a["err"], a["ctas"],
-                                     None)
+                                     a["bt"], a["maxp"], a["lens"], a["maxl"], a["psz"], a["B"], a["Hq"], a["Hkv"],
+                                     a["D"], a["P"], a["np_"], a["sm"], a["out"], a["odt"], a["ws"], a["wsb"],
+                                     a["err"], a["ctas"], None)
 
 
 def test_fused_argument_errors(lib):

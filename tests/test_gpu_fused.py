@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _ws(pkv, wl, dev, max_ctas=0):
-    n = pkv.pkv_decode_workspace_size(wl.batch, wl.hq, wl.hkv, 128, wl.page_size, max_ctas)
+    n = pkv.pkv_decode_workspace_size(wl.batch, wl.hq, wl.hkv, 128, wl.max_len, wl.page_size, max_ctas)
     return torch.full((n,), 0xFF, dtype=torch.uint8, device=dev)
 
 
@@ -27,7 +27,7 @@ def _separate(pkv, wl, dev, dtype, max_ctas=0):
                           f.err)
     out = torch.empty(f.q.shape, dtype=torch.float32, device=dev)
     pkv.pkv_paged_gqa_decode(f.q, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, out, _ws(pkv, wl, dev, max_ctas), None,
-                             f.err, max_ctas)
+                             f.err, max_ctas, max_seq_len=f.max_len, seq_page_sizes=f.psz)
     torch.cuda.synchronize()
     return f, out
 
@@ -37,7 +37,8 @@ def _fused(pkv, wl, dev, dtype, max_ctas=0):
     k, v = step_tokens(wl, 0, dev)
     out = torch.empty(f.q.shape, dtype=torch.float32, device=dev)
     pkv.pkv_append_decode_fp8(k.to(dtype), v.to(dtype), f.q, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, out,
-                              _ws(pkv, wl, dev, max_ctas), None, f.err, max_ctas)
+                              _ws(pkv, wl, dev, max_ctas), None, f.err, max_ctas, max_seq_len=f.max_len,
+                              seq_page_sizes=f.psz)
     torch.cuda.synchronize()
     return f, out
 
@@ -53,7 +54,19 @@ def _fused(pkv, wl, dev, dtype, max_ctas=0):
 ])
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 def test_fused_equals_separate(pkv, cuda_device, lens, append, hq, hkv, page, dtype):
-    wl = workloads.Workload(60, "fused", lens, append, hq, hkv, page, pool_factor=1.5, seed=31)
+    _fused_vs_separate(pkv, cuda_device, lens, append, hq, hkv, page, dtype, None)
+
+
+@pytest.mark.parametrize("lens,append,hq,hkv,sizes", [
+    ([63, 100, 17, 300], 2, 16, 2, [64, 16, 32, 64]),     # new tokens inside runs of pool pages
+    ([1000, 5, 250], 1, 64, 8, [256, 16, 64]),
+])
+def test_fused_equals_separate_per_sequence_pages(pkv, cuda_device, lens, append, hq, hkv, sizes):
+    _fused_vs_separate(pkv, cuda_device, lens, append, hq, hkv, 16, torch.float32, sizes)
+
+
+def _fused_vs_separate(pkv, cuda_device, lens, append, hq, hkv, page, dtype, sizes):
+    wl = workloads.Workload(60, "fused", lens, append, hq, hkv, page, pool_factor=1.5, seed=31, page_sizes=sizes)
     for ctas in (0, 3):
         fs, out_s = _separate(pkv, wl, cuda_device, dtype, ctas)
         ff, out_f = _fused(pkv, wl, cuda_device, dtype, ctas)

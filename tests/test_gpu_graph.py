@@ -17,7 +17,7 @@ def test_graph_captured_layer_loop_matches_eager(pkv, cuda_device):
         f = fill_gpu(wl, layer, cuda_device, step_append=False)
         k, v = step_tokens(wl, layer, cuda_device)
         layers.append((f, k, v))
-    n = pkv.pkv_decode_workspace_size(wl.batch, wl.hq, wl.hkv, 128, wl.page_size)
+    n = pkv.pkv_decode_workspace_size(wl.batch, wl.hq, wl.hkv, 128, wl.max_pages * wl.page_size, wl.page_size)
     ws = torch.zeros(n, dtype=torch.uint8, device=cuda_device)
     outs = [torch.empty(wl.batch, wl.hq, 128, dtype=torch.bfloat16, device=cuda_device) for _ in layers]
 

@@ -1,0 +1,38 @@
+"""A decode call whose KV is far larger than the benchmarked ones: 128
+sequences of 128K tokens on the Llama-3-70B attention geometry (64 query / 8
+kv heads), 34 GB of FP8 K and V.  Spread over the persistent grid's workers
+that is about 4500 chunks of 16 tokens per worker, where one unbroken
+tensor-core accumulation chain would drift (its fp32 accumulation rounds
+toward zero); the kernel cuts each worker's range every 512 chunks, so the
+sampled rows must stay within max-abs 1e-4 of the oracle, well inside the
+2e-3 bound."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from tests.gpu_fill import assert_close, errors, fill_gpu, oracle_rows, sample_pairs
+
+pytestmark = pytest.mark.gpu
+
+
+def test_batch_128_at_128k_sampled_rows(pkv, cuda_device):
+    free, _ = torch.cuda.mem_get_info(cuda_device)
+    wl = workloads.Workload(57, "llama3_70b_b128_l131072", [131072] * 128, 0, 64, 8, 16, seed=41)
+    need = 2 * wl.num_pages * wl.hkv * wl.page_size * wl.head_dim
+    assert need < 0.8 * free, f"needs {need / 1e9:.1f} GB of the {free / 1e9:.1f} GB free"
+    f = fill_gpu(wl, 0, cuda_device)
+    out = pkv.paged_gqa_decode(f.q, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, out_dtype=torch.float32,
+                               device_error=f.err)
+    torch.cuda.synchronize()
+    assert int(f.err.item()) == 0
+    pairs = sample_pairs(wl, 6, seed=5)
+    exp = oracle_rows(wl, 0, pairs, f.ks.cpu().numpy(), f.vs.cpu().numpy())
+    got = out.double().cpu().numpy()
+    g = np.stack([got[b, i] for (b, i) in pairs])
+    r = np.stack([exp[p] for p in pairs])
+    assert_close(g, r, "batch 128 x 128K")
+    max_abs, _ = errors(g, r)
+    assert max_abs <= 1e-4, max_abs
+    del f
+    torch.cuda.empty_cache()

@@ -6,7 +6,11 @@
   * closed forms: a 1-token context returns dequant(V) exactly; K = 0 gives
     the mean of V; a 2-token case gives sigmoid weights; L = 0 gives zeros;
   * invariants: softmax weights sum to 1; a random permutation of physical
-    pages (block table permuted alike) leaves every output bit unchanged.
+    pages (block table permuted alike) leaves every output bit unchanged;
+  * per-sequence page sizes (a P_b-token page is a run of P_b / P pool
+    pages): dense brute force on mixed 16/32/64/256-token pages, and the same
+    result as the uniform P-token table that lists every pool page of the
+    runs.
 """
 import math
 
@@ -47,7 +51,8 @@ def _check_dense(wl, tol=1e-12):
     q = wl.q()
     bt = wl.block_table().numpy()
     lens = np.array(wl.seq_lens, np.int32)
-    out = oracle.paged_decode(q.view(torch.uint16).numpy(), kc, vc, ks, vs, bt, lens)
+    psz = np.array(wl.page_sizes, np.int32) if wl.page_sizes is not None else None
+    out = oracle.paged_decode(q.view(torch.uint16).numpy(), kc, vc, ks, vs, bt, lens, seq_page_sizes=psz)
     out = out.reshape(wl.batch, wl.hq, wl.head_dim)
     for b in range(wl.batch):
         ref = dense_attention(q[b].double().numpy(), dk[b], dv[b], SM)
@@ -191,3 +196,41 @@ def test_bad_block_table_entry_is_reported():
     with pytest.raises(ValueError):
         oracle.paged_decode(np.zeros((1, 1, 128), np.uint16), kc, kc, np.ones(1, np.float32),
                             np.ones(1, np.float32), np.array([[5]], np.int32), np.array([3], np.int32))
+
+
+@pytest.mark.parametrize("lens,sizes,P", [
+    ([37, 100, 1, 300, 64], [16, 64, 32, 64, 16], 16),
+    ([200, 513, 31], [32, 256, 64], 32),
+    ([1000, 17], [256, 16], 16),
+])
+def test_per_sequence_page_sizes_match_dense(lens, sizes, P):
+    wl = workloads.Workload(92, "varpage", lens, 0, 16, 2, P, pool_factor=1.5, seed=13, page_sizes=sizes)
+    _check_dense(wl)
+
+
+def test_per_sequence_page_sizes_equal_expanded_uniform_table():
+    """A table of P_b-token pages reads exactly what a table of P-token pages
+    reads when it lists, for every logical page, its P_b / P pool pages in
+    order."""
+    lens, sizes, P = [300, 77, 129, 5], [64, 16, 32, 64], 16
+    wl = workloads.Workload(93, "varpage", lens, 0, 8, 2, P, pool_factor=1.25, seed=17, page_sizes=sizes)
+    kc, vc, ks, vs, _, _ = _fill(wl)
+    bt = wl.block_table().numpy()
+    wide = np.full((wl.batch, max((L + P - 1) // P for L in wl.seq_lens)), -1, np.int32)
+    for b, L in enumerate(wl.seq_lens):
+        for t in range(0, L, P):                                # pool page of every P-token block
+            wide[b, t // P] = bt[b, t // sizes[b]] + (t % sizes[b]) // P
+    q = wl.q().view(torch.uint16).numpy()
+    lens_np = np.array(wl.seq_lens, np.int32)
+    a = oracle.paged_decode(q, kc, vc, ks, vs, bt, lens_np, seq_page_sizes=np.array(sizes, np.int32))
+    b_ = oracle.paged_decode(q, kc, vc, ks, vs, wide, lens_np)
+    assert np.array_equal(a, b_)
+    # reading the table as if every page had P tokens (a planted mistake: the
+    # logical page index taken with P) differs on the sequences with P_b > P
+    short = np.minimum(lens_np, bt.shape[1] * P).astype(np.int32)
+    a_s = oracle.paged_decode(q, kc, vc, ks, vs, bt, short, seq_page_sizes=np.array(sizes, np.int32))
+    c = oracle.paged_decode(q, kc, vc, ks, vs, bt, short).reshape(wl.batch, wl.hq, -1)
+    a_s = a_s.reshape(wl.batch, wl.hq, -1)
+    for b in range(wl.batch):
+        same = np.allclose(a_s[b], c[b], rtol=1e-6, atol=1e-9)
+        assert same == (sizes[b] == P or short[b] <= P), b

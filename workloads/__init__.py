@@ -120,6 +120,7 @@ class Workload:
     seed: int = 0
     head_dim: int = HEAD_DIM
     notes: str = ""
+    page_sizes: list | None = None      # tokens per page of each sequence (runs of pool pages); None: page_size
     _bt: torch.Tensor | None = field(default=None, repr=False)
 
     @property
@@ -134,43 +135,93 @@ class Workload:
     def seq_lens(self) -> list:
         return [l + self.append for l in self.prefill_lens]
 
+    def seq_page_size(self, b: int) -> int:
+        return self.page_sizes[b] if self.page_sizes is not None else self.page_size
+
     @property
     def pages_per_seq(self) -> list:
-        P = self.page_size
-        return [(l + P - 1) // P for l in self.seq_lens]
+        """Block-table entries (logical pages of P_b tokens) of every sequence."""
+        return [(l + self.seq_page_size(b) - 1) // self.seq_page_size(b) for b, l in enumerate(self.seq_lens)]
 
     @property
     def max_pages(self) -> int:
         return max(1, max(self.pages_per_seq))
 
     @property
+    def max_len(self) -> int:
+        """Capacity of a table row at the largest page size (a bound of seq_lens)."""
+        return self.max_pages * max(self.seq_page_size(b) for b in range(self.batch))
+
+    @property
     def needed_pages(self) -> int:
-        return sum(self.pages_per_seq)
+        """Pool pages the sequences occupy (a P_b-token page is P_b / P pool pages)."""
+        P = self.page_size
+        return sum(n * (self.seq_page_size(b) // P) for b, n in enumerate(self.pages_per_seq))
+
+    def _groups(self):
+        """Variable page sizes: the pool is cut into groups of R = max P_b / P
+        consecutive pages; for every ratio r = P_b / P the number of groups its
+        runs of r pages need."""
+        P = self.page_size
+        R = max(self.seq_page_size(b) for b in range(self.batch)) // P
+        need = {}
+        for b, n in enumerate(self.pages_per_seq):
+            r = self.seq_page_size(b) // P
+            need[r] = need.get(r, 0) + n
+        return R, {r: (n * r + R - 1) // R for r, n in need.items()}
 
     @property
     def num_pages(self) -> int:
-        return max(1, int(math.ceil(self.needed_pages * self.pool_factor)))
+        if self.page_sizes is None:
+            return max(1, int(math.ceil(self.needed_pages * self.pool_factor)))
+        R, groups = self._groups()
+        return R * max(1, int(math.ceil(sum(groups.values()) * self.pool_factor)))
+
+    def _perm(self, n: int, salt: int) -> torch.Tensor:
+        h = hash_u32(stream_key(self.seed, self.index, 77, salt) if salt else stream_key(self.seed, self.index, 77),
+                     torch.arange(n, dtype=torch.int64))
+        return torch.argsort(h * n + torch.arange(n), stable=True)   # ties impossible
 
     def block_table(self) -> torch.Tensor:
-        """int32 [B, max_pages] on the CPU; unused entries are -1."""
+        """int32 [B, max_pages] on the CPU; unused entries are -1.  With
+        per-sequence page sizes an entry is the first pool page of a run of
+        P_b / P consecutive pool pages."""
         if self._bt is None:
-            n = self.num_pages
-            h = hash_u32(stream_key(self.seed, self.index, 77), torch.arange(n, dtype=torch.int64))
-            perm = torch.argsort(h * n + torch.arange(n), stable=True)   # ties impossible
             bt = torch.full((self.batch, self.max_pages), -1, dtype=torch.int32)
-            pos = 0
-            for b, np_b in enumerate(self.pages_per_seq):
-                bt[b, :np_b] = perm[pos:pos + np_b].to(torch.int32)
-                pos += np_b
+            if self.page_sizes is None:
+                n = self.num_pages
+                perm = self._perm(n, 0)
+                pos = 0
+                for b, np_b in enumerate(self.pages_per_seq):
+                    bt[b, :np_b] = perm[pos:pos + np_b].to(torch.int32)
+                    pos += np_b
+            else:
+                P = self.page_size
+                R, groups = self._groups()
+                gperm = self._perm(self.num_pages // R, 0)          # groups in random pool order
+                gpos = 0
+                runs = {}
+                for r in sorted(groups, reverse=True):
+                    g = gperm[gpos:gpos + groups[r]]
+                    gpos += groups[r]
+                    starts = (g.view(-1, 1) * R + torch.arange(0, R, r).view(1, -1)).reshape(-1)
+                    runs[r] = starts[self._perm(starts.numel(), r)]   # runs of r pages in random order
+                used = {r: 0 for r in runs}
+                for b, np_b in enumerate(self.pages_per_seq):
+                    r = self.seq_page_size(b) // P
+                    bt[b, :np_b] = runs[r][used[r]:used[r] + np_b].to(torch.int32)
+                    used[r] += np_b
             self._bt = bt
         return self._bt
 
     def slots(self, b: int, t0: int, t1: int) -> torch.Tensor:
-        """int64 cache slots of tokens t0..t1-1 of sequence b (CPU)."""
-        P = self.page_size
+        """int64 cache slots of tokens t0..t1-1 of sequence b (CPU): the table
+        entry of the token's logical page times P plus its offset in that page
+        (a P_b-token page spans P_b / P consecutive pool pages)."""
+        P, Pb = self.page_size, self.seq_page_size(b)
         t = torch.arange(t0, t1, dtype=torch.int64)
-        pages = self.block_table()[b].to(torch.int64)[t // P]
-        return pages * P + t % P
+        pages = self.block_table()[b].to(torch.int64)[t // Pb]
+        return pages * P + t % Pb
 
     # ---------------- values ----------------
     def _kv_key(self, layer: int, which: int, b: int, h: int) -> int:
@@ -239,8 +290,12 @@ class Workload:
         return sum(self.seq_lens) * self.hkv * 2 * self.head_dim
 
     def describe(self) -> dict:
+        extra = {}
+        if self.page_sizes is not None:
+            extra = {"seq_page_sizes": {str(p): sum(1 for b in range(self.batch) if self.seq_page_size(b) == p)
+                                        for p in sorted(set(self.page_sizes))}}
         return {"workload": self.name, "batch": self.batch, "hq": self.hq, "hkv": self.hkv,
-                "head_dim": self.head_dim, "page_size": self.page_size,
+                "head_dim": self.head_dim, "page_size": self.page_size, **extra,
                 "seq_len_min": min(self.seq_lens), "seq_len_max": max(self.seq_lens),
                 "sum_seq_len": sum(self.seq_lens), "layers": self.layers,
                 "append_per_seq": self.append, "pool_pages": self.num_pages}
@@ -254,9 +309,27 @@ def _log_uniform_lens(seed: int, n: int, lo: int, hi: int) -> list:
     return [min(max(l, lo), hi) for l in out]
 
 
-def config(i: int, page_size: int | None = None, seed: int = 0) -> Workload:
+def dynamic_page_sizes(lens: list, short: int = 16, long: int = 64, long_from: int = 8192) -> list:
+    """Per-sequence page sizes by length: `long`-token pages for sequences
+    longer than long_from tokens, `short`-token pages otherwise (the Llama 3
+    production notes' dynamic page size: 16-token pages below 1024 tokens,
+    64-token pages above 8192; between the two they give no size, and the
+    default 16 is kept)."""
+    return [long if l > long_from else short for l in lens]
+
+
+def config(i: int, page_size: int | None = None, seed: int = 0, dynamic_pages: bool = False) -> Workload:
     """The five decode workloads (tiny parity case, Llama-3 8B and 70B layer
-    shapes, 128K long context, mixed serving batch)."""
+    shapes, 128K long context, mixed serving batch).  dynamic_pages (mixed
+    batch only): 16-token pool pages, 64-token pages for sequences above 8192
+    tokens."""
+    if dynamic_pages:
+        if i != 4:
+            raise ValueError("dynamic page sizes are defined for the mixed serving batch")
+        lens = _log_uniform_lens(seed, 64, 512, 131072)
+        return Workload(4, "mixed_b64_loguniform_512_131072_p16_64dyn", lens, 1, 64, 8, 16, layers=80, seed=seed,
+                        page_sizes=dynamic_page_sizes([l + 1 for l in lens]),
+                        notes="log-uniform lengths, 80 layers per step, 64-token pages above 8192 tokens")
     if i == 0:
         return Workload(0, "tiny_b2_l37_100_g8", [37, 100], 0, 8, 1, page_size or 16, seed=seed,
                         notes="shuffled block table, no append")
