@@ -223,7 +223,7 @@ def run_gpu(args, rank, world):
     pkv.load()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    wl = workloads.config(args.config, page_size=args.page)
+    wl = workloads.config(args.config, page_size=args.page, dynamic_pages=args.dynamic_pages)
     kv_bytes = wl.kv_bytes()
     # distinct layer caches rotated step by step so a step never finds the
     # previous step's KV in L2 (each cache alone is already larger than L2)
@@ -234,8 +234,10 @@ def run_gpu(args, rank, world):
     steps_in = [_step_inputs(wl, l, dev) for l in range(n_layers)]
     bt = wl.block_table().to(dev)
     lens = torch.tensor(wl.seq_lens, dtype=torch.int32, device=dev)
+    psz = torch.tensor(wl.page_sizes, dtype=torch.int32, device=dev) if wl.page_sizes is not None else None
+    max_len = wl.max_len
     out = torch.empty((wl.batch, wl.hq, wl.head_dim), dtype=torch.bfloat16, device=dev)
-    ws = pkv.decode_workspace(wl.batch, wl.hq, wl.hkv, wl.page_size, dev, max_seq_len=wl.max_pages * wl.page_size)
+    ws = pkv.decode_workspace(wl.batch, wl.hq, wl.hkv, wl.page_size, dev, max_seq_len=max_len)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
 
@@ -253,10 +255,10 @@ def run_gpu(args, rank, world):
                 evs[l][0].record(stream)
             if s["k_new"] is not None and not args.separate:
                 pkv.pkv_append_decode_fp8(s["k_new"], s["v_new"], s["q"], c["kc"], c["vc"], c["ks"], c["vs"], bt, lens,
-                                          out, ws, device_error=err)
+                                          out, ws, device_error=err, max_seq_len=max_len, seq_page_sizes=psz)
             else:
                 pkv.pkv_paged_gqa_decode(s["q"], c["kc"], c["vc"], c["ks"], c["vs"], bt, lens, out, ws,
-                                         device_error=err)
+                                         device_error=err, max_seq_len=max_len, seq_page_sizes=psz)
             if evs is not None:
                 evs[l][1].record(stream)
 
@@ -309,6 +311,23 @@ def run_gpu(args, rank, world):
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop() if rank == 0 else None
+    # Host cost of one call alone: enqueue a few layer passes behind a GPU
+    # spin long enough that the launch queue never fills, so the time is the
+    # binding's and the library's host work, not back-pressure from the GPU.
+    n_host = min(per_step, 16)
+    torch.cuda._sleep(int(2e8))
+    hh0 = time.perf_counter()
+    for l in range(n_host):
+        c = layers[l % n_layers]
+        s = steps_in[l % n_layers]
+        if s["k_new"] is not None and not args.separate:
+            pkv.pkv_append_decode_fp8(s["k_new"], s["v_new"], s["q"], c["kc"], c["vc"], c["ks"], c["vs"], bt, lens,
+                                      out, ws, device_error=err, max_seq_len=max_len, seq_page_sizes=psz)
+        else:
+            pkv.pkv_paged_gqa_decode(s["q"], c["kc"], c["vc"], c["ks"], c["vs"], bt, lens, out, ws,
+                                     device_error=err, max_seq_len=max_len, seq_page_sizes=psz)
+    host_call_us = 1e6 * (time.perf_counter() - hh0) / n_host
+    torch.cuda.synchronize()
     total_ms = t_start.elapsed_time(t_end)
     if graphs is None:
         decode_ms = [a.elapsed_time(b) for ev in evs for a, b in ev]
@@ -323,7 +342,7 @@ def run_gpu(args, rank, world):
     # pass's own inputs (q and the new K/V rows) are staged back to back
     # (256-byte aligned) in one pinned buffer and cross with one copy, as a
     # serving loop would stage them.
-    seq_stage = _HostStage({"bt": bt, "lens": lens})
+    seq_stage = _HostStage({"bt": bt, "lens": lens, **({"psz": psz} if psz is not None else {})})
     host = []
     for l in range(n_layers):
         s = steps_in[l]
@@ -346,10 +365,11 @@ def run_gpu(args, rank, world):
                                       c["vs"], c["kc"], c["vc"], err)
             if "k_new" in d and not args.separate:
                 pkv.pkv_append_decode_fp8(d["k_new"], d["v_new"], d["q"], c["kc"], c["vc"], c["ks"], c["vs"],
-                                          d["bt"], d["lens"], out, ws, device_error=err)
+                                          d["bt"], d["lens"], out, ws, device_error=err, max_seq_len=max_len,
+                                          seq_page_sizes=d.get("psz"))
             else:
                 pkv.pkv_paged_gqa_decode(d["q"], c["kc"], c["vc"], c["ks"], c["vs"], d["bt"], d["lens"], out, ws,
-                                         device_error=err)
+                                         device_error=err, max_seq_len=max_len, seq_page_sizes=d.get("psz"))
             out_host.copy_(out, non_blocking=True)
 
     for i in range(3):
@@ -406,7 +426,11 @@ def run_gpu(args, rank, world):
         "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
-        "host_us_per_call": round(1e6 * host_s / (args.steps * (1 if graphs is not None else per_step)), 2),
+        "host": {"us_per_call": round(host_call_us, 2),
+                 "enqueue_us_per_call_in_timed_loop": round(
+                     1e6 * host_s / (args.steps * (1 if graphs is not None else per_step)), 2),
+                 "note": "us_per_call: binding + library host work of one call with the GPU busy elsewhere; "
+                         "the timed loop's enqueue time also includes waiting on a full launch queue"},
         "clocks": clk,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -724,6 +748,7 @@ class OracleRig:
         self.q = wl.q().view(torch.uint16).numpy()
         self.bt = wl.block_table().numpy()
         self.lens = np.array(wl.seq_lens, np.int32)
+        self.psz = np.array(wl.page_sizes, np.int32) if wl.page_sizes is not None else None
         self.filled = set()
 
     def _rows(self, which, b, t0, t1):
@@ -758,7 +783,7 @@ class OracleRig:
                 self.oracle.kv_append(kn, sl, self.ks, self.kc)
                 self.oracle.kv_append(vn, sl, self.vs, self.vc)
         self.oracle.paged_decode(self.q, self.kc, self.vc, self.ks, self.vs, self.bt, self.lens, sel=sel,
-                                 threads=threads)
+                                 threads=threads, seq_page_sizes=self.psz)
         dt = time.perf_counter() - t0
         return dt, sum(wl.seq_lens[b] for b in seqs) * hk * 2 * wl.head_dim
 
@@ -784,7 +809,7 @@ def cpu_baseline(wl, budget_s: float, gen_device="cpu") -> dict:
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    wl = workloads.config(args.config, page_size=args.page)
+    wl = workloads.config(args.config, page_size=args.page, dynamic_pages=args.dynamic_pages)
     threads = len(os.sched_getaffinity(0))
     rig = OracleRig(wl)
     seqs = sample_sequences(wl)
@@ -827,6 +852,8 @@ def main():
     ap.add_argument("--config", type=int, default=4,
                     help="decode workload (default 4: the mixed 64-sequence 512..128K batch, 80 layers)")
     ap.add_argument("--page", type=int, default=None)
+    ap.add_argument("--dynamic-pages", action="store_true",
+                    help="mixed batch: 16-token pages, 64-token pages for sequences above 8192 tokens")
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--rotate", type=int, default=0, help="distinct layer caches (0 = auto)")
     ap.add_argument("--e2e-steps", type=int, default=200)
