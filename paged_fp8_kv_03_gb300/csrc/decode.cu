@@ -736,102 +736,119 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
 }
 
-constexpr int kMergeThreads = kHeadDim;   // one thread per dimension
+// One CTA per (sequence, kv head) segment, one warp per query head g of its
+// group; lane j owns dimensions 4j .. 4j+3.  The warp merges the partial
+// states the workers covering the segment wrote for head g, in list order,
+// and writes the output row.  Pieces are taken 16 at a time: lane i of the
+// warp finds the slot of piece i and loads its (m, l); every lane loads its
+// four dimensions of all 16 accumulators; then one exact rescale folds the
+// batch into the running (M, L, A).  The order is fixed, so results are
+// deterministic.
+//
+// Where a segment's pieces are: with one sub-piece per worker range
+// (subs == 1) and at least as many chunk-heads as workers, piece i was
+// written by worker w0 + i; with fewer chunk-heads than workers every worker
+// owns at most one, and piece i comes from the worker owning position start
+// + i; with subs > 1 a worker's range is also cut every kChainChunks chunks
+// and the pieces are walked worker by worker.
+constexpr int kMergeBatch = 16;
 
-// One CTA per (segment, head g): merges the partial states that the workers
-// covering the segment wrote for that head, in list order, and writes the
-// output row.  With one sub-piece per worker range (subs == 1) the pieces
-// come from the consecutive workers w0..w1 when the list has at least as many
-// chunk-heads as workers, and otherwise (every worker owns at most one
-// chunk-head) piece i comes from the worker owning position start + i.  With
-// subs > 1 a worker's range is also cut every kChainChunks chunks, and the
-// pieces are walked worker by worker.
-__global__ void __launch_bounds__(kMergeThreads) splitk_merge_kernel(const DecodeArgs a)
+__global__ void __launch_bounds__(32 * PKV_MAX_GROUP) splitk_merge_kernel(const DecodeArgs a)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid has finished
-    const int seg = blockIdx.x, g = blockIdx.y, d = threadIdx.x;
+    const int seg = blockIdx.x, g = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const SegRecord r = a.segs[seg];
+    const DecodeHeader hd = *a.header;
     if (r.w0 < 0)
         return;
-    const DecodeHeader hd = *a.header;
     const int64_t total = hd.total;
     const int subs = hd.subs;
     const int workers = a.num_ctas * kWarps;
     const int b = seg / a.hkv, h = seg % a.hkv;
-    auto slot = [&](int s) { return a.partials + (static_cast<int64_t>(s + seg) * a.group + g) * kPartialStride; };
+    const bool walk = subs > 1;
+    const bool dense = total >= workers;
+    // pieces known up front (subs == 1); the walk counts them as it goes
+    const int n_known = dense ? worker_of(r.start + r.n - 1, total, workers) - r.w0 + 1 : r.n;
+    // walk state (subs > 1): worker w, its range [lo_w, hi_w), offset k of the next piece in it
+    const int64_t end = r.start + r.n;
+    int w = r.w0;
+    int64_t lo_w = static_cast<int64_t>(w) * total / workers;
+    int64_t hi_w = static_cast<int64_t>(w + 1) * total / workers;
+    int64_t k = r.start - lo_w;
 
-    constexpr int kGroup = 8;
-    float M = -INFINITY, L = 0.f, A = 0.f;
-    // Folds up to kGroup pieces (slot indices in sl[0..n)): all loads issued
-    // together, then an exact rescale into the running (M, L, A).  Every
-    // thread computes the same M and L; the order is fixed, so results are
-    // deterministic.
-    auto fold = [&](const int (&sl)[kGroup], int n) {
-        float m[kGroup], l[kGroup], v[kGroup];
-#pragma unroll
-        for (int i = 0; i < kGroup; ++i) {
-            if (i < n) {
-                const float *p = slot(sl[i]);
-                m[i] = p[kHeadDim];
-                l[i] = p[kHeadDim + 1];
-                v[i] = p[d];
-            }
-        }
-        float mc = M;
-#pragma unroll
-        for (int i = 0; i < kGroup; ++i)
-            if (i < n)
-                mc = fmaxf(mc, m[i]);
-        const float r0 = ex2_approx(M - mc);          // 0 on the first group (M = -inf)
-        L *= r0;
-        A *= r0;
-#pragma unroll
-        for (int i = 0; i < kGroup; ++i) {
-            if (i < n) {
-                const float f = ex2_approx(m[i] - mc);
-                L += l[i] * f;
-                A += v[i] * f;
-            }
-        }
-        M = mc;
-    };
-
-    int sl[kGroup];
-    int n = 0;
-    if (subs == 1) {
-        const int w1 = worker_of(r.start + r.n - 1, total, workers);
-        const bool dense = total >= workers;
-        const int n_pieces = dense ? w1 - r.w0 + 1 : r.n;
-        for (int i = 0; i < n_pieces; ++i) {
-            sl[n++] = dense ? r.w0 + i : worker_of(r.start + i, total, workers);
-            if (n == kGroup) {
-                fold(sl, n);
-                n = 0;
-            }
-        }
-    } else {
-        const int64_t end = r.start + r.n;
-        int64_t x = r.start;
-        int w = r.w0;
-        while (x < end) {
-            const int64_t lo_w = static_cast<int64_t>(w) * total / workers;
-            const int64_t hi_w = static_cast<int64_t>(w + 1) * total / workers;
-            const int64_t e = end < hi_w ? end : hi_w;
-            for (int64_t k = x - lo_w; lo_w + k < e; k = (k / kChainChunks + 1) * kChainChunks) {
-                sl[n++] = w * subs + static_cast<int>(k / kChainChunks);
-                if (n == kGroup) {
-                    fold(sl, n);
-                    n = 0;
+    float M = -INFINITY, L = 0.f;
+    float A[4] = {0.f, 0.f, 0.f, 0.f};
+    for (int i0 = 0;; i0 += kMergeBatch) {
+        // slot of piece i0 + lane (lanes >= the batch size: -1)
+        int my_slot = -1;
+        int nb;
+        if (!walk) {
+            nb = min(kMergeBatch, n_known - i0);
+            if (nb <= 0)
+                break;
+            if (lane < nb)
+                my_slot = dense ? r.w0 + i0 + lane : worker_of(r.start + i0 + lane, total, workers);
+        } else {
+            nb = 0;
+            while (nb < kMergeBatch && lo_w + k < end) {
+                if (lane == nb)
+                    my_slot = w * subs + static_cast<int>(k / kChainChunks);
+                ++nb;
+                k = (k / kChainChunks + 1) * kChainChunks;          // next sub-piece of this worker
+                if (lo_w + k >= hi_w) {                              // next worker: starts at its range start
+                    ++w;
+                    lo_w = hi_w;
+                    hi_w = static_cast<int64_t>(w + 1) * total / workers;
+                    k = 0;
                 }
             }
-            x = e;
-            ++w;
+            if (nb == 0)
+                break;
         }
+        float m = -INFINITY, l = 0.f;
+        if (my_slot >= 0) {
+            const float *p = a.partials + (static_cast<int64_t>(my_slot + seg) * a.group + g) * kPartialStride;
+            m = p[kHeadDim];
+            l = p[kHeadDim + 1];
+        }
+        float4 v[kMergeBatch];
+#pragma unroll
+        for (int i = 0; i < kMergeBatch; ++i) {
+            const int si = __shfl_sync(kFull, my_slot, i);
+            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < nb)
+                v[i] = *reinterpret_cast<const float4 *>(
+                    a.partials + (static_cast<int64_t>(si + seg) * a.group + g) * kPartialStride + 4 * lane);
+        }
+        float mb = m;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
+        const float mn = fmaxf(M, mb);
+        const float r0 = ex2_approx(M - mn);                     // 0 on the first batch (M = -inf)
+        const float sc = my_slot >= 0 ? ex2_approx(m - mn) : 0.f;
+        float ls = sc * l;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            ls += __shfl_xor_sync(kFull, ls, o);
+        L = L * r0 + ls;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            A[c] *= r0;
+#pragma unroll
+        for (int i = 0; i < kMergeBatch; ++i) {
+            const float si = __shfl_sync(kFull, sc, i);
+            A[0] += si * v[i].x;
+            A[1] += si * v[i].y;
+            A[2] += si * v[i].z;
+            A[3] += si * v[i].w;
+        }
+        M = mn;
     }
-    if (n > 0)
-        fold(sl, n);
-    const float vsc = __ldg(a.v_scale + h);
-    store_out(a, static_cast<int64_t>(b) * a.hq + static_cast<int64_t>(h) * a.group + g, d, A * (vsc / L));
+    const float f = __ldg(a.v_scale + h) / L;
+    const int64_t row = static_cast<int64_t>(b) * a.hq + static_cast<int64_t>(h) * a.group + g;
+    store_pair(a, row, 4 * lane, A[0] * f, A[1] * f);
+    store_pair(a, row, 4 * lane + 2, A[2] * f, A[3] * f);
 }
 
 }  // namespace
@@ -855,8 +872,8 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, co
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.batch * a.hkv), static_cast<unsigned>(a.group), 1);
-    cfg.blockDim = dim3(kMergeThreads, 1, 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(a.batch * a.hkv), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * a.group), 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];

@@ -185,10 +185,17 @@ def test_full_size_configs_sampled(pkv, cuda_device, cfg, page, n_bh, layer, dyn
     g = np.stack([got[b, i] for (b, i) in pairs])
     r = np.stack([exp[p] for p in pairs])
     assert_close(g, r, f"config {cfg} P={page} layer {layer}")
+    # within one bf16 ulp of the oracle rounded to bf16 wherever that ulp
+    # (>= 2^-12 for |o| >= 2^-4) is well above the fp32-mode error; nearer to
+    # zero the absolute tolerance governs (an ulp there can be smaller than
+    # the fp32 rounding of a long accumulation)
     g16 = got16.double().cpu().numpy()
     g16 = np.stack([g16[b, i] for (b, i) in pairs])
     r16 = torch.from_numpy(r).to(torch.bfloat16).double().numpy()
-    assert np.all(np.abs(g16 - r16) <= bf16_ulp(r) * 1.0001)
+    big = np.abs(r) >= 2.0 ** -4
+    assert big.any()
+    assert np.all(np.abs(g16 - r16)[big] <= bf16_ulp(r)[big] * 1.0001)
+    assert np.abs(g16 - r).max() <= 2e-3 + 0.5 * bf16_ulp(r).max()
     del f
     torch.cuda.empty_cache()
 
