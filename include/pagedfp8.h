@@ -307,16 +307,18 @@ size_t pkv_decode_noalloc_scratch_bytes(void);
  * L = seq_lens[b] (the length INCLUDING the chunk), row c sits at position
  * p = L - n_b + c, and for every query head i (h = i / G, G = num_q_heads /
  * num_kv_heads):
- *     s_t = sm_scale * sum_d q[cu_q[b]+c][i][d] * E4M3(k_cache[pg(t)][h][t % P][d]) * k_scale[h]
+ *     s_t = sm_scale * sum_d q[cu_q[b]+c][i][d] * E4M3(k_cache[pg(t)][h][row(t)][d]) * k_scale[h]
  *     w_t = softmax_t(s_t)                              for t <= p (causal)
- *     out[cu_q[b]+c][i][d] = sum_t w_t * E4M3(v_cache[pg(t)][h][t % P][d]) * v_scale[h]
- * with pg(t) = block_table[b][t / P].  A chunk of one query is exactly one
- * decode step.  Two launches: the visible K/V of every sequence with a
- * non-empty chunk are first widened once from the pages to 16 bits (exact: K
- * as bf16, V as f16) in the workspace, then the attention runs on the tcgen05
- * tensor cores (q K^T on bf16 operands; the softmax weights as two f16 parts
- * against f16 V; fp32 accumulation, the PV accumulator added into a second
- * fp32 accumulator every 16 key tiles).  Deterministic.
+ *     out[cu_q[b]+c][i][d] = sum_t w_t * E4M3(v_cache[pg(t)][h][row(t)][d]) * v_scale[h]
+ * with pg and row as in pkv_paged_gqa_decode (per-sequence page sizes
+ * included).  A chunk of one query is exactly one decode step.  Two
+ * launches: the visible K/V of every sequence with a non-empty chunk are
+ * first widened once from the pages to 16 bits (exact: K as bf16, V as f16)
+ * into the workspace, packed sequence after sequence, then the attention
+ * runs on the tcgen05 tensor cores (q K^T on bf16 operands; the softmax
+ * weights as two f16 parts against f16 V; fp32 accumulation, the PV
+ * accumulator added into a second fp32 accumulator every 16 key tiles).
+ * Deterministic.
  *
  *   q              device bf16 [total_q][num_q_heads][head_dim], 16-byte
  *                  aligned.
@@ -324,11 +326,20 @@ size_t pkv_decode_noalloc_scratch_bytes(void);
  *                  cu_q[batch] <= total_q.
  *   total_q        rows of q and out.
  *   max_q_len      an upper bound of the chunk lengths n_b (sizes the grid).
- *   max_kv_len     an upper bound of seq_lens (sizes the workspace).
+ *   max_kv_len     an upper bound of seq_lens.
+ *   max_total_kv   0, or an upper bound of the sum of seq_lens[b] over the
+ *                  sequences with a non-empty chunk (with max_kv_len, sizes
+ *                  the workspace: a batch of one long prompt and many short
+ *                  chunks needs room for the long one only once).
  *   seq_lens       device int32 [batch]; a sequence with n_b > max_q_len,
- *                  seq_lens[b] < n_b, seq_lens[b] > max_kv_len or >
- *                  max_pages_per_seq * page_size, or inconsistent cu_q, sets
- *                  PKV_DEVERR_SEQLEN and its rows are not written.
+ *                  seq_lens[b] < n_b, seq_lens[b] > max_kv_len or beyond
+ *                  its table row, or inconsistent cu_q, sets
+ *                  PKV_DEVERR_SEQLEN and its rows are not written; so does a
+ *                  sequence whose widened copy would not fit the workspace
+ *                  (the sum bound exceeded).
+ *   seq_page_sizes device int32 [batch] or NULL, as in pkv_paged_gqa_decode
+ *                  (an invalid entry sets PKV_DEVERR_PAGESIZE and the
+ *                  sequence's rows are not written).
  *   block_table    entries of pages the chunk's positions need must lie in
  *                  [0, num_pages); others set PKV_DEVERR_PAGE and the page
  *                  reads as zeros.
@@ -336,23 +347,25 @@ size_t pkv_decode_noalloc_scratch_bytes(void);
  *                  PKV_F32, 16-byte aligned.  Rows outside every chunk are
  *                  not written.
  *   workspace      device, >= pkv_prefill_workspace_size(batch, num_kv_heads,
- *                  max_kv_len) bytes, 256-byte aligned: the 16-bit copies
- *                  of K and V (overwritten every call; must not be shared by
- *                  calls that overlap on the GPU).
+ *                  max_kv_len, max_total_kv) bytes, 256-byte aligned: the
+ *                  sequences' region offsets, then the 16-bit copies of K
+ *                  and V (overwritten every call; must not be shared by calls
+ *                  that overlap on the GPU).
  *   sm_scale       softmax scale, > 0 (normally 1/sqrt(head_dim)); k_scale
  *                  entries must be positive (calibration gives absmax/448,
  *                  floored at 1e-12).
  *   Caches, scales, head_dim (128), page sizes, G (1..8) and device_error as
  *   in pkv_paged_gqa_decode.  batch * num_kv_heads * ceil(max_q_len /
- *   (128 / G)) must be below 2^31.
+ *   (128 / G)) must be below 2^31, and so must the copies' rows.
  */
-size_t pkv_prefill_workspace_size(int batch, int num_kv_heads, int max_kv_len);
+size_t pkv_prefill_workspace_size(int batch, int num_kv_heads, int max_kv_len, int64_t max_total_kv);
 
 pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, int max_q_len,
                              const uint8_t *k_cache, const uint8_t *v_cache,
                              const float *k_scale, const float *v_scale,
                              const int32_t *block_table, int max_pages_per_seq,
-                             const int32_t *seq_lens, int batch, int max_kv_len,
+                             const int32_t *seq_lens, const int32_t *seq_page_sizes,
+                             int batch, int max_kv_len, int64_t max_total_kv,
                              int num_q_heads, int num_kv_heads, int head_dim,
                              int page_size, int64_t num_pages, float sm_scale,
                              void *out, int out_dtype,

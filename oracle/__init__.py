@@ -83,7 +83,7 @@ def _load():
         lib.oracle_paged_decode.argtypes = [P, P, P, P, P, P, i32, P, P, i32, i32, i32, i32,
                                             i32, i64, dbl, P, i64, P, P, i64, i32]
         lib.oracle_paged_prefill.restype = i32
-        lib.oracle_paged_prefill.argtypes = [P, P, P, P, P, P, P, i32, P, i32, i32, i32, i32, i32, i64, dbl, P,
+        lib.oracle_paged_prefill.argtypes = [P, P, P, P, P, P, P, i32, P, P, i32, i32, i32, i32, i32, i64, dbl, P,
                                              i32]
         lib.oracle_kv_absmax_update.restype = None
         lib.oracle_kv_absmax_update.argtypes = [P, i32, i64, i32, i32, P]
@@ -218,10 +218,11 @@ def kv_scale_from_max(running_max) -> np.ndarray:
 
 
 def paged_prefill(q_bits, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens,
-                  sm_scale: float | None = None, threads: int = 1) -> np.ndarray:
+                  sm_scale: float | None = None, threads: int = 1, seq_page_sizes=None) -> np.ndarray:
     """fp64 chunked-prefill attention.  q_bits: [T, Hq, D] bf16 bit patterns,
     the chunks of all sequences back to back; cu_q: [B + 1] row offsets;
-    seq_lens[b] includes the chunk.  Returns out [T, Hq, D] (fp64)."""
+    seq_lens[b] includes the chunk; seq_page_sizes as in paged_decode.
+    Returns out [T, Hq, D] (fp64)."""
     q_bits = _c(q_bits, np.uint16)
     cu_q = _c(cu_q, np.int32)
     k_cache = _c(k_cache, np.uint8)
@@ -236,11 +237,16 @@ def paged_prefill(q_bits, cu_q, k_cache, v_cache, k_scale, v_scale, block_table,
     if (v_cache.shape != k_cache.shape or D2 != D or cu_q.shape != (B + 1,) or block_table.shape[0] != B
             or cu_q[0] != 0 or cu_q[-1] != T):
         raise ValueError("shape mismatch")
+    if seq_page_sizes is not None:
+        seq_page_sizes = _c(seq_page_sizes, np.int32)
+        if seq_page_sizes.shape != (B,):
+            raise ValueError("seq_page_sizes shape mismatch")
     if sm_scale is None:
         sm_scale = 1.0 / np.sqrt(D)
     out = np.zeros((T, Hq, D), np.float64)
     st = _load().oracle_paged_prefill(_ptr(q_bits), _ptr(cu_q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale),
                                       _ptr(v_scale), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                      _ptr(seq_page_sizes) if seq_page_sizes is not None else None,
                                       B, Hq, Hkv, D, P, NP, float(sm_scale), _ptr(out), int(threads))
     if st != 0:
         raise ValueError(f"oracle_paged_prefill failed with status {st}")

@@ -397,12 +397,14 @@ void oracle_kv_scale_from_max(const float *running_max, int Hkv, float *scale)
  * counts the chunk, so with n = cu_q[b+1] - cu_q[b] its queries sit at
  * positions L - n .. L - 1.  The query at position p attends to cached tokens
  * 0 .. p, exactly as oracle_paged_decode does for a sequence of length p + 1.
+ * page_sizes: per-sequence page sizes as in oracle_paged_decode, or NULL.
  * out: [T][Hq][D] fp64.  A sequence with L < n is an error (status 3); its
  * rows are left untouched.  `threads` workers split each row's heads.
  * Returns 0 or the first non-zero status. */
 int oracle_paged_prefill(const uint16_t *q, const int32_t *cu_q, const uint8_t *k_cache, const uint8_t *v_cache,
                          const float *k_scale, const float *v_scale,
                          const int32_t *block_table, int max_pages, const int32_t *seq_lens,
+                         const int32_t *page_sizes,
                          int B, int Hq, int Hkv, int D, int P, int64_t num_pages,
                          double sm_scale, double *out, int threads)
 {
@@ -425,7 +427,8 @@ int oracle_paged_prefill(const uint16_t *q, const int32_t *cu_q, const uint8_t *
             int32_t len = seq_lens[b] - n + c + 1;       /* keys 0 .. position */
             int64_t row = (int64_t)cu_q[b] + c;
             int st = oracle_paged_decode(q + row * Hq * D, k_cache, v_cache, k_scale, v_scale,
-                                         block_table + (int64_t)b * max_pages, max_pages, &len, NULL, 1, Hq, Hkv, D, P,
+                                         block_table + (int64_t)b * max_pages, max_pages, &len,
+                                         page_sizes ? page_sizes + b : NULL, 1, Hq, Hkv, D, P,
                                          num_pages, sm_scale, sel, Hq, out + row * Hq * D, NULL, 0, threads);
             if (st && !status)
                 status = st;

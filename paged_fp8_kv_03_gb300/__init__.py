@@ -76,10 +76,10 @@ def load() -> ctypes.CDLL:
         lib.pkv_decode_noalloc_scratch_bytes.restype = sz
         lib.pkv_decode_noalloc_scratch_bytes.argtypes = []
         lib.pkv_prefill_workspace_size.restype = sz
-        lib.pkv_prefill_workspace_size.argtypes = [i32, i32, i32]
+        lib.pkv_prefill_workspace_size.argtypes = [i32, i32, i32, i64]
         lib.pkv_paged_prefill.restype = i32
-        lib.pkv_paged_prefill.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, i32, i32,
-                                          i32, i64, ctypes.c_float, vp, i32, vp, sz, vp, vp]
+        lib.pkv_paged_prefill.argtypes = [vp, vp, i32, i32, vp, vp, vp, vp, vp, i32, vp, vp, i32, i32, i64, i32, i32,
+                                          i32, i32, i64, ctypes.c_float, vp, i32, vp, sz, vp, vp]
         lib.pkv_read_device_error.restype = i32
         lib.pkv_read_device_error.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int32), vp]
         lib.pkv_test_withhold_load.restype = None
@@ -424,17 +424,20 @@ def paged_gqa_decode(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_len
     return out
 
 
-def pkv_prefill_workspace_size(batch, num_kv_heads, max_kv_len) -> int:
-    return int(load().pkv_prefill_workspace_size(int(batch), int(num_kv_heads), int(max_kv_len)))
+def pkv_prefill_workspace_size(batch, num_kv_heads, max_kv_len, max_total_kv=0) -> int:
+    return int(load().pkv_prefill_workspace_size(int(batch), int(num_kv_heads), int(max_kv_len),
+                                                 int(max_total_kv)))
 
 
 def pkv_paged_prefill(q, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, max_q_len,
-                      max_kv_len, workspace, sm_scale=None, device_error=None, stream=None) -> None:
+                      max_kv_len, workspace, sm_scale=None, device_error=None, stream=None, max_total_kv=0,
+                      seq_page_sizes=None) -> None:
     """q bf16 [total_q, Hq, 128] (the chunks of all sequences back to back);
     cu_q int32 [B + 1] row offsets; seq_lens int32 [B] (lengths including the
-    chunk); caches, scales and block_table as for decode; out [total_q, Hq,
-    128] bf16 or fp32; max_q_len / max_kv_len bounds of the chunk lengths and
-    of seq_lens; workspace uint8 (pkv_prefill_workspace_size bytes)."""
+    chunk); caches, scales, block_table and seq_page_sizes as for decode; out
+    [total_q, Hq, 128] bf16 or fp32; max_q_len / max_kv_len bounds of the
+    chunk lengths and of seq_lens, max_total_kv (0 or) a bound of their sum;
+    workspace uint8 (pkv_prefill_workspace_size bytes)."""
     _need(q, "q", torch.bfloat16, 3)
     _need(cu_q, "cu_q", torch.int32, 1)
     _need(k_cache, "k_cache", torch.uint8, 4)
@@ -454,33 +457,38 @@ def pkv_paged_prefill(q, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, 
         raise ValueError("q / cache / out shapes disagree")
     if block_table.shape[0] != B or cu_q.shape[0] != B + 1:
         raise ValueError("block_table / cu_q shapes disagree with seq_lens")
-    _same_device(q, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace, device_error)
+    _check_page_sizes(seq_page_sizes, B)
+    _same_device(q, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace, device_error,
+                 seq_page_sizes)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     with _device_of(q):
         st = load().pkv_paged_prefill(_ptr(q), _ptr(cu_q), T, int(max_q_len), _ptr(k_cache), _ptr(v_cache),
                                       _ptr(k_scale), _ptr(v_scale), _ptr(block_table), block_table.shape[1],
-                                      _ptr(seq_lens), B, int(max_kv_len), Hq, Hkv, D, P, NP, float(sm_scale), _ptr(out),
-                                      _act_code(out), _ptr(workspace), workspace.numel(), _ptr(device_error),
-                                      _stream(stream))
+                                      _ptr(seq_lens), _ptr(seq_page_sizes), B, int(max_kv_len), int(max_total_kv),
+                                      Hq, Hkv, D, P, NP, float(sm_scale), _ptr(out), _act_code(out),
+                                      _ptr(workspace), workspace.numel(), _ptr(device_error), _stream(stream))
     if st != 0:
         raise PkvError(st, "pkv_paged_prefill")
 
 
 def paged_prefill(q, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, max_q_len, out=None,
                   out_dtype=torch.bfloat16, max_kv_len=None, workspace=None, sm_scale=None, device_error=None,
-                  stream=None) -> torch.Tensor:
+                  stream=None, max_total_kv=0, seq_page_sizes=None) -> torch.Tensor:
     """Allocating convenience form: max_kv_len defaults to the block table's
-    capacity (max_pages x page size), the workspace to a fresh buffer."""
+    capacity (max_pages x page size; give it with seq_page_sizes), the
+    workspace to a fresh buffer."""
     if out is None:
         out = torch.empty(q.shape, dtype=out_dtype, device=q.device)
     if max_kv_len is None:
+        if seq_page_sizes is not None:
+            raise ValueError("give max_kv_len when seq_page_sizes is given")
         max_kv_len = block_table.shape[1] * k_cache.shape[2]
     if workspace is None:
-        workspace = torch.empty(pkv_prefill_workspace_size(seq_lens.shape[0], k_cache.shape[1], max_kv_len),
-                                dtype=torch.uint8, device=q.device)
+        workspace = torch.empty(pkv_prefill_workspace_size(seq_lens.shape[0], k_cache.shape[1], max_kv_len,
+                                                           max_total_kv), dtype=torch.uint8, device=q.device)
     pkv_paged_prefill(q, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, max_q_len,
-                      max_kv_len, workspace, sm_scale, device_error, stream)
+                      max_kv_len, workspace, sm_scale, device_error, stream, max_total_kv, seq_page_sizes)
     return out
 
 

@@ -76,18 +76,17 @@ bool make_q_map(CUtensorMap *tm, const void *q, int total_q, int hq, int group, 
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The 16-bit copies of K (bf16) or V (f16), [rows][kv_pad][128], as a 3-D
-// tensor (128 dims, kv_pad keys, rows = sequences x kv heads); one box = 64
-// dims of 128 keys, 128-byte swizzled: one column block of an MMA operand tile.
-bool make_kv16_map(CUtensorMap *tm, const void *base, int rows, int kv_pad, CUtensorMapDataType dtype)
+// The 16-bit copies of K (bf16) or V (f16), [rows][128], as a 3-D tensor
+// (128 dims, rows keys, 1); one box = 64 dims of 128 keys, 128-byte swizzled:
+// one column block of an MMA operand tile.
+bool make_kv16_map(CUtensorMap *tm, const void *base, long long rows, CUtensorMapDataType dtype)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return false;
-    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(kv_pad),
-                                static_cast<cuuint64_t>(rows)};
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows), 1};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kHeadDim) * 2,
-                                   static_cast<cuuint64_t>(kv_pad) * kHeadDim * 2};
+                                   static_cast<cuuint64_t>(rows) * kHeadDim * 2};
     const cuuint32_t box[3] = {64u, 128u, 1u};
     const cuuint32_t estr[3] = {1, 1, 1};
     return fn(tm, dtype, 3, const_cast<void *>(base), dims, strides, box, estr,
@@ -423,58 +422,64 @@ pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dt
                        workspace_bytes, device_error, max_ctas, stream);
 }
 
-size_t pkv_prefill_workspace_size(int batch, int num_kv_heads, int max_kv_len)
+size_t pkv_prefill_workspace_size(int batch, int num_kv_heads, int max_kv_len, int64_t max_total_kv)
 {
-    if (batch < 0 || num_kv_heads <= 0 || max_kv_len < 0)
+    if (batch < 0 || num_kv_heads <= 0 || max_kv_len < 0 || max_total_kv < 0)
         return 0;
-    return prefill_workspace_bytes(batch, num_kv_heads, max_kv_len);
+    return prefill_workspace_bytes(batch, num_kv_heads, max_kv_len, max_total_kv);
 }
 
 pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, int max_q_len, const uint8_t *k_cache,
                              const uint8_t *v_cache, const float *k_scale, const float *v_scale,
-                             const int32_t *block_table, int max_pages_per_seq, const int32_t *seq_lens, int batch,
-                             int max_kv_len, int num_q_heads, int num_kv_heads, int head_dim, int page_size,
-                             int64_t num_pages, float sm_scale, void *out, int out_dtype, void *workspace,
-                             size_t workspace_bytes, int32_t *device_error, cudaStream_t stream)
+                             const int32_t *block_table, int max_pages_per_seq, const int32_t *seq_lens,
+                             const int32_t *seq_page_sizes, int batch, int max_kv_len, int64_t max_total_kv,
+                             int num_q_heads, int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
+                             float sm_scale, void *out, int out_dtype, void *workspace, size_t workspace_bytes,
+                             int32_t *device_error, cudaStream_t stream)
 {
     pkv_status st = check_decode_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_seq,
                                        num_pages);
     if (st != PKV_OK)
         return st;
-    if (total_q < 0 || max_q_len < 0 || max_kv_len < 0)
+    if (total_q < 0 || max_q_len < 0 || max_kv_len < 0 || max_total_kv < 0)
         return PKV_ERR_SHAPE;
     if (out_dtype != PKV_F32 && out_dtype != PKV_BF16)
         return PKV_ERR_DTYPE;
     if (!(sm_scale > 0.f) || isinf(sm_scale))            // the kernel scales raw scores after their maximum
         return PKV_ERR_SHAPE;
+    if (seq_page_sizes && static_cast<int64_t>(max_pages_per_seq) * 256 >= (int64_t(1) << 31))
+        return PKV_ERR_UNSUPPORTED;
     if (batch == 0 || total_q == 0 || max_q_len == 0)
         return PKV_OK;
     if (!q || !cu_q || !k_cache || !v_cache || !k_scale || !v_scale || !block_table || !seq_lens || !out)
         return PKV_ERR_NULL;
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         !aligned(cu_q, 4) || !aligned(block_table, 4) || !aligned(seq_lens, 4) || !aligned(k_scale, 4) ||
-        !aligned(v_scale, 4) || !aligned(device_error, 4))
+        !aligned(v_scale, 4) || !aligned(device_error, 4) || !aligned(seq_page_sizes, 4))
         return PKV_ERR_ALIGN;
     const int group = num_q_heads / num_kv_heads;
     const int tpt = 128 / group;
     const int64_t max_tiles = (static_cast<int64_t>(max_q_len) + tpt - 1) / tpt;
     if (static_cast<int64_t>(batch) * num_kv_heads * max_tiles >= (int64_t(1) << 31))
         return PKV_ERR_UNSUPPORTED;
-    const int64_t kv_pad = (static_cast<int64_t>(max_kv_len) + 127) / 128 * 128;
-    if (kv_pad == 0 || kv_pad >= (int64_t(1) << 31) || static_cast<int64_t>(batch) * num_kv_heads >= (int64_t(1) << 31))
-        return max_kv_len == 0 ? PKV_OK : PKV_ERR_UNSUPPORTED;
+    if (max_kv_len == 0)
+        return PKV_OK;                                   // no sequence can hold a query
+    const long long rows = prefill_rows_bound(batch, num_kv_heads, max_kv_len, max_total_kv);
+    if (rows >= (int64_t(1) << 31) || batch + 1 + 8 > 49152)
+        return PKV_ERR_UNSUPPORTED;
     if (!workspace || !aligned(workspace, 256) ||
-        workspace_bytes < prefill_workspace_bytes(batch, num_kv_heads, max_kv_len))
+        workspace_bytes < prefill_workspace_bytes(batch, num_kv_heads, max_kv_len, max_total_kv))
         return PKV_ERR_WORKSPACE;
-    __half *k16 = static_cast<__half *>(workspace);
-    __half *v16 = k16 + static_cast<size_t>(batch) * num_kv_heads * kv_pad * kHeadDim;
+    int *tile_off = static_cast<int *>(workspace);
+    __half *k16 = reinterpret_cast<__half *>(static_cast<uint8_t *>(workspace) + prefill_header_bytes(batch));
+    __half *v16 = k16 + static_cast<size_t>(rows) * kHeadDim;
 
     alignas(64) CUtensorMap tm_q;
     alignas(64) CUtensorMap tm_k;
     alignas(64) CUtensorMap tm_v;
     if (!make_q_map(&tm_q, q, total_q, num_q_heads, group, tpt) ||
-        !make_kv16_map(&tm_k, k16, batch * num_kv_heads, static_cast<int>(kv_pad), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) ||
-        !make_kv16_map(&tm_v, v16, batch * num_kv_heads, static_cast<int>(kv_pad), CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
+        !make_kv16_map(&tm_k, k16, rows, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) ||
+        !make_kv16_map(&tm_v, v16, rows, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
         return PKV_ERR_CUDA;
 
     PrefillArgs a;
@@ -496,8 +501,11 @@ pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, in
     a.num_pages = num_pages;
     a.k_cache = k_cache;
     a.v_cache = v_cache;
+    a.page_sizes = seq_page_sizes;
+    a.pool_log2 = 31 - __builtin_clz(static_cast<unsigned>(page_size));
     a.max_kv_len = max_kv_len;
-    a.kv_pad = static_cast<int>(kv_pad);
+    a.tile_off = tile_off;
+    a.rows_cap = rows;
     a.k16 = k16;
     a.v16 = v16;
     // Test facility for the timeout path (pkv_test_withhold_load): that CTA

@@ -65,17 +65,9 @@ __device__ __forceinline__ int clamp_len(int L, int cap)
     return L < 0 ? 0 : (L > cap ? cap : L);
 }
 
-// log2 of sequence b's page size in tokens (its pages are runs of
-// P_b / page_size consecutive pool pages), or -1 if P_b is not a power of two
-// in [page_size, 256].
 __device__ __forceinline__ int page_log2_of(const DecodeArgs &a, int b)
 {
-    if (a.page_sizes == nullptr)
-        return a.pool_log2;
-    const int pb = __ldg(a.page_sizes + b);
-    if (pb < a.page_size || pb > 256 || (pb & (pb - 1)) != 0)
-        return -1;
-    return 31 - __clz(pb);
+    return seq_page_log2(a, b);
 }
 
 // Tokens of sequence b the call attends: seq_lens[b] clamped to [0, min(max_len,
@@ -90,19 +82,9 @@ __device__ __forceinline__ int seq_len_of(const DecodeArgs &a, int b)
     return clamp_len(__ldg(a.seq_lens + b), cap);
 }
 
-// Pool page and row of token t of sequence b (lp = page_log2_of): entry
-// bt[b][t / P_b] is the first pool page of the run holding the logical page,
-// offset o = t % P_b lies in pool page entry + o / P, row o % P.  Returns
-// false for an entry outside the pool.
 __device__ __forceinline__ bool token_page(const DecodeArgs &a, int b, int lp, int t, int &phys, int &row)
 {
-    const int entry = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + (t >> lp));
-    const int o = t & ((1 << lp) - 1);
-    if (entry < 0 || entry >= a.num_pages)
-        return false;
-    phys = entry + (o >> a.pool_log2);
-    row = o & (a.page_size - 1);
-    return phys < a.num_pages;
+    return seq_token_page(a, b, lp, t, phys, row);
 }
 
 __device__ __forceinline__ int chunks_of(const int *ps, int b)

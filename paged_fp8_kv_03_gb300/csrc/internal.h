@@ -101,10 +101,15 @@ struct PrefillArgs {
     int page_size;
     int64_t num_pages;
     const uint8_t *k_cache, *v_cache;
-    int max_kv_len;                 // bound of seq_lens; the 16-bit copies hold kv_pad rows per (sequence, kv head)
-    int kv_pad;                     // max_kv_len rounded up to a key tile (128)
-    __half *k16, *v16;              // 16-bit copies [batch * hkv][kv_pad][128] (caller workspace):
-                                    // K as bf16 bits, V as f16, both exact widenings of E4M3
+    const int32_t *page_sizes;      // [batch] tokens per page of each sequence, or nullptr: all page_size
+    int pool_log2;                  // log2(page_size)
+    int max_kv_len;                 // bound of seq_lens
+    int *tile_off;                  // [batch + 1] first 128-row tile of each sequence's widened region (caller
+                                    // workspace, written by the widening kernel, read by the attention kernel)
+    long long rows_cap;             // rows of the 16-bit copies the workspace holds
+    __half *k16, *v16;              // 16-bit copies [rows_cap][128] (caller workspace): sequence b's kv head h
+                                    // owns rows 128 * tile_off[b] + h * pad(L_b) .. + pad(L_b) - 1, pad = L
+                                    // rounded up to 128; K as bf16 bits, V as f16, exact widenings of E4M3
     int withhold_block;             // failure-detection test hook (-1 = off)
     float sm_scale_log2;
     void *out;
@@ -112,11 +117,30 @@ struct PrefillArgs {
     int32_t *err;
 };
 
-// Workspace of pkv_paged_prefill: the 16-bit copies of K (bf16) and V (f16).
-inline size_t prefill_workspace_bytes(int batch, int hkv, int max_kv_len)
+// Workspace of pkv_paged_prefill: the tile offsets of the sequences'
+// regions (256-byte rounded), then the 16-bit copies of K (bf16) and of V
+// (f16), each [rows][128].  Rows: the kv heads times the sum over sequences
+// of L_b rounded up to 128, bounded by max_kv_len per sequence and, when
+// given (> 0), by max_total_kv over the batch.
+inline size_t prefill_header_bytes(int batch)
 {
-    const size_t pad = (static_cast<size_t>(max_kv_len) + 127) / 128 * 128;
-    return 2 * static_cast<size_t>(batch) * hkv * pad * 128 * sizeof(__half);
+    return ((static_cast<size_t>(batch) + 1) * sizeof(int) + 255) & ~size_t(255);
+}
+
+inline long long prefill_rows_bound(int batch, int hkv, int max_kv_len, long long max_total_kv)
+{
+    long long tiles = static_cast<long long>(batch) * ((static_cast<long long>(max_kv_len) + 127) / 128);
+    if (max_total_kv > 0) {
+        const long long t2 = (max_total_kv + 127) / 128 + batch;   // sum of ceil(L_b / 128) <= sum L_b / 128 + batch
+        tiles = t2 < tiles ? t2 : tiles;
+    }
+    return tiles * 128 * hkv;
+}
+
+inline size_t prefill_workspace_bytes(int batch, int hkv, int max_kv_len, long long max_total_kv)
+{
+    return prefill_header_bytes(batch) +
+           2 * static_cast<size_t>(prefill_rows_bound(batch, hkv, max_kv_len, max_total_kv)) * 128 * sizeof(__half);
 }
 
 // Workspace = header + segment records (rounded to 256 bytes), then the
@@ -133,6 +157,39 @@ inline __host__ __device__ long long decode_subs(long long total, long long work
     const long long per = (total + workers - 1) / workers;
     const long long s = (per + kChainChunks - 1) / kChainChunks;
     return s < 1 ? 1 : s;
+}
+
+// ---------------------------------------------------------------- page walk
+// Shared by decode and prefill (Args: DecodeArgs or PrefillArgs).  Sequence
+// b's pages hold P_b tokens: a run of P_b / page_size consecutive pool pages
+// whose first page is the block-table entry (P_b = page_size unless per-
+// sequence page sizes are given).
+
+// log2(P_b), or -1 if P_b is not a power of two in [page_size, 256].
+template <typename Args>
+__device__ __forceinline__ int seq_page_log2(const Args &a, int b)
+{
+    if (a.page_sizes == nullptr)
+        return a.pool_log2;
+    const int pb = __ldg(a.page_sizes + b);
+    if (pb < a.page_size || pb > 256 || (pb & (pb - 1)) != 0)
+        return -1;
+    return 31 - __clz(pb);
+}
+
+// Pool page and row of token t of sequence b (lp = seq_page_log2): entry
+// bt[b][t / P_b], offset o = t % P_b in pool page entry + o / page_size, row
+// o % page_size.  False for an entry (or page) outside the pool.
+template <typename Args>
+__device__ __forceinline__ bool seq_token_page(const Args &a, int b, int lp, int t, int &phys, int &row)
+{
+    const int entry = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + (t >> lp));
+    const int o = t & ((1 << lp) - 1);
+    if (entry < 0 || entry >= a.num_pages)
+        return false;
+    phys = entry + (o >> a.pool_log2);
+    row = o & (a.page_size - 1);
+    return phys < a.num_pages;
 }
 
 // Host helpers (api.cu).

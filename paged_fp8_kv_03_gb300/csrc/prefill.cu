@@ -210,66 +210,129 @@ __device__ __forceinline__ bool elect_one()
 
 // Checks a sequence's sizes; false (and PKV_DEVERR_SEQLEN when `report`) when
 // the chunk or its length are inconsistent.
-__device__ __forceinline__ bool sequence_ok(const PrefillArgs &a, int q0, int q1, int L, bool report)
+__device__ __forceinline__ bool sequence_ok(const PrefillArgs &a, int b, int q0, int q1, int L, bool report)
 {
     const int n = q1 - q0;
+    const int lp = seq_page_log2(a, b);
     const bool ok = q0 >= 0 && n >= 0 && q1 <= a.total_q && n <= a.max_q_len && L >= n && L <= a.max_kv_len &&
-                    static_cast<int64_t>(L) <= static_cast<int64_t>(a.max_pages) * a.page_size;
+                    lp >= 0 && static_cast<int64_t>(L) <= (static_cast<int64_t>(a.max_pages) << lp);
     if (!ok && report && a.err)
-        atomicOr(a.err, PKV_DEVERR_SEQLEN);
+        atomicOr(a.err, lp < 0 ? PKV_DEVERR_PAGESIZE : PKV_DEVERR_SEQLEN);
     return ok;
 }
 
+// 128-row tiles of sequence b's widened region (all its kv heads): zero for a
+// sequence with an empty or inconsistent chunk.
+__device__ __forceinline__ long long region_tiles(const PrefillArgs &a, int b)
+{
+    const int q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1);
+    const int L = __ldg(a.seq_lens + b);
+    if (q1 - q0 <= 0 || !sequence_ok(a, b, q0, q1, L, false))
+        return 0;
+    return static_cast<long long>(a.hkv) * ((L + kKeys - 1) / kKeys);
+}
+
 // ---------------------------------------------------------------------- widening
-// One thread per 16 FP8 bytes (16 dims of one key row of one kv head) of K and
-// of V: reads them through the block table and writes 32 bytes of f16 to the
-// dense copies.  Rows from L up to the next multiple of 128 are zeros.
-// Sequences with an empty or inconsistent chunk are skipped.
+// Every CTA first lays out the regions: tile_off[b] = the first 128-row tile
+// of sequence b's region, a prefix sum of region_tiles (saturated just past
+// the workspace's capacity, so a region that does not fit is recognisable);
+// CTA 0 also stores them for the attention kernel and flags sequences whose
+// region does not fit.  Then one thread per 16 FP8 bytes (16 dims of one key
+// row of one kv head) of K and of V reads them through the block table and
+// writes 32 bytes of 16-bit values to the region.  Rows from L up to the next
+// multiple of 128 are zeros.
 __global__ void __launch_bounds__(256) kv_widen_kernel(const PrefillArgs a)
 {
-    const int64_t per_head = static_cast<int64_t>(a.kv_pad) * 8;   // pieces of one (sequence, kv head)
-    const int64_t total = static_cast<int64_t>(a.batch) * a.hkv * per_head;
+    extern __shared__ int off[];                         // [batch + 1], then 8 warp sums
+    int *warp_sum = off + a.batch + 1;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const long long cap_tiles = a.rows_cap / 128;
+    {
+        const int chunk = (a.batch + 255) / 256;
+        const int b0 = min(a.batch, tid * chunk), b1 = min(a.batch, b0 + chunk);
+        long long local = 0;
+        for (int b = b0; b < b1; ++b)
+            local += region_tiles(a, b);
+        // saturate: nothing past cap_tiles + 1 matters
+        int loc = static_cast<int>(local < cap_tiles + 1 ? local : cap_tiles + 1);
+        int incl = loc;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(kAll, incl, o);
+            if (lane >= o)
+                incl = min(incl + v, static_cast<int>(cap_tiles + 1));
+        }
+        if (lane == 31)
+            warp_sum[warp] = incl;
+        __syncthreads();
+        int base = 0;
+        for (int w = 0; w < warp; ++w)
+            base = min(base + warp_sum[w], static_cast<int>(cap_tiles + 1));
+        int run = min(base + incl - loc, static_cast<int>(cap_tiles + 1));
+        for (int b = b0; b < b1; ++b) {
+            off[b] = run;
+            run = static_cast<int>(min(run + region_tiles(a, b), cap_tiles + 1));
+        }
+        if (tid == 255)
+            off[a.batch] = min(base + incl, static_cast<int>(cap_tiles + 1));
+        __syncthreads();
+        if (blockIdx.x == 0) {
+            for (int b = tid; b <= a.batch; b += 256) {
+                a.tile_off[b] = off[b];
+                if (b < a.batch && off[b + 1] > cap_tiles && off[b + 1] > off[b] && a.err)
+                    atomicOr(a.err, PKV_DEVERR_SEQLEN);          // its region does not fit the workspace
+            }
+        }
+    }
+    const int64_t end_tile = min(static_cast<long long>(off[a.batch]), cap_tiles);
+    const int64_t total = end_tile * 128 * 8;
     for (int64_t u = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; u < total;
          u += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t bh = u / per_head;
-        const int r = static_cast<int>((u - bh * per_head) >> 3);  // key row
-        const int e = static_cast<int>(u & 7);                      // dims 16 e .. 16 e + 15
-        const int b = static_cast<int>(bh / a.hkv);
-        const int h = static_cast<int>(bh - static_cast<int64_t>(b) * a.hkv);
-        const int q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1);
+        const int64_t R = u >> 3;                               // row of the copies
+        const int e = static_cast<int>(u & 7);                  // dims 16 e .. 16 e + 15
+        const int tile = static_cast<int>(R >> 7);
+        int lo = 0, hi = a.batch - 1;                           // the sequence whose region holds the tile
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (off[mid] <= tile)
+                lo = mid;
+            else
+                hi = mid - 1;
+        }
+        const int b = lo;
+        if (off[b + 1] > cap_tiles)
+            continue;                                           // region past the workspace: flagged above
         const int L = __ldg(a.seq_lens + b);
-        if (q1 - q0 <= 0 || !sequence_ok(a, q0, q1, L, false))
-            continue;
-        if (r >= ((L + kKeys - 1) / kKeys) * kKeys)
-            continue;
+        const int pad = ((L + kKeys - 1) / kKeys) * kKeys;
+        const int local = static_cast<int>(R - static_cast<int64_t>(off[b]) * 128);
+        const int h = local / pad, r = local - h * pad;
         uint4 k = make_uint4(0, 0, 0, 0), v = make_uint4(0, 0, 0, 0);
         if (r < L) {
-            const int pg = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + r / a.page_size);
-            if (pg >= 0 && pg < a.num_pages) {
-                const int64_t src = ((static_cast<int64_t>(pg) * a.hkv + h) * a.page_size + r % a.page_size) * kHeadDim
-                                    + 16 * e;
+            int pg, row;
+            if (seq_token_page(a, b, seq_page_log2(a, b), r, pg, row)) {
+                const int64_t src = ((static_cast<int64_t>(pg) * a.hkv + h) * a.page_size + row) * kHeadDim + 16 * e;
                 k = __ldg(reinterpret_cast<const uint4 *>(a.k_cache + src));
                 v = __ldg(reinterpret_cast<const uint4 *>(a.v_cache + src));
             } else if (e == 0 && a.err) {
                 atomicOr(a.err, PKV_DEVERR_PAGE);
             }
         }
-        const int64_t dst = (bh * a.kv_pad + r) * kHeadDim + 16 * e;   // in f16 elements
-        uint4 lo, hi;
-        e4m3x4_to_f16x4(k.x, lo.x, lo.y);
-        e4m3x4_to_f16x4(k.y, lo.z, lo.w);
-        e4m3x4_to_f16x4(k.z, hi.x, hi.y);
-        e4m3x4_to_f16x4(k.w, hi.z, hi.w);
-        reinterpret_cast<uint4 *>(a.k16 + dst)[0] =
-            make_uint4(f16x2_to_bf16x2(lo.x), f16x2_to_bf16x2(lo.y), f16x2_to_bf16x2(lo.z), f16x2_to_bf16x2(lo.w));
-        reinterpret_cast<uint4 *>(a.k16 + dst)[1] =
-            make_uint4(f16x2_to_bf16x2(hi.x), f16x2_to_bf16x2(hi.y), f16x2_to_bf16x2(hi.z), f16x2_to_bf16x2(hi.w));
-        e4m3x4_to_f16x4(v.x, lo.x, lo.y);
-        e4m3x4_to_f16x4(v.y, lo.z, lo.w);
-        e4m3x4_to_f16x4(v.z, hi.x, hi.y);
-        e4m3x4_to_f16x4(v.w, hi.z, hi.w);
-        reinterpret_cast<uint4 *>(a.v16 + dst)[0] = lo;
-        reinterpret_cast<uint4 *>(a.v16 + dst)[1] = hi;
+        const int64_t dst = R * kHeadDim + 16 * e;              // in 16-bit elements
+        uint4 lo4, hi4;
+        e4m3x4_to_f16x4(k.x, lo4.x, lo4.y);
+        e4m3x4_to_f16x4(k.y, lo4.z, lo4.w);
+        e4m3x4_to_f16x4(k.z, hi4.x, hi4.y);
+        e4m3x4_to_f16x4(k.w, hi4.z, hi4.w);
+        reinterpret_cast<uint4 *>(a.k16 + dst)[0] = make_uint4(f16x2_to_bf16x2(lo4.x), f16x2_to_bf16x2(lo4.y),
+                                                               f16x2_to_bf16x2(lo4.z), f16x2_to_bf16x2(lo4.w));
+        reinterpret_cast<uint4 *>(a.k16 + dst)[1] = make_uint4(f16x2_to_bf16x2(hi4.x), f16x2_to_bf16x2(hi4.y),
+                                                               f16x2_to_bf16x2(hi4.z), f16x2_to_bf16x2(hi4.w));
+        e4m3x4_to_f16x4(v.x, lo4.x, lo4.y);
+        e4m3x4_to_f16x4(v.y, lo4.z, lo4.w);
+        e4m3x4_to_f16x4(v.z, hi4.x, hi4.y);
+        e4m3x4_to_f16x4(v.w, hi4.z, hi4.w);
+        reinterpret_cast<uint4 *>(a.v16 + dst)[0] = lo4;
+        reinterpret_cast<uint4 *>(a.v16 + dst)[1] = hi4;
     }
 }
 
@@ -291,8 +354,14 @@ __global__ void __launch_bounds__(kPThreads, 1)
     const int q0 = __ldg(a.cu_q + b), q1 = __ldg(a.cu_q + b + 1);
     const int n = q1 - q0;
     const int L = __ldg(a.seq_lens + b);
-    if (!sequence_ok(a, q0, q1, L, qt == 0 && h == 0 && threadIdx.x == 0))
+    if (!sequence_ok(a, b, q0, q1, L, qt == 0 && h == 0 && threadIdx.x == 0))
         return;
+    // this sequence's widened region (laid out by the widening kernel); a
+    // region past the workspace was flagged there and is not attended
+    const int off0 = __ldg(a.tile_off + b), off1 = __ldg(a.tile_off + b + 1);
+    if (off1 > a.rows_cap / 128 || off1 - off0 != a.hkv * ((L + kKeys - 1) / kKeys))
+        return;
+    const int row0 = off0 * 128 + h * (off1 - off0) / a.hkv * 128;   // first row of this kv head's copy
     const int t0 = qt * tpt;                             // first token of the tile in the chunk
     if (t0 >= n)
         return;
@@ -353,7 +422,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
             const uint64_t pol = l2_policy_evict_first();
             tma_load_3d(sb + PS::kQ, &tm_q, 0, h * G, q0 + t0, bar(PS::Q_FULL), pol);
             tma_load_3d(sb + PS::kQ + 16384, &tm_q, 64, h * G, q0 + t0, bar(PS::Q_FULL), pol);
-            const int z = b * a.hkv + h;
+            const int z = 0;
             uint32_t karmed[kKStages] = {}, varmed[kVStages] = {};
             bool ok = true;
             for (int t = 0; ok && t < nt; ++t) {
@@ -367,8 +436,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 if (t > 0 || static_cast<int>(blockIdx.x) != a.withhold_block) {
                     mbar_arrive_expect_tx(bar(PS::K_FULL + ks), PS::kTile);
                     karmed[ks] = static_cast<uint32_t>(t / kKStages) + 1;
-                    tma_load_3d_plain(sb + PS::kK16 + ks * PS::kTile, &tm_k, 0, t * kKeys, z, bar(PS::K_FULL + ks));
-                    tma_load_3d_plain(sb + PS::kK16 + ks * PS::kTile + 16384, &tm_k, 64, t * kKeys, z,
+                    tma_load_3d_plain(sb + PS::kK16 + ks * PS::kTile, &tm_k, 0, row0 + t * kKeys, z,
+                                      bar(PS::K_FULL + ks));
+                    tma_load_3d_plain(sb + PS::kK16 + ks * PS::kTile + 16384, &tm_k, 64, row0 + t * kKeys, z,
                                       bar(PS::K_FULL + ks));
                 }
                 if (t >= kVStages &&
@@ -378,8 +448,9 @@ __global__ void __launch_bounds__(kPThreads, 1)
                 }
                 mbar_arrive_expect_tx(bar(PS::V_FULL + vs), PS::kTile);
                 varmed[vs] = static_cast<uint32_t>(t / kVStages) + 1;
-                tma_load_3d_plain(sb + PS::kV16 + vs * PS::kTile, &tm_v, 0, t * kKeys, z, bar(PS::V_FULL + vs));
-                tma_load_3d_plain(sb + PS::kV16 + vs * PS::kTile + 16384, &tm_v, 64, t * kKeys, z,
+                tma_load_3d_plain(sb + PS::kV16 + vs * PS::kTile, &tm_v, 0, row0 + t * kKeys, z,
+                                  bar(PS::V_FULL + vs));
+                tma_load_3d_plain(sb + PS::kV16 + vs * PS::kTile + 16384, &tm_v, 64, row0 + t * kKeys, z,
                                   bar(PS::V_FULL + vs));
             }
             // No copy may still be landing when the CTA leaves.
@@ -718,13 +789,21 @@ cudaError_t launch_paged_prefill(const PrefillArgs &a, const CUtensorMap &tm_q, 
             g_prefill_attr[dev] = true;
         }
     }
-    const int64_t pieces = static_cast<int64_t>(a.batch) * a.hkv * a.kv_pad * 8;
+    const int64_t pieces = a.rows_cap * 8;
     int64_t wblocks = (pieces + 255) / 256;
     const int64_t cap = static_cast<int64_t>(device_sm_count()) * 16;
     if (wblocks > cap)
         wblocks = cap;
-    if (wblocks > 0)
-        kv_widen_kernel<<<static_cast<unsigned>(wblocks), 256, 0, stream>>>(a);
+    if (wblocks < 1)
+        wblocks = 1;                                     // CTA 0 always lays out the regions
+    const size_t wsmem = (static_cast<size_t>(a.batch) + 1 + 8) * sizeof(int);
+    if (wsmem > 48 * 1024) {
+        e = cudaFuncSetAttribute(kv_widen_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(wsmem));
+        if (e != cudaSuccess)
+            return e;
+    }
+    kv_widen_kernel<<<static_cast<unsigned>(wblocks), 256, wsmem, stream>>>(a);
     paged_prefill_kernel<<<static_cast<unsigned>(grid), kPThreads, PS::bytes(), stream>>>(tm_q, tm_k16, tm_v16, a);
     return cudaGetLastError();
 }

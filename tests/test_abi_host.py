@@ -174,12 +174,14 @@ def test_prefill_argument_errors(lib):
     c = _status_codes()
 
     def pre(**kw):
-        a = dict(q=A16, cu=A16, T=64, mq=32, kc=A16, vc=A16b, ks=A16, vs=A16, bt=A16, maxp=4, lens=A16, B=2,
-                 mkv=64, Hq=16, Hkv=2, D=128, P=16, np_=8, sm=0.088, out=A16, odt=1, ws=A16, wsb=1 << 24, err=None)
+        a = dict(q=A16, cu=A16, T=64, mq=32, kc=A16, vc=A16b, ks=A16, vs=A16, bt=A16, maxp=4, lens=A16, psz=None,
+                 B=2, mkv=64, mtot=0, Hq=16, Hkv=2, D=128, P=16, np_=8, sm=0.088, out=A16, odt=1, ws=A16,
+                 wsb=1 << 24, err=None)
         a.update(kw)
         return lib.pkv_paged_prefill(a["q"], a["cu"], a["T"], a["mq"], a["kc"], a["vc"], a["ks"], a["vs"],
-                                     a["bt"], a["maxp"], a["lens"], a["B"], a["mkv"], a["Hq"], a["Hkv"], a["D"],
-                                     a["P"], a["np_"], a["sm"], a["out"], a["odt"], a["ws"], a["wsb"], a["err"], None)
+                                     a["bt"], a["maxp"], a["lens"], a["psz"], a["B"], a["mkv"], a["mtot"], a["Hq"],
+                                     a["Hkv"], a["D"], a["P"], a["np_"], a["sm"], a["out"], a["odt"], a["ws"],
+                                     a["wsb"], a["err"], None)
     assert pre(T=-1) == c["PKV_ERR_SHAPE"]
     assert pre(mq=-1) == c["PKV_ERR_SHAPE"]
     assert pre(mkv=-1) == c["PKV_ERR_SHAPE"]
@@ -201,11 +203,17 @@ def test_prefill_argument_errors(lib):
     assert pre(ws=None) == c["PKV_ERR_WORKSPACE"]
     assert pre(ws=ctypes.c_void_p(0x10010)) == c["PKV_ERR_WORKSPACE"]          # not 256-byte aligned
     need = pkv.pkv_prefill_workspace_size(2, 2, 64)
-    assert need == 2 * 2 * 2 * 128 * 128 * 2                                    # K and V, kv rows padded to 128
+    assert need == 256 + 2 * 2 * 2 * 128 * 128 * 2                              # offsets, then K and V rows padded to 128
     assert pre(wsb=need - 1) == c["PKV_ERR_WORKSPACE"]
+    # a bound on the lengths' sum shrinks the copies: 3 sequences of up to 128K, 130K tokens in all
+    assert pkv.pkv_prefill_workspace_size(3, 8, 131072, 133120) == 256 + 2 * 8 * (1040 + 3) * 128 * 128 * 2
+    assert pkv.pkv_prefill_workspace_size(3, 8, 131072) == 256 + 2 * 8 * 3 * 1024 * 128 * 128 * 2
+    assert pre(mtot=-1) == c["PKV_ERR_SHAPE"]
+    assert pre(psz=ctypes.c_void_p(0x10001)) == c["PKV_ERR_ALIGN"]
     assert pre(T=0, q=None, cu=None, out=None) == c["PKV_OK"]          # nothing to compute
     assert pre(mq=0, q=None, cu=None, out=None) == c["PKV_OK"]
     assert pkv.pkv_prefill_workspace_size(-1, 2, 64) == 0
+    assert pkv.pkv_prefill_workspace_size(2, 2, 64, -5) == 0
 
 
 def test_read_device_error_argument_errors(lib):

@@ -22,6 +22,10 @@ def _cu(chunks):
     return np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
 
 
+def _psz_np(wl):
+    return np.array(wl.page_sizes, np.int32) if wl.page_sizes is not None else None
+
+
 def _oracle_pools(wl):
     ks, vs = wl.scales(0)
     shape = (wl.num_pages, wl.hkv, wl.page_size, wl.head_dim)
@@ -34,27 +38,29 @@ def _oracle_pools(wl):
     return kco, vco, ks.numpy(), vs.numpy()
 
 
-def _prefill(pkv, f, q, cu, max_q_len, out_dtype=torch.float32, err=None, bt=None, lens=None, fill=float("nan")):
+def _prefill(pkv, f, q, cu, max_q_len, out_dtype=torch.float32, err=None, bt=None, lens=None, fill=float("nan"),
+             max_total_kv=0):
     out = torch.full(q.shape, fill, dtype=out_dtype, device=q.device)
     pkv.paged_prefill(q, cu, f.kc, f.vc, f.ks, f.vs, f.bt if bt is None else bt, f.lens if lens is None else lens,
-                      max_q_len, out=out, device_error=f.err if err is None else err)
+                      max_q_len, out=out, device_error=f.err if err is None else err, max_kv_len=f.max_len,
+                      max_total_kv=max_total_kv, seq_page_sizes=f.psz)
     torch.cuda.synchronize()
     return out
 
 
-def _run_case(pkv, dev, lens, chunks, hq, hkv, page, seed=31):
-    wl = workloads.Workload(60, "prefill", lens, 0, hq, hkv, page, pool_factor=1.5, seed=seed)
+def _run_case(pkv, dev, lens, chunks, hq, hkv, page, seed=31, sizes=None, max_total_kv=0):
+    wl = workloads.Workload(60, "prefill", lens, 0, hq, hkv, page, pool_factor=1.5, seed=seed, page_sizes=sizes)
     f = fill_gpu(wl, 0, dev)
     cu = _cu(chunks)
     T = int(cu[-1])
     q = wl.q_rows(0, T)
     qd = q.to(dev)
     cud = torch.from_numpy(cu).to(dev)
-    got = _prefill(pkv, f, qd, cud, max(chunks))
+    got = _prefill(pkv, f, qd, cud, max(chunks), max_total_kv=max_total_kv)
     assert int(f.err.item()) == 0
     kco, vco, ks, vs = _oracle_pools(wl)
     ref = oracle.paged_prefill(q.view(torch.uint16).numpy(), cu, kco, vco, ks, vs, wl.block_table().numpy(),
-                               np.array(lens, np.int32), threads=8)
+                               np.array(lens, np.int32), threads=8, seq_page_sizes=_psz_np(wl))
     ma, rel = assert_close(got.double().cpu().numpy(), ref, f"prefill {lens} {chunks} G={hq // hkv} P={page}")
     return wl, f, qd, cud, got, ma, rel
 
@@ -71,6 +77,33 @@ def _run_case(pkv, dev, lens, chunks, hq, hkv, page, seed=31):
 ])
 def test_prefill_matches_oracle(pkv, cuda_device, lens, chunks, hq, hkv, page):
     _run_case(pkv, cuda_device, lens, chunks, hq, hkv, page)
+
+
+@pytest.mark.parametrize("lens,chunks,hq,hkv,sizes", [
+    ([300, 129, 1000, 70], [17, 129, 256, 70], 64, 8, [64, 16, 256, 32]),
+    ([9000, 700], [500, 700], 32, 8, [64, 16]),          # the notes' 16 / 64 split by length
+])
+def test_prefill_per_sequence_page_sizes(pkv, cuda_device, lens, chunks, hq, hkv, sizes):
+    _run_case(pkv, cuda_device, lens, chunks, hq, hkv, 16, sizes=sizes)
+
+
+def test_prefill_workspace_sized_by_total_length(pkv, cuda_device):
+    """One long prompt chunk beside many short ones, with the workspace sized
+    by the lengths' sum (not batch x longest): same rows as the default
+    workspace, the oracle's within tolerance; a sum bound that is too small is
+    reported and leaves the rows that do not fit unwritten."""
+    lens = [4000] + [40 + 7 * i for i in range(15)]
+    chunks = [1000] + [40 + 7 * i for i in range(15)]
+    wl, f, q, cu, got, _, _ = _run_case(pkv, cuda_device, lens, chunks, 32, 8, 16, max_total_kv=sum(lens))
+    small = pkv.pkv_prefill_workspace_size(len(lens), 8, f.max_len, sum(lens))
+    big = pkv.pkv_prefill_workspace_size(len(lens), 8, f.max_len)
+    assert small * 8 < big
+    again = _prefill(pkv, f, q, cu, max(chunks))
+    assert torch.equal(again, got)
+    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
+    out = _prefill(pkv, f, q, cu, max(chunks), err=err, max_total_kv=1000, fill=5.0)
+    assert int(err.item()) & pkv.DEVERR_SEQLEN
+    assert torch.all(out == 5.0)                         # the long chunk's region alone exceeds the bound
 
 
 def test_bf16_output_is_rounded_fp32_and_deterministic(pkv, cuda_device):

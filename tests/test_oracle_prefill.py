@@ -52,15 +52,16 @@ def _dense_causal(q, k, v, first):
     return out
 
 
-@pytest.mark.parametrize("chunks,page", [([5, 0, 3, 1], 16), ([40, 7, 3, 70], 32), ([40, 1, 0, 9], 64)])
-def test_prefill_matches_dense_causal(chunks, page):
-    wl = workloads.Workload(95, "prefill", [40, 70, 3, 70], 0, 8, 2, page, seed=9)
+@pytest.mark.parametrize("chunks,page,sizes", [([5, 0, 3, 1], 16, None), ([40, 7, 3, 70], 32, None),
+                                               ([40, 1, 0, 9], 64, None), ([40, 9, 3, 70], 16, [64, 16, 32, 64])])
+def test_prefill_matches_dense_causal(chunks, page, sizes):
+    wl = workloads.Workload(95, "prefill", [40, 70, 3, 70], 0, 8, 2, page, seed=9, page_sizes=sizes)
     kc, vc, ks, vs, dk, dv = _fill(wl)
     cu = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
     q = wl.q_rows(0, int(cu[-1]))
     lens = np.array(wl.seq_lens, np.int32)
     out = oracle.paged_prefill(q.view(torch.uint16).numpy(), cu, kc, vc, ks, vs, wl.block_table().numpy(), lens,
-                               threads=4)
+                               threads=4, seq_page_sizes=None if sizes is None else np.array(sizes, np.int32))
     for b, L in enumerate(wl.seq_lens):
         n = chunks[b]
         ref = _dense_causal(q[cu[b]:cu[b + 1]].double().numpy(), dk[b], dv[b], L - n)
