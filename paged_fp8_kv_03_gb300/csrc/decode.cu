@@ -65,9 +65,17 @@ __device__ __forceinline__ int clamp_len(int L, int cap)
     return L < 0 ? 0 : (L > cap ? cap : L);
 }
 
+// log2 of sequence b's page size in tokens (its pages are runs of
+// P_b / page_size consecutive pool pages), or -1 if P_b is not a power of two
+// in [page_size, 256].
 __device__ __forceinline__ int page_log2_of(const DecodeArgs &a, int b)
 {
-    return seq_page_log2(a, b);
+    if (a.page_sizes == nullptr)
+        return a.pool_log2;
+    const int pb = __ldg(a.page_sizes + b);
+    if (pb < a.page_size || pb > 256 || (pb & (pb - 1)) != 0)
+        return -1;
+    return 31 - __clz(pb);
 }
 
 // Tokens of sequence b the call attends: seq_lens[b] clamped to [0, min(max_len,
@@ -82,9 +90,19 @@ __device__ __forceinline__ int seq_len_of(const DecodeArgs &a, int b)
     return clamp_len(__ldg(a.seq_lens + b), cap);
 }
 
+// Pool page and row of token t of sequence b (lp = page_log2_of): entry
+// bt[b][t / P_b] is the first pool page of the run holding the logical page,
+// offset o = t % P_b lies in pool page entry + o / P, row o % P.  Returns
+// false for an entry outside the pool.
 __device__ __forceinline__ bool token_page(const DecodeArgs &a, int b, int lp, int t, int &phys, int &row)
 {
-    return seq_token_page(a, b, lp, t, phys, row);
+    const int entry = __ldg(a.block_table + static_cast<int64_t>(b) * a.max_pages + (t >> lp));
+    const int o = t & ((1 << lp) - 1);
+    if (entry < 0 || entry >= a.num_pages)
+        return false;
+    phys = entry + (o >> a.pool_log2);
+    row = o & (a.page_size - 1);
+    return phys < a.num_pages;
 }
 
 __device__ __forceinline__ int chunks_of(const int *ps, int b)
@@ -434,9 +452,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 {
     using S = Smem;
     constexpr int kStages = S::kStages;
-    // programmatic dependent launch: nothing is read before the previous
-    // kernel on the stream has finished and its writes are visible
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
@@ -721,14 +736,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
 }
 
-// One CTA per (sequence, kv head) segment with 16 warps: kMergeParts = 16 / G
-// warps per query head g of its group, lane j owning dimensions 4j .. 4j+3.
-// The warps of a head take turns over the segment's pieces in batches of 16
-// (batch k goes to part k % kMergeParts): lane i of the warp finds the slot
-// of piece i of the batch and loads its (m, l), every lane loads its four
-// dimensions of all 16 accumulators, and one exact rescale folds the batch
-// into the warp's running (M, L, A).  The parts of a head are then combined
-// through shared memory in part order.  The order is fixed, so results are
+// One CTA per (sequence, kv head) segment, one warp per query head g of its
+// group; lane j owns dimensions 4j .. 4j+3.  The warp merges the partial
+// states the workers covering the segment wrote for head g, in list order,
+// and writes the output row.  Pieces are taken 16 at a time: lane i of the
+// warp finds the slot of piece i and loads its (m, l); every lane loads its
+// four dimensions of all 16 accumulators; then one exact rescale folds the
+// batch into the running (M, L, A).  The order is fixed, so results are
 // deterministic.
 //
 // Where a segment's pieces are: with one sub-piece per worker range
@@ -736,20 +750,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 // written by worker w0 + i; with fewer chunk-heads than workers every worker
 // owns at most one, and piece i comes from the worker owning position start
 // + i; with subs > 1 a worker's range is also cut every kChainChunks chunks
-// and the pieces are walked worker by worker (every warp of the head walks
-// the whole list and keeps its own batches).
+// and the pieces are walked worker by worker.
 constexpr int kMergeBatch = 16;
-constexpr int kMergeThreads = 512;
 
-__global__ void __launch_bounds__(kMergeThreads) splitk_merge_kernel(const DecodeArgs a)
+__global__ void __launch_bounds__(32 * PKV_MAX_GROUP) splitk_merge_kernel(const DecodeArgs a)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid has finished
-    // the next call's decode kernel may start launching; it waits for this grid
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    __shared__ float part_state[kMergeThreads / 32][kHeadDim + 4];
-    const int seg = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int parts = kMergeThreads / 32 / a.group;          // warps per query head
-    const int g = warp / parts, part = warp - g * parts;
+    const int seg = blockIdx.x, g = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const SegRecord r = a.segs[seg];
     const DecodeHeader hd = *a.header;
     if (r.w0 < 0)
@@ -771,107 +778,77 @@ __global__ void __launch_bounds__(kMergeThreads) splitk_merge_kernel(const Decod
 
     float M = -INFINITY, L = 0.f;
     float A[4] = {0.f, 0.f, 0.f, 0.f};
-    if (g < a.group) {
-        for (int bi = 0;; ++bi) {
-            const int i0 = bi * kMergeBatch;
-            const bool mine = (bi % parts) == part;
-            // slot of piece i0 + lane (lanes >= the batch size, or another part's batch: -1)
-            int my_slot = -1;
-            int nb;
-            if (!walk) {
-                nb = min(kMergeBatch, n_known - i0);
-                if (nb <= 0)
-                    break;
-                if (!mine)
-                    continue;
-                if (lane < nb)
-                    my_slot = dense ? r.w0 + i0 + lane : worker_of(r.start + i0 + lane, total, workers);
-            } else {
-                nb = 0;
-                while (nb < kMergeBatch && lo_w + k < end) {
-                    if (lane == nb)
-                        my_slot = w * subs + static_cast<int>(k / kChainChunks);
-                    ++nb;
-                    k = (k / kChainChunks + 1) * kChainChunks;          // next sub-piece of this worker
-                    if (lo_w + k >= hi_w) {                              // next worker: starts at its range start
-                        ++w;
-                        lo_w = hi_w;
-                        hi_w = static_cast<int64_t>(w + 1) * total / workers;
-                        k = 0;
-                    }
+    for (int i0 = 0;; i0 += kMergeBatch) {
+        // slot of piece i0 + lane (lanes >= the batch size: -1)
+        int my_slot = -1;
+        int nb;
+        if (!walk) {
+            nb = min(kMergeBatch, n_known - i0);
+            if (nb <= 0)
+                break;
+            if (lane < nb)
+                my_slot = dense ? r.w0 + i0 + lane : worker_of(r.start + i0 + lane, total, workers);
+        } else {
+            nb = 0;
+            while (nb < kMergeBatch && lo_w + k < end) {
+                if (lane == nb)
+                    my_slot = w * subs + static_cast<int>(k / kChainChunks);
+                ++nb;
+                k = (k / kChainChunks + 1) * kChainChunks;          // next sub-piece of this worker
+                if (lo_w + k >= hi_w) {                              // next worker: starts at its range start
+                    ++w;
+                    lo_w = hi_w;
+                    hi_w = static_cast<int64_t>(w + 1) * total / workers;
+                    k = 0;
                 }
-                if (nb == 0)
-                    break;
-                if (!mine)
-                    continue;
             }
-            float m = -INFINITY, l = 0.f;
-            if (my_slot >= 0) {
-                const float *p = a.partials + (static_cast<int64_t>(my_slot + seg) * a.group + g) * kPartialStride;
-                m = p[kHeadDim];
-                l = p[kHeadDim + 1];
-            }
-            float4 v[kMergeBatch];
-#pragma unroll
-            for (int i = 0; i < kMergeBatch; ++i) {
-                const int si = __shfl_sync(kFull, my_slot, i);
-                v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-                if (i < nb)
-                    v[i] = *reinterpret_cast<const float4 *>(
-                        a.partials + (static_cast<int64_t>(si + seg) * a.group + g) * kPartialStride + 4 * lane);
-            }
-            float mb = m;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
-            const float mn = fmaxf(M, mb);
-            const float r0 = ex2_approx(M - mn);                     // 0 on the first batch (M = -inf)
-            const float sc = my_slot >= 0 ? ex2_approx(m - mn) : 0.f;
-            float ls = sc * l;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1)
-                ls += __shfl_xor_sync(kFull, ls, o);
-            L = L * r0 + ls;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-                A[c] *= r0;
-#pragma unroll
-            for (int i = 0; i < kMergeBatch; ++i) {
-                const float si = __shfl_sync(kFull, sc, i);
-                A[0] += si * v[i].x;
-                A[1] += si * v[i].y;
-                A[2] += si * v[i].z;
-                A[3] += si * v[i].w;
-            }
-            M = mn;
+            if (nb == 0)
+                break;
         }
-        *reinterpret_cast<float4 *>(&part_state[warp][4 * lane]) = make_float4(A[0], A[1], A[2], A[3]);
-        if (lane == 0) {
-            part_state[warp][kHeadDim] = M;
-            part_state[warp][kHeadDim + 1] = L;
+        float m = -INFINITY, l = 0.f;
+        if (my_slot >= 0) {
+            const float *p = a.partials + (static_cast<int64_t>(my_slot + seg) * a.group + g) * kPartialStride;
+            m = p[kHeadDim];
+            l = p[kHeadDim + 1];
         }
+        float4 v[kMergeBatch];
+#pragma unroll
+        for (int i = 0; i < kMergeBatch; ++i) {
+            const int si = __shfl_sync(kFull, my_slot, i);
+            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (i < nb)
+                v[i] = *reinterpret_cast<const float4 *>(
+                    a.partials + (static_cast<int64_t>(si + seg) * a.group + g) * kPartialStride + 4 * lane);
+        }
+        float mb = m;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            mb = fmaxf(mb, __shfl_xor_sync(kFull, mb, o));
+        const float mn = fmaxf(M, mb);
+        const float r0 = ex2_approx(M - mn);                     // 0 on the first batch (M = -inf)
+        const float sc = my_slot >= 0 ? ex2_approx(m - mn) : 0.f;
+        float ls = sc * l;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            ls += __shfl_xor_sync(kFull, ls, o);
+        L = L * r0 + ls;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            A[c] *= r0;
+#pragma unroll
+        for (int i = 0; i < kMergeBatch; ++i) {
+            const float si = __shfl_sync(kFull, sc, i);
+            A[0] += si * v[i].x;
+            A[1] += si * v[i].y;
+            A[2] += si * v[i].z;
+            A[3] += si * v[i].w;
+        }
+        M = mn;
     }
-    __syncthreads();
-    if (g >= a.group || part != 0)
-        return;
-    // combine the head's parts in order (a part without pieces has M = -inf, L = 0)
-    float Mt = -INFINITY;
-    for (int q = 0; q < parts; ++q)
-        Mt = fmaxf(Mt, part_state[warp + q][kHeadDim]);
-    float Lt = 0.f, At[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int q = 0; q < parts; ++q) {
-        const float f = ex2_approx(part_state[warp + q][kHeadDim] - Mt);
-        Lt += part_state[warp + q][kHeadDim + 1] * f;
-        const float4 pa = *reinterpret_cast<const float4 *>(&part_state[warp + q][4 * lane]);
-        At[0] += pa.x * f;
-        At[1] += pa.y * f;
-        At[2] += pa.z * f;
-        At[3] += pa.w * f;
-    }
-    const float f = __ldg(a.v_scale + h) / Lt;
+    const float f = __ldg(a.v_scale + h) / L;
     const int64_t row = static_cast<int64_t>(b) * a.hq + static_cast<int64_t>(h) * a.group + g;
-    store_pair(a, row, 4 * lane, At[0] * f, At[1] * f);
-    store_pair(a, row, 4 * lane + 2, At[2] * f, At[3] * f);
+    store_pair(a, row, 4 * lane, A[0] * f, A[1] * f);
+    store_pair(a, row, 4 * lane + 2, A[2] * f, A[3] * f);
 }
 
 }  // namespace
@@ -889,28 +866,19 @@ const void *decode_kernel_for(int /*page_size*/)
 cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                 int page_size, cudaStream_t stream)
 {
-    // Both kernels are programmatic dependent launches: the decode grid may be
-    // scheduled while the previous kernel on the stream drains (it waits for
-    // that kernel before reading anything), the merge grid while the decode
-    // grid drains (it waits for it likewise).
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cudaLaunchConfig_t dcfg = {};
-    dcfg.gridDim = dim3(static_cast<unsigned>(a.num_ctas), 1, 1);
-    dcfg.blockDim = dim3(kThreads, 1, 1);
-    dcfg.dynamicSmemBytes = decode_smem_bytes(page_size, a.batch);
-    dcfg.stream = stream;
-    dcfg.attrs = attr;
-    dcfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&dcfg, paged_gqa_decode_kernel, tm_k, tm_v, a);
+    const size_t smem = decode_smem_bytes(page_size, a.batch);
+    paged_gqa_decode_kernel<<<a.num_ctas, kThreads, smem, stream>>>(tm_k, tm_v, a);
+    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.batch * a.hkv), 1, 1);
-    cfg.blockDim = dim3(kMergeThreads, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * a.group), 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, splitk_merge_kernel, a);
