@@ -633,7 +633,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         Unit rng[2];                // [cur]: the math's unit, [cur ^ ahead]: the copies' unit
         int cur, ahead;
         int icount;                 // chunks of the copies' unit
-        int append_at;              // chunk of the copies' unit before which its new tokens are stored (-1: none)
+        int append_at[2];           // per unit of rng[]: chunk before which its new tokens are stored (-1: none)
         int have_big, claims_left;
         Loc nbase;                  // copies: first chunk of the next block-table batch
     };
@@ -682,7 +682,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint32_t pending = 0, pend_par = 0;
     int fi = 0, fc = 0;                        // chunks issued / consumed by this warp (all units)
 
-    auto start_copies = [&](const Unit &u) {   // warp-uniform
+    auto start_copies = [&](const Unit &u, int slot) {   // warp-uniform; u is rng[slot]
         const int n = u.hi - u.lo;
         const Loc l0 = locate(pstart, a.batch, a.hkv, u.lo);
         const Loc nb = advance(pstart, a.batch, a.hkv, l0, 32);
@@ -697,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         __syncwarp();
         if (lane == 0) {
             ws->icount = n;
-            ws->append_at = at;
+            ws->append_at[slot] = at;
             ws->nbase = nb;
         }
         __syncwarp();
@@ -721,12 +721,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                     ws->ahead = 1;
                 }
                 __syncwarp();
-                start_copies(u);
+                start_copies(u, slot);
             }
             // next stop: the first chunk that may hold a new token while the
             // math has not stored them yet (it does so when it starts the
             // unit), else the unit's end
-            const int at = ws->append_at;
+            const int at = ws->append_at[ws->cur ^ ws->ahead];
             ievent = at >= 0 ? at : ws->icount;
             if (iq == ievent)
                 return false;
@@ -771,15 +771,20 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     // unit, outside the chunk loop; the copies of that unit stop short of the
     // first chunk that may hold one until then (the copies are then in the
     // same unit: they never run more than one unit ahead).
-    auto store_new_tokens = [&](const Unit &u) {
-        if (ws->append_at < 0)
+    // The math's unit is rng[cur]; if the copies are still in it, they may
+    // now go past its new tokens.
+    auto store_new_tokens = [&]() {
+        const int c = ws->cur;
+        if (ws->append_at[c] < 0)
             return;
+        const Unit u = ws->rng[c];
         append_own_tokens(a, pstart, u.lo, u.hi, lane);
         __syncwarp();
         if (lane == 0)
-            ws->append_at = -1;
+            ws->append_at[c] = -1;
         __syncwarp();
-        ievent = ws->icount;
+        if (!ws->ahead)
+            ievent = ws->icount;
     };
 
     {
@@ -790,9 +795,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (lane == 0)
             ws->rng[0] = u0;
         __syncwarp();
-        start_copies(u0);
+        start_copies(u0, 0);
         fill();                                  // the unit's chunks before its new tokens go out first
-        store_new_tokens(u0);
+        store_new_tokens();
     }
     fill();
 
@@ -818,7 +823,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             cu = ws->rng[nc];
             cpos = cu.lo;
             cons = locate(pstart, a.batch, a.hkv, cpos);
-            store_new_tokens(cu);
+            store_new_tokens();
             fill();
             continue;
         }
