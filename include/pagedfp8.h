@@ -47,10 +47,6 @@
  *   PKV_DEVERR_PAGESIZE  a per-sequence page size that is not a power of two
  *                        in [page_size, 256] (the sequence is treated as
  *                        empty: zero output rows)
- *   PKV_DEVERR_WORKSPACE the decode workspace's work counter was not in its
- *                        ready state when the call started (a fresh
- *                        workspace must be zeroed once; outputs undefined;
- *                        the call leaves the workspace ready again)
  * The word is sticky: clear it (pkv_read_device_error with clear = 1, or
  * cudaMemsetAsync) before a call whose errors you want to attribute.
  */
@@ -88,8 +84,7 @@ enum {
     PKV_DEVERR_PAGE = 2,
     PKV_DEVERR_SEQLEN = 4,
     PKV_DEVERR_TIMEOUT = 8,
-    PKV_DEVERR_PAGESIZE = 16,
-    PKV_DEVERR_WORKSPACE = 32
+    PKV_DEVERR_PAGESIZE = 16
 };
 
 /* Build limits. */
@@ -179,15 +174,12 @@ size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
  * pool pages, and its table entry is the first of them ([N] §3.2: 16-token
  * pages for short sequences, 64-token pages for long ones).  L == 0 gives a
  * zero row.  Long contexts are split across warps (split-K /
- * flash-decoding): the list of (sequence, kv head, 16-token chunk) work is
- * cut into fixed units, one static unit per warp for 4/5 of it and small
- * units that the warps take in turn for the rest, so that warps on faster
- * SMs do more; no piece accumulates more than 512 chunks into one partial
- * state, and a second kernel merges the partial softmax states exactly
- * (log-sum-exp) in list order.  The units do not depend on which warp takes
- * them, so results are deterministic run to run and independent of where
- * the pages sit in the pool.  Two kernel launches (the second is a
- * programmatic dependent launch that overlaps the first one's tail).
+ * flash-decoding); no warp accumulates more than 512 chunks of 16 tokens
+ * into one partial state, and a second kernel merges the partial softmax
+ * states exactly (log-sum-exp) in a fixed order: results are deterministic
+ * run to run and independent of where the pages sit in the pool.  Two kernel
+ * launches (the second is a programmatic dependent launch that overlaps the
+ * first one's tail).
  *
  *   q              device bf16 [batch][num_q_heads][head_dim] (|q| < 65504).
  *   k_cache, v_cache device uint8 pools (layout above), 16-byte aligned.
@@ -208,15 +200,10 @@ size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
  *                  PKV_BF16 (bf16, RNE of the fp32 result) or PKV_F32.
  *   workspace      device, >= pkv_decode_workspace_size(batch, num_q_heads,
  *                  num_kv_heads, head_dim, max_seq_len, page_size, max_ctas)
- *                  bytes, 256-byte aligned: a header (the work plan and the
- *                  counter the split-K workers take their share of the work
- *                  from), per-(sequence, kv head) records, then the partial
- *                  states.  Zero its first 256 bytes once before its first
- *                  call (e.g. cudaMemsetAsync); every call leaves them ready
- *                  for the next one (a call that finds them otherwise sets
- *                  PKV_DEVERR_WORKSPACE).  The rest needs no initialisation.
- *                  One workspace must not be shared by calls that overlap on
- *                  the GPU.
+ *                  bytes, 256-byte aligned: a header, per-(sequence, kv
+ *                  head) records, then the partial states.  Contents need no
+ *                  initialisation; one workspace must not be shared by calls
+ *                  that overlap on the GPU.
  *   device_error   device int32 or NULL (bits above).
  *   max_ctas       0 = one persistent CTA per resident slot on the device;
  *                  > 0 caps the CTA count (changes the split, not the math).

@@ -27,7 +27,7 @@ import torch
 from . import build as _build
 
 PKV_F32, PKV_BF16 = 0, 1
-DEVERR_SLOT, DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT, DEVERR_PAGESIZE, DEVERR_WORKSPACE = 1, 2, 4, 8, 16, 32
+DEVERR_SLOT, DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT, DEVERR_PAGESIZE = 1, 2, 4, 8, 16
 HEAD_DIM = 128
 MAX_GROUP = 8
 MAX_BATCH = 8192
@@ -400,7 +400,7 @@ def decode_workspace(batch, num_q_heads, num_kv_heads, page_size, device=None, m
                                           max_ctas)
         if n == 0:
             raise PkvError(4, "pkv_decode_workspace_size")
-        ws = torch.zeros(n, dtype=torch.uint8, device=device)     # the header must start zeroed
+        ws = torch.empty(n, dtype=torch.uint8, device=device)
         _ws_cache[key] = ws
     return ws
 
@@ -497,4 +497,4 @@ __all__ = ["load", "lib_path", "pkv_kv_append_fp8", "pkv_paged_gqa_decode", "pkv
            "append_decode_fp8", "pkv_kv_calibrate", "pkv_paged_prefill", "paged_prefill", "pkv_prefill_workspace_size",
            "pkv_status_string", "pkv_version", "pkv_read_device_error", "pkv_test_withhold_load", "kv_append_fp8", "paged_gqa_decode", "decode_workspace",
            "PkvError", "PKV_F32", "PKV_BF16", "DEVERR_SLOT", "DEVERR_PAGE", "DEVERR_SEQLEN",
-           "DEVERR_TIMEOUT", "DEVERR_PAGESIZE", "DEVERR_WORKSPACE"]
+           "DEVERR_TIMEOUT", "DEVERR_PAGESIZE"]

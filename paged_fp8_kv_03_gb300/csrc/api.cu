@@ -163,34 +163,15 @@ int decode_num_ctas(int page_size, int batch, int max_ctas)
     return c;
 }
 
-// Largest list of chunk-heads a call with these sizes can have.
-long long decode_list_bound(int batch, int hkv, long long max_len)
-{
-    return static_cast<long long>(batch) * hkv * ((max_len + 15) / 16);
-}
-
 // Workspace for a call whose sequences are at most max_len tokens: header and
-// segment records, then one partial slot per piece a plan can produce: every
-// big unit's sub-pieces (none when the largest list has no big units), every
-// small unit, one per segment.  The plan of the largest possible list bounds
-// every smaller one: sub-pieces grow with the list, and the small units hold
-// a fifth of the list plus at most one worker's share, in units of 8 chunks
-// or more, and number at most 4 per worker unless units reach kChainChunks.
+// segment records, then one partial slot per (worker, sub-piece) plus one per
+// segment.  The sub-pieces per worker follow from the largest possible list.
 size_t decode_workspace_bytes(int batch, int hq, int hkv, long long max_len, int num_ctas)
 {
     const long long workers = static_cast<long long>(num_ctas) * kWarps;
-    const long long total_max = decode_list_bound(batch, hkv, max_len);
-    if (total_max >= (1ll << 31))
-        return 0;
-    const DecodePlan p = decode_plan(static_cast<int>(total_max), static_cast<int>(workers));
-    const long long rem_max = total_max / 5 + workers;
-    long long n_small = 4 * workers;
-    if (rem_max / kChainChunks + 1 > n_small)
-        n_small = rem_max / kChainChunks + 1;
-    if (rem_max / 8 + 1 < n_small)
-        n_small = rem_max / 8 + 1;
-    const long long big_slots = p.big > 0 ? workers * p.subs : 0;
-    const size_t slots = static_cast<size_t>(big_slots + n_small) + static_cast<size_t>(batch) * hkv;
+    const long long total_max = static_cast<long long>(batch) * hkv * ((max_len + 15) / 16);
+    const long long subs = decode_subs(total_max, workers);
+    const size_t slots = static_cast<size_t>(workers * subs) + static_cast<size_t>(batch) * hkv;
     const size_t bytes = slots * static_cast<size_t>(hq / hkv) * kPartialStride * sizeof(float);
     return decode_segment_bytes(batch, hkv) + ((bytes + 255) & ~size_t(255));
 }
@@ -259,7 +240,7 @@ pkv_status decode_impl(const void *k_new, const void *v_new, int in_dtype, int n
         return PKV_ERR_WORKSPACE;
 
     const long long max_len = effective_max_len(max_seq_len, max_pages_per_seq, page_size);
-    if (max_len >= (int64_t(1) << 31) || decode_list_bound(batch, num_kv_heads, max_len) >= (int64_t(1) << 31))
+    if (max_len >= (int64_t(1) << 31))
         return PKV_ERR_UNSUPPORTED;
     const int ctas = decode_num_ctas(page_size, batch, max_ctas);
     if (ctas <= 0)

@@ -153,62 +153,6 @@ __device__ __forceinline__ int worker_of(int64_t x, int64_t total, int workers)
     return static_cast<int>(((x + 1) * workers - 1) / total);
 }
 
-// A unit of the plan: list positions [lo, hi), the slot base of its pieces,
-// and which unit it is (tag = index of a big unit, or -1 - index of a small one).
-struct Unit {
-    int lo, hi, base, tag;
-};
-
-__device__ __forceinline__ Unit big_unit(const DecodePlan &p, int u)
-{
-    Unit r;
-    r.lo = u * p.big;
-    r.hi = r.lo + p.big;
-    r.base = u * p.subs;
-    r.tag = u;
-    return r;
-}
-
-__device__ __forceinline__ Unit small_unit(const DecodePlan &p, int workers, int j)
-{
-    Unit r;
-    r.lo = p.small0 + j * p.small;
-    r.hi = min(p.total, r.lo + p.small);
-    r.base = (p.big > 0 ? workers * p.subs : 0) + j;
-    r.tag = -1 - j;
-    return r;
-}
-
-// The unit holding list position x (x < total).
-__device__ __forceinline__ Unit unit_at(const DecodePlan &p, int workers, int x)
-{
-    if (x < p.small0)
-        return big_unit(p, x / p.big);
-    return small_unit(p, workers, (x - p.small0) / p.small);
-}
-
-// The unit after u in list order.
-__device__ __forceinline__ Unit next_unit(const DecodePlan &p, int workers, const Unit &u)
-{
-    if (u.tag >= 0 && u.tag + 1 < workers)
-        return big_unit(p, u.tag + 1);
-    return small_unit(p, workers, u.tag >= 0 ? 0 : -u.tag);
-}
-
-// End of the piece that starts at list position x inside unit u, for a
-// segment ending at `end`: the segment end, the unit end or the next
-// kChainChunks cut of the unit.
-__device__ __forceinline__ int piece_end(const Unit &u, int x, int end)
-{
-    const int cut = u.lo + ((x - u.lo) / kChainChunks + 1) * kChainChunks;
-    return min(min(end, u.hi), cut);
-}
-
-__device__ __forceinline__ int piece_slot(const Unit &u, int x)
-{
-    return u.base + (x - u.lo) / kChainChunks;
-}
-
 struct Smem {
     static constexpr int kTile = kChunk * kHeadDim;         // bytes of one K (or V) chunk tile
     static constexpr int kStageBytes = 2 * kTile;
@@ -217,9 +161,7 @@ struct Smem {
     static constexpr int kBar = kWarps * kWarpRing;         // full[kWarps][kStages]
     static constexpr int kFlag = kBar + kWarps * kStages * 8;   // abort flag
     static constexpr int kWarpSum = kFlag + 16;             // scan scratch (kWarps ints)
-    static constexpr int kPlan = kWarpSum + 32;             // the work plan (every thread reads it)
-    static constexpr int kWarpState = kPlan + 64;           // per-warp unit bookkeeping (128 bytes each)
-    static constexpr int kPstart = kWarpState + kWarps * 128;
+    static constexpr int kPstart = kWarpSum + 32;
     static size_t bytes(int batch) { return static_cast<size_t>(kPstart) + 4u * (batch + 1) + 1024u; }
 };
 
@@ -575,180 +517,95 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
     const int workers = a.num_ctas * kWarps;
     const int worker = blockIdx.x * kWarps + warp;
-    DecodePlan *splan = reinterpret_cast<DecodePlan *>(smem + S::kPlan);
-    if (tid == 0)
-        *splan = decode_plan(pstart[a.batch] * a.hkv, workers);
-    __syncthreads();
-    const DecodePlan &plan = *splan;
+    const int64_t total = static_cast<int64_t>(pstart[a.batch]) * a.hkv;
+    const int subs = static_cast<int>(decode_subs(total, workers));
 
-    // Segment records for the merge kernel (where each segment lies in the
-    // list, and whether it has more than one piece), and the plan.
+    // Segment records for the merge kernel: where each segment lies in the
+    // list and whether its pieces need merging (it spans several workers, or
+    // a sub-piece cut of its worker falls inside it).
     if (blockIdx.x == 0) {
         for (int sg = tid; sg < a.batch * a.hkv; sg += kThreads) {
             const int b = sg / a.hkv, h = sg % a.hkv, np = chunks_of(pstart, b);
             SegRecord r;
-            const int start = pstart[b] * a.hkv + h * np;
-            r.start = start;
+            r.start = static_cast<long long>(pstart[b]) * a.hkv + static_cast<long long>(h) * np;
             r.n = np;
-            r.merge = 0;
+            r.w0 = -1;
             if (np > 0) {
-                const Unit u = unit_at(plan, workers, start);
-                r.merge = piece_end(u, start, start + np) < start + np ? 1 : 0;
+                const int w0 = worker_of(r.start, total, workers), w1 = worker_of(r.start + np - 1, total, workers);
+                const int64_t lo0 = static_cast<int64_t>(w0) * total / workers;
+                if (w0 != w1 || (r.start - lo0) / kChainChunks != (r.start + np - 1 - lo0) / kChainChunks)
+                    r.w0 = w0;
             }
             a.segs[sg] = r;
         }
-        if (tid == 0)
-            a.header->plan = plan;
+        if (tid == 0) {
+            DecodeHeader hd;
+            hd.total = total;
+            hd.subs = subs;
+            hd.pad = 0;
+            *a.header = hd;
+        }
     }
     // Let the merge kernel get scheduled now; it waits for this grid to finish.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    const int64_t lo = static_cast<int64_t>(worker) * total / workers;
+    const int64_t hi = static_cast<int64_t>(worker + 1) * total / workers;
+    if (lo >= hi)
+        return;                                  // warp-level: no CTA barrier follows
+    const int n_total = static_cast<int>(hi - lo);
+
+    // Fused append: if a page that may receive new tokens is among the first
+    // kStages pages of this worker, store the tokens before any load; otherwise
+    // start the loads first and store while they are in flight (those pages
+    // are issued later, after the stores and their proxy fence).
+    const bool append_early =
+        a.k_new != nullptr && first_tail_chunk(a, pstart, lo, hi) < S::kStages;
+    if (append_early)
+        append_own_tokens(a, pstart, lo, hi, lane);
 
     const uint32_t ring = smem_addr(smem) + warp * S::kWarpRing;
     const uint32_t bars = smem_addr(smem + S::kBar) + warp * kStages * 8;
     const uint64_t policy = l2_policy_evict_first();
-    // TMA coordinates (z = pool page * hkv + head, y = first row in that pool
-    // page) of the chunk `lane` positions after `base`, or (0, 0) past `limit`
-    // lanes; an entry outside the pool sets PKV_DEVERR_PAGE and addresses the
-    // first out-of-pool tile, which reads as zeros.
-    auto batch_tile = [&](Loc base, int limit) -> int2 {
-        if (lane >= limit)
-            return make_int2(0, 0);
-        const Loc l = advance(pstart, a.batch, a.hkv, base, lane);
+    const int zoob = static_cast<int>(a.num_pages * a.hkv);   // first out-of-pool tile: reads zeros
+    // TMA coordinates of a chunk: tile z = pool page * hkv + head, row y = the
+    // chunk's first row within that pool page.
+    auto tile_zy = [&](Loc l) -> int2 {
         int phys, row;
         if (!token_page(a, l.b, page_log2_of(a, l.b), l.ck * kChunk, phys, row)) {
             if (a.err)
                 atomicOr(a.err, PKV_DEVERR_PAGE);
-            return make_int2(static_cast<int>(a.num_pages * a.hkv), 0);
+            return make_int2(zoob, 0);
         }
         return make_int2(phys * a.hkv + l.h, row);
     };
 
-    // ---- the warp's units: its big unit, then small units claimed in order.
-    // The copy side runs up to kStages chunks ahead of the math, so it may
-    // already be in the next unit: ws->rng[] holds the unit the math is in
-    // and the one the copies are in (ws->ahead = 1 when they differ).  This
-    // bookkeeping, touched once per unit, lives in shared memory so the
-    // per-chunk state keeps its registers.
-    struct WarpState {
-        Unit rng[2];                // [cur]: the math's unit, [cur ^ ahead]: the copies' unit
-        int cur, ahead;
-        int icount;                 // chunks of the copies' unit
-        int append_at[2];           // per unit of rng[]: chunk before which its new tokens are stored (-1: none)
-        int have_big, claims_left;
-        Loc nbase;                  // copies: first chunk of the next block-table batch
-    };
-    static_assert(sizeof(WarpState) <= 128, "warp state");
-    WarpState *ws = reinterpret_cast<WarpState *>(smem + S::kWarpState) + warp;
-    if (lane == 0) {
-        ws->cur = 0;
-        ws->ahead = 0;
-        ws->have_big = plan.big > 0;
-        ws->claims_left = 1;
-    }
-    __syncwarp();
-    auto next_range = [&](Unit &u) -> bool {               // warp-uniform
-        if (ws->have_big) {
-            __syncwarp();
-            if (lane == 0)
-                ws->have_big = 0;
-            u = big_unit(plan, worker);
-            return true;
-        }
-        if (!ws->claims_left)
-            return false;
-        int j = 0;
-        if (lane == 0)
-            j = atomicAdd(&a.header->claim, 1);
-        j = __shfl_sync(kFull, j, 0);
-        if (j >= plan.n_small) {
-            if (lane == 0)
-                ws->claims_left = 0;
-            __syncwarp();
-            return false;
-        }
-        u = small_unit(plan, workers, j);
-        return true;
-    };
-
-    // copy side, per chunk: position iq within its unit, the next position
-    // that needs the slow path (unit end or new tokens to store), and the
-    // block-table entries of chunks [32 fb, 32 fb + 32) in zcur, the next 32
-    // in znext
-    int iq = 0, ievent = 0, fb = 0;
-    int2 zcur = make_int2(0, 0), znext = make_int2(0, 0);
+    // ---- block-table batches: zcur holds chunks [32*fb, 32*fb+32), znext the next 32
+    Loc cons = locate(pstart, a.batch, a.hkv, lo);
+    Loc nbase = advance(pstart, a.batch, a.hkv, cons, 32);
+    int2 zcur = lane < n_total ? tile_zy(advance(pstart, a.batch, a.hkv, cons, lane)) : make_int2(0, 0);
+    int2 znext = 32 + lane < n_total ? tile_zy(advance(pstart, a.batch, a.hkv, nbase, lane)) : make_int2(0, 0);
+    int fb = 0;
     // Warp-uniform bookkeeping of the ring: bit s of `pending` is set while
     // stage s has a copy in flight that nobody has waited for yet, bit s of
     // `pend_par` is the parity of that fill.  Used only to drain after an abort.
     uint32_t pending = 0, pend_par = 0;
-    int fi = 0, fc = 0;                        // chunks issued / consumed by this warp (all units)
 
-    auto start_copies = [&](const Unit &u, int slot) {   // warp-uniform; u is rng[slot]
-        const int n = u.hi - u.lo;
-        const Loc l0 = locate(pstart, a.batch, a.hkv, u.lo);
-        const Loc nb = advance(pstart, a.batch, a.hkv, l0, 32);
-        zcur = batch_tile(l0, n);
-        znext = batch_tile(nb, n - 32);
-        int at = -1;
-        if (a.k_new != nullptr) {
-            const int t = first_tail_chunk(a, pstart, u.lo, u.hi);
-            if (t < n)
-                at = t;
-        }
-        __syncwarp();
-        if (lane == 0) {
-            ws->icount = n;
-            ws->append_at[slot] = at;
-            ws->nbase = nb;
-        }
-        __syncwarp();
-        iq = 0;
-        fb = 0;
-        ievent = at >= 0 ? at : n;
-    };
-
-    auto issue_one = [&]() -> bool {           // warp-uniform; false: nothing to issue now
-        if (iq == ievent) {                    // slow path: unit end, or new tokens to store first
-            if (iq == ws->icount) {
-                if (ws->ahead)
-                    return false;              // already one unit ahead of the math
-                Unit u;
-                if (!next_range(u))
-                    return false;
-                const int slot = ws->cur ^ 1;
-                __syncwarp();
-                if (lane == 0) {
-                    ws->rng[slot] = u;
-                    ws->ahead = 1;
-                }
-                __syncwarp();
-                start_copies(u, slot);
-            }
-            // next stop: the first chunk that may hold a new token while the
-            // math has not stored them yet (it does so when it starts the
-            // unit), else the unit's end
-            const int at = ws->append_at[ws->cur ^ ws->ahead];
-            ievent = at >= 0 ? at : ws->icount;
-            if (iq == ievent)
-                return false;
-        }
-        if (iq >= 32 * (fb + 1)) {
+    auto issue = [&](int f) {                    // warp-uniform; chunk f goes to stage f % kStages
+        if (f >= 32 * (fb + 1)) {
             zcur = znext;
             ++fb;
-            const Loc nb = advance(pstart, a.batch, a.hkv, ws->nbase, 32);
-            znext = batch_tile(nb, ws->icount - 32 * (fb + 1));
-            __syncwarp();
-            if (lane == 0)
-                ws->nbase = nb;
-            __syncwarp();
+            nbase = advance(pstart, a.batch, a.hkv, nbase, 32);
+            znext = 32 * (fb + 1) + lane < n_total ? tile_zy(advance(pstart, a.batch, a.hkv, nbase, lane))
+                                                   : make_int2(0, 0);
         }
-        const int z = __shfl_sync(kFull, zcur.x, iq & 31);
-        const int y = __shfl_sync(kFull, zcur.y, iq & 31);
-        // Test hook: the selected worker never loads its first chunk, so its
+        const int z = __shfl_sync(kFull, zcur.x, f & 31);
+        const int y = __shfl_sync(kFull, zcur.y, f & 31);
+        // Test hook: the selected worker never loads its first page, so its
         // first wait must run out (failure-detection test; -1 = off).
-        const bool withheld = worker == a.withhold_worker && fi == 0;
+        const bool withheld = worker == a.withhold_worker && f == 0;
         const int go = __shfl_sync(kFull, (lane == 0 && !*abort_flag && !withheld) ? 1 : 0, 0);
-        const int s = fi % kStages;
         if (go) {
+            const int s = f % kStages;
             if (lane == 0) {
                 const uint32_t dst = ring + s * S::kStageBytes;
                 mbar_arrive_expect_tx(bars + 8 * s, 2 * S::kTile);
@@ -756,82 +613,25 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 tma_load_3d(dst + S::kTile, &tm_v, 0, y, z, bars + 8 * s, policy);
             }
             pending |= 1u << s;
-            pend_par = (pend_par & ~(1u << s)) | ((static_cast<uint32_t>(fi / kStages) & 1u) << s);
-        }
-        ++iq;
-        ++fi;
-        return true;
-    };
-    auto fill = [&]() {                         // keep kStages chunks in flight
-        while (fi < fc + kStages && issue_one()) {
+            pend_par = (pend_par & ~(1u << s)) | ((static_cast<uint32_t>(f / kStages) & 1u) << s);
         }
     };
-
-    // The math stores a unit's new tokens (fused append) when it starts the
-    // unit, outside the chunk loop; the copies of that unit stop short of the
-    // first chunk that may hold one until then (the copies are then in the
-    // same unit: they never run more than one unit ahead).
-    // The math's unit is rng[cur]; if the copies are still in it, they may
-    // now go past its new tokens.
-    auto store_new_tokens = [&]() {
-        const int c = ws->cur;
-        if (ws->append_at[c] < 0)
-            return;
-        const Unit u = ws->rng[c];
-        append_own_tokens(a, pstart, u.lo, u.hi, lane);
-        __syncwarp();
-        if (lane == 0)
-            ws->append_at[c] = -1;
-        __syncwarp();
-        if (!ws->ahead)
-            ievent = ws->icount;
-    };
-
-    {
-        Unit u0;
-        if (!next_range(u0))
-            return;                              // no work for this warp (no CTA barrier follows)
-        __syncwarp();
-        if (lane == 0)
-            ws->rng[0] = u0;
-        __syncwarp();
-        start_copies(u0, 0);
-        fill();                                  // the unit's chunks before its new tokens go out first
-        store_new_tokens();
-    }
-    fill();
+    for (int f = 0; f < kStages && f < n_total; ++f)
+        issue(f);
+    if (a.k_new != nullptr && !append_early)
+        append_own_tokens(a, pstart, lo, hi, lane);
 
     const int gid = lane >> 2, t4 = lane & 3;
     const TileOffsets off = tile_offsets(lane);
-    Unit cu = ws->rng[0];
-    int cpos = cu.lo;
-    Loc cons = locate(pstart, a.batch, a.hkv, cpos);
-    while (true) {
-        if (cpos == cu.hi) {                     // this unit is done: on to the next one
-            if (!ws->ahead) {
-                fill();                          // claims the next unit if the copies have not yet
-                if (!ws->ahead)
-                    break;                       // no unit left
-            }
-            const int nc = ws->cur ^ 1;
-            __syncwarp();
-            if (lane == 0) {
-                ws->cur = nc;
-                ws->ahead = 0;
-            }
-            __syncwarp();
-            cu = ws->rng[nc];
-            cpos = cu.lo;
-            cons = locate(pstart, a.batch, a.hkv, cpos);
-            store_new_tokens();
-            fill();
-            continue;
-        }
+    int st = 0;                                  // stage of page k
+    uint32_t ph = 0;                             // its fill parity
+    int k = 0;
+    while (k < n_total) {
         const int np = chunks_of(pstart, cons.b);
-        // a piece ends at its segment's end, its unit's end, or the unit's
-        // next kChainChunks cut
-        const int n_piece = piece_end(cu, cpos, cpos + (np - cons.ck)) - cpos;
-        const int slot_index = piece_slot(cu, cpos);
+        // a piece ends at its segment's end, the worker's range end, or the
+        // next sub-piece cut (every kChainChunks chunks of the range)
+        const int n_piece = min(min(np - cons.ck, n_total - k), kChainChunks - (k & (kChainChunks - 1)));
+        const int slot_index = worker * subs + k / kChainChunks;
         const int L = seq_len_of(a, cons.b);
         const bool whole = (cons.ck == 0) && (n_piece == np);
         const int seg = cons.b * a.hkv + cons.h;
@@ -861,10 +661,14 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             for (int c = 0; c < 4; ++c)
                 acc[sg][c] = 0.f;
 
-        for (int j = 0; j < n_piece; ++j) {
+        for (int j = 0; j < n_piece; ++j, ++k) {
             const int nv = min(kChunk, L - (cons.ck + j) * kChunk);
-            const int s = fc % kStages;
-            const uint32_t par = static_cast<uint32_t>(fc / kStages) & 1u;
+            const int s = st;
+            const uint32_t par = ph;
+            if (++st == kStages) {
+                st = 0;
+                ph ^= 1u;
+            }
             const bool ready = wait_warp(bars + 8 * s, par, abort_flag, a.err, lane);
             if (ready)
                 pending &= ~(1u << s);
@@ -874,10 +678,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             TileFrags fr;
             if (ready)
                 load_tile(kt, kt + S::kTile, off, fr);
-            ++fc;
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncwarp();
-            fill();
+            if (k + kStages < n_total) {
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                issue(k + kStages);
+            }
             if (ready) {
                 if (nv >= kChunk)
                     process_tile<false>(fr, kChunk, qa, scale2, m_ref, lsum, acc, lane);
@@ -919,7 +724,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 slot[gid * kPartialStride + kHeadDim + 1] = lsum;
             }
         }
-        cpos += n_piece;
         cons = advance(pstart, a.batch, a.hkv, cons, n_piece);
     }
 
@@ -934,51 +738,72 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
 // One CTA per (sequence, kv head) segment, one warp per query head g of its
 // group; lane j owns dimensions 4j .. 4j+3.  The warp merges the partial
-// states of the segment's pieces for head g in list order and writes the
-// output row.  Pieces are taken 16 at a time: lane i of the warp finds the
-// slot of piece i (walking the plan's units from the segment's start) and
-// loads its (m, l); every lane loads its four dimensions of all 16
-// accumulators; then one exact rescale folds the batch into the running
-// (M, L, A).  The order is fixed, so results are deterministic.
+// states the workers covering the segment wrote for head g, in list order,
+// and writes the output row.  Pieces are taken 16 at a time: lane i of the
+// warp finds the slot of piece i and loads its (m, l); every lane loads its
+// four dimensions of all 16 accumulators; then one exact rescale folds the
+// batch into the running (M, L, A).  The order is fixed, so results are
+// deterministic.
 //
-// CTA 0 also checks and resets the workspace's claim counter: every worker
-// claims until the small units run out, so it must read n_small + workers;
-// it is set back to 0 for the next call.
+// Where a segment's pieces are: with one sub-piece per worker range
+// (subs == 1) and at least as many chunk-heads as workers, piece i was
+// written by worker w0 + i; with fewer chunk-heads than workers every worker
+// owns at most one, and piece i comes from the worker owning position start
+// + i; with subs > 1 a worker's range is also cut every kChainChunks chunks
+// and the pieces are walked worker by worker.
 constexpr int kMergeBatch = 16;
 
 __global__ void __launch_bounds__(32 * PKV_MAX_GROUP) splitk_merge_kernel(const DecodeArgs a)
 {
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid has finished
     const int seg = blockIdx.x, g = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int workers = a.num_ctas * kWarps;
-    const DecodePlan plan = a.header->plan;
-    if (seg == 0 && threadIdx.x == 0) {
-        const int claimed = a.header->claim;
-        if (claimed != plan.n_small + workers && a.err)
-            atomicOr(a.err, PKV_DEVERR_WORKSPACE);
-        a.header->claim = 0;
-    }
     const SegRecord r = a.segs[seg];
-    if (!r.merge)
+    const DecodeHeader hd = *a.header;
+    if (r.w0 < 0)
         return;
+    const int64_t total = hd.total;
+    const int subs = hd.subs;
+    const int workers = a.num_ctas * kWarps;
     const int b = seg / a.hkv, h = seg % a.hkv;
-    const int end = static_cast<int>(r.start) + r.n;
-    int x = static_cast<int>(r.start);           // start of the next piece to find
-    Unit u = unit_at(plan, workers, x);
+    const bool walk = subs > 1;
+    const bool dense = total >= workers;
+    // pieces known up front (subs == 1); the walk counts them as it goes
+    const int n_known = dense ? worker_of(r.start + r.n - 1, total, workers) - r.w0 + 1 : r.n;
+    // walk state (subs > 1): worker w, its range [lo_w, hi_w), offset k of the next piece in it
+    const int64_t end = r.start + r.n;
+    int w = r.w0;
+    int64_t lo_w = static_cast<int64_t>(w) * total / workers;
+    int64_t hi_w = static_cast<int64_t>(w + 1) * total / workers;
+    int64_t k = r.start - lo_w;
 
     float M = -INFINITY, L = 0.f;
     float A[4] = {0.f, 0.f, 0.f, 0.f};
-    while (x < end) {
-        // slot of piece i0 + lane (lanes >= the batch size: -1); every lane walks the same pieces
+    for (int i0 = 0;; i0 += kMergeBatch) {
+        // slot of piece i0 + lane (lanes >= the batch size: -1)
         int my_slot = -1;
-        int nb = 0;
-        while (nb < kMergeBatch && x < end) {
-            if (lane == nb)
-                my_slot = piece_slot(u, x);
-            ++nb;
-            x = piece_end(u, x, end);
-            if (x < end && x >= u.hi)
-                u = next_unit(plan, workers, u);
+        int nb;
+        if (!walk) {
+            nb = min(kMergeBatch, n_known - i0);
+            if (nb <= 0)
+                break;
+            if (lane < nb)
+                my_slot = dense ? r.w0 + i0 + lane : worker_of(r.start + i0 + lane, total, workers);
+        } else {
+            nb = 0;
+            while (nb < kMergeBatch && lo_w + k < end) {
+                if (lane == nb)
+                    my_slot = w * subs + static_cast<int>(k / kChainChunks);
+                ++nb;
+                k = (k / kChainChunks + 1) * kChainChunks;          // next sub-piece of this worker
+                if (lo_w + k >= hi_w) {                              // next worker: starts at its range start
+                    ++w;
+                    lo_w = hi_w;
+                    hi_w = static_cast<int64_t>(w + 1) * total / workers;
+                    k = 0;
+                }
+            }
+            if (nb == 0)
+                break;
         }
         float m = -INFINITY, l = 0.f;
         if (my_slot >= 0) {

@@ -43,55 +43,17 @@ struct AppendArgs {
 // rounds toward zero, so error would otherwise grow with the chain).
 constexpr int kChainChunks = 512;
 
-// Decode work plan.  The (sequence, kv head) segments are laid end to end as
-// one list of chunk-heads (16 tokens of one kv head); the list is cut into
-// fixed units, the same in every CTA and in the merge kernel: every worker
-// warp owns one "big" unit (4/5 of the list in all, `big` chunks each), and
-// the rest is cut into "small" units of `small` chunks that the workers claim
-// in order from a counter once their big unit is done, so warps on faster SMs
-// take more of them.  A piece (the part of a segment inside one unit, cut
-// again every kChainChunks chunks of the unit) accumulates into one partial
-// state; slot of a piece = unit base + (offset in unit) / kChainChunks +
-// segment index, with unit base = u * subs for big unit u and (big > 0 ?
-// workers * subs : 0) + j for small unit j.  The units and pieces do not depend on which warp
-// processes them, so results are deterministic.
-struct DecodePlan {
-    int total;                      // chunk-heads in the list (the host bounds it below 2^31)
-    int big;                        // chunks of a big unit (0: no big units)
-    int small0;                     // list position where the small units start (= workers * big)
-    int small;                      // chunks of a small unit (8 .. kChainChunks)
-    int n_small;                    // small units
-    int subs;                       // pieces of a big unit at most: ceil(big / kChainChunks), >= 1
-};
-
-inline __host__ __device__ DecodePlan decode_plan(int total, int workers)
-{
-    DecodePlan p;
-    p.total = total;
-    p.big = static_cast<int>((static_cast<long long>(total) * 4) / (5ll * workers));
-    p.small0 = p.big * workers;
-    const int rem = total - p.small0;
-    int s = static_cast<int>((static_cast<long long>(rem) + 4ll * workers - 1) / (4ll * workers));
-    s = s < 8 ? 8 : (s > kChainChunks ? kChainChunks : s);
-    p.small = s;
-    p.n_small = (rem + s - 1) / s;
-    const int subs = (p.big + kChainChunks - 1) / kChainChunks;
-    p.subs = subs < 1 ? 1 : subs;
-    return p;
-}
-
-// Decode workspace: a 64-byte header, one record per (sequence, kv head)
-// segment, then the partial-state slots.
+// Decode workspace: a header, one record per (sequence, kv head) segment,
+// then the partial-state slots.
 struct DecodeHeader {
-    DecodePlan plan;                // written by CTA 0 of the decode kernel
-    int claim;                      // next small unit: 0 before a call, reset by the merge kernel
-    int pad[9];
+    long long total;                // chunk-heads in the list (all segments)
+    int subs;                       // sub-pieces per worker range: ceil(ceil(total / workers) / kChainChunks)
+    int pad;
 };
-static_assert(sizeof(DecodeHeader) == 64, "decode workspace header");
 struct SegRecord {
     long long start;                // list position of the segment's first chunk-head
     int n;                          // its chunks (0: empty sequence)
-    int merge;                      // 1: more than one piece (merged by the merge kernel), 0: written directly
+    int w0;                         // worker of its first chunk; -1: one piece, nothing to merge
 };
 
 struct DecodeArgs {
@@ -115,9 +77,9 @@ struct DecodeArgs {
     int new_bf16;
     int n_new;
     uint8_t *k_pool, *v_pool;       // the pools the tensor maps describe (for the stores)
-    DecodeHeader *header;           // workspace header (plan written by CTA 0; claim counter)
+    DecodeHeader *header;           // workspace header (written by CTA 0)
     SegRecord *segs;                // [batch * hkv] segment records (written by CTA 0)
-    float *partials;                // [workers * subs + n_small + batch * hkv][group][kPartialStride]
+    float *partials;                // [num_ctas * kWarps * subs + batch * hkv][group][kPartialStride]
     int32_t *err;
     int num_ctas;
     int withhold_worker;            // failure-detection test hook (-1 = off)
@@ -188,6 +150,15 @@ inline size_t decode_segment_bytes(int batch, int hkv)
     return (sizeof(DecodeHeader) + static_cast<size_t>(batch) * hkv * sizeof(SegRecord) + 255) & ~size_t(255);
 }
 
+// Sub-pieces per worker range for a list of `total` chunk-heads over
+// `workers` workers (at least 1).
+inline __host__ __device__ long long decode_subs(long long total, long long workers)
+{
+    const long long per = (total + workers - 1) / workers;
+    const long long s = (per + kChainChunks - 1) / kChainChunks;
+    return s < 1 ? 1 : s;
+}
+
 // ---------------------------------------------------------------- page walk
 // Shared by decode and prefill (Args: DecodeArgs or PrefillArgs).  Sequence
 // b's pages hold P_b tokens: a run of P_b / page_size consecutive pool pages
@@ -232,7 +203,6 @@ size_t decode_smem_bytes(int page_size, int batch);
 const void *decode_kernel_for(int page_size);
 int decode_num_ctas(int page_size, int batch, int max_ctas);
 size_t decode_workspace_bytes(int batch, int hq, int hkv, long long max_len, int num_ctas);
-long long decode_list_bound(int batch, int hkv, long long max_len);
 size_t prefill_smem_bytes();
 cudaError_t launch_paged_prefill(const PrefillArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k16,
                                  const CUtensorMap &tm_v16, cudaStream_t stream);

@@ -20,9 +20,7 @@ def _poisoned_workspace(pkv, f, max_ctas):
     """A workspace full of NaN bytes: reading a slot nobody wrote shows up."""
     wl = f.wl
     n = pkv.pkv_decode_workspace_size(wl.batch, wl.hq, wl.hkv, 128, f.max_len, wl.page_size, max_ctas)
-    ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=f.q.device)
-    ws[:256] = 0                                               # the header starts zeroed (API contract)
-    return ws
+    return torch.full((n,), 0xFF, dtype=torch.uint8, device=f.q.device)
 
 
 def _decode(pkv, f, out_dtype=torch.float32, max_ctas=0, err=None, bt=None, lens=None, kc=None, vc=None,
@@ -247,7 +245,7 @@ def test_per_sequence_page_sizes(pkv, cuda_device, lens, sizes, hq, hkv, page):
         for t in range(0, L, page):
             wide[b, t // page] = bt[b, t // sizes[b]] + (t % sizes[b]) // page
     n = pkv.pkv_decode_workspace_size(wl.batch, hq, hkv, 128, f.max_len, page)
-    ws = torch.zeros(n, dtype=torch.uint8, device=cuda_device)
+    ws = torch.empty(n, dtype=torch.uint8, device=cuda_device)
     plain = pkv.paged_gqa_decode(f.q, f.kc, f.vc, f.ks, f.vs, torch.from_numpy(wide).to(cuda_device), f.lens,
                                  out_dtype=torch.float32, workspace=ws, max_seq_len=f.max_len)
     torch.cuda.synchronize()
@@ -310,28 +308,3 @@ def test_closed_forms_uniform_and_one_hot_weights(pkv, cuda_device):
     got = out.double().cpu().numpy()
     assert np.abs(got[:, :, :L] - w).max() <= 2e-6
     assert np.all(got[:, :, L:] == 0)
-
-
-def test_workspace_header_contract(pkv, cuda_device):
-    """The split-K workers take small units of work from a counter in the
-    workspace header: a header that does not start zeroed is reported
-    (outputs undefined), and the call leaves it ready, so the next call is
-    exact; calls in a row on one workspace keep working."""
-    wl = workloads.Workload(58, "header", [3000, 40, 5000, 700], 0, 16, 4, 16, seed=9)
-    f = fill_gpu(wl, 0, cuda_device)
-    ref = _full_oracle(wl, f)
-    n = pkv.pkv_decode_workspace_size(wl.batch, wl.hq, wl.hkv, 128, f.max_len, wl.page_size)
-    ws = torch.zeros(n, dtype=torch.uint8, device=cuda_device)
-    ws[:64] = 1                                                        # a header that was not zeroed
-    err = torch.zeros(1, dtype=torch.int32, device=cuda_device)
-    pkv.paged_gqa_decode(f.q, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, out_dtype=torch.float32, workspace=ws,
-                         device_error=err, max_seq_len=f.max_len)
-    torch.cuda.synchronize()
-    assert int(err.item()) & pkv.DEVERR_WORKSPACE
-    for _ in range(3):
-        err.zero_()
-        out = pkv.paged_gqa_decode(f.q, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, out_dtype=torch.float32,
-                                   workspace=ws, device_error=err, max_seq_len=f.max_len)
-        torch.cuda.synchronize()
-        assert int(err.item()) == 0
-        assert_close(out.double().cpu().numpy(), ref, "after the header was reset")

@@ -15,9 +15,7 @@ pytestmark = pytest.mark.gpu
 
 def _ws(pkv, wl, dev, max_ctas=0):
     n = pkv.pkv_decode_workspace_size(wl.batch, wl.hq, wl.hkv, 128, wl.max_len, wl.page_size, max_ctas)
-    ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=dev)
-    ws[:256] = 0                                               # the header starts zeroed (API contract)
-    return ws
+    return torch.full((n,), 0xFF, dtype=torch.uint8, device=dev)
 
 
 def _separate(pkv, wl, dev, dtype, max_ctas=0):

@@ -18,7 +18,6 @@ def _ref(pkv, f, out_dtype):
     wl = f.wl
     n = pkv.pkv_decode_workspace_size(wl.batch, wl.hq, wl.hkv, 128, wl.max_pages * wl.page_size, wl.page_size)
     ws = torch.full((n,), 0xFF, dtype=torch.uint8, device=f.q.device)
-    ws[:256] = 0                                               # the header starts zeroed (API contract)
     out = torch.empty(f.q.shape, dtype=out_dtype, device=f.q.device)
     pkv.pkv_paged_gqa_decode(f.q, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, out, ws)
     return out
