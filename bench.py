@@ -314,7 +314,9 @@ def run_gpu(args, rank, world):
     # Host cost of one call alone: enqueue a few layer passes behind a GPU
     # spin long enough that the launch queue never fills, so the time is the
     # binding's and the library's host work, not back-pressure from the GPU.
-    n_host = min(per_step, 16)
+    # Always 16 calls (cycling over the layers), so every workload averages
+    # over the same count.
+    n_host = 16
     torch.cuda._sleep(int(2e8))
     hh0 = time.perf_counter()
     for l in range(n_host):
