@@ -240,6 +240,18 @@ def run_gpu(args, rank, world):
     ws = pkv.decode_workspace(wl.batch, wl.hq, wl.hkv, wl.page_size, dev, max_seq_len=max_len)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    # Split weights: measured once per device on layer 0 of this workload
+    # (setup, untimed; the library's calibration call), or the even split.
+    split = "even"
+    if not args.no_calibrate:
+        c0, s0 = layers[0], steps_in[0]
+        weights = pkv.pkv_decode_calibrate_split(s0["q"], c0["kc"], c0["vc"], c0["ks"], c0["vs"], bt, lens, out, ws,
+                                                 rounds=args.calibrate_rounds, max_seq_len=max_len,
+                                                 seq_page_sizes=psz)
+        split = (f"calibrated per-CTA weights ({args.calibrate_rounds} rounds, {len(weights)} CTAs, "
+                 f"weights {min(weights)}..{max(weights)})")
+    else:
+        pkv.pkv_decode_set_split_weights(None)
 
     per_step = wl.layers      # layer passes per decode step (80 for the mixed serving batch)
 
@@ -416,7 +428,7 @@ def run_gpu(args, rank, world):
                    "layer_caches_resident": n_layers,
                    "l2": "inputs larger than L2: each layer cache exceeds the 129 MB L2 and "
                          f"{n_layers} distinct caches rotate layer pass by layer pass",
-                   "parallelism": f"replicas x{world}"},
+                   "parallelism": f"replicas x{world}", "split": split},
         "path": ("kv_append_fp8 + paged_gqa_decode (two calls)" if (wl.append and args.separate) else
                  "append_decode_fp8 (append fused into the decode launch)" if wl.append else "paged_gqa_decode")
                 + (", CUDA-graph replay" if args.graph else ""),
@@ -863,6 +875,9 @@ def main():
     ap.add_argument("--ref-seconds", type=float, default=90.0,
                     help="oracle time budget of the whole --impl reference run")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-calibrate", action="store_true",
+                    help="decode: keep the even split (no per-CTA split weights)")
+    ap.add_argument("--calibrate-rounds", type=int, default=4)
     ap.add_argument("--graph", action="store_true", help="replay each step from a captured CUDA graph")
     ap.add_argument("--separate", action="store_true",
                     help="time kv_append_fp8 and paged_gqa_decode as two calls instead of the fused step")

@@ -30,9 +30,11 @@
  * Ownership: the caller owns every buffer (caches, tables, outputs, the
  * decode workspace).  The library allocates no device memory, keeps no state
  * between calls beyond a per-device cache of device properties, the driver
- * entry point it uses to describe tensors for the TMA unit, and never
+ * entry point it uses to describe tensors for the TMA unit and the optional
+ * per-device split weights (pkv_decode_set_split_weights), and never
  * synchronises the stream.  Calls are asynchronous on `stream`; the status
- * reports argument errors found on the host and launch errors only.
+ * reports argument errors found on the host and launch errors only
+ * (pkv_last_cuda_error names the CUDA error behind a PKV_ERR_CUDA).
  *
  * Device-side error word: kernels OR bits into *device_error (int32, device
  * memory, may be NULL) instead of reading or writing out of bounds:
@@ -47,6 +49,9 @@
  *   PKV_DEVERR_PAGESIZE  a per-sequence page size that is not a power of two
  *                        in [page_size, 256] (the sequence is treated as
  *                        empty: zero output rows)
+ *   PKV_DEVERR_INTERNAL  the decode's own split-K bookkeeping pointed outside
+ *                        the workspace (the access was skipped; outputs are
+ *                        not valid; not expected to happen)
  * The word is sticky: clear it (pkv_read_device_error with clear = 1, or
  * cudaMemsetAsync) before a call whose errors you want to attribute.
  */
@@ -84,7 +89,8 @@ enum {
     PKV_DEVERR_PAGE = 2,
     PKV_DEVERR_SEQLEN = 4,
     PKV_DEVERR_TIMEOUT = 8,
-    PKV_DEVERR_PAGESIZE = 16
+    PKV_DEVERR_PAGESIZE = 16,
+    PKV_DEVERR_INTERNAL = 32
 };
 
 /* Build limits. */
@@ -150,10 +156,11 @@ pkv_status pkv_kv_calibrate(const void *k_new, const void *v_new, int in_dtype,
  * call with these sizes whose seq_lens are all <= max_seq_len (partial
  * softmax states of the split-K pass: one slot per split-K worker and
  * sub-piece of its range, plus one per (sequence, kv head)).  Returns 0 for
- * sizes the library rejects.  max_ctas as in pkv_paged_gqa_decode.  Grows
- * with batch * max_seq_len only once the list is longer than 512 chunks of
- * 16 tokens per worker (for example about 38 MB at batch 64, 8 kv heads,
- * G = 8 and 128K tokens on a 152-SM GPU).
+ * sizes the library rejects.  max_ctas as in pkv_paged_gqa_decode.  Covers
+ * every split the weights of pkv_decode_set_split_weights can give.  Grows
+ * with batch * max_seq_len only once the list is longer than about 300
+ * chunks of 16 tokens per worker (for example about 61 MB at batch 64, 8 kv
+ * heads, G = 8 and 128K tokens on a 152-SM GPU).
  */
 size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
                                  int head_dim, int max_seq_len, int page_size, int max_ctas);
@@ -255,6 +262,64 @@ pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dt
                                  void *out, int out_dtype,
                                  void *workspace, size_t workspace_bytes,
                                  int32_t *device_error, int max_ctas, cudaStream_t stream);
+
+/*
+ * Split weights -- how the decode call shares the cache among its workers.
+ * Decode is bound by the rate at which the whole cache streams in ([N] §3.2),
+ * so the call ends when its slowest worker does.  The workers are the warps
+ * of a persistent grid; by default every warp takes an equal share of the
+ * list of 16-token chunks.  The SMs of one GPU do not all stream equally
+ * fast, and the grid's CTAs land on the same SMs call after call, so equal
+ * shares leave the fast SMs idle while the slow ones finish.  With weights,
+ * CTA c's four warps take shares proportional to weights[c]: with
+ * C(w) = 4 * (weights[0] + ... + weights[c-1]) + j * weights[c] for warp j
+ * of CTA c, worker w covers list positions [T * C(w) / CT, T * C(w + 1) / CT)
+ * of the T chunks, CT = C(4n).  Equal weights give exactly the default split.
+ * The math is unchanged; the pieces the split cuts (and so the last bits of
+ * the result, within the accuracy bound) depend on the weights, and stay
+ * deterministic for fixed weights.
+ *
+ * pkv_decode_set_split_weights installs n weights, each an integer in
+ * [96, 160], for the current device; they apply to decode calls
+ * (pkv_paged_gqa_decode, pkv_append_decode_fp8 and the allocation-free entry
+ * point) whose grid has exactly n CTAs, and the others split evenly.  n == 0
+ * removes them.  Copies n + 1 integers to device memory the decode kernels
+ * read, synchronously: do not call it while a decode call is in flight on
+ * the device, or during stream capture.  Errors: PKV_ERR_SHAPE (n outside
+ * [0, 1024] or a weight outside [96, 160]), PKV_ERR_NULL, PKV_ERR_CUDA.
+ *
+ * pkv_decode_get_split_weights copies the current device's weights to
+ * weights[0 .. *n) (*n = 0: none; PKV_ERR_SHAPE if *n > capacity).
+ *
+ * pkv_decode_calibrate_split measures them: it runs `rounds` (1..64) times
+ * three decode calls with the given arguments (as pkv_paged_gqa_decode; out
+ * and workspace are written, max_ctas sets the grid), each timed per CTA
+ * with the global timer, synchronising `stream` after each, and moves every
+ * CTA's weight towards the share it streams in the time all CTAs take
+ * together.  Starts from equal weights, leaves the result installed (and
+ * copies it to weights_out[0 .. n), if weights_out is given, with n in
+ * *n_out).  On an error the device's weights are removed.  A setup-time
+ * call: a few ms of GPU time plus host synchronisation; not capturable.
+ */
+pkv_status pkv_decode_set_split_weights(const uint8_t *weights, int n);
+/*
+ * The CUDA runtime error (cudaError_t value) behind the calling thread's last
+ * PKV_ERR_CUDA status, 0 if none, and its name in *name (if name is given).
+ */
+int pkv_last_cuda_error(const char **name);
+pkv_status pkv_decode_get_split_weights(uint8_t *weights, int capacity, int *n);
+pkv_status pkv_decode_calibrate_split(const void *q,
+                                      const uint8_t *k_cache, const uint8_t *v_cache,
+                                      const float *k_scale, const float *v_scale,
+                                      const int32_t *block_table, int max_pages_per_seq,
+                                      const int32_t *seq_lens, int max_seq_len,
+                                      const int32_t *seq_page_sizes,
+                                      int batch, int num_q_heads, int num_kv_heads, int head_dim,
+                                      int page_size, int64_t num_pages, float sm_scale,
+                                      void *out, int out_dtype,
+                                      void *workspace, size_t workspace_bytes, int max_ctas,
+                                      int rounds, uint8_t *weights_out, int capacity, int *n_out,
+                                      cudaStream_t stream);
 
 /*
  * paged_gqa_decode without a caller workspace, for callers that cannot

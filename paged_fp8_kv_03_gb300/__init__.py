@@ -8,6 +8,8 @@ stream.  The entry points mirror the C ABI in ``include/pagedfp8.h``:
 * ``pkv_paged_gqa_decode``    -- grouped-query decode attention over the pages
 * ``pkv_append_decode_fp8``    -- both in one launch (one whole decode step)
 * ``pkv_kv_calibrate``         -- running |K|, |V| maxima per kv head and the scales
+* ``pkv_decode_calibrate_split``, ``pkv_decode_set_split_weights``,
+  ``pkv_decode_get_split_weights`` -- per-CTA weights of the decode split
 * ``pkv_decode_workspace_size``, ``pkv_status_string``, ``pkv_version``
 
 ``kv_append_fp8`` / ``paged_gqa_decode`` are the same calls with the output
@@ -27,7 +29,7 @@ import torch
 from . import build as _build
 
 PKV_F32, PKV_BF16 = 0, 1
-DEVERR_SLOT, DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT, DEVERR_PAGESIZE = 1, 2, 4, 8, 16
+DEVERR_SLOT, DEVERR_PAGE, DEVERR_SEQLEN, DEVERR_TIMEOUT, DEVERR_PAGESIZE, DEVERR_INTERNAL = 1, 2, 4, 8, 16, 32
 HEAD_DIM = 128
 MAX_GROUP = 8
 MAX_BATCH = 8192
@@ -38,7 +40,11 @@ _lock = threading.Lock()
 
 class PkvError(RuntimeError):
     def __init__(self, status: int, what: str):
-        super().__init__(f"{what}: status {status} ({pkv_status_string(status)})")
+        msg = f"{what}: status {status} ({pkv_status_string(status)})"
+        if status == 6:
+            code, name = pkv_last_cuda_error()
+            msg += f" [{name} ({code})]"
+        super().__init__(msg)
         self.status = status
 
 
@@ -82,6 +88,16 @@ def load() -> ctypes.CDLL:
                                           i32, i32, i64, ctypes.c_float, vp, i32, vp, sz, vp, vp]
         lib.pkv_read_device_error.restype = i32
         lib.pkv_read_device_error.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int32), vp]
+        lib.pkv_decode_set_split_weights.restype = i32
+        lib.pkv_decode_set_split_weights.argtypes = [vp, i32]
+        lib.pkv_decode_get_split_weights.restype = i32
+        lib.pkv_decode_get_split_weights.argtypes = [vp, i32, ctypes.POINTER(ctypes.c_int)]
+        lib.pkv_decode_calibrate_split.restype = i32
+        lib.pkv_decode_calibrate_split.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, i32, i32, i32,
+                                                   i64, f32, vp, i32, vp, sz, i32, i32, vp, i32,
+                                                   ctypes.POINTER(ctypes.c_int), vp]
+        lib.pkv_last_cuda_error.restype = i32
+        lib.pkv_last_cuda_error.argtypes = [ctypes.POINTER(ctypes.c_char_p)]
         lib.pkv_test_withhold_load.restype = None
         lib.pkv_test_withhold_load.argtypes = [i32]
         lib.pkv_status_string.restype = ctypes.c_char_p
@@ -104,11 +120,84 @@ def pkv_read_device_error(device_error, clear: bool = False, stream=None) -> int
     return int(code.value)
 
 
+def pkv_decode_set_split_weights(weights, device=None) -> None:
+    """Install per-CTA split weights (ints in [96, 160]) for decode calls on
+    `device` (default: the current one) whose grid has len(weights) CTAs;
+    None or an empty sequence removes them (even split)."""
+    w = bytes(int(x) for x in (weights if weights is not None else []))
+    if any(x > 255 for x in (weights if weights is not None else [])):
+        raise PkvError(1, "pkv_decode_set_split_weights")
+    buf = (ctypes.c_uint8 * max(1, len(w))).from_buffer_copy(w if w else b"\0")
+    with _device_of_index(device):
+        st = load().pkv_decode_set_split_weights(ctypes.addressof(buf), len(w))
+    if st != 0:
+        raise PkvError(st, "pkv_decode_set_split_weights")
+
+
+def pkv_decode_get_split_weights(device=None) -> list:
+    """The split weights installed for `device` (empty: even split)."""
+    cap = 1024
+    buf = (ctypes.c_uint8 * cap)()
+    n = ctypes.c_int(0)
+    with _device_of_index(device):
+        st = load().pkv_decode_get_split_weights(ctypes.addressof(buf), cap, ctypes.byref(n))
+    if st != 0:
+        raise PkvError(st, "pkv_decode_get_split_weights")
+    return list(buf[:n.value])
+
+
+def pkv_decode_calibrate_split(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace,
+                               sm_scale=None, max_ctas=0, rounds=4, stream=None, max_seq_len=0,
+                               seq_page_sizes=None) -> list:
+    """Measure and install split weights for decode calls shaped like this
+    one (runs 3 * rounds decode calls on these inputs, writing out and
+    workspace, and synchronises the stream).  Returns the weights."""
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k_cache, "k_cache", torch.uint8, 4)
+    _need(v_cache, "v_cache", torch.uint8, 4)
+    _need(k_scale, "k_scale", torch.float32, 1)
+    _need(v_scale, "v_scale", torch.float32, 1)
+    _need(block_table, "block_table", torch.int32, 2)
+    _need(seq_lens, "seq_lens", torch.int32, 1)
+    _need(out, "out", dim=3)
+    _need(workspace, "workspace", torch.uint8)
+    B, Hq, D = q.shape
+    NP, Hkv, P, D2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or D2 != D or out.shape != q.shape:
+        raise ValueError("q / cache / out shapes disagree")
+    if block_table.shape[0] != B or seq_lens.shape[0] != B:
+        raise ValueError("block_table / seq_lens shapes disagree with q")
+    _check_page_sizes(seq_page_sizes, B)
+    _same_device(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace, seq_page_sizes)
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(D)
+    cap = 1024
+    buf = (ctypes.c_uint8 * cap)()
+    n = ctypes.c_int(0)
+    with _device_of(q):
+        st = load().pkv_decode_calibrate_split(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),
+                                               _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                               int(max_seq_len), _ptr(seq_page_sizes), B, Hq, Hkv, D, P, NP,
+                                               float(sm_scale), _ptr(out), _act_code(out), _ptr(workspace),
+                                               workspace.numel(), int(max_ctas), int(rounds),
+                                               ctypes.addressof(buf), cap, ctypes.byref(n), _stream(stream))
+    if st != 0:
+        raise PkvError(st, "pkv_decode_calibrate_split")
+    return list(buf[:n.value])
+
+
 def pkv_test_withhold_load(index: int) -> None:
     """Test facility (failure-detection tests only): decode worker warp /
     prefill CTA `index` skips its first load so its bounded wait runs out;
     a negative index turns it off."""
     load().pkv_test_withhold_load(int(index))
+
+
+def pkv_last_cuda_error():
+    """(code, name) of the CUDA error behind this thread's last PKV_ERR_CUDA."""
+    name = ctypes.c_char_p()
+    code = load().pkv_last_cuda_error(ctypes.byref(name))
+    return int(code), (name.value or b"").decode()
 
 
 def pkv_status_string(status: int) -> str:
@@ -137,6 +226,12 @@ def _device_of(t):
     if t.device.index == torch.cuda.current_device():
         return contextlib.nullcontext()
     return torch.cuda.device(t.device)
+
+
+def _device_of_index(device):
+    if device is None:
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
 
 
 def _same_device(ref, *ts):
@@ -495,6 +590,8 @@ def paged_prefill(q, cu_q, k_cache, v_cache, k_scale, v_scale, block_table, seq_
 __all__ = ["load", "lib_path", "pkv_kv_append_fp8", "pkv_paged_gqa_decode", "pkv_decode_workspace_size",
            "pkv_paged_gqa_decode_noalloc", "pkv_decode_noalloc_scratch_bytes", "pkv_append_decode_fp8",
            "append_decode_fp8", "pkv_kv_calibrate", "pkv_paged_prefill", "paged_prefill", "pkv_prefill_workspace_size",
-           "pkv_status_string", "pkv_version", "pkv_read_device_error", "pkv_test_withhold_load", "kv_append_fp8", "paged_gqa_decode", "decode_workspace",
+           "pkv_status_string", "pkv_version", "pkv_read_device_error", "pkv_test_withhold_load", "kv_append_fp8",
+           "paged_gqa_decode", "decode_workspace", "pkv_decode_set_split_weights", "pkv_decode_get_split_weights",
+           "pkv_decode_calibrate_split",
            "PkvError", "PKV_F32", "PKV_BF16", "DEVERR_SLOT", "DEVERR_PAGE", "DEVERR_SEQLEN",
-           "DEVERR_TIMEOUT", "DEVERR_PAGESIZE"]
+           "DEVERR_TIMEOUT", "DEVERR_PAGESIZE", "DEVERR_INTERNAL", "pkv_last_cuda_error"]

@@ -1,11 +1,13 @@
 // C entry points: argument checks on the host, TMA tensor descriptions of the
 // page pools, grid sizing and launches.  Nothing here allocates device memory.
 #include <math.h>
+#include <stdio.h>
 
 #include <atomic>
 #include <map>
 #include <mutex>
 #include <tuple>
+#include <vector>
 
 #include "internal.h"
 
@@ -15,9 +17,32 @@ namespace {
 
 std::mutex g_mu;
 std::map<int, int> g_sm_count;                              // device -> SMs
-std::map<std::tuple<int, int, size_t>, int> g_occupancy;     // (device, P, smem) -> CTAs per SM
-std::map<std::tuple<int, int>, size_t> g_smem_attr;          // (device, P) -> max dynamic smem set
+std::map<std::tuple<int, const void *, size_t>, int> g_occupancy;   // (device, kernel, smem) -> CTAs per SM
+// (device, kernel) -> the kernel's dynamic shared memory limit set so far
+// (only ever raised: every page size runs the same kernel, so a limit per
+// page size would let one page size's smaller setting undercut another's
+// launch).
+std::map<std::tuple<int, const void *>, size_t> g_smem_attr;
 std::atomic<int> g_withhold{-1};                            // failure-detection test facility (-1 = off)
+
+// Weighted split of each device: the per-CTA weights for one grid size (the
+// prefix sums live in the decode module's device table).  Absent: even split.
+struct SplitState {
+    std::vector<uint8_t> weights;
+    long long ct = 0;                                       // 4 * sum of the weights
+    int wmin = 0, wmax = 0;
+};
+std::map<int, SplitState> g_split;                          // device -> weights
+thread_local int t_last_cuda = 0;                           // error behind this thread's last PKV_ERR_CUDA
+thread_local const char *t_last_site = "";                  // the call that failed
+thread_local char t_last_text[160];
+
+pkv_status cuda_failed(cudaError_t e, const char *site = "")
+{
+    t_last_cuda = e == cudaSuccess ? static_cast<int>(cudaErrorUnknown) : static_cast<int>(e);
+    t_last_site = site;
+    return PKV_ERR_CUDA;
+}
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *,
@@ -130,33 +155,43 @@ int decode_num_ctas(int page_size, int batch, int max_ctas)
 {
     const int dev = current_device();
     const int sms = device_sm_count();
-    if (dev < 0 || sms <= 0)
+    if (dev < 0 || sms <= 0) {
+        cuda_failed(cudaGetLastError(), "device query");
         return 0;
+    }
     const size_t smem = decode_smem_bytes(page_size, batch);
     const void *kern = decode_kernel_for(page_size);
     int per_sm = 0;
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        auto key_attr = std::make_tuple(dev, page_size);
+        auto key_attr = std::make_tuple(dev, kern);
         auto ia = g_smem_attr.find(key_attr);
         if (ia == g_smem_attr.end() || ia->second < smem) {
-            if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-                cudaSuccess)
+            const cudaError_t e =
+                cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+            if (e != cudaSuccess) {
+                cuda_failed(e, "cudaFuncSetAttribute (decode shared memory)");
                 return 0;
+            }
             g_smem_attr[key_attr] = smem;
         }
-        auto key = std::make_tuple(dev, page_size, smem);
+        auto key = std::make_tuple(dev, kern, smem);
         auto it = g_occupancy.find(key);
         if (it != g_occupancy.end()) {
             per_sm = it->second;
         } else {
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem) != cudaSuccess)
+            const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+            if (e != cudaSuccess) {
+                cuda_failed(e, "cudaOccupancyMaxActiveBlocksPerMultiprocessor (decode)");
                 return 0;
+            }
             g_occupancy[key] = per_sm;
         }
     }
-    if (per_sm <= 0)
+    if (per_sm <= 0) {
+        cuda_failed(cudaErrorInvalidConfiguration, "decode occupancy is 0 CTAs per SM");
         return 0;
+    }
     int c = per_sm * sms;
     if (max_ctas > 0 && max_ctas < c)
         c = max_ctas;
@@ -165,12 +200,14 @@ int decode_num_ctas(int page_size, int batch, int max_ctas)
 
 // Workspace for a call whose sequences are at most max_len tokens: header and
 // segment records, then one partial slot per (worker, sub-piece) plus one per
-// segment.  The sub-pieces per worker follow from the largest possible list.
+// segment.  The sub-pieces per worker follow from the largest possible list
+// and the longest range any allowed set of split weights gives (a weight at
+// most kSplitWeightMax / kSplitWeightMin times the smallest).
 size_t decode_workspace_bytes(int batch, int hq, int hkv, long long max_len, int num_ctas)
 {
     const long long workers = static_cast<long long>(num_ctas) * kWarps;
     const long long total_max = static_cast<long long>(batch) * hkv * ((max_len + 15) / 16);
-    const long long subs = decode_subs(total_max, workers);
+    const long long subs = decode_subs(total_max, kSplitWeightMax, workers * kSplitWeightMin);
     const size_t slots = static_cast<size_t>(workers * subs) + static_cast<size_t>(batch) * hkv;
     const size_t bytes = slots * static_cast<size_t>(hq / hkv) * kPartialStride * sizeof(float);
     return decode_segment_bytes(batch, hkv) + ((bytes + 255) & ~size_t(255));
@@ -214,7 +251,8 @@ pkv_status decode_impl(const void *k_new, const void *v_new, int in_dtype, int n
                        int max_pages_per_seq, const int32_t *seq_lens, int max_seq_len, const int32_t *seq_page_sizes,
                        int batch, int num_q_heads, int num_kv_heads, int head_dim, int page_size, int64_t num_pages,
                        float sm_scale, void *out, int out_dtype, void *workspace, size_t workspace_bytes,
-                       int32_t *device_error, int max_ctas, cudaStream_t stream)
+                       int32_t *device_error, int max_ctas, cudaStream_t stream, bool probe = false,
+                       int *probe_ctas = nullptr)
 {
     pkv_status st = check_decode_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_seq,
                                        num_pages);
@@ -244,7 +282,7 @@ pkv_status decode_impl(const void *k_new, const void *v_new, int in_dtype, int n
         return PKV_ERR_UNSUPPORTED;
     const int ctas = decode_num_ctas(page_size, batch, max_ctas);
     if (ctas <= 0)
-        return PKV_ERR_CUDA;
+        return PKV_ERR_CUDA;                     // decode_num_ctas recorded the failing call
     if (workspace_bytes < decode_workspace_bytes(batch, num_q_heads, num_kv_heads, max_len, ctas))
         return PKV_ERR_WORKSPACE;
 
@@ -252,7 +290,7 @@ pkv_status decode_impl(const void *k_new, const void *v_new, int in_dtype, int n
     alignas(64) CUtensorMap tm_v;
     if (!make_page_map(&tm_k, k_cache, num_pages, num_kv_heads, page_size) ||
         !make_page_map(&tm_v, v_cache, num_pages, num_kv_heads, page_size))
-        return PKV_ERR_CUDA;
+        return cuda_failed(cudaErrorInvalidValue, "cuTensorMapEncodeTiled (page pools)");
 
     DecodeArgs a;
     a.q = static_cast<const __nv_bfloat16 *>(q);
@@ -288,7 +326,62 @@ pkv_status decode_impl(const void *k_new, const void *v_new, int in_dtype, int n
     // warp skips its first page's loads, so its first wait runs out (about
     // 2 s) and the call reports PKV_DEVERR_TIMEOUT.  -1: no effect.
     a.withhold_worker = g_withhold.load(std::memory_order_relaxed);
-    return launch_paged_decode(a, tm_k, tm_v, page_size, stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    a.split = 0;
+    a.split_ct = 0;
+    a.split_wmin = a.split_wmax = 1;
+    a.probe = probe ? 1 : 0;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        auto it = g_split.find(current_device());
+        if (it != g_split.end() && static_cast<int>(it->second.weights.size()) == ctas) {
+            a.split = 1;
+            a.split_ct = it->second.ct;
+            a.split_wmin = it->second.wmin;
+            a.split_wmax = it->second.wmax;
+        }
+    }
+    if (probe_ctas)
+        *probe_ctas = ctas;
+    const size_t slot_bytes = static_cast<size_t>(a.group) * kPartialStride * sizeof(float);
+    a.num_slots = static_cast<long long>((workspace_bytes - decode_segment_bytes(batch, num_kv_heads)) / slot_bytes);
+    const char *site = "";
+    const cudaError_t e = launch_paged_decode(a, tm_k, tm_v, page_size, stream, &site);
+    return e == cudaSuccess ? PKV_OK : cuda_failed(e, site);
+}
+
+// Installs weights (n of them, each in [kSplitWeightMin, kSplitWeightMax]) for
+// the current device; n == 0 removes them (even split).
+pkv_status set_split(const uint8_t *weights, int n)
+{
+    if (n < 0 || n > kMaxSplitCtas || (n > 0 && !weights))
+        return n < 0 || n > kMaxSplitCtas ? PKV_ERR_SHAPE : PKV_ERR_NULL;
+    SplitState st;
+    std::vector<uint32_t> prefix(static_cast<size_t>(n) + 1, 0u);
+    st.wmin = kSplitWeightMax;
+    st.wmax = kSplitWeightMin;
+    for (int c = 0; c < n; ++c) {
+        const int w = weights[c];
+        if (w < kSplitWeightMin || w > kSplitWeightMax)
+            return PKV_ERR_SHAPE;
+        prefix[c + 1] = prefix[c] + static_cast<uint32_t>(w);
+        st.wmin = w < st.wmin ? w : st.wmin;
+        st.wmax = w > st.wmax ? w : st.wmax;
+    }
+    const int dev = current_device();
+    if (dev < 0)
+        return cuda_failed(cudaGetLastError());
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (n == 0) {
+        g_split.erase(dev);
+        return PKV_OK;
+    }
+    const cudaError_t e = upload_split_prefix(prefix.data(), n);
+    if (e != cudaSuccess)
+        return cuda_failed(e);
+    st.weights.assign(weights, weights + n);
+    st.ct = static_cast<long long>(kWarps) * prefix[n];
+    g_split[dev] = st;
+    return PKV_OK;
 }
 
 }  // namespace
@@ -312,13 +405,18 @@ pkv_status pkv_read_device_error(const int32_t *device_error, int clear, int32_t
     if (!aligned(device_error, 4))
         return PKV_ERR_ALIGN;
     int32_t word = 0;
-    if (cudaMemcpyAsync(&word, device_error, sizeof(word), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
-        return PKV_ERR_CUDA;
-    if (cudaStreamSynchronize(stream) != cudaSuccess)
-        return PKV_ERR_CUDA;
+    cudaError_t e = cudaMemcpyAsync(&word, device_error, sizeof(word), cudaMemcpyDeviceToHost, stream);
+    if (e != cudaSuccess)
+        return cuda_failed(e);
+    e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess)
+        return cuda_failed(e);
     *code = word;
-    if (clear && cudaMemsetAsync(const_cast<int32_t *>(device_error), 0, sizeof(word), stream) != cudaSuccess)
-        return PKV_ERR_CUDA;
+    if (clear) {
+        e = cudaMemsetAsync(const_cast<int32_t *>(device_error), 0, sizeof(word), stream);
+        if (e != cudaSuccess)
+            return cuda_failed(e);
+    }
     return PKV_OK;
 }
 
@@ -370,7 +468,8 @@ pkv_status pkv_kv_append_fp8(const void *k_new, const void *v_new, int in_dtype,
     a.num_pages = num_pages;
     a.page_size = page_size;
     a.err = device_error;
-    return launch_kv_append(a, stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    const cudaError_t e = launch_kv_append(a, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_failed(e);
 }
 
 size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads, int head_dim, int max_seq_len,
@@ -420,6 +519,135 @@ pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dt
                        k_scale, v_scale, block_table, max_pages_per_seq, seq_lens, max_seq_len, seq_page_sizes, batch,
                        num_q_heads, num_kv_heads, head_dim, page_size, num_pages, sm_scale, out, out_dtype, workspace,
                        workspace_bytes, device_error, max_ctas, stream);
+}
+
+pkv_status pkv_decode_set_split_weights(const uint8_t *weights, int n)
+{
+    return set_split(weights, n);
+}
+
+int pkv_last_cuda_error(const char **name)
+{
+    if (name) {
+        snprintf(t_last_text, sizeof(t_last_text), "%s%s%s",
+                 t_last_cuda ? cudaGetErrorName(static_cast<cudaError_t>(t_last_cuda)) : "cudaSuccess",
+                 *t_last_site ? " in " : "", t_last_site);
+        *name = t_last_text;
+    }
+    return t_last_cuda;
+}
+
+pkv_status pkv_decode_get_split_weights(uint8_t *weights, int capacity, int *n)
+{
+    if (!n || capacity < 0 || (capacity > 0 && !weights))
+        return PKV_ERR_NULL;
+    const int dev = current_device();
+    if (dev < 0)
+        return cuda_failed(cudaGetLastError());
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_split.find(dev);
+    const int have = it == g_split.end() ? 0 : static_cast<int>(it->second.weights.size());
+    *n = have;
+    if (have > capacity)
+        return PKV_ERR_SHAPE;
+    for (int c = 0; c < have; ++c)
+        weights[c] = it->second.weights[c];
+    return PKV_OK;
+}
+
+pkv_status pkv_decode_calibrate_split(const void *q, const uint8_t *k_cache, const uint8_t *v_cache,
+                                      const float *k_scale, const float *v_scale, const int32_t *block_table,
+                                      int max_pages_per_seq, const int32_t *seq_lens, int max_seq_len,
+                                      const int32_t *seq_page_sizes, int batch, int num_q_heads, int num_kv_heads,
+                                      int head_dim, int page_size, int64_t num_pages, float sm_scale, void *out,
+                                      int out_dtype, void *workspace, size_t workspace_bytes, int max_ctas,
+                                      int rounds, uint8_t *weights_out, int capacity, int *n_out,
+                                      cudaStream_t stream)
+{
+    if (rounds < 1 || rounds > 64)
+        return PKV_ERR_SHAPE;
+    if (batch <= 0)
+        return PKV_ERR_SHAPE;
+    if (check_decode_shape(batch, num_q_heads, num_kv_heads, head_dim, page_size, max_pages_per_seq, num_pages) !=
+        PKV_OK)
+        return PKV_ERR_SHAPE;
+    const int ctas = decode_num_ctas(page_size, batch, max_ctas);
+    if (ctas <= 0)
+        return PKV_ERR_CUDA;
+    if (ctas > kMaxSplitCtas)
+        return PKV_ERR_UNSUPPORTED;
+    constexpr int kCallsPerRound = 3;
+    constexpr double kMean = 0.5 * (kSplitWeightMin + kSplitWeightMax);
+    std::vector<uint8_t> w(static_cast<size_t>(ctas), static_cast<uint8_t>(kMean));
+    std::vector<unsigned long long> times(static_cast<size_t>(ctas) * 2);
+    pkv_status st = set_split(w.data(), ctas);
+    for (int r = 0; r < rounds && st == PKV_OK; ++r) {
+        // Finish (F) and start (S) of every CTA, relative to the first CTA's start.
+        std::vector<double> F(static_cast<size_t>(ctas), 0.0), S(static_cast<size_t>(ctas), 0.0);
+        for (int call = 0; call < kCallsPerRound && st == PKV_OK; ++call) {
+            int used = 0;
+            const cudaError_t ce = clear_split_probe(ctas, stream);
+            if (ce != cudaSuccess) {
+                st = cuda_failed(ce);
+                break;
+            }
+            st = decode_impl(nullptr, nullptr, PKV_F32, 0, q, const_cast<uint8_t *>(k_cache),
+                             const_cast<uint8_t *>(v_cache), k_scale, v_scale, block_table, max_pages_per_seq,
+                             seq_lens, max_seq_len, seq_page_sizes, batch, num_q_heads, num_kv_heads, head_dim,
+                             page_size, num_pages, sm_scale, out, out_dtype, workspace, workspace_bytes, nullptr,
+                             max_ctas, stream, true, &used);
+            if (st != PKV_OK)
+                break;
+            cudaError_t re = used != ctas ? cudaErrorInvalidValue : cudaStreamSynchronize(stream);
+            if (re == cudaSuccess)
+                re = read_split_probe(times.data(), ctas);
+            if (re != cudaSuccess) {
+                st = cuda_failed(re);
+                break;
+            }
+            unsigned long long t0 = times[0];
+            for (int c = 1; c < ctas; ++c)
+                t0 = times[2 * c] < t0 ? times[2 * c] : t0;
+            for (int c = 0; c < ctas; ++c) {
+                S[c] += static_cast<double>(times[2 * c] - t0) / kCallsPerRound;
+                F[c] += static_cast<double>(times[2 * c + 1] > t0 ? times[2 * c + 1] - t0 : 0) / kCallsPerRound;
+            }
+        }
+        if (st != PKV_OK)
+            break;
+        // Each CTA streams its share at rate w_c / (F_c - S_c); for all to
+        // finish together at the mean finish time its new share is that rate
+        // times (mean F - S_c).  Normalised to the middle of the weight range.
+        double fbar = 0.0;
+        for (int c = 0; c < ctas; ++c)
+            fbar += F[c] / ctas;
+        std::vector<double> nw(static_cast<size_t>(ctas), kMean);
+        double sum = 0.0;
+        for (int c = 0; c < ctas; ++c) {
+            const double busy = F[c] - S[c], left = fbar - S[c];
+            nw[c] = (busy > 0.0 && left > 0.0) ? w[c] * left / busy : w[c];
+            sum += nw[c];
+        }
+        for (int c = 0; c < ctas; ++c) {
+            double v = sum > 0.0 ? nw[c] * kMean * ctas / sum : kMean;
+            v = v < kSplitWeightMin ? kSplitWeightMin : (v > kSplitWeightMax ? kSplitWeightMax : v);
+            w[c] = static_cast<uint8_t>(v + 0.5);
+        }
+        st = set_split(w.data(), ctas);
+    }
+    if (st != PKV_OK) {
+        set_split(nullptr, 0);
+        return st;
+    }
+    if (n_out)
+        *n_out = ctas;
+    if (weights_out) {
+        if (capacity < ctas)
+            return PKV_ERR_SHAPE;
+        for (int c = 0; c < ctas; ++c)
+            weights_out[c] = w[c];
+    }
+    return PKV_OK;
 }
 
 size_t pkv_prefill_workspace_size(int batch, int num_kv_heads, int max_kv_len, int64_t max_total_kv)
@@ -480,7 +708,7 @@ pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, in
     if (!make_q_map(&tm_q, q, total_q, num_q_heads, group, tpt) ||
         !make_kv16_map(&tm_k, k16, rows, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) ||
         !make_kv16_map(&tm_v, v16, rows, CU_TENSOR_MAP_DATA_TYPE_FLOAT16))
-        return PKV_ERR_CUDA;
+        return cuda_failed(cudaErrorInvalidValue);
 
     PrefillArgs a;
     a.cu_q = cu_q;
@@ -515,7 +743,8 @@ pkv_status pkv_paged_prefill(const void *q, const int32_t *cu_q, int total_q, in
     a.out = out;
     a.out_f32 = out_dtype == PKV_F32;
     a.err = device_error;
-    return launch_paged_prefill(a, tm_q, tm_k, tm_v, stream) == cudaSuccess ? PKV_OK : PKV_ERR_CUDA;
+    const cudaError_t e = launch_paged_prefill(a, tm_q, tm_k, tm_v, stream);
+    return e == cudaSuccess ? PKV_OK : cuda_failed(e);
 }
 
 }  // extern "C"

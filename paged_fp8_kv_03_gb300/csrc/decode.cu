@@ -12,12 +12,16 @@
 //
 // Work split.  The (sequence, kv head) segments are laid end to end as one
 // list of "page-heads" (one page of one kv head, 2 x P x 128 bytes).  Every
-// warp of the persistent grid is an independent worker that takes an equal
+// warp of the persistent grid is an independent worker that takes a
 // contiguous range of that list, whatever the sequence lengths (split-K /
-// flash-decoding with exact balance).  A worker's range cuts segments into
+// flash-decoding): an equal share, or a share proportional to its CTA's
+// weight when the host has installed weights for this grid (the CTAs land on
+// the same SMs call after call, and some SMs stream slower than others, so
+// calibrated weights let every worker finish at the same time).  A worker's
+// range cuts segments into
 // pieces; a piece covering a whole segment writes the final output, the
 // others write a partial softmax state (running max m, sum l, unnormalised
-// accumulator) into workspace slot (worker + segment).  A second kernel, one
+// accumulator) into workspace slot (worker, sub-piece) + segment.  A second kernel, one
 // CTA per (segment, head) with a thread per dimension, merges the pieces in
 // worker order (deterministic); it is a programmatic dependent launch, so it
 // is already resident when the first kernel's last warps finish.
@@ -147,10 +151,47 @@ __device__ Loc advance(const int *ps, int batch, int hkv, Loc l, int64_t n)
     return l;
 }
 
-// Worker whose range holds list position x (ranges are [w*T/W, (w+1)*T/W)).
-__device__ __forceinline__ int worker_of(int64_t x, int64_t total, int workers)
+// Weighted split: prefix sums of the per-CTA weights of the current device
+// (entry c = sum of the weights of CTAs 0 .. c-1), written by the host between
+// calls; and the calibration's per-CTA start / end times (global timer, ns).
+__device__ uint32_t g_split_prefix[kMaxSplitCtas + 1];
+__device__ unsigned long long g_split_probe[kMaxSplitCtas][2];
+
+// The split of one call.  pre == nullptr: the even split (C(w) = w, CT = workers).
+struct Split {
+    const uint32_t *pre;   // weight prefix sums (global or shared memory), num_ctas + 1 entries
+    int ctas;
+    int64_t ct;            // C(workers)
+};
+
+__device__ __forceinline__ Split make_split(const DecodeArgs &a, const uint32_t *pre)
 {
-    return static_cast<int>(((x + 1) * workers - 1) / total);
+    Split sp;
+    sp.ctas = a.num_ctas;
+    sp.pre = a.split ? pre : nullptr;
+    sp.ct = a.split ? a.split_ct : static_cast<int64_t>(a.num_ctas) * kWarps;
+    return sp;
+}
+
+// First list position of worker w's range, T * C(w) / CT (w = workers gives T).
+// Clamped to [0, T], so even a table rewritten during a call (a misuse) keeps
+// every range, and so every slot index, inside the list.
+__device__ __forceinline__ int64_t range_lo(const Split &sp, int64_t total, int w)
+{
+    int64_t cw;
+    if (sp.pre == nullptr) {
+        cw = w;
+    } else {
+        const int c = w / kWarps, j = w % kWarps;
+        if (c >= sp.ctas) {
+            cw = sp.ct;
+        } else {
+            const uint32_t p0 = sp.pre[c], p1 = sp.pre[c + 1];
+            cw = static_cast<int64_t>(kWarps) * p0 + static_cast<int64_t>(j) * (p1 - p0);
+        }
+    }
+    const int64_t x = total * cw / sp.ct;
+    return x < 0 ? 0 : (x > total ? total : x);
 }
 
 struct Smem {
@@ -446,6 +487,34 @@ __device__ __noinline__ void append_own_tokens(const DecodeArgs &a, const int *p
     __syncwarp();
 }
 
+// Segment records for the merge kernel, for the segments this worker's range
+// [lo, hi) touches: the worker holding a segment's first chunk writes where
+// the segment lies and whether its pieces need merging (-1: its piece is the
+// whole segment, the output is final), the worker holding its last chunk
+// writes its own index.  Pieces end at a segment's end, the range's end or
+// every kChainChunks chunks of the range, as in the streaming loop.
+__device__ __noinline__ void write_records(const DecodeArgs &a, const int *pstart, int64_t lo, int64_t hi, int worker)
+{
+    Loc l = locate(pstart, a.batch, a.hkv, lo);
+    int64_t k = 0;
+    const int64_t n_total = hi - lo;
+    while (k < n_total && l.b < a.batch) {
+        const int np = chunks_of(pstart, l.b);
+        const int n_piece = static_cast<int>(min(min(static_cast<int64_t>(np - l.ck), n_total - k),
+                                                 static_cast<int64_t>(kChainChunks - (k & (kChainChunks - 1)))));
+        SegRecord *rec = a.segs + l.b * a.hkv + l.h;
+        if (l.ck == 0) {
+            rec->start = static_cast<long long>(pstart[l.b]) * a.hkv + static_cast<long long>(l.h) * np;
+            rec->n = np;
+            rec->w0 = n_piece == np ? -1 : worker;
+        }
+        if (l.ck + n_piece == np)
+            rec->w1 = worker;
+        k += n_piece;
+        l = advance(pstart, a.batch, a.hkv, l, n_piece);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     paged_gqa_decode_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                             const DecodeArgs a)
@@ -456,6 +525,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (a.probe && tid == 0)
+        g_split_probe[blockIdx.x][0] = global_timer_ns();
     int *pstart = reinterpret_cast<int *>(smem + S::kPstart);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kFlag);
     int *warp_sum = reinterpret_cast<int *>(smem + S::kWarpSum);
@@ -505,53 +576,41 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         __syncthreads();
     }
 
-    // Sequences with no tokens: nobody streams them, so write their zero rows here.
+    // Sequences with no tokens: nobody streams them, so write their zero rows
+    // (and a record telling the merge kernel to skip them) here.
     for (int sg = blockIdx.x; sg < a.batch * a.hkv; sg += a.num_ctas) {
         const int b = sg / a.hkv;
         if (chunks_of(pstart, b) == 0) {
             const int64_t row0 = static_cast<int64_t>(b) * a.hq + static_cast<int64_t>(sg % a.hkv) * a.group;
             for (int e = tid; e < a.group * kHeadDim; e += kThreads)
                 store_out(a, row0 + (e >> 7), e & (kHeadDim - 1), 0.f);
+            if (tid == 0) {
+                a.segs[sg].n = 0;
+                a.segs[sg].w0 = -1;
+            }
         }
     }
 
-    const int workers = a.num_ctas * kWarps;
     const int worker = blockIdx.x * kWarps + warp;
     const int64_t total = static_cast<int64_t>(pstart[a.batch]) * a.hkv;
-    const int subs = static_cast<int>(decode_subs(total, workers));
-
-    // Segment records for the merge kernel: where each segment lies in the
-    // list and whether its pieces need merging (it spans several workers, or
-    // a sub-piece cut of its worker falls inside it).
-    if (blockIdx.x == 0) {
-        for (int sg = tid; sg < a.batch * a.hkv; sg += kThreads) {
-            const int b = sg / a.hkv, h = sg % a.hkv, np = chunks_of(pstart, b);
-            SegRecord r;
-            r.start = static_cast<long long>(pstart[b]) * a.hkv + static_cast<long long>(h) * np;
-            r.n = np;
-            r.w0 = -1;
-            if (np > 0) {
-                const int w0 = worker_of(r.start, total, workers), w1 = worker_of(r.start + np - 1, total, workers);
-                const int64_t lo0 = static_cast<int64_t>(w0) * total / workers;
-                if (w0 != w1 || (r.start - lo0) / kChainChunks != (r.start + np - 1 - lo0) / kChainChunks)
-                    r.w0 = w0;
-            }
-            a.segs[sg] = r;
-        }
-        if (tid == 0) {
-            DecodeHeader hd;
-            hd.total = total;
-            hd.subs = subs;
-            hd.pad = 0;
-            *a.header = hd;
-        }
+    const Split sp = make_split(a, g_split_prefix);
+    const int subs = static_cast<int>(decode_subs(total, a.split ? a.split_wmax : 1, sp.ct));
+    if (blockIdx.x == 0 && tid == 0) {
+        DecodeHeader hd;
+        hd.total = total;
+        hd.subs = subs;
+        hd.pad = 0;
+        *a.header = hd;
     }
     // Let the merge kernel get scheduled now; it waits for this grid to finish.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int64_t lo = static_cast<int64_t>(worker) * total / workers;
-    const int64_t hi = static_cast<int64_t>(worker + 1) * total / workers;
-    if (lo >= hi)
-        return;                                  // warp-level: no CTA barrier follows
+    const int64_t lo = range_lo(sp, total, worker);
+    const int64_t hi = range_lo(sp, total, worker + 1);
+    if (lo >= hi) {                              // warp-level: no CTA barrier follows
+        if (a.probe && lane == 0)
+            atomicMax(&g_split_probe[blockIdx.x][1], static_cast<unsigned long long>(global_timer_ns()));
+        return;
+    }
     const int n_total = static_cast<int>(hi - lo);
 
     // Fused append: if a page that may receive new tokens is among the first
@@ -620,6 +679,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         issue(f);
     if (a.k_new != nullptr && !append_early)
         append_own_tokens(a, pstart, lo, hi, lane);
+    if (lane == 0)                               // while the first loads are in flight
+        write_records(a, pstart, lo, hi, worker);
+    __syncwarp();
 
     const int gid = lane >> 2, t4 = lane & 3;
     const TileOffsets off = tile_offsets(lane);
@@ -708,6 +770,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 if (h1)
                     store_pair(a, row0 + 2 * t4 + 1, d, acc[sg][1] * s1, acc[sg][3] * s1);
             }
+        } else if (static_cast<int64_t>(slot_index) + seg >= a.num_slots) {
+            if (a.err && lane == 0)
+                atomicOr(a.err, PKV_DEVERR_INTERNAL);
         } else {
             float *slot = a.partials + static_cast<int64_t>(slot_index + seg) * a.group * kPartialStride;
 #pragma unroll
@@ -734,6 +799,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (pending & (1u << s))
                 wait_thread(bars + 8 * s, (pend_par >> s) & 1u, abort_flag, a.err, false);
     }
+    if (a.probe && lane == 0)
+        atomicMax(&g_split_probe[blockIdx.x][1], static_cast<unsigned long long>(global_timer_ns()));
 }
 
 // One CTA per (sequence, kv head) segment, one warp per query head g of its
@@ -746,34 +813,39 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 // deterministic.
 //
 // Where a segment's pieces are: with one sub-piece per worker range
-// (subs == 1) and at least as many chunk-heads as workers, piece i was
-// written by worker w0 + i; with fewer chunk-heads than workers every worker
-// owns at most one, and piece i comes from the worker owning position start
-// + i; with subs > 1 a worker's range is also cut every kChainChunks chunks
-// and the pieces are walked worker by worker.
+// (subs == 1) and no empty range, piece i was written by worker w0 + i and the
+// last one by w1; otherwise (a range cut every kChainChunks chunks, or ranges
+// of no chunk when the list is shorter than the workers' shares) the pieces are
+// walked worker by worker.
 constexpr int kMergeBatch = 16;
 
 __global__ void __launch_bounds__(32 * PKV_MAX_GROUP) splitk_merge_kernel(const DecodeArgs a)
 {
+    __shared__ uint32_t pre_s[kMaxSplitCtas + 1];
+    if (a.split) {                               // the split's weight prefix sums (inputs, not the decode's output)
+        for (int c = threadIdx.x; c <= a.num_ctas; c += blockDim.x)
+            pre_s[c] = g_split_prefix[c];
+        __syncthreads();
+    }
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid has finished
     const int seg = blockIdx.x, g = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const SegRecord r = a.segs[seg];
     const DecodeHeader hd = *a.header;
-    if (r.w0 < 0)
+    if (r.n <= 0 || r.w0 < 0)
         return;
     const int64_t total = hd.total;
     const int subs = hd.subs;
-    const int workers = a.num_ctas * kWarps;
+    const Split sp = make_split(a, pre_s);
     const int b = seg / a.hkv, h = seg % a.hkv;
-    const bool walk = subs > 1;
-    const bool dense = total >= workers;
-    // pieces known up front (subs == 1); the walk counts them as it goes
-    const int n_known = dense ? worker_of(r.start + r.n - 1, total, workers) - r.w0 + 1 : r.n;
-    // walk state (subs > 1): worker w, its range [lo_w, hi_w), offset k of the next piece in it
+    // every range holds at least one chunk-head when T * wmin >= CT
+    const bool dense = total * (a.split ? a.split_wmin : 1) >= sp.ct;
+    const bool walk = subs > 1 || !dense;
+    const int n_known = r.w1 - r.w0 + 1;
+    // walk state: worker w, its range [lo_w, hi_w), offset k of the next piece in it
     const int64_t end = r.start + r.n;
     int w = r.w0;
-    int64_t lo_w = static_cast<int64_t>(w) * total / workers;
-    int64_t hi_w = static_cast<int64_t>(w + 1) * total / workers;
+    int64_t lo_w = range_lo(sp, total, w);
+    int64_t hi_w = range_lo(sp, total, w + 1);
     int64_t k = r.start - lo_w;
 
     float M = -INFINITY, L = 0.f;
@@ -787,7 +859,7 @@ __global__ void __launch_bounds__(32 * PKV_MAX_GROUP) splitk_merge_kernel(const 
             if (nb <= 0)
                 break;
             if (lane < nb)
-                my_slot = dense ? r.w0 + i0 + lane : worker_of(r.start + i0 + lane, total, workers);
+                my_slot = r.w0 + i0 + lane;
         } else {
             nb = 0;
             while (nb < kMergeBatch && lo_w + k < end) {
@@ -795,16 +867,21 @@ __global__ void __launch_bounds__(32 * PKV_MAX_GROUP) splitk_merge_kernel(const 
                     my_slot = w * subs + static_cast<int>(k / kChainChunks);
                 ++nb;
                 k = (k / kChainChunks + 1) * kChainChunks;          // next sub-piece of this worker
-                if (lo_w + k >= hi_w) {                              // next worker: starts at its range start
-                    ++w;
-                    lo_w = hi_w;
-                    hi_w = static_cast<int64_t>(w + 1) * total / workers;
+                if (lo_w + k >= hi_w) {                              // next worker with chunks: starts at its range start
+                    do {
+                        ++w;
+                        lo_w = hi_w;
+                        hi_w = range_lo(sp, total, w + 1);
+                    } while (hi_w <= lo_w && lo_w < end);
                     k = 0;
                 }
             }
             if (nb == 0)
                 break;
         }
+        const bool bad = my_slot >= 0 && static_cast<int64_t>(my_slot) + seg >= a.num_slots;
+        if (bad)
+            my_slot = -1;                                           // skipped, flagged below
         float m = -INFINITY, l = 0.f;
         if (my_slot >= 0) {
             const float *p = a.partials + (static_cast<int64_t>(my_slot + seg) * a.group + g) * kPartialStride;
@@ -816,10 +893,12 @@ __global__ void __launch_bounds__(32 * PKV_MAX_GROUP) splitk_merge_kernel(const 
         for (int i = 0; i < kMergeBatch; ++i) {
             const int si = __shfl_sync(kFull, my_slot, i);
             v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (i < nb)
+            if (si >= 0)                                            // lanes >= nb hold -1
                 v[i] = *reinterpret_cast<const float4 *>(
                     a.partials + (static_cast<int64_t>(si + seg) * a.group + g) * kPartialStride + 4 * lane);
         }
+        if (__any_sync(kFull, bad) && lane == 0 && a.err)
+            atomicOr(a.err, PKV_DEVERR_INTERNAL);
         float mb = m;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1)
@@ -864,13 +943,15 @@ const void *decode_kernel_for(int /*page_size*/)
 }
 
 cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                                int page_size, cudaStream_t stream)
+                                int page_size, cudaStream_t stream, const char **site)
 {
     const size_t smem = decode_smem_bytes(page_size, a.batch);
+    *site = "decode kernel launch";
     paged_gqa_decode_kernel<<<a.num_ctas, kThreads, smem, stream>>>(tm_k, tm_v, a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
+    *site = "split-K merge kernel launch";
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(a.batch * a.hkv), 1, 1);
     cfg.blockDim = dim3(static_cast<unsigned>(32 * a.group), 1, 1);
@@ -882,6 +963,31 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, co
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     return cudaLaunchKernelEx(&cfg, splitk_merge_kernel, a);
+}
+
+cudaError_t upload_split_prefix(const uint32_t *prefix, int n)
+{
+    if (n < 1 || n > kMaxSplitCtas)
+        return cudaErrorInvalidValue;
+    return cudaMemcpyToSymbol(g_split_prefix, prefix, (static_cast<size_t>(n) + 1) * sizeof(uint32_t));
+}
+
+cudaError_t clear_split_probe(int n, cudaStream_t stream)
+{
+    if (n < 1 || n > kMaxSplitCtas)
+        return cudaErrorInvalidValue;
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_split_probe);
+    if (e != cudaSuccess)
+        return e;
+    return cudaMemsetAsync(p, 0, static_cast<size_t>(n) * 2 * sizeof(unsigned long long), stream);
+}
+
+cudaError_t read_split_probe(unsigned long long *times, int n)
+{
+    if (n < 1 || n > kMaxSplitCtas)
+        return cudaErrorInvalidValue;
+    return cudaMemcpyFromSymbol(times, g_split_probe, static_cast<size_t>(n) * 2 * sizeof(unsigned long long));
 }
 
 }  // namespace pkv

@@ -43,17 +43,31 @@ struct AppendArgs {
 // rounds toward zero, so error would otherwise grow with the chain).
 constexpr int kChainChunks = 512;
 
+// Weighted split.  Worker warp w = 4c + j of CTA c takes a share of the
+// chunk-head list proportional to its CTA's weight (an integer in
+// [kSplitWeightMin, kSplitWeightMax]; equal weights give the plain even split):
+// with C(w) = 4 * sum_{c' < c} weight[c'] + j * weight[c] and CT = C(workers),
+// worker w's range is [T * C(w) / CT, T * C(w + 1) / CT) (integer division).
+// Weights are set per device for one grid size (a calibration measures how
+// fast the SMs the CTAs land on stream their share); calls with another grid
+// size split evenly.
+constexpr int kMaxSplitCtas = 1024;
+constexpr int kSplitWeightMin = 96;
+constexpr int kSplitWeightMax = 160;
+
 // Decode workspace: a header, one record per (sequence, kv head) segment,
 // then the partial-state slots.
 struct DecodeHeader {
     long long total;                // chunk-heads in the list (all segments)
-    int subs;                       // sub-pieces per worker range: ceil(ceil(total / workers) / kChainChunks)
+    int subs;                       // sub-pieces per worker range: ceil(max range length / kChainChunks)
     int pad;
 };
 struct SegRecord {
     long long start;                // list position of the segment's first chunk-head
     int n;                          // its chunks (0: empty sequence)
     int w0;                         // worker of its first chunk; -1: one piece, nothing to merge
+    int w1;                         // worker of its last chunk
+    int pad;
 };
 
 struct DecodeArgs {
@@ -78,11 +92,20 @@ struct DecodeArgs {
     int n_new;
     uint8_t *k_pool, *v_pool;       // the pools the tensor maps describe (for the stores)
     DecodeHeader *header;           // workspace header (written by CTA 0)
-    SegRecord *segs;                // [batch * hkv] segment records (written by CTA 0)
+    SegRecord *segs;                // [batch * hkv] segment records (written by the workers holding a
+                                    // segment's first and last chunk)
     float *partials;                // [num_ctas * kWarps * subs + batch * hkv][group][kPartialStride]
     int32_t *err;
     int num_ctas;
     int withhold_worker;            // failure-detection test hook (-1 = off)
+    // Split: split == 0 is the even split (CT = workers, every weight 1); else
+    // the per-CTA weight prefix sums sit in device memory (see decode.cu) and
+    // split_ct = C(workers), split_wmin / split_wmax bound the weights.
+    int split;
+    long long split_ct;
+    int split_wmin, split_wmax;
+    int probe;                      // calibration: record each CTA's start and end time
+    long long num_slots;            // partial-state slots the workspace holds (accesses beyond: skipped, flagged)
 };
 
 // Chunked prefill (csrc/prefill.cu).  The queries of all sequences are rows
@@ -150,11 +173,13 @@ inline size_t decode_segment_bytes(int batch, int hkv)
     return (sizeof(DecodeHeader) + static_cast<size_t>(batch) * hkv * sizeof(SegRecord) + 255) & ~size_t(255);
 }
 
-// Sub-pieces per worker range for a list of `total` chunk-heads over
-// `workers` workers (at least 1).
-inline __host__ __device__ long long decode_subs(long long total, long long workers)
+// Sub-pieces per worker range for a list of `total` chunk-heads: no range is
+// longer than ceil(total * wmax / ct) chunks (wmax the largest weight, ct =
+// C(workers); even split: wmax = 1, ct = workers), and a range is cut every
+// kChainChunks of them.  At least 1.
+inline __host__ __device__ long long decode_subs(long long total, long long wmax, long long ct)
 {
-    const long long per = (total + workers - 1) / workers;
+    const long long per = (total * wmax + ct - 1) / ct;
     const long long s = (per + kChainChunks - 1) / kChainChunks;
     return s < 1 ? 1 : s;
 }
@@ -207,6 +232,11 @@ size_t prefill_smem_bytes();
 cudaError_t launch_paged_prefill(const PrefillArgs &a, const CUtensorMap &tm_q, const CUtensorMap &tm_k16,
                                  const CUtensorMap &tm_v16, cudaStream_t stream);
 cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
-                                int page_size, cudaStream_t stream);
+                                int page_size, cudaStream_t stream, const char **site);
+// Weighted split tables of the current device (decode.cu): the weight prefix
+// sums (n + 1 entries) and the calibration's per-CTA [start, end] times.
+cudaError_t upload_split_prefix(const uint32_t *prefix, int n);
+cudaError_t clear_split_probe(int n, cudaStream_t stream);
+cudaError_t read_split_probe(unsigned long long *times, int n);
 
 }  // namespace pkv

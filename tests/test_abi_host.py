@@ -227,3 +227,28 @@ def test_read_device_error_argument_errors(lib):
 def test_withhold_facility_is_off_at_load_and_settable(lib):
     lib.pkv_test_withhold_load(-5)          # any negative index turns it off
     lib.pkv_test_withhold_load(-1)
+
+
+def test_split_weight_argument_errors(lib):
+    """Weights outside [96, 160], more than 1024 CTAs or a NULL array are
+    rejected before any CUDA call; so are calibration requests with no
+    rounds or no sequences."""
+    c = _status_codes()
+    ok = (ctypes.c_uint8 * 4)(96, 128, 150, 160)
+    low = (ctypes.c_uint8 * 4)(96, 95, 128, 128)
+    high = (ctypes.c_uint8 * 4)(128, 161, 128, 128)
+    assert lib.pkv_decode_set_split_weights(ctypes.addressof(low), 4) == c["PKV_ERR_SHAPE"]
+    assert lib.pkv_decode_set_split_weights(ctypes.addressof(high), 4) == c["PKV_ERR_SHAPE"]
+    assert lib.pkv_decode_set_split_weights(ctypes.addressof(ok), -1) == c["PKV_ERR_SHAPE"]
+    assert lib.pkv_decode_set_split_weights(ctypes.addressof(ok), 1025) == c["PKV_ERR_SHAPE"]
+    assert lib.pkv_decode_set_split_weights(None, 4) == c["PKV_ERR_NULL"]
+    assert lib.pkv_decode_get_split_weights(ctypes.addressof(ok), 4, None) == c["PKV_ERR_NULL"]
+    n = ctypes.c_int(0)
+    assert lib.pkv_decode_get_split_weights(None, 4, ctypes.byref(n)) == c["PKV_ERR_NULL"]
+
+    def cal(rounds=4, B=2):
+        return lib.pkv_decode_calibrate_split(A16, A16, A16b, A16, A16, A16, 8, A16, 0, None, B, 16, 8, 128, 16, 100,
+                                              0.088, A16, 0, A16, 1 << 20, 0, rounds, None, 0, None, None)
+    assert cal(rounds=0) == c["PKV_ERR_SHAPE"]
+    assert cal(rounds=65) == c["PKV_ERR_SHAPE"]
+    assert cal(B=0) == c["PKV_ERR_SHAPE"]

@@ -308,3 +308,17 @@ def test_closed_forms_uniform_and_one_hot_weights(pkv, cuda_device):
     got = out.double().cpu().numpy()
     assert np.abs(got[:, :, :L] - w).max() <= 2e-6
     assert np.all(got[:, :, L:] == 0)
+
+
+def test_page_sizes_and_batches_interleaved(pkv, cuda_device):
+    """Every page size runs the same kernel, whose shared memory grows with
+    the batch: a call with another page size and a smaller batch in between
+    must not lower the limit a larger batch needs."""
+    big = workloads.Workload(53, "big", [1, 2, 15, 16, 17, 31, 33, 40, 90], 0, 8, 1, 16, seed=2)
+    small = workloads.Workload(54, "small", [4097, 1, 999], 0, 64, 8, 32, seed=3)
+    fb = fill_gpu(big, 0, cuda_device)
+    fs = fill_gpu(small, 0, cuda_device)
+    ref_b, ref_s = _full_oracle(big, fb), _full_oracle(small, fs)
+    for _ in range(2):
+        assert_close(_decode(pkv, fb, max_ctas=7).double().cpu().numpy(), ref_b, "P=16, batch 9")
+        assert_close(_decode(pkv, fs, max_ctas=7).double().cpu().numpy(), ref_s, "P=32, batch 3")
