@@ -196,6 +196,52 @@ __device__ __forceinline__ void split_pair(float p0, float p1, uint32_t &hi, uin
     lo = f32x2_to_f16x2(p0 - h0, p1 - h1);
 }
 
+// Packed pairs of fp32 (one 64-bit register pair): the paired add and fma
+// run two lanes of fp32 arithmetic per instruction, each rounded exactly as
+// the scalar operation, so results equal the scalar code bit for bit.
+__device__ __forceinline__ uint64_t f2_pack(float a, float b)
+{
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+    return r;
+}
+
+__device__ __forceinline__ float2 f2_unpack(uint64_t r)
+{
+    float2 v;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(v.x), "=f"(v.y) : "l"(r));
+    return v;
+}
+
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b)
+{
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c)
+{
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
+// max(a, b, c) in one instruction (exact, like two fmaxf).
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // True in exactly one lane of the (converged) warp.
 __device__ __forceinline__ bool elect_one()
 {
@@ -594,33 +640,43 @@ __global__ void __launch_bounds__(kPThreads, 1)
 #pragma unroll
             for (int c = 0; c < 2; ++c)
 #pragma unroll
-                for (int k = 0; k < 32; ++k)
-                    mx[k & 7] = fmaxf(mx[k & 7], __uint_as_float(x[c][k]));
+                for (int k = 0; k < 32; k += 2)
+                    mx[(k >> 1) & 7] = max3(mx[(k >> 1) & 7], __uint_as_float(x[c][k]), __uint_as_float(x[c][k + 1]));
             const float mh = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                    fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7]))) * sl2;
             // P = 2^(x sl2 - mm) <= 2^8 as f16 hi + lo, written over each 32-column
             // piece of S (hi in its first 16 columns, lo in the last 16); returns
             // the half row's sum of P.
+            // Pairs of elements go through the paired fp32 add / fma (fewer
+            // instructions on the softmax warps' issue slots; same roundings).
             auto emit = [&](float mm) -> float {
-                float ls[8];
+                uint64_t ls[4];                            // ls[i] = sums of elements 2i, 2i+1 (mod 8)
 #pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    ls[k] = 0.f;
+                for (int k = 0; k < 4; ++k)
+                    ls[k] = 0ull;
+                const uint64_t sl2x2 = f2_pack(sl2, sl2), nmm = f2_pack(-mm, -mm);
 #pragma unroll
                 for (int c = 0; c < 2; ++c) {
                     uint32_t ph[16], pl[16];
 #pragma unroll
                     for (int q = 0; q < 16; ++q) {
-                        const float p0 = ex2_approx(fmaf(__uint_as_float(x[c][2 * q]), sl2, -mm));
-                        const float p1 = ex2_approx(fmaf(__uint_as_float(x[c][2 * q + 1]), sl2, -mm));
-                        ls[(2 * q) & 7] += p0;
-                        ls[(2 * q + 1) & 7] += p1;
-                        split_pair(p0, p1, ph[q], pl[q]);
+                        const float2 y = f2_unpack(
+                            f2_fma(f2_pack(__uint_as_float(x[c][2 * q]), __uint_as_float(x[c][2 * q + 1])), sl2x2, nmm));
+                        const float p0 = ex2_approx(y.x), p1 = ex2_approx(y.y);
+                        const uint64_t pp = f2_pack(p0, p1);
+                        ls[q & 3] = f2_add(ls[q & 3], pp);
+                        // hi = P with its low 13 mantissa bits cleared, lo = the rest (split_pair)
+                        const float h0 = __uint_as_float(__float_as_uint(p0) & 0xFFFFE000u);
+                        const float h1 = __uint_as_float(__float_as_uint(p1) & 0xFFFFE000u);
+                        ph[q] = f32x2_to_f16x2(h0, h1);
+                        const float2 r = f2_unpack(f2_sub(pp, f2_pack(h0, h1)));
+                        pl[q] = f32x2_to_f16x2(r.x, r.y);
                     }
                     tc::st16(s_tm + 32 * c, ph);
                     tc::st16(s_tm + 32 * c + 16, pl);
                 }
-                return ((ls[0] + ls[1]) + (ls[2] + ls[3])) + ((ls[4] + ls[5]) + (ls[6] + ls[7]));
+                const float2 s0 = f2_unpack(ls[0]), s1 = f2_unpack(ls[1]), s2 = f2_unpack(ls[2]), s3 = f2_unpack(ls[3]);
+                return ((s0.x + s0.y) + (s1.x + s1.y)) + ((s2.x + s2.y) + (s3.x + s3.y));
             };
             // Publish this half's maximum to the other half's warp (same lane
             // quarter).  While it is in flight, compute P with the running
