@@ -154,13 +154,11 @@ pkv_status pkv_kv_calibrate(const void *k_new, const void *v_new, int in_dtype,
 /*
  * Workspace bytes pkv_paged_gqa_decode needs on the current device for a
  * call with these sizes whose seq_lens are all <= max_seq_len (partial
- * softmax states of the split-K pass: one slot per split-K worker and
- * sub-piece of its range, plus one per (sequence, kv head)).  Returns 0 for
- * sizes the library rejects.  max_ctas as in pkv_paged_gqa_decode.  Covers
- * every split the weights of pkv_decode_set_split_weights can give.  Grows
- * with batch * max_seq_len only once the list is longer than about 300
- * chunks of 16 tokens per worker (for example about 61 MB at batch 64, 8 kv
- * heads, G = 8 and 128K tokens on a 152-SM GPU).
+ * softmax states of the split-K pass: one slot per split-K worker plus one
+ * per (sequence, kv head)).  Returns 0 for sizes the library rejects.
+ * max_ctas as in pkv_paged_gqa_decode.  Independent of max_seq_len and of
+ * the split weights (about 8 MB at batch 64, 8 kv heads, G = 8 on a 152-SM
+ * GPU).
  */
 size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
                                  int head_dim, int max_seq_len, int page_size, int max_ctas);
@@ -181,8 +179,9 @@ size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
  * pool pages, and its table entry is the first of them ([N] §3.2: 16-token
  * pages for short sequences, 64-token pages for long ones).  L == 0 gives a
  * zero row.  Long contexts are split across warps (split-K /
- * flash-decoding); no warp accumulates more than 512 chunks of 16 tokens
- * into one partial state, and a second kernel merges the partial softmax
+ * flash-decoding); no warp chains more than 128 chunks of 16 tokens on the
+ * tensor cores (longer ranges fold their accumulator into their partial
+ * state in fp32 every 128 chunks), and a second kernel merges the partial softmax
  * states exactly (log-sum-exp) in a fixed order: results are deterministic
  * run to run and independent of where the pages sit in the pool.  Two kernel
  * launches (the second is a programmatic dependent launch that overlaps the
@@ -195,9 +194,9 @@ size_t pkv_decode_workspace_size(int batch, int num_q_heads, int num_kv_heads,
  *   seq_lens       device int32 [batch]; must satisfy
  *                  0 <= seq_lens[b] <= min(max_seq_len, max_pages_per_seq * P_b)
  *                  (violations set PKV_DEVERR_SEQLEN and are clamped).
- *   max_seq_len    host bound of seq_lens (sizes the workspace); 0 means
- *                  max_pages_per_seq * page_size (pass the real bound when
- *                  seq_page_sizes is given).
+ *   max_seq_len    host bound of seq_lens (lengths above it are clamped
+ *                  and flagged); 0 means max_pages_per_seq * page_size
+ *                  (pass the real bound when seq_page_sizes is given).
  *   seq_page_sizes device int32 [batch] or NULL: tokens per page of each
  *                  sequence, a power of two in [page_size, 256] (others set
  *                  PKV_DEVERR_PAGESIZE and the sequence reads as empty).

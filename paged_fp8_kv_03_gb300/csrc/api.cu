@@ -198,17 +198,14 @@ int decode_num_ctas(int page_size, int batch, int max_ctas)
     return c;
 }
 
-// Workspace for a call whose sequences are at most max_len tokens: header and
-// segment records, then one partial slot per (worker, sub-piece) plus one per
-// segment.  The sub-pieces per worker follow from the largest possible list
-// and the longest range any allowed set of split weights gives (a weight at
-// most kSplitWeightMax / kSplitWeightMin times the smallest).
-size_t decode_workspace_bytes(int batch, int hq, int hkv, long long max_len, int num_ctas)
+// Workspace: header and segment records, then one partial slot per worker
+// plus one per segment (a piece is a worker's range within one segment; its
+// slot is worker + segment, distinct for every piece).  Independent of the
+// sequence lengths.
+size_t decode_workspace_bytes(int batch, int hq, int hkv, long long /*max_len*/, int num_ctas)
 {
     const long long workers = static_cast<long long>(num_ctas) * kWarps;
-    const long long total_max = static_cast<long long>(batch) * hkv * ((max_len + 15) / 16);
-    const long long subs = decode_subs(total_max, kSplitWeightMax, workers * kSplitWeightMin);
-    const size_t slots = static_cast<size_t>(workers * subs) + static_cast<size_t>(batch) * hkv;
+    const size_t slots = static_cast<size_t>(workers) + static_cast<size_t>(batch) * hkv;
     const size_t bytes = slots * static_cast<size_t>(hq / hkv) * kPartialStride * sizeof(float);
     return decode_segment_bytes(batch, hkv) + ((bytes + 255) & ~size_t(255));
 }

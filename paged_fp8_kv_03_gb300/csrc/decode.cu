@@ -21,7 +21,7 @@
 // range cuts segments into
 // pieces; a piece covering a whole segment writes the final output, the
 // others write a partial softmax state (running max m, sum l, unnormalised
-// accumulator) into workspace slot (worker, sub-piece) + segment.  A second kernel, one
+// accumulator) into workspace slot worker + segment.  A second kernel, one
 // CTA per (segment, head) with a thread per dimension, merges the pieces in
 // worker order (deterministic); it is a programmatic dependent launch, so it
 // is already resident when the first kernel's last warps finish.
@@ -202,7 +202,8 @@ struct Smem {
     static constexpr int kBar = kWarps * kWarpRing;         // full[kWarps][kStages]
     static constexpr int kFlag = kBar + kWarps * kStages * 8;   // abort flag
     static constexpr int kWarpSum = kFlag + 16;             // scan scratch (kWarps ints)
-    static constexpr int kPstart = kWarpSum + 32;
+    static constexpr int kFoldM = kWarpSum + 32;            // per warp: the running maximum of each head at its last fold
+    static constexpr int kPstart = kFoldM + kWarps * PKV_MAX_GROUP * 4;
     static size_t bytes(int batch) { return static_cast<size_t>(kPstart) + 4u * (batch + 1) + 1024u; }
 };
 
@@ -491,8 +492,8 @@ __device__ __noinline__ void append_own_tokens(const DecodeArgs &a, const int *p
 // [lo, hi) touches: the worker holding a segment's first chunk writes where
 // the segment lies and whether its pieces need merging (-1: its piece is the
 // whole segment, the output is final), the worker holding its last chunk
-// writes its own index.  Pieces end at a segment's end, the range's end or
-// every kChainChunks chunks of the range, as in the streaming loop.
+// writes its own index.  Pieces end at a segment's end or the range's end,
+// as in the streaming loop.
 __device__ __noinline__ void write_records(const DecodeArgs &a, const int *pstart, int64_t lo, int64_t hi, int worker)
 {
     Loc l = locate(pstart, a.batch, a.hkv, lo);
@@ -500,8 +501,7 @@ __device__ __noinline__ void write_records(const DecodeArgs &a, const int *pstar
     const int64_t n_total = hi - lo;
     while (k < n_total && l.b < a.batch) {
         const int np = chunks_of(pstart, l.b);
-        const int n_piece = static_cast<int>(min(min(static_cast<int64_t>(np - l.ck), n_total - k),
-                                                 static_cast<int64_t>(kChainChunks - (k & (kChainChunks - 1)))));
+        const int n_piece = static_cast<int>(min(static_cast<int64_t>(np - l.ck), n_total - k));
         SegRecord *rec = a.segs + l.b * a.hkv + l.h;
         if (l.ck == 0) {
             rec->start = static_cast<long long>(pstart[l.b]) * a.hkv + static_cast<long long>(l.h) * np;
@@ -594,11 +594,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int worker = blockIdx.x * kWarps + warp;
     const int64_t total = static_cast<int64_t>(pstart[a.batch]) * a.hkv;
     const Split sp = make_split(a, g_split_prefix);
-    const int subs = static_cast<int>(decode_subs(total, a.split ? a.split_wmax : 1, sp.ct));
     if (blockIdx.x == 0 && tid == 0) {
         DecodeHeader hd;
         hd.total = total;
-        hd.subs = subs;
         hd.pad = 0;
         *a.header = hd;
     }
@@ -690,10 +688,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     int k = 0;
     while (k < n_total) {
         const int np = chunks_of(pstart, cons.b);
-        // a piece ends at its segment's end, the worker's range end, or the
-        // next sub-piece cut (every kChainChunks chunks of the range)
-        const int n_piece = min(min(np - cons.ck, n_total - k), kChainChunks - (k & (kChainChunks - 1)));
-        const int slot_index = worker * subs + k / kChainChunks;
+        // a piece ends at its segment's end or the worker's range end
+        const int n_piece = min(np - cons.ck, n_total - k);
+        const int slot_index = worker;
         const int L = seq_len_of(a, cons.b);
         const bool whole = (cons.ck == 0) && (n_piece == np);
         const int seg = cons.b * a.hkv + cons.h;
@@ -717,6 +714,55 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 
         float m_ref = -INFINITY, lsum = 0.f;
         float acc[8][4];
+        // Fold: add the accumulator stored in the piece's slot (if any), rescaled
+        // from the maxima it was stored with to the current ones, into acc; with
+        // store, write acc back as the new fold and restart acc from zero.  Keeps
+        // every tensor-core accumulation chain within kFoldChunks chunks.
+        // folded: the slot already holds a fold (after the first kFoldChunks).
+        auto fold = [&](bool folded, bool store) {
+            const int64_t sidx = static_cast<int64_t>(slot_index) + seg;
+            if (sidx >= a.num_slots) {
+                if (a.err && lane == 0)
+                    atomicOr(a.err, PKV_DEVERR_INTERNAL);
+                return;
+            }
+            float *slot = a.partials + sidx * a.group * kPartialStride;
+            float *fm = reinterpret_cast<float *>(smem + S::kFoldM) + warp * PKV_MAX_GROUP;
+            const float m0 = __shfl_sync(kFull, m_ref, 8 * t4), m1 = __shfl_sync(kFull, m_ref, 8 * t4 + 4);
+            const bool h0 = 2 * t4 < a.group, h1 = 2 * t4 + 1 < a.group;
+            const float f0 = (folded && h0) ? ex2_approx(fm[2 * t4] - m0) : 0.f;
+            const float f1 = (folded && h1) ? ex2_approx(fm[2 * t4 + 1] - m1) : 0.f;
+#pragma unroll
+            for (int sg = 0; sg < 8; ++sg) {
+                float2 *p0 = reinterpret_cast<float2 *>(slot + (2 * t4) * kPartialStride + 16 * sg + 2 * gid);
+                float2 *p1 = reinterpret_cast<float2 *>(slot + (2 * t4 + 1) * kPartialStride + 16 * sg + 2 * gid);
+                if (folded && h0) {
+                    const float2 v = *p0;
+                    acc[sg][0] = fmaf(v.x, f0, acc[sg][0]);
+                    acc[sg][2] = fmaf(v.y, f0, acc[sg][2]);
+                }
+                if (folded && h1) {
+                    const float2 v = *p1;
+                    acc[sg][1] = fmaf(v.x, f1, acc[sg][1]);
+                    acc[sg][3] = fmaf(v.y, f1, acc[sg][3]);
+                }
+                if (store) {
+                    if (h0)
+                        *p0 = make_float2(acc[sg][0], acc[sg][2]);
+                    if (h1)
+                        *p1 = make_float2(acc[sg][1], acc[sg][3]);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        acc[sg][c] = 0.f;
+                }
+            }
+            if (store) {
+                __syncwarp();                    // every lane has read the old maxima
+                if (t4 == 0 && gid < a.group)
+                    fm[gid] = m_ref;
+                __syncwarp();
+            }
+        };
 #pragma unroll
         for (int sg = 0; sg < 8; ++sg)
 #pragma unroll
@@ -751,7 +797,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 else
                     process_tile<true>(fr, nv, qa, scale2, m_ref, lsum, acc, lane);
             }
+            if (((j + 1) % kFoldChunks) == 0 && j + 1 < n_piece)
+                fold(j + 1 > kFoldChunks, true);
         }
+        if (n_piece > kFoldChunks)
+            fold(true, false);
 
         // ---- end of piece
         lsum += __shfl_xor_sync(kFull, lsum, 1);
@@ -812,11 +862,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 // batch into the running (M, L, A).  The order is fixed, so results are
 // deterministic.
 //
-// Where a segment's pieces are: with one sub-piece per worker range
-// (subs == 1) and no empty range, piece i was written by worker w0 + i and the
-// last one by w1; otherwise (a range cut every kChainChunks chunks, or ranges
-// of no chunk when the list is shorter than the workers' shares) the pieces are
-// walked worker by worker.
+// Where a segment's pieces are: with no empty range, piece i was written by
+// worker w0 + i and the last one by w1; otherwise (ranges of no chunk when the
+// list is shorter than the workers' shares) the pieces are walked worker by
+// worker, skipping the empty ranges.
 constexpr int kMergeBatch = 16;
 
 __global__ void __launch_bounds__(32 * PKV_MAX_GROUP) splitk_merge_kernel(const DecodeArgs a)
@@ -834,12 +883,11 @@ __global__ void __launch_bounds__(32 * PKV_MAX_GROUP) splitk_merge_kernel(const 
     if (r.n <= 0 || r.w0 < 0)
         return;
     const int64_t total = hd.total;
-    const int subs = hd.subs;
     const Split sp = make_split(a, pre_s);
     const int b = seg / a.hkv, h = seg % a.hkv;
     // every range holds at least one chunk-head when T * wmin >= CT
     const bool dense = total * (a.split ? a.split_wmin : 1) >= sp.ct;
-    const bool walk = subs > 1 || !dense;
+    const bool walk = !dense;
     const int n_known = r.w1 - r.w0 + 1;
     // walk state: worker w, its range [lo_w, hi_w), offset k of the next piece in it
     const int64_t end = r.start + r.n;
@@ -864,17 +912,14 @@ __global__ void __launch_bounds__(32 * PKV_MAX_GROUP) splitk_merge_kernel(const 
             nb = 0;
             while (nb < kMergeBatch && lo_w + k < end) {
                 if (lane == nb)
-                    my_slot = w * subs + static_cast<int>(k / kChainChunks);
+                    my_slot = w;
                 ++nb;
-                k = (k / kChainChunks + 1) * kChainChunks;          // next sub-piece of this worker
-                if (lo_w + k >= hi_w) {                              // next worker with chunks: starts at its range start
-                    do {
-                        ++w;
-                        lo_w = hi_w;
-                        hi_w = range_lo(sp, total, w + 1);
-                    } while (hi_w <= lo_w && lo_w < end);
-                    k = 0;
-                }
+                do {                                                 // next worker with chunks: starts at its range start
+                    ++w;
+                    lo_w = hi_w;
+                    hi_w = range_lo(sp, total, w + 1);
+                } while (hi_w <= lo_w && lo_w < end);
+                k = 0;
             }
             if (nb == 0)
                 break;

@@ -37,11 +37,12 @@ struct AppendArgs {
     int32_t *err;
 };
 
-// Longest chain of 16-token chunks one decode worker accumulates into one
-// partial state: a worker whose range is longer cuts it into sub-pieces at
-// every kChainChunks chunks of its range (the tensor cores' fp32 accumulation
-// rounds toward zero, so error would otherwise grow with the chain).
-constexpr int kChainChunks = 512;
+// Longest chain of 16-token chunks a decode worker accumulates on the tensor
+// cores: every kFoldChunks chunks of a piece it adds its accumulator into the
+// piece's partial-state slot in fp32 (round to nearest) and restarts it from
+// zero (the tensor cores' fp32 accumulation rounds toward zero, so the error
+// of one unbroken chain grows with its length).
+constexpr int kFoldChunks = 128;
 
 // Weighted split.  Worker warp w = 4c + j of CTA c takes a share of the
 // chunk-head list proportional to its CTA's weight (an integer in
@@ -59,8 +60,7 @@ constexpr int kSplitWeightMax = 160;
 // then the partial-state slots.
 struct DecodeHeader {
     long long total;                // chunk-heads in the list (all segments)
-    int subs;                       // sub-pieces per worker range: ceil(max range length / kChainChunks)
-    int pad;
+    long long pad;
 };
 struct SegRecord {
     long long start;                // list position of the segment's first chunk-head
@@ -94,7 +94,7 @@ struct DecodeArgs {
     DecodeHeader *header;           // workspace header (written by CTA 0)
     SegRecord *segs;                // [batch * hkv] segment records (written by the workers holding a
                                     // segment's first and last chunk)
-    float *partials;                // [num_ctas * kWarps * subs + batch * hkv][group][kPartialStride]
+    float *partials;                // [num_ctas * kWarps + batch * hkv][group][kPartialStride]: slot worker + segment
     int32_t *err;
     int num_ctas;
     int withhold_worker;            // failure-detection test hook (-1 = off)
@@ -171,17 +171,6 @@ inline size_t prefill_workspace_bytes(int batch, int hkv, int max_kv_len, long l
 inline size_t decode_segment_bytes(int batch, int hkv)
 {
     return (sizeof(DecodeHeader) + static_cast<size_t>(batch) * hkv * sizeof(SegRecord) + 255) & ~size_t(255);
-}
-
-// Sub-pieces per worker range for a list of `total` chunk-heads: no range is
-// longer than ceil(total * wmax / ct) chunks (wmax the largest weight, ct =
-// C(workers); even split: wmax = 1, ct = workers), and a range is cut every
-// kChainChunks of them.  At least 1.
-inline __host__ __device__ long long decode_subs(long long total, long long wmax, long long ct)
-{
-    const long long per = (total * wmax + ct - 1) / ct;
-    const long long s = (per + kChainChunks - 1) / kChainChunks;
-    return s < 1 ? 1 : s;
 }
 
 // ---------------------------------------------------------------- page walk

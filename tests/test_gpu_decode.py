@@ -201,15 +201,15 @@ def test_full_size_configs_sampled(pkv, cuda_device, cfg, page, n_bh, layer, dyn
 
 
 @pytest.mark.parametrize("lens,hq,hkv,page,ctas", [
-    ([8200, 8200, 3000, 9000], 16, 2, 16, 1),     # about 890 chunks per worker: 2 sub-pieces
-    ([16384] * 4, 8, 2, 32, 1),                  # 2048 chunks per worker: 4 sub-pieces
+    ([8200, 8200, 3000, 9000], 16, 2, 16, 1),     # about 890 chunks per worker: 6 folds
+    ([16384] * 4, 8, 2, 32, 1),                  # 2048 chunks per worker: 15 folds
     ([16384, 40, 16384, 1, 12000], 32, 8, 16, 3),
 ])
-def test_accumulation_chain_is_cut_into_sub_pieces(pkv, cuda_device, lens, hq, hkv, page, ctas):
-    """With few workers each one's range spans thousands of chunks; it is cut
-    every 512 chunks into separately accumulated partial states, which the
-    merge kernel folds with the other workers' pieces.  All rows against the
-    oracle, the same calls with many workers alike."""
+def test_accumulation_chain_is_folded(pkv, cuda_device, lens, hq, hkv, page, ctas):
+    """With few workers each one's range spans thousands of chunks; every 128
+    chunks a worker adds its tensor-core accumulator into its piece's slot in
+    fp32 and restarts it, so no accumulation chain is longer than 128 chunks.
+    All rows against the oracle, the same calls with many workers alike."""
     wl = workloads.Workload(54, "chain", lens, 0, hq, hkv, page, pool_factor=1.2, seed=23)
     f = fill_gpu(wl, 0, cuda_device)
     ref = _full_oracle(wl, f)

@@ -3,9 +3,10 @@ sequences of 128K tokens on the Llama-3-70B attention geometry (64 query / 8
 kv heads), 34 GB of FP8 K and V.  Spread over the persistent grid's workers
 that is about 4500 chunks of 16 tokens per worker, where one unbroken
 tensor-core accumulation chain would drift (its fp32 accumulation rounds
-toward zero); the kernel cuts each worker's range every 512 chunks, so the
-sampled rows must stay within max-abs 1e-4 of the oracle, well inside the
-2e-3 bound."""
+toward zero); every 128 chunks a worker adds its accumulator into its
+partial state in fp32 and restarts it, so the sampled rows must stay within
+max-abs 1e-4 of the oracle, well inside the 2e-3 bound, with the even split
+and with calibrated split weights alike."""
 import numpy as np
 import pytest
 import torch
@@ -35,5 +36,21 @@ def test_batch_128_at_128k_sampled_rows(pkv, cuda_device):
     max_abs, rel = errors(g, r)
     print(f"batch 128 x 128K: max_abs {max_abs:.3e} rel_l2 {rel:.3e}")
     assert max_abs <= 1e-4, max_abs
+    # the same with calibrated split weights (uneven ranges, their own cuts)
+    ws = pkv.decode_workspace(wl.batch, wl.hq, wl.hkv, wl.page_size, cuda_device, 0, f.max_len)
+    try:
+        w = pkv.pkv_decode_calibrate_split(f.q, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, out, ws, rounds=1,
+                                           max_seq_len=f.max_len)
+        assert len(w) > 0
+        out_w = pkv.paged_gqa_decode(f.q, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, out_dtype=torch.float32,
+                                     device_error=f.err, max_seq_len=f.max_len, workspace=ws)
+        torch.cuda.synchronize()
+        assert int(f.err.item()) == 0
+        gw = np.stack([out_w.double().cpu().numpy()[b, i] for (b, i) in pairs])
+        max_abs_w, rel_w = errors(gw, r)
+        print(f"batch 128 x 128K, calibrated split: max_abs {max_abs_w:.3e} rel_l2 {rel_w:.3e}")
+        assert max_abs_w <= 1e-4, max_abs_w
+    finally:
+        pkv.pkv_decode_set_split_weights(None)
     del f
     torch.cuda.empty_cache()

@@ -4,9 +4,9 @@ Per-CTA weights change only how the list of chunks is cut among the workers,
 never the math: outputs stay within the tolerance of the oracle (max-abs <=
 2e-3, rel-L2 <= 1e-3), pages written by the fused append are bit-identical,
 equal weights reproduce the even split bit for bit, and weights installed
-for another grid size are ignored.  Covers ranges cut into sub-pieces
-(longer than 512 chunks) and lists shorter than the workers' shares (empty
-ranges).
+for another grid size are ignored.  Covers ranges long enough to fold their
+accumulator (more than 128 chunks) and lists shorter than the workers'
+shares (empty ranges).
 """
 import numpy as np
 import pytest
@@ -86,9 +86,9 @@ def test_lists_shorter_than_the_shares(pkv, cuda_device):
         assert_close(_decode(pkv, f, max_ctas=50).double().cpu().numpy(), ref, f"seed={seed}")
 
 
-def test_long_ranges_cut_into_sub_pieces(pkv, cuda_device):
+def test_long_ranges_fold_their_accumulators(pkv, cuda_device):
     """Two CTAs at weights 96 and 160: the second CTA's warps take about 680
-    chunks each, cut at 512."""
+    chunks each, folded every 128."""
     wl = workloads.Workload(64, "long", [40000, 30000], 0, 8, 1, 16, seed=9)
     f = fill_gpu(wl, 0, cuda_device)
     ref = _full_oracle(wl, f)
