@@ -367,8 +367,28 @@ def run_gpu(args, rank, world):
     out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     h2d = seq_stage.nbytes + per_step * host[0].nbytes
     d2h = per_step * out.numel() * out.element_size()
+    # As a serving loop would, the copies run on their own streams: layer
+    # pass g+1's inputs cross while pass g computes, pass g-1's output while
+    # pass g computes; events guard every reuse of a staging or output buffer.
+    s_in = torch.cuda.Stream(dev)
+    s_out = torch.cuda.Stream(dev)
+    outs = [out, torch.empty_like(out)]
+    read_done = [None] * n_layers      # compute finished with staging buffer g % n_layers
+    seq_done = [None]                  # compute finished with the step's block table and lengths
+    out_free = [None, None]            # output buffer's copy to the host finished
 
-    def e2e_step(i):
+    def upload(g):
+        with torch.cuda.stream(s_in):
+            if read_done[g % n_layers] is not None:
+                s_in.wait_event(read_done[g % n_layers])
+            d = host[g % n_layers].upload(dev)
+            ready = torch.cuda.Event()
+            ready.record(s_in)
+        return d, ready
+
+    def e2e_step_serial(i):
+        # One layer pass per step: its copies and its compute depend on one
+        # another, so there is nothing to overlap; all on the compute stream.
         sq = seq_stage.upload(dev)
         for l in range(per_step):
             g = i * per_step + l
@@ -386,14 +406,60 @@ def run_gpu(args, rank, world):
                                          device_error=err, max_seq_len=max_len, seq_page_sizes=d.get("psz"))
             out_host.copy_(out, non_blocking=True)
 
+    def e2e_step(i):
+        if per_step == 1:
+            return e2e_step_serial(i)
+        with torch.cuda.stream(s_in):
+            if seq_done[0] is not None:
+                s_in.wait_event(seq_done[0])
+            sq = seq_stage.upload(dev)
+            sq_ready = torch.cuda.Event()
+            sq_ready.record(s_in)
+        stream.wait_event(sq_ready)
+        nxt = upload(i * per_step)
+        for l in range(per_step):
+            g = i * per_step + l
+            c = layers[g % n_layers]
+            d, ready = nxt
+            stream.wait_event(ready)
+            d = dict(d, **sq)
+            ob = outs[g % 2]
+            if out_free[g % 2] is not None:
+                stream.wait_event(out_free[g % 2])
+            if "k_new" in d and args.separate:
+                pkv.pkv_kv_append_fp8(d["k_new"].flatten(0, 1), d["v_new"].flatten(0, 1), d["slots"], c["ks"],
+                                      c["vs"], c["kc"], c["vc"], err)
+            if "k_new" in d and not args.separate:
+                pkv.pkv_append_decode_fp8(d["k_new"], d["v_new"], d["q"], c["kc"], c["vc"], c["ks"], c["vs"],
+                                          d["bt"], d["lens"], ob, ws, device_error=err, max_seq_len=max_len,
+                                          seq_page_sizes=d.get("psz"))
+            else:
+                pkv.pkv_paged_gqa_decode(d["q"], c["kc"], c["vc"], c["ks"], c["vs"], d["bt"], d["lens"], ob, ws,
+                                         device_error=err, max_seq_len=max_len, seq_page_sizes=d.get("psz"))
+            done = torch.cuda.Event()
+            done.record(stream)
+            read_done[g % n_layers] = done
+            if l + 1 < per_step:
+                nxt = upload(g + 1)                    # crosses while pass g computes
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(done)
+                out_host.copy_(ob, non_blocking=True)
+                freed = torch.cuda.Event()
+                freed.record(s_out)
+            out_free[g % 2] = freed
+        seq_done[0] = done
+
     for i in range(3):
         e2e_step(i)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
+    s_in.wait_event(e0)                                # no copy starts before the timed region
     for i in range(e2e_steps):
         e2e_step(i)
+    if per_step > 1:
+        stream.wait_event(out_free[(e2e_steps * per_step - 1) % 2])   # the last output is on the host
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
