@@ -350,6 +350,34 @@ def run_gpu(args, rank, world):
     total_ms = max_over_ranks(total_ms, world, dev)
     assert int(err.item()) == 0, f"device error word {int(err.item())}"
 
+    # ---- kv_append_fp8 alone: one layer pass's new tokens (B x append rows of
+    # every kv head) quantised into their pages, as the two-call path issues
+    # it; the same rows rewrite the same bytes, so repeating it changes nothing.
+    append_us = None
+    if steps_in[0]["k_new"] is not None:
+        c0, s0 = layers[0], steps_in[0]
+        kf, vf = s0["k_new"].flatten(0, 1), s0["v_new"].flatten(0, 1)
+        for _ in range(20):
+            pkv.pkv_kv_append_fp8(kf, vf, s0["slots"], c0["ks"], c0["vs"], c0["kc"], c0["vc"], err)
+        # The launches are enqueued behind a GPU spin longer than the host
+        # needs to enqueue them, so they run back to back: the events time
+        # the GPU, not the host's pace (a lone small launch would be timed
+        # with the binding's host work inside it).
+        n_app = 200
+        torch.cuda.synchronize()
+        torch.cuda._sleep(int(2e7))
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(n_app):
+            pkv.pkv_kv_append_fp8(kf, vf, s0["slots"], c0["ks"], c0["vs"], c0["kc"], c0["vc"], err)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        append_us = {"us_per_call": round(1e3 * a0.elapsed_time(a1) / n_app, 3),
+                     "calls": n_app, "tokens": int(kf.shape[0]), "kv_heads": wl.hkv,
+                     "note": "kv_append_fp8 alone on one layer pass's new rows, launches back to back (in the "
+                             "timed step the append is fused into the decode launch unless --separate)"}
+
     # ---- end to end through the public API with host buffers
     e2e_steps = min(args.steps, args.e2e_steps)
     # The step's block table and lengths cross once per step; each layer
@@ -502,7 +530,8 @@ def run_gpu(args, rank, world):
                      "achieved": round(achieved, 2), "peak": peak, "peak_kind": peak_kind,
                      "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": traffic, "algorithmic_bytes_per_launch": kv_bytes,
-                     "avg_launch_us": round(dec_ms * 1e3, 3)},
+                     "avg_launch_us": round(dec_ms * 1e3, 3),
+                     "median_launch_us": round(statistics.median(decode_ms) * 1e3, 3)},
         "e2e": {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": "GB/s",
                 "ms_per_step": round(e2e_ms, 6), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
@@ -513,6 +542,8 @@ def run_gpu(args, rank, world):
                          "the timed loop's enqueue time also includes waiting on a full launch queue"},
         "clocks": clk,
     }
+    if append_us is not None:
+        line["kv_append_fp8"] = append_us
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds, gen_device=dev)
     if rank == 0:
