@@ -868,16 +868,23 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 // worker, skipping the empty ranges.
 constexpr int kMergeBatch = 16;
 
-__global__ void __launch_bounds__(32 * PKV_MAX_GROUP) splitk_merge_kernel(const DecodeArgs a)
+// kSub warps per query head: with segments of many pieces (few segments
+// against many workers) the warps of a head take turns over the batches and
+// their states are combined in shared memory at the end, in sub-warp order.
+template <int kSub>
+__global__ void __launch_bounds__(32 * PKV_MAX_GROUP * kSub) splitk_merge_kernel(const DecodeArgs a)
 {
     __shared__ uint32_t pre_s[kMaxSplitCtas + 1];
+    __shared__ __align__(16) float red_a[kSub > 1 ? PKV_MAX_GROUP * kSub : 1][32 * 4];   // read and written as float4
+    __shared__ float red_ml[kSub > 1 ? PKV_MAX_GROUP * kSub : 1][2];
     if (a.split) {                               // the split's weight prefix sums (inputs, not the decode's output)
         for (int c = threadIdx.x; c <= a.num_ctas; c += blockDim.x)
             pre_s[c] = g_split_prefix[c];
         __syncthreads();
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid has finished
-    const int seg = blockIdx.x, g = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int seg = blockIdx.x, wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = wi / kSub, sub = wi % kSub;
     const SegRecord r = a.segs[seg];
     const DecodeHeader hd = *a.header;
     if (r.n <= 0 || r.w0 < 0)
@@ -898,7 +905,8 @@ __global__ void __launch_bounds__(32 * PKV_MAX_GROUP) splitk_merge_kernel(const 
 
     float M = -INFINITY, L = 0.f;
     float A[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int i0 = 0;; i0 += kMergeBatch) {
+    // the walk (empty ranges in the list) is sequential: sub-warp 0 alone
+    for (int i0 = sub * kMergeBatch; walk ? sub == 0 : true; i0 += kSub * kMergeBatch) {
         // slot of piece i0 + lane (lanes >= the batch size: -1)
         int my_slot = -1;
         int nb;
@@ -969,6 +977,36 @@ __global__ void __launch_bounds__(32 * PKV_MAX_GROUP) splitk_merge_kernel(const 
         }
         M = mn;
     }
+    if constexpr (kSub > 1) {
+        *reinterpret_cast<float4 *>(&red_a[wi][4 * lane]) = make_float4(A[0], A[1], A[2], A[3]);
+        if (lane == 0) {
+            red_ml[wi][0] = M;
+            red_ml[wi][1] = L;
+        }
+        __syncthreads();
+        if (sub != 0)
+            return;
+        float Mt = M;
+#pragma unroll
+        for (int s2 = 1; s2 < kSub; ++s2)
+            Mt = fmaxf(Mt, red_ml[wi + s2][0]);
+        const float r0 = ex2_approx(M - Mt);
+        L *= r0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+            A[c] *= r0;
+#pragma unroll
+        for (int s2 = 1; s2 < kSub; ++s2) {
+            const float ms = red_ml[wi + s2][0];
+            const float rs = ms == -INFINITY ? 0.f : ex2_approx(ms - Mt);   // a sub-warp with no pieces adds nothing
+            const float4 as = *reinterpret_cast<const float4 *>(&red_a[wi + s2][4 * lane]);
+            L += red_ml[wi + s2][1] * rs;
+            A[0] += as.x * rs;
+            A[1] += as.y * rs;
+            A[2] += as.z * rs;
+            A[3] += as.w * rs;
+        }
+    }
     const float f = __ldg(a.v_scale + h) / L;
     const int64_t row = static_cast<int64_t>(b) * a.hq + static_cast<int64_t>(h) * a.group + g;
     store_pair(a, row, 4 * lane, A[0] * f, A[1] * f);
@@ -998,8 +1036,12 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, co
         return e;
     *site = "split-K merge kernel launch";
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(a.batch * a.hkv), 1, 1);
-    cfg.blockDim = dim3(static_cast<unsigned>(32 * a.group), 1, 1);
+    // Two warps per query head when the segments average 32 pieces or more
+    // (few long segments against many workers: at least two batches each).
+    const int segs = a.batch * a.hkv;
+    const bool wide = static_cast<long long>(a.num_ctas) * kWarps >= 32ll * segs;
+    cfg.gridDim = dim3(static_cast<unsigned>(segs), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * a.group * (wide ? 2 : 1)), 1, 1);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -1007,7 +1049,7 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, co
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, splitk_merge_kernel, a);
+    return wide ? cudaLaunchKernelEx(&cfg, splitk_merge_kernel<2>, a) : cudaLaunchKernelEx(&cfg, splitk_merge_kernel<1>, a);
 }
 
 cudaError_t upload_split_prefix(const uint32_t *prefix, int n)
