@@ -303,7 +303,9 @@ pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dt
 pkv_status pkv_decode_set_split_weights(const uint8_t *weights, int n);
 /*
  * The CUDA runtime error (cudaError_t value) behind the calling thread's last
- * PKV_ERR_CUDA status, 0 if none, and its name in *name (if name is given).
+ * PKV_ERR_CUDA status, 0 if none; with name given, *name points to a text
+ * naming the error and the call that failed (owned by the library, valid
+ * until the thread's next pkv_last_cuda_error call).
  */
 int pkv_last_cuda_error(const char **name);
 pkv_status pkv_decode_get_split_weights(uint8_t *weights, int capacity, int *n);
