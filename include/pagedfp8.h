@@ -383,7 +383,7 @@ size_t pkv_decode_noalloc_scratch_bytes(void);
  * into the workspace, packed sequence after sequence, then the attention
  * runs on the tcgen05 tensor cores (q K^T on bf16 operands; the softmax
  * weights as two f16 parts against f16 V; fp32 accumulation, the PV
- * accumulator added into a second fp32 accumulator every 16 key tiles).
+ * accumulator added into a second fp32 accumulator every 32 key tiles).
  * Deterministic.
  *
  *   q              device bf16 [total_q][num_q_heads][head_dim], 16-byte

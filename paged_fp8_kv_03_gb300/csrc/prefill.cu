@@ -64,7 +64,7 @@ namespace {
 constexpr int kRows = 128;                       // M: rows of a query tile
 constexpr int kKeys = 128;                       // keys per tile
 constexpr int kKStages = 2, kVStages = 3;        // operand rings: K bf16, V f16
-constexpr int kFold = 16;                        // key tiles per tensor-core accumulation segment of O
+constexpr int kFold = 32;                        // key tiles per tensor-core accumulation segment of O
 constexpr int kSmWarp0 = 2;                      // first softmax warp
 constexpr int kSmWarps = 8;
 constexpr int kPThreads = 32 * (kSmWarp0 + kSmWarps);

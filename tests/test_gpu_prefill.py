@@ -232,9 +232,10 @@ def test_full_size_last_16k_chunk_of_128k_sampled(pkv, cuda_device):
         assert_close(got[r, i][None], row[None], f"row {r} head {i}")
     # The tensor cores' fp32 accumulation rounds toward zero; one accumulator
     # chained over the whole 128K context drifted to max-abs 1.1e-3 on these
-    # inputs.  Folding it every 16 key tiles keeps the drift under 1e-4, well
+    # inputs.  Folding it every 32 key tiles keeps the drift under 1e-4, well
     # inside the bound above: hold the kernel to that.
-    max_abs, _ = errors(np.stack([got[r, i] for (r, i) in ref]), np.stack(list(ref.values())))
+    max_abs, rel = errors(np.stack([got[r, i] for (r, i) in ref]), np.stack(list(ref.values())))
+    print(f"prefill, last 16K chunk of a 128K prompt: max_abs {max_abs:.3e} rel_l2 {rel:.3e}")
     assert max_abs <= 3e-4, max_abs
     assert torch.isfinite(out).all()
 
