@@ -974,7 +974,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-calibrate", action="store_true",
                     help="decode: keep the even split (no per-CTA split weights)")
-    ap.add_argument("--calibrate-rounds", type=int, default=4)
+    ap.add_argument("--calibrate-rounds", type=int, default=6)
     ap.add_argument("--graph", action="store_true", help="replay each step from a captured CUDA graph")
     ap.add_argument("--separate", action="store_true",
                     help="time kv_append_fp8 and paged_gqa_decode as two calls instead of the fused step")

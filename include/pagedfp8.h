@@ -279,28 +279,30 @@ pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dt
  * deterministic for fixed weights.
  *
  * pkv_decode_set_split_weights installs n weights, each an integer in
- * [96, 160], for the current device; they apply to decode calls
+ * [768, 1280] (1024 +- 25%), for the current device; they apply to decode calls
  * (pkv_paged_gqa_decode, pkv_append_decode_fp8 and the allocation-free entry
  * point) whose grid has exactly n CTAs, and the others split evenly.  n == 0
  * removes them.  Copies n + 1 integers to device memory the decode kernels
  * read, synchronously: do not call it while a decode call is in flight on
  * the device, or during stream capture.  Errors: PKV_ERR_SHAPE (n outside
- * [0, 1024] or a weight outside [96, 160]), PKV_ERR_NULL, PKV_ERR_CUDA.
+ * [0, 1024] or a weight outside [768, 1280]), PKV_ERR_NULL, PKV_ERR_CUDA.
  *
  * pkv_decode_get_split_weights copies the current device's weights to
  * weights[0 .. *n) (*n = 0: none; PKV_ERR_SHAPE if *n > capacity).
  *
  * pkv_decode_calibrate_split measures them: it runs `rounds` (1..64) times
- * three decode calls with the given arguments (as pkv_paged_gqa_decode; out
+ * four decode calls with the given arguments (as pkv_paged_gqa_decode; out
  * and workspace are written, max_ctas sets the grid), each timed per CTA
- * with the global timer, synchronising `stream` after each, and moves every
- * CTA's weight towards the share it streams in the time all CTAs take
- * together.  Starts from equal weights, leaves the result installed (and
+ * with the global timer, synchronising `stream` after each; every round
+ * sets each CTA's weight to the share it streams in the time all CTAs take
+ * together, and the result is the average of the rounds after the first
+ * (the first moves the weights from equal to near the balance).  Starts
+ * from equal weights, leaves the result installed (and
  * copies it to weights_out[0 .. n), if weights_out is given, with n in
  * *n_out).  On an error the device's weights are removed.  A setup-time
  * call: a few ms of GPU time plus host synchronisation; not capturable.
  */
-pkv_status pkv_decode_set_split_weights(const uint8_t *weights, int n);
+pkv_status pkv_decode_set_split_weights(const uint16_t *weights, int n);
 /*
  * The CUDA runtime error (cudaError_t value) behind the calling thread's last
  * PKV_ERR_CUDA status, 0 if none; with name given, *name points to a text
@@ -308,7 +310,7 @@ pkv_status pkv_decode_set_split_weights(const uint8_t *weights, int n);
  * until the thread's next pkv_last_cuda_error call).
  */
 int pkv_last_cuda_error(const char **name);
-pkv_status pkv_decode_get_split_weights(uint8_t *weights, int capacity, int *n);
+pkv_status pkv_decode_get_split_weights(uint16_t *weights, int capacity, int *n);
 pkv_status pkv_decode_calibrate_split(const void *q,
                                       const uint8_t *k_cache, const uint8_t *v_cache,
                                       const float *k_scale, const float *v_scale,
@@ -319,7 +321,7 @@ pkv_status pkv_decode_calibrate_split(const void *q,
                                       int page_size, int64_t num_pages, float sm_scale,
                                       void *out, int out_dtype,
                                       void *workspace, size_t workspace_bytes, int max_ctas,
-                                      int rounds, uint8_t *weights_out, int capacity, int *n_out,
+                                      int rounds, uint16_t *weights_out, int capacity, int *n_out,
                                       cudaStream_t stream);
 
 /*

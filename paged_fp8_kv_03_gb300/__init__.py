@@ -121,13 +121,13 @@ def pkv_read_device_error(device_error, clear: bool = False, stream=None) -> int
 
 
 def pkv_decode_set_split_weights(weights, device=None) -> None:
-    """Install per-CTA split weights (ints in [96, 160]) for decode calls on
+    """Install per-CTA split weights (ints in [768, 1280]) for decode calls on
     `device` (default: the current one) whose grid has len(weights) CTAs;
     None or an empty sequence removes them (even split)."""
-    w = bytes(int(x) for x in (weights if weights is not None else []))
-    if any(x > 255 for x in (weights if weights is not None else [])):
-        raise PkvError(1, "pkv_decode_set_split_weights")
-    buf = (ctypes.c_uint8 * max(1, len(w))).from_buffer_copy(w if w else b"\0")
+    w = [int(x) for x in (weights if weights is not None else [])]
+    if any(x < 0 or x > 0xFFFF for x in w):
+        raise PkvError(2, "pkv_decode_set_split_weights")
+    buf = (ctypes.c_uint16 * max(1, len(w)))(*w)
     with _device_of_index(device):
         st = load().pkv_decode_set_split_weights(ctypes.addressof(buf), len(w))
     if st != 0:
@@ -137,7 +137,7 @@ def pkv_decode_set_split_weights(weights, device=None) -> None:
 def pkv_decode_get_split_weights(device=None) -> list:
     """The split weights installed for `device` (empty: even split)."""
     cap = 1024
-    buf = (ctypes.c_uint8 * cap)()
+    buf = (ctypes.c_uint16 * cap)()
     n = ctypes.c_int(0)
     with _device_of_index(device):
         st = load().pkv_decode_get_split_weights(ctypes.addressof(buf), cap, ctypes.byref(n))
@@ -147,10 +147,10 @@ def pkv_decode_get_split_weights(device=None) -> list:
 
 
 def pkv_decode_calibrate_split(q, k_cache, v_cache, k_scale, v_scale, block_table, seq_lens, out, workspace,
-                               sm_scale=None, max_ctas=0, rounds=4, stream=None, max_seq_len=0,
+                               sm_scale=None, max_ctas=0, rounds=6, stream=None, max_seq_len=0,
                                seq_page_sizes=None) -> list:
     """Measure and install split weights for decode calls shaped like this
-    one (runs 3 * rounds decode calls on these inputs, writing out and
+    one (runs 4 * rounds decode calls on these inputs, writing out and
     workspace, and synchronises the stream).  Returns the weights."""
     _need(q, "q", torch.bfloat16, 3)
     _need(k_cache, "k_cache", torch.uint8, 4)
@@ -172,7 +172,7 @@ def pkv_decode_calibrate_split(q, k_cache, v_cache, k_scale, v_scale, block_tabl
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(D)
     cap = 1024
-    buf = (ctypes.c_uint8 * cap)()
+    buf = (ctypes.c_uint16 * cap)()
     n = ctypes.c_int(0)
     with _device_of(q):
         st = load().pkv_decode_calibrate_split(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(k_scale), _ptr(v_scale),

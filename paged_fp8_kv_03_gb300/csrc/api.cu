@@ -28,7 +28,7 @@ std::atomic<int> g_withhold{-1};                            // failure-detection
 // Weighted split of each device: the per-CTA weights for one grid size (the
 // prefix sums live in the decode module's device table).  Absent: even split.
 struct SplitState {
-    std::vector<uint8_t> weights;
+    std::vector<uint16_t> weights;
     long long ct = 0;                                       // 4 * sum of the weights
     int wmin = 0, wmax = 0;
 };
@@ -348,7 +348,7 @@ pkv_status decode_impl(const void *k_new, const void *v_new, int in_dtype, int n
 
 // Installs weights (n of them, each in [kSplitWeightMin, kSplitWeightMax]) for
 // the current device; n == 0 removes them (even split).
-pkv_status set_split(const uint8_t *weights, int n)
+pkv_status set_split(const uint16_t *weights, int n)
 {
     if (n < 0 || n > kMaxSplitCtas || (n > 0 && !weights))
         return n < 0 || n > kMaxSplitCtas ? PKV_ERR_SHAPE : PKV_ERR_NULL;
@@ -518,7 +518,7 @@ pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dt
                        workspace_bytes, device_error, max_ctas, stream);
 }
 
-pkv_status pkv_decode_set_split_weights(const uint8_t *weights, int n)
+pkv_status pkv_decode_set_split_weights(const uint16_t *weights, int n)
 {
     return set_split(weights, n);
 }
@@ -534,7 +534,7 @@ int pkv_last_cuda_error(const char **name)
     return t_last_cuda;
 }
 
-pkv_status pkv_decode_get_split_weights(uint8_t *weights, int capacity, int *n)
+pkv_status pkv_decode_get_split_weights(uint16_t *weights, int capacity, int *n)
 {
     if (!n || capacity < 0 || (capacity > 0 && !weights))
         return PKV_ERR_NULL;
@@ -558,7 +558,7 @@ pkv_status pkv_decode_calibrate_split(const void *q, const uint8_t *k_cache, con
                                       const int32_t *seq_page_sizes, int batch, int num_q_heads, int num_kv_heads,
                                       int head_dim, int page_size, int64_t num_pages, float sm_scale, void *out,
                                       int out_dtype, void *workspace, size_t workspace_bytes, int max_ctas,
-                                      int rounds, uint8_t *weights_out, int capacity, int *n_out,
+                                      int rounds, uint16_t *weights_out, int capacity, int *n_out,
                                       cudaStream_t stream)
 {
     if (rounds < 1 || rounds > 64)
@@ -573,10 +573,16 @@ pkv_status pkv_decode_calibrate_split(const void *q, const uint8_t *k_cache, con
         return PKV_ERR_CUDA;
     if (ctas > kMaxSplitCtas)
         return PKV_ERR_UNSUPPORTED;
-    constexpr int kCallsPerRound = 3;
+    constexpr int kCallsPerRound = 4;
     constexpr double kMean = 0.5 * (kSplitWeightMin + kSplitWeightMax);
-    std::vector<uint8_t> w(static_cast<size_t>(ctas), static_cast<uint8_t>(kMean));
+    auto quantise = [](double v) {
+        v = v < kSplitWeightMin ? kSplitWeightMin : (v > kSplitWeightMax ? kSplitWeightMax : v);
+        return static_cast<uint16_t>(v + 0.5);
+    };
+    std::vector<double> wd(static_cast<size_t>(ctas), kMean), avg(static_cast<size_t>(ctas), 0.0);
+    std::vector<uint16_t> w(static_cast<size_t>(ctas), quantise(kMean));
     std::vector<unsigned long long> times(static_cast<size_t>(ctas) * 2);
+    int n_avg = 0;
     pkv_status st = set_split(w.data(), ctas);
     for (int r = 0; r < rounds && st == PKV_OK; ++r) {
         // Finish (F) and start (S) of every CTA, relative to the first CTA's start.
@@ -626,10 +632,25 @@ pkv_status pkv_decode_calibrate_split(const void *q, const uint8_t *k_cache, con
             sum += nw[c];
         }
         for (int c = 0; c < ctas; ++c) {
-            double v = sum > 0.0 ? nw[c] * kMean * ctas / sum : kMean;
-            v = v < kSplitWeightMin ? kSplitWeightMin : (v > kSplitWeightMax ? kSplitWeightMax : v);
-            w[c] = static_cast<uint8_t>(v + 0.5);
+            wd[c] = sum > 0.0 ? nw[c] * kMean * ctas / sum : kMean;
+            w[c] = quantise(wd[c]);
         }
+        // The first round moves the weights from equal to near the balance;
+        // later rounds estimate the same balance again, and their average
+        // (not their last) is kept, so one call's timing noise does not.
+        if (r > 0 || rounds == 1) {
+            for (int c = 0; c < ctas; ++c)
+                avg[c] += wd[c];
+            ++n_avg;
+        }
+        st = set_split(w.data(), ctas);
+    }
+    if (st == PKV_OK && n_avg > 0) {
+        double sum = 0.0;
+        for (int c = 0; c < ctas; ++c)
+            sum += avg[c];
+        for (int c = 0; c < ctas; ++c)
+            w[c] = quantise(sum > 0.0 ? avg[c] * kMean * ctas / sum : kMean);
         st = set_split(w.data(), ctas);
     }
     if (st != PKV_OK) {

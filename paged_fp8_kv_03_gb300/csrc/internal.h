@@ -53,8 +53,8 @@ constexpr int kFoldChunks = 128;
 // fast the SMs the CTAs land on stream their share); calls with another grid
 // size split evenly.
 constexpr int kMaxSplitCtas = 1024;
-constexpr int kSplitWeightMin = 96;
-constexpr int kSplitWeightMax = 160;
+constexpr int kSplitWeightMin = 768;                   // weights are 1024 +- 25%, in steps of 1/1024
+constexpr int kSplitWeightMax = 1280;
 
 // Decode workspace: a header, one record per (sequence, kv head) segment,
 // then the partial-state slots.

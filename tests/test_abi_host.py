@@ -230,13 +230,13 @@ def test_withhold_facility_is_off_at_load_and_settable(lib):
 
 
 def test_split_weight_argument_errors(lib):
-    """Weights outside [96, 160], more than 1024 CTAs or a NULL array are
+    """Weights outside [768, 1280], more than 1024 CTAs or a NULL array are
     rejected before any CUDA call; so are calibration requests with no
     rounds or no sequences."""
     c = _status_codes()
-    ok = (ctypes.c_uint8 * 4)(96, 128, 150, 160)
-    low = (ctypes.c_uint8 * 4)(96, 95, 128, 128)
-    high = (ctypes.c_uint8 * 4)(128, 161, 128, 128)
+    ok = (ctypes.c_uint16 * 4)(768, 1024, 1100, 1280)
+    low = (ctypes.c_uint16 * 4)(768, 767, 1024, 1024)
+    high = (ctypes.c_uint16 * 4)(1024, 1281, 1024, 1024)
     assert lib.pkv_decode_set_split_weights(ctypes.addressof(low), 4) == c["PKV_ERR_SHAPE"]
     assert lib.pkv_decode_set_split_weights(ctypes.addressof(high), 4) == c["PKV_ERR_SHAPE"]
     assert lib.pkv_decode_set_split_weights(ctypes.addressof(ok), -1) == c["PKV_ERR_SHAPE"]

@@ -27,11 +27,11 @@ def _even_split(pkv, cuda_device):
 
 
 def _weights(n, seed):
-    return np.random.default_rng(seed).integers(96, 161, n).tolist()
+    return np.random.default_rng(seed).integers(768, 1281, n).tolist()
 
 
 @pytest.mark.parametrize("ctas", [1, 7, 50])
-@pytest.mark.parametrize("value", [96, 128, 160])
+@pytest.mark.parametrize("value", [768, 1024, 1280])
 def test_equal_weights_are_the_even_split(pkv, cuda_device, ctas, value):
     wl = workloads.Workload(60, "eq", [700, 33, 1601, 16, 0, 4097], 0, 32, 8, 16, pool_factor=1.5, seed=3)
     f = fill_gpu(wl, 0, cuda_device)
@@ -87,14 +87,14 @@ def test_lists_shorter_than_the_shares(pkv, cuda_device):
 
 
 def test_long_ranges_fold_their_accumulators(pkv, cuda_device):
-    """Two CTAs at weights 96 and 160: the second CTA's warps take about 680
+    """Two CTAs at weights 768 and 1280: the second CTA's warps take about 680
     chunks each, folded every 128."""
     wl = workloads.Workload(64, "long", [40000, 30000], 0, 8, 1, 16, seed=9)
     f = fill_gpu(wl, 0, cuda_device)
     ref = _full_oracle(wl, f)
     even = _decode(pkv, f, max_ctas=2).double().cpu().numpy()
     assert_close(even, ref, "even")
-    for w in ([96, 160], [160, 96], [150, 100]):
+    for w in ([768, 1280], [1280, 768], [1200, 800]):
         pkv.pkv_decode_set_split_weights(w)
         assert_close(_decode(pkv, f, max_ctas=2).double().cpu().numpy(), ref, f"weights={w}")
 
@@ -127,7 +127,7 @@ def test_calibrate_installs_weights_and_stays_deterministic(pkv, cuda_device):
     ws = pkv.decode_workspace(wl.batch, wl.hq, wl.hkv, wl.page_size, cuda_device, 0, f.max_len)
     w = pkv.pkv_decode_calibrate_split(f.q, f.kc, f.vc, f.ks, f.vs, f.bt, f.lens, out, ws, rounds=2,
                                        max_seq_len=f.max_len)
-    assert len(w) > 0 and all(96 <= x <= 160 for x in w)
+    assert len(w) > 0 and all(768 <= x <= 1280 for x in w)
     assert pkv.pkv_decode_get_split_weights() == w
     a = _decode(pkv, f)
     b = _decode(pkv, f)
