@@ -200,7 +200,7 @@ int decode_num_ctas(int page_size, int batch, int max_ctas)
 
 // Workspace: header and segment records, then one partial slot per worker
 // plus one per segment (a piece is a worker's range within one segment; its
-// slot is worker + segment, distinct for every piece).  Independent of the
+// slot is worker + the segment's rank in list order, distinct for every piece).  Independent of the
 // sequence lengths.
 size_t decode_workspace_bytes(int batch, int hq, int hkv, long long /*max_len*/, int num_ctas)
 {

@@ -21,7 +21,7 @@
 // range cuts segments into
 // pieces; a piece covering a whole segment writes the final output, the
 // others write a partial softmax state (running max m, sum l, unnormalised
-// accumulator) into workspace slot worker + segment.  A second kernel, one
+// accumulator) into workspace slot worker + (the segment's rank in the list).  A second kernel, one
 // CTA per (segment, head) with a thread per dimension, merges the pieces in
 // worker order (deterministic); it is a programmatic dependent launch, so it
 // is already resident when the first kernel's last warps finish.
@@ -114,37 +114,43 @@ __device__ __forceinline__ int chunks_of(const int *ps, int b)
     return ps[b + 1] - ps[b];
 }
 
-// Segment (b, h) covers list positions [ps[b]*hkv + h*np_b, ... + np_b).
+// The list is head-major: all sequences' chunks of kv head 0, then of head 1,
+// ...; segment (b, h) covers list positions [h*ps[batch] + ps[b], ... + np_b).
+// (Head-major keeps a batch's short sequences apart in the list, so a
+// worker's range crosses fewer segment boundaries than with the heads of one
+// sequence side by side.)
 __device__ Loc locate(const int *ps, int batch, int hkv, int64_t x)
 {
-    int lo = 0, hi = batch - 1;
+    const int64_t per_head = ps[batch];                  // chunks of one head over all sequences
+    Loc l;
+    l.h = static_cast<int>(x / per_head);
+    const int rem = static_cast<int>(x - static_cast<int64_t>(l.h) * per_head);
+    int lo = 0, hi = batch - 1;                          // the last sequence starting at or before rem
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (static_cast<int64_t>(ps[mid]) * hkv <= x)
+        if (ps[mid] <= rem)
             lo = mid;
         else
             hi = mid - 1;
     }
-    const int64_t rem = x - static_cast<int64_t>(ps[lo]) * hkv;
-    const int np = chunks_of(ps, lo);
-    Loc l;
     l.b = lo;
-    l.h = static_cast<int>(rem / np);
-    l.ck = static_cast<int>(rem % np);
+    l.ck = rem - ps[lo];
+    (void)hkv;
     return l;
 }
 
+// n chunk-heads further along the list (past its end: h == hkv).
 __device__ Loc advance(const int *ps, int batch, int hkv, Loc l, int64_t n)
 {
     int64_t pg = l.ck + n;
-    while (l.b < batch) {
+    while (l.h < hkv) {
         const int np = chunks_of(ps, l.b);
         if (pg < np)
             break;
         pg -= np;
-        if (++l.h == hkv) {
-            l.h = 0;
-            ++l.b;
+        if (++l.b == batch) {
+            l.b = 0;
+            ++l.h;
         }
     }
     l.ck = static_cast<int>(pg);
@@ -499,12 +505,12 @@ __device__ __noinline__ void write_records(const DecodeArgs &a, const int *pstar
     Loc l = locate(pstart, a.batch, a.hkv, lo);
     int64_t k = 0;
     const int64_t n_total = hi - lo;
-    while (k < n_total && l.b < a.batch) {
+    while (k < n_total && l.h < a.hkv) {
         const int np = chunks_of(pstart, l.b);
         const int n_piece = static_cast<int>(min(static_cast<int64_t>(np - l.ck), n_total - k));
         SegRecord *rec = a.segs + l.b * a.hkv + l.h;
         if (l.ck == 0) {
-            rec->start = static_cast<long long>(pstart[l.b]) * a.hkv + static_cast<long long>(l.h) * np;
+            rec->start = static_cast<long long>(l.h) * pstart[a.batch] + pstart[l.b];
             rec->n = np;
             rec->w0 = n_piece == np ? -1 : worker;
         }
@@ -694,6 +700,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int L = seq_len_of(a, cons.b);
         const bool whole = (cons.ck == 0) && (n_piece == np);
         const int seg = cons.b * a.hkv + cons.h;
+        // the segment's rank in list order: slot worker + rank is distinct for
+        // every piece because worker and rank both grow along the list
+        const int rank = cons.h * a.batch + cons.b;
         const float scale2 = __ldg(a.k_scale + cons.h) * a.sm_scale_log2;
 
         // Q fragment for k-step kk: head gid, dims 16kk + 4t4 + {0,1} and {2,3}.
@@ -720,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         // every tensor-core accumulation chain within kFoldChunks chunks.
         // folded: the slot already holds a fold (after the first kFoldChunks).
         auto fold = [&](bool folded, bool store) {
-            const int64_t sidx = static_cast<int64_t>(slot_index) + seg;
+            const int64_t sidx = static_cast<int64_t>(slot_index) + rank;
             if (sidx >= a.num_slots) {
                 if (a.err && lane == 0)
                     atomicOr(a.err, PKV_DEVERR_INTERNAL);
@@ -820,11 +829,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
                 if (h1)
                     store_pair(a, row0 + 2 * t4 + 1, d, acc[sg][1] * s1, acc[sg][3] * s1);
             }
-        } else if (static_cast<int64_t>(slot_index) + seg >= a.num_slots) {
+        } else if (static_cast<int64_t>(slot_index) + rank >= a.num_slots) {
             if (a.err && lane == 0)
                 atomicOr(a.err, PKV_DEVERR_INTERNAL);
         } else {
-            float *slot = a.partials + static_cast<int64_t>(slot_index + seg) * a.group * kPartialStride;
+            float *slot = a.partials + static_cast<int64_t>(slot_index + rank) * a.group * kPartialStride;
 #pragma unroll
             for (int sg = 0; sg < 8; ++sg) {
                 const int d = 16 * sg + 2 * gid;
@@ -884,6 +893,7 @@ __global__ void __launch_bounds__(32 * PKV_MAX_GROUP * kSub) splitk_merge_kernel
     }
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid has finished
     const int seg = blockIdx.x, wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int rank = (seg % a.hkv) * a.batch + seg / a.hkv;   // the segment's rank in list order (head-major)
     const int g = wi / kSub, sub = wi % kSub;
     const SegRecord r = a.segs[seg];
     const DecodeHeader hd = *a.header;
@@ -932,12 +942,12 @@ __global__ void __launch_bounds__(32 * PKV_MAX_GROUP * kSub) splitk_merge_kernel
             if (nb == 0)
                 break;
         }
-        const bool bad = my_slot >= 0 && static_cast<int64_t>(my_slot) + seg >= a.num_slots;
+        const bool bad = my_slot >= 0 && static_cast<int64_t>(my_slot) + rank >= a.num_slots;
         if (bad)
             my_slot = -1;                                           // skipped, flagged below
         float m = -INFINITY, l = 0.f;
         if (my_slot >= 0) {
-            const float *p = a.partials + (static_cast<int64_t>(my_slot + seg) * a.group + g) * kPartialStride;
+            const float *p = a.partials + (static_cast<int64_t>(my_slot + rank) * a.group + g) * kPartialStride;
             m = p[kHeadDim];
             l = p[kHeadDim + 1];
         }
@@ -948,7 +958,7 @@ __global__ void __launch_bounds__(32 * PKV_MAX_GROUP * kSub) splitk_merge_kernel
             v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
             if (si >= 0)                                            // lanes >= nb hold -1
                 v[i] = *reinterpret_cast<const float4 *>(
-                    a.partials + (static_cast<int64_t>(si + seg) * a.group + g) * kPartialStride + 4 * lane);
+                    a.partials + (static_cast<int64_t>(si + rank) * a.group + g) * kPartialStride + 4 * lane);
         }
         if (__any_sync(kFull, bad) && lane == 0 && a.err)
             atomicOr(a.err, PKV_DEVERR_INTERNAL);

@@ -94,7 +94,7 @@ struct DecodeArgs {
     DecodeHeader *header;           // workspace header (written by CTA 0)
     SegRecord *segs;                // [batch * hkv] segment records (written by the workers holding a
                                     // segment's first and last chunk)
-    float *partials;                // [num_ctas * kWarps + batch * hkv][group][kPartialStride]: slot worker + segment
+    float *partials;                // [num_ctas * kWarps + batch * hkv][group][kPartialStride]: slot worker + list rank of the segment
     int32_t *err;
     int num_ctas;
     int withhold_worker;            // failure-detection test hook (-1 = off)
