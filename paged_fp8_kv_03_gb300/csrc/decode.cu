@@ -11,7 +11,8 @@
 // design streams every KV byte exactly once at full HBM rate.
 //
 // Work split.  The (sequence, kv head) segments are laid end to end as one
-// list of "page-heads" (one page of one kv head, 2 x P x 128 bytes).  Every
+// list of "page-heads" (one page of one kv head, 2 x P x 128 bytes), kv head
+// by kv head (every sequence's segment of head 0, then of head 1, ...).  Every
 // warp of the persistent grid is an independent worker that takes a
 // contiguous range of that list, whatever the sequence lengths (split-K /
 // flash-decoding): an equal share, or a share proportional to its CTA's
