@@ -180,25 +180,31 @@ __device__ __forceinline__ Split make_split(const DecodeArgs &a, const uint32_t 
     return sp;
 }
 
-// First list position of worker w's range, T * C(w) / CT (w = workers gives T).
-// Clamped to [0, T], so even a table rewritten during a call (a misuse) keeps
-// every range, and so every slot index, inside the list.
-__device__ __forceinline__ int64_t range_lo(const Split &sp, int64_t total, int w)
+// List position T * cw / CT of weight position cw = C(w), clamped to [0, T],
+// so even a table rewritten during a call (a misuse) keeps every range, and
+// so every slot index, inside the list.
+__device__ __forceinline__ int64_t range_at(const Split &sp, int64_t total, int64_t cw)
 {
-    int64_t cw;
-    if (sp.pre == nullptr) {
-        cw = w;
-    } else {
-        const int c = w / kWarps, j = w % kWarps;
-        if (c >= sp.ctas) {
-            cw = sp.ct;
-        } else {
-            const uint32_t p0 = sp.pre[c], p1 = sp.pre[c + 1];
-            cw = static_cast<int64_t>(kWarps) * p0 + static_cast<int64_t>(j) * (p1 - p0);
-        }
-    }
     const int64_t x = total * cw / sp.ct;
     return x < 0 ? 0 : (x > total ? total : x);
+}
+
+// C(j) for warp j in [0, kWarps] of CTA c, given the CTA's prefix sums p0 =
+// P(c) and p1 = P(c + 1) (C(4) is C of the next CTA's warp 0); even split: 4c + j.
+__device__ __forceinline__ int64_t split_cw(const Split &sp, int c, int j, uint32_t p0, uint32_t p1)
+{
+    if (sp.pre == nullptr)
+        return static_cast<int64_t>(c) * kWarps + j;
+    return static_cast<int64_t>(kWarps) * p0 + static_cast<int64_t>(j) * (p1 - p0);
+}
+
+// First list position of worker w's range, T * C(w) / CT (w = workers gives T).
+__device__ __forceinline__ int64_t range_lo(const Split &sp, int64_t total, int w)
+{
+    const int c = w / kWarps, j = w % kWarps;
+    if (sp.pre == nullptr)
+        return range_at(sp, total, split_cw(sp, c, j, 0u, 0u));
+    return range_at(sp, total, c >= sp.ctas ? sp.ct : split_cw(sp, c, j, sp.pre[c], sp.pre[c + 1]));
 }
 
 struct Smem {
@@ -210,7 +216,8 @@ struct Smem {
     static constexpr int kFlag = kBar + kWarps * kStages * 8;   // abort flag
     static constexpr int kWarpSum = kFlag + 16;             // scan scratch (kWarps ints)
     static constexpr int kFoldM = kWarpSum + 32;            // per warp: the running maximum of each head at its last fold
-    static constexpr int kPstart = kFoldM + kWarps * PKV_MAX_GROUP * 4;
+    static constexpr int kArgs = kFoldM + kWarps * PKV_MAX_GROUP * 4;   // a copy of the call's arguments
+    static constexpr int kPstart = kArgs + (static_cast<int>(sizeof(DecodeArgs)) + 15) / 16 * 16;
     static size_t bytes(int batch) { return static_cast<size_t>(kPstart) + 4u * (batch + 1) + 1024u; }
 };
 
@@ -417,82 +424,51 @@ __device__ __forceinline__ void process_tile(TileFrags &fr, int nv, const uint32
     }
 }
 
-// Index (within this worker's range) of the first chunk that may hold one of
-// the step's new tokens: they lie in a segment's last 1 + ceil(n_new / 16)
-// chunks.  Uses only the chunk offsets in shared memory.  n_total if none.
-__device__ int first_tail_chunk(const DecodeArgs &a, const int *pstart, int64_t lo, int64_t hi)
+// Fused append, one chunk: the worker that consumes chunk ck of segment (b, h)
+// (exactly one worker owns each chunk) quantises the step's new tokens that
+// fall in it, stores them to the pool for later calls, and writes the same
+// bytes into the chunk's copy in its ring, which the TMA filled before (or
+// while) the stores reached the pool.  So this call never reads its own
+// stores back: no proxy fence, and neither the stores nor the loads wait for
+// the other.  Lanes split the 128 dims, 4 each; lane i's 4 bytes of row r sit
+// in 16-byte unit (i / 4) XOR (r mod 8) of the row (the TMA's 128-byte swizzle).
+// Called after the chunk's wait, before its rows are read.
+__device__ __noinline__ void store_new_tokens(const DecodeArgs &a, int b, int h, int ck, int L, uint32_t kt,
+                                              uint32_t vt, int lane)
 {
-    const int tail_pages = 1 + (a.n_new + kChunk - 1) / kChunk;
-    Loc l = locate(pstart, a.batch, a.hkv, lo);
-    int64_t cur = lo;
-    while (cur < hi) {
-        const int np = chunks_of(pstart, l.b);
-        const int n_piece = static_cast<int>(min(static_cast<int64_t>(np - l.ck), hi - cur));
-        const int first = max(l.ck, np - tail_pages);
-        if (first < l.ck + n_piece)
-            return static_cast<int>(cur - lo) + (first - l.ck);
-        cur += n_piece;
-        l = advance(pstart, a.batch, a.hkv, l, n_piece);
-    }
-    return static_cast<int>(hi - lo);
-}
-
-// Fused append: this worker quantises and stores the new tokens that fall in
-// the page-heads it owns (exactly one worker owns each page-head, so nobody
-// else reads or writes them in this call), then orders those generic-proxy
-// stores before its own TMA reads.  Lanes split the 128 dims, 4 each.
-__device__ __noinline__ void append_own_tokens(const DecodeArgs &a, const int *pstart, int64_t lo, int64_t hi,
-                                               int lane)
-{
-    Loc l = locate(pstart, a.batch, a.hkv, lo);
-    int64_t cur = lo;
-    const int tail_pages = 1 + (a.n_new + kChunk - 1) / kChunk;   // new tokens live in a segment's last chunks
-    while (cur < hi) {
-        const int np = chunks_of(pstart, l.b);
-        const int n_piece = static_cast<int>(min(static_cast<int64_t>(np - l.ck), hi - cur));
-        if (l.ck + n_piece <= np - tail_pages) {           // this piece cannot hold a new token
-            cur += n_piece;
-            l = advance(pstart, a.batch, a.hkv, l, n_piece);
-            continue;
+    const int lp = page_log2_of(a, b);
+    const int t0 = max(ck * kChunk, L - a.n_new), t1 = min(ck * kChunk + kChunk, L);
+    for (int t = t0; t < t1; ++t) {
+        int phys, row;
+        if (!token_page(a, b, lp, t, phys, row))
+            continue;   // the chunk's page is outside the pool: flagged at its issue, read as zeros
+        const int j = t - (L - a.n_new);
+        const int64_t src = ((static_cast<int64_t>(b) * a.n_new + j) * a.hkv + h) * kHeadDim + 4 * lane;
+        const int64_t dst = ((static_cast<int64_t>(phys) * a.hkv + h) * a.page_size + row) * kHeadDim + 4 * lane;
+        float k4[4], v4[4];
+        if (a.new_bf16) {
+            const uint2 kb = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(a.k_new) + src));
+            const uint2 vb = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(a.v_new) + src));
+            k4[0] = __uint_as_float(kb.x << 16); k4[1] = __uint_as_float(kb.x & 0xFFFF0000u);
+            k4[2] = __uint_as_float(kb.y << 16); k4[3] = __uint_as_float(kb.y & 0xFFFF0000u);
+            v4[0] = __uint_as_float(vb.x << 16); v4[1] = __uint_as_float(vb.x & 0xFFFF0000u);
+            v4[2] = __uint_as_float(vb.y << 16); v4[3] = __uint_as_float(vb.y & 0xFFFF0000u);
+        } else {
+            const float4 kf = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(a.k_new) + src));
+            const float4 vf = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(a.v_new) + src));
+            k4[0] = kf.x; k4[1] = kf.y; k4[2] = kf.z; k4[3] = kf.w;
+            v4[0] = vf.x; v4[1] = vf.y; v4[2] = vf.z; v4[3] = vf.w;
         }
-        const int L = seq_len_of(a, l.b);
-        const int lp = page_log2_of(a, l.b);
-        const int first = max(0, L - a.n_new);            // positions [first, L) are new
-        for (int t = first; t < L; ++t) {
-            const int ck = t / kChunk;                     // the worker owning this chunk stores the token
-            if (ck < l.ck || ck >= l.ck + n_piece)
-                continue;
-            int phys, row;
-            if (!token_page(a, l.b, lp, t, phys, row)) {
-                if (a.err && lane == 0)
-                    atomicOr(a.err, PKV_DEVERR_PAGE);
-                continue;
-            }
-            const int j = t - (L - a.n_new);
-            const int64_t src = ((static_cast<int64_t>(l.b) * a.n_new + j) * a.hkv + l.h) * kHeadDim + 4 * lane;
-            const int64_t dst = ((static_cast<int64_t>(phys) * a.hkv + l.h) * a.page_size + row) * kHeadDim + 4 * lane;
-            float k4[4], v4[4];
-            if (a.new_bf16) {
-                const uint2 kb = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(a.k_new) + src));
-                const uint2 vb = __ldg(reinterpret_cast<const uint2 *>(static_cast<const __nv_bfloat16 *>(a.v_new) + src));
-                k4[0] = __uint_as_float(kb.x << 16); k4[1] = __uint_as_float(kb.x & 0xFFFF0000u);
-                k4[2] = __uint_as_float(kb.y << 16); k4[3] = __uint_as_float(kb.y & 0xFFFF0000u);
-                v4[0] = __uint_as_float(vb.x << 16); v4[1] = __uint_as_float(vb.x & 0xFFFF0000u);
-                v4[2] = __uint_as_float(vb.y << 16); v4[3] = __uint_as_float(vb.y & 0xFFFF0000u);
-            } else {
-                const float4 kf = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(a.k_new) + src));
-                const float4 vf = __ldg(reinterpret_cast<const float4 *>(static_cast<const float *>(a.v_new) + src));
-                k4[0] = kf.x; k4[1] = kf.y; k4[2] = kf.z; k4[3] = kf.w;
-                v4[0] = vf.x; v4[1] = vf.y; v4[2] = vf.z; v4[3] = vf.w;
-            }
-            *reinterpret_cast<uint32_t *>(a.k_pool + dst) = quantise4(k4[0], k4[1], k4[2], k4[3], __ldg(a.k_scale + l.h));
-            *reinterpret_cast<uint32_t *>(a.v_pool + dst) = quantise4(v4[0], v4[1], v4[2], v4[3], __ldg(a.v_scale + l.h));
-        }
-        cur += n_piece;
-        l = advance(pstart, a.batch, a.hkv, l, n_piece);
+        const uint32_t kq = quantise4(k4[0], k4[1], k4[2], k4[3], __ldg(a.k_scale + h));
+        const uint32_t vq = quantise4(v4[0], v4[1], v4[2], v4[3], __ldg(a.v_scale + h));
+        *reinterpret_cast<uint32_t *>(a.k_pool + dst) = kq;
+        *reinterpret_cast<uint32_t *>(a.v_pool + dst) = vq;
+        const int r = t - ck * kChunk;
+        const uint32_t off = static_cast<uint32_t>(r * kHeadDim + (((lane >> 2) ^ (r & 7)) << 4) + 4 * (lane & 3));
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(kt + off), "r"(kq) : "memory");
+        asm volatile("st.shared.u32 [%0], %1;" ::"r"(vt + off), "r"(vq) : "memory");
     }
-    asm volatile("fence.proxy.async;" ::: "memory");   // stores above -> this warp's TMA reads
-    __syncwarp();
+    __syncwarp();   // every lane's patch before any lane reads the rows
 }
 
 // Segment records for the merge kernel, for the segments this worker's range
@@ -534,6 +510,13 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (a.probe && tid == 0)
         g_split_probe[blockIdx.x][0] = global_timer_ns();
+    // This CTA's weight prefix sums P(c), P(c + 1): loaded first, so that the
+    // load overlaps the page-offset pass (the ranges need both).
+    uint32_t pre_c0 = 0u, pre_c1 = 0u;
+    if (a.split) {
+        pre_c0 = g_split_prefix[blockIdx.x];
+        pre_c1 = g_split_prefix[blockIdx.x + 1];
+    }
     int *pstart = reinterpret_cast<int *>(smem + S::kPstart);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kFlag);
     int *warp_sum = reinterpret_cast<int *>(smem + S::kWarpSum);
@@ -555,6 +538,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         if (lane == 31)
             warp_sum[warp] = incl;
         if (tid == 0) {
+            // The out-of-line helpers below take the arguments by reference;
+            // given the kernel parameter itself they would read every field
+            // through its global address, one memory round trip each at the
+            // start of the call, so they get this shared-memory copy.
+            *reinterpret_cast<DecodeArgs *>(smem + S::kArgs) = a;
             *abort_flag = 0;
             const uint32_t bar0 = smem_addr(smem + S::kBar);
             for (int s = 0; s < kWarps * kStages; ++s)
@@ -609,8 +597,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     // Let the merge kernel get scheduled now; it waits for this grid to finish.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int64_t lo = range_lo(sp, total, worker);
-    const int64_t hi = range_lo(sp, total, worker + 1);
+    const int64_t lo = range_at(sp, total, split_cw(sp, blockIdx.x, warp, pre_c0, pre_c1));
+    const int64_t hi = range_at(sp, total, split_cw(sp, blockIdx.x, warp + 1, pre_c0, pre_c1));
     if (lo >= hi) {                              // warp-level: no CTA barrier follows
         if (a.probe && lane == 0)
             atomicMax(&g_split_probe[blockIdx.x][1], static_cast<unsigned long long>(global_timer_ns()));
@@ -618,14 +606,9 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     const int n_total = static_cast<int>(hi - lo);
 
-    // Fused append: if a page that may receive new tokens is among the first
-    // kStages pages of this worker, store the tokens before any load; otherwise
-    // start the loads first and store while they are in flight (those pages
-    // are issued later, after the stores and their proxy fence).
-    const bool append_early =
-        a.k_new != nullptr && first_tail_chunk(a, pstart, lo, hi) < S::kStages;
-    if (append_early)
-        append_own_tokens(a, pstart, lo, hi, lane);
+    // (The fused append needs nothing here: the worker owning a chunk with new
+    // tokens stores them when it consumes the chunk, see store_new_tokens.)
+    const DecodeArgs &a_s = *reinterpret_cast<const DecodeArgs *>(smem + S::kArgs);
 
     const uint32_t ring = smem_addr(smem) + warp * S::kWarpRing;
     const uint32_t bars = smem_addr(smem + S::kBar) + warp * kStages * 8;
@@ -682,11 +665,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     };
     for (int f = 0; f < kStages && f < n_total; ++f)
         issue(f);
-    if (a.k_new != nullptr && !append_early)
-        append_own_tokens(a, pstart, lo, hi, lane);
-    if (lane == 0)                               // while the first loads are in flight
-        write_records(a, pstart, lo, hi, worker);
-    __syncwarp();
+    // Records: only a range holding some segment's first or last chunk writes one.
+    if (cons.ck == 0 || n_total > chunks_of(pstart, cons.b) - cons.ck - 1) {
+        if (lane == 0)                           // while the first loads are in flight
+            write_records(a_s, pstart, lo, hi, worker);
+        __syncwarp();
+    }
 
     const int gid = lane >> 2, t4 = lane & 3;
     const TileOffsets off = tile_offsets(lane);
@@ -700,7 +684,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         const int slot_index = worker;
         const int L = seq_len_of(a, cons.b);
         const bool whole = (cons.ck == 0) && (n_piece == np);
-        const int seg = cons.b * a.hkv + cons.h;
         // the segment's rank in list order: slot worker + rank is distinct for
         // every piece because worker and rank both grow along the list
         const int rank = cons.h * a.batch + cons.b;
@@ -791,6 +774,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
             if (ready)
                 pending &= ~(1u << s);
             const uint32_t kt = ring + s * S::kStageBytes;
+            if (a.k_new != nullptr && ready && (cons.ck + j + 1) * kChunk > L - a.n_new)
+                store_new_tokens(a_s, cons.b, cons.h, cons.ck + j, L, kt, kt + S::kTile, lane);
             // Copy the chunk into registers, then hand the stage straight back
             // to the TMA unit so every stage stays in flight during the math.
             TileFrags fr;
@@ -863,59 +848,65 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         atomicMax(&g_split_probe[blockIdx.x][1], static_cast<unsigned long long>(global_timer_ns()));
 }
 
-// One CTA per (sequence, kv head) segment, one warp per query head g of its
-// group; lane j owns dimensions 4j .. 4j+3.  The warp merges the partial
-// states the workers covering the segment wrote for head g, in list order,
-// and writes the output row.  Pieces are taken 16 at a time: lane i of the
-// warp finds the slot of piece i and loads its (m, l); every lane loads its
-// four dimensions of all 16 accumulators; then one exact rescale folds the
-// batch into the running (M, L, A).  The order is fixed, so results are
-// deterministic.
+// One CTA per (segment, query head g of its group), so that the merge's reads
+// spread over the whole GPU; lane j owns dimensions 4j .. 4j+3.  The CTA
+// merges the partial states the workers covering the segment wrote for head
+// g, in list order, and writes the output row.  Pieces are taken 16 at a
+// time: lane i finds the slot of piece i and loads its (m, l); every lane
+// stages its four dimensions of all 16 accumulators in shared memory; then
+// one exact rescale folds the batch into the running (M, L, A).  The order is
+// fixed, so results are deterministic.
 //
 // Where a segment's pieces are: with no empty range, piece i was written by
-// worker w0 + i and the last one by w1; otherwise (ranges of no chunk when the
-// list is shorter than the workers' shares) the pieces are walked worker by
-// worker, skipping the empty ranges.
+// worker w0 + i and the last one by w1 (the segment's record); otherwise
+// (ranges of no chunk when the list is shorter than the workers' shares) the
+// pieces are walked worker by worker, skipping the empty ranges.
 constexpr int kMergeBatch = 16;
 
-// kSub warps per query head: with segments of many pieces (few segments
-// against many workers) the warps of a head take turns over the batches and
-// their states are combined in shared memory at the end, in sub-warp order.
+// kSub warps per CTA: with segments of many pieces (few segments against many
+// workers) they take turns over the batches and their states are combined in
+// shared memory at the end, in sub-warp order.
 template <int kSub>
-__global__ void __launch_bounds__(32 * PKV_MAX_GROUP * kSub) splitk_merge_kernel(const DecodeArgs a)
+__global__ void __launch_bounds__(32 * kSub) splitk_merge_kernel(const DecodeArgs a)
 {
     __shared__ uint32_t pre_s[kMaxSplitCtas + 1];
-    __shared__ __align__(16) float red_a[kSub > 1 ? PKV_MAX_GROUP * kSub : 1][32 * 4];   // read and written as float4
-    __shared__ float red_ml[kSub > 1 ? PKV_MAX_GROUP * kSub : 1][2];
+    __shared__ __align__(16) float red_a[kSub > 1 ? kSub : 1][32 * 4];   // read and written as float4
+    __shared__ float red_ml[kSub > 1 ? kSub : 1][2];
+    extern __shared__ float4 merge_stage[];      // [kSub][kMergeBatch][32]: the batches' accumulators
+    const int seg = blockIdx.x / a.group, g = blockIdx.x % a.group;
+    const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = wi;
+    const int b = seg / a.hkv, h = seg % a.hkv;
+    const int rank = h * a.batch + b;            // the segment's rank in list order (head-major)
+
     if (a.split) {                               // the split's weight prefix sums (inputs, not the decode's output)
         for (int c = threadIdx.x; c <= a.num_ctas; c += blockDim.x)
             pre_s[c] = g_split_prefix[c];
         __syncthreads();
     }
+    const float vsc = __ldg(a.v_scale + h);
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid has finished
-    const int seg = blockIdx.x, wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int rank = (seg % a.hkv) * a.batch + seg / a.hkv;   // the segment's rank in list order (head-major)
-    const int g = wi / kSub, sub = wi % kSub;
     const SegRecord r = a.segs[seg];
     const DecodeHeader hd = *a.header;
     if (r.n <= 0 || r.w0 < 0)
-        return;
-    const int64_t total = hd.total;
+        return;   // empty (the decode kernel wrote its zero rows) or one piece (its worker wrote the output)
+    const int64_t total = hd.total, start = r.start;
+    const int n_seg = r.n, w0 = r.w0, w1 = r.w1;
     const Split sp = make_split(a, pre_s);
-    const int b = seg / a.hkv, h = seg % a.hkv;
+
     // every range holds at least one chunk-head when T * wmin >= CT
     const bool dense = total * (a.split ? a.split_wmin : 1) >= sp.ct;
     const bool walk = !dense;
-    const int n_known = r.w1 - r.w0 + 1;
+    const int n_known = w1 - w0 + 1;
     // walk state: worker w, its range [lo_w, hi_w), offset k of the next piece in it
-    const int64_t end = r.start + r.n;
-    int w = r.w0;
+    const int64_t end = start + n_seg;
+    int w = w0;
     int64_t lo_w = range_lo(sp, total, w);
     int64_t hi_w = range_lo(sp, total, w + 1);
-    int64_t k = r.start - lo_w;
+    int64_t k = start - lo_w;
 
     float M = -INFINITY, L = 0.f;
     float A[4] = {0.f, 0.f, 0.f, 0.f};
+    float4 *stage = merge_stage + wi * (kMergeBatch * 32) + lane;   // this lane's [kMergeBatch] entries, 32 apart
     // the walk (empty ranges in the list) is sequential: sub-warp 0 alone
     for (int i0 = sub * kMergeBatch; walk ? sub == 0 : true; i0 += kSub * kMergeBatch) {
         // slot of piece i0 + lane (lanes >= the batch size: -1)
@@ -926,7 +917,7 @@ __global__ void __launch_bounds__(32 * PKV_MAX_GROUP * kSub) splitk_merge_kernel
             if (nb <= 0)
                 break;
             if (lane < nb)
-                my_slot = r.w0 + i0 + lane;
+                my_slot = w0 + i0 + lane;
         } else {
             nb = 0;
             while (nb < kMergeBatch && lo_w + k < end) {
@@ -952,15 +943,21 @@ __global__ void __launch_bounds__(32 * PKV_MAX_GROUP * kSub) splitk_merge_kernel
             m = p[kHeadDim];
             l = p[kHeadDim + 1];
         }
-        float4 v[kMergeBatch];
+        // This lane's 4 dims of the batch's accumulators, staged in shared
+        // memory by asynchronous copies that are all in flight together (one
+        // round trip per batch, however the loop is scheduled); pieces past
+        // the batch (slot -1) are zero-filled.  Each lane reads back only
+        // what it staged.
 #pragma unroll
         for (int i = 0; i < kMergeBatch; ++i) {
             const int si = __shfl_sync(kFull, my_slot, i);
-            v[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (si >= 0)                                            // lanes >= nb hold -1
-                v[i] = *reinterpret_cast<const float4 *>(
-                    a.partials + (static_cast<int64_t>(si + rank) * a.group + g) * kPartialStride + 4 * lane);
+            const float *src =
+                a.partials + (static_cast<int64_t>(si >= 0 ? si + rank : 0) * a.group + g) * kPartialStride + 4 * lane;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_addr(stage + 32 * i)), "l"(src),
+                         "r"(si >= 0 ? 16 : 0)
+                         : "memory");
         }
+        asm volatile("cp.async.commit_group;" ::: "memory");
         if (__any_sync(kFull, bad) && lane == 0 && a.err)
             atomicOr(a.err, PKV_DEVERR_INTERNAL);
         float mb = m;
@@ -978,13 +975,15 @@ __global__ void __launch_bounds__(32 * PKV_MAX_GROUP * kSub) splitk_merge_kernel
 #pragma unroll
         for (int c = 0; c < 4; ++c)
             A[c] *= r0;
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
 #pragma unroll
         for (int i = 0; i < kMergeBatch; ++i) {
             const float si = __shfl_sync(kFull, sc, i);
-            A[0] += si * v[i].x;
-            A[1] += si * v[i].y;
-            A[2] += si * v[i].z;
-            A[3] += si * v[i].w;
+            const float4 v = stage[32 * i];
+            A[0] += si * v.x;
+            A[1] += si * v.y;
+            A[2] += si * v.z;
+            A[3] += si * v.w;
         }
         M = mn;
     }
@@ -1018,7 +1017,7 @@ __global__ void __launch_bounds__(32 * PKV_MAX_GROUP * kSub) splitk_merge_kernel
             A[3] += as.w * rs;
         }
     }
-    const float f = __ldg(a.v_scale + h) / L;
+    const float f = vsc / L;
     const int64_t row = static_cast<int64_t>(b) * a.hq + static_cast<int64_t>(h) * a.group + g;
     store_pair(a, row, 4 * lane, A[0] * f, A[1] * f);
     store_pair(a, row, 4 * lane + 2, A[2] * f, A[3] * f);
@@ -1036,6 +1035,13 @@ const void *decode_kernel_for(int /*page_size*/)
     return reinterpret_cast<const void *>(&paged_gqa_decode_kernel);
 }
 
+// Dynamic shared memory of a merge CTA with `warps` warps: the staged batch
+// (8 KB a warp; at most 32 KB, within the default limit).
+static size_t merge_stage_bytes(int warps)
+{
+    return static_cast<size_t>(warps) * kMergeBatch * 32 * sizeof(float4);
+}
+
 cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                 int page_size, cudaStream_t stream, const char **site)
 {
@@ -1047,20 +1053,24 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, co
         return e;
     *site = "split-K merge kernel launch";
     cudaLaunchConfig_t cfg = {};
-    // Two warps per query head when the segments average 32 pieces or more
-    // (few long segments against many workers: at least two batches each).
+    // One CTA per (segment, query head), kSub warps taking turns over the
+    // batches of 16 pieces: 2 when the segments average 16 pieces or more, 4
+    // from 48 (few long segments against many workers).
     const int segs = a.batch * a.hkv;
-    const bool wide = static_cast<long long>(a.num_ctas) * kWarps >= 32ll * segs;
-    cfg.gridDim = dim3(static_cast<unsigned>(segs), 1, 1);
-    cfg.blockDim = dim3(static_cast<unsigned>(32 * a.group * (wide ? 2 : 1)), 1, 1);
-    cfg.dynamicSmemBytes = 0;
+    const long long workers = static_cast<long long>(a.num_ctas) * kWarps;
+    const int sub = workers >= 48ll * segs ? 4 : (workers >= 16ll * segs ? 2 : 1);
+    cfg.gridDim = dim3(static_cast<unsigned>(segs * a.group), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * sub), 1, 1);
+    cfg.dynamicSmemBytes = merge_stage_bytes(sub);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return wide ? cudaLaunchKernelEx(&cfg, splitk_merge_kernel<2>, a) : cudaLaunchKernelEx(&cfg, splitk_merge_kernel<1>, a);
+    if (sub == 4)
+        return cudaLaunchKernelEx(&cfg, splitk_merge_kernel<4>, a);
+    return sub == 2 ? cudaLaunchKernelEx(&cfg, splitk_merge_kernel<2>, a) : cudaLaunchKernelEx(&cfg, splitk_merge_kernel<1>, a);
 }
 
 cudaError_t upload_split_prefix(const uint32_t *prefix, int n)
