@@ -49,6 +49,8 @@
 // in flight and returns.
 #include <math.h>
 
+#include <mutex>
+
 #include "internal.h"
 
 namespace pkv {
@@ -848,10 +850,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
         atomicMax(&g_split_probe[blockIdx.x][1], static_cast<unsigned long long>(global_timer_ns()));
 }
 
-// One CTA per (segment, query head g of its group), so that the merge's reads
-// spread over the whole GPU; lane j owns dimensions 4j .. 4j+3.  The CTA
-// merges the partial states the workers covering the segment wrote for head
-// g, in list order, and writes the output row.  Pieces are taken 16 at a
+// One warp per (segment, query head g of its group), or kSub warps when the
+// segments have many pieces (a CTA per (segment, head) then, so that the
+// merge's reads spread over the whole GPU); lane j owns dimensions 4j ..
+// 4j+3.  The warps merge the partial states the workers covering the segment
+// wrote for head g, in list order, and write the output row.  Pieces are taken 16 at a
 // time: lane i finds the slot of piece i and loads its (m, l); every lane
 // stages its four dimensions of all 16 accumulators in shared memory; then
 // one exact rescale folds the batch into the running (M, L, A).  The order is
@@ -863,26 +866,24 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
 // pieces are walked worker by worker, skipping the empty ranges.
 constexpr int kMergeBatch = 16;
 
-// kSub warps per CTA: with segments of many pieces (few segments against many
-// workers) they take turns over the batches and their states are combined in
-// shared memory at the end, in sub-warp order.
+// kSub warps per head: with segments of many pieces (few segments against
+// many workers) they take turns over the batches and their states are
+// combined in shared memory at the end, in sub-warp order.
 template <int kSub>
-__global__ void __launch_bounds__(32 * kSub) splitk_merge_kernel(const DecodeArgs a)
+__global__ void __launch_bounds__(kSub == 1 ? 32 * PKV_MAX_GROUP : 32 * kSub) splitk_merge_kernel(const DecodeArgs a)
 {
     __shared__ uint32_t pre_s[kMaxSplitCtas + 1];
     __shared__ __align__(16) float red_a[kSub > 1 ? kSub : 1][32 * 4];   // read and written as float4
     __shared__ float red_ml[kSub > 1 ? kSub : 1][2];
-    extern __shared__ float4 merge_stage[];      // [kSub][kMergeBatch][32]: the batches' accumulators
-    const int seg = blockIdx.x / a.group, g = blockIdx.x % a.group;
-    const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31, sub = wi;
+    extern __shared__ float4 merge_stage[];      // [warps][kMergeBatch][32]: the batches' accumulators
+    const int wi = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // kSub = 1: one CTA per segment, warp g merges query head g; else one CTA
+    // per (segment, head g), its kSub warps taking turns over the batches
+    const int seg = kSub == 1 ? blockIdx.x : blockIdx.x / a.group;
+    const int g = kSub == 1 ? wi : blockIdx.x % a.group, sub = kSub == 1 ? 0 : wi;
     const int b = seg / a.hkv, h = seg % a.hkv;
     const int rank = h * a.batch + b;            // the segment's rank in list order (head-major)
 
-    if (a.split) {                               // the split's weight prefix sums (inputs, not the decode's output)
-        for (int c = threadIdx.x; c <= a.num_ctas; c += blockDim.x)
-            pre_s[c] = g_split_prefix[c];
-        __syncthreads();
-    }
     const float vsc = __ldg(a.v_scale + h);
     asm volatile("griddepcontrol.wait;" ::: "memory");   // the decode grid has finished
     const SegRecord r = a.segs[seg];
@@ -896,13 +897,21 @@ __global__ void __launch_bounds__(32 * kSub) splitk_merge_kernel(const DecodeArg
     // every range holds at least one chunk-head when T * wmin >= CT
     const bool dense = total * (a.split ? a.split_wmin : 1) >= sp.ct;
     const bool walk = !dense;
+    if (walk && a.split) {                       // the walk reads the split's weight prefix sums
+        for (int c = threadIdx.x; c <= a.num_ctas; c += blockDim.x)
+            pre_s[c] = g_split_prefix[c];
+        __syncthreads();
+    }
     const int n_known = w1 - w0 + 1;
     // walk state: worker w, its range [lo_w, hi_w), offset k of the next piece in it
     const int64_t end = start + n_seg;
     int w = w0;
-    int64_t lo_w = range_lo(sp, total, w);
-    int64_t hi_w = range_lo(sp, total, w + 1);
-    int64_t k = start - lo_w;
+    int64_t lo_w = 0, hi_w = 0, k = 0;
+    if (walk) {
+        lo_w = range_lo(sp, total, w);
+        hi_w = range_lo(sp, total, w + 1);
+        k = start - lo_w;
+    }
 
     float M = -INFINITY, L = 0.f;
     float A[4] = {0.f, 0.f, 0.f, 0.f};
@@ -1036,11 +1045,14 @@ const void *decode_kernel_for(int /*page_size*/)
 }
 
 // Dynamic shared memory of a merge CTA with `warps` warps: the staged batch
-// (8 KB a warp; at most 32 KB, within the default limit).
+// (8 KB a warp).
 static size_t merge_stage_bytes(int warps)
 {
     return static_cast<size_t>(warps) * kMergeBatch * 32 * sizeof(float4);
 }
+
+static std::mutex g_merge_mu;
+static bool g_merge_attr[64];   // per device: the merge kernel's shared-memory limit is raised
 
 cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, const CUtensorMap &tm_v,
                                 int page_size, cudaStream_t stream, const char **site)
@@ -1053,15 +1065,35 @@ cudaError_t launch_paged_decode(const DecodeArgs &a, const CUtensorMap &tm_k, co
         return e;
     *site = "split-K merge kernel launch";
     cudaLaunchConfig_t cfg = {};
-    // One CTA per (segment, query head), kSub warps taking turns over the
-    // batches of 16 pieces: 2 when the segments average 16 pieces or more, 4
-    // from 48 (few long segments against many workers).
+    // One warp per query head (one CTA per segment) while the segments average
+    // fewer than 16 pieces; else one CTA per (segment, query head) whose 2
+    // warps (from 16 pieces) or 4 (from 48: few long segments against many
+    // workers) take turns over the batches of 16 pieces.
     const int segs = a.batch * a.hkv;
     const long long workers = static_cast<long long>(a.num_ctas) * kWarps;
     const int sub = workers >= 48ll * segs ? 4 : (workers >= 16ll * segs ? 2 : 1);
-    cfg.gridDim = dim3(static_cast<unsigned>(segs * a.group), 1, 1);
-    cfg.blockDim = dim3(static_cast<unsigned>(32 * sub), 1, 1);
-    cfg.dynamicSmemBytes = merge_stage_bytes(sub);
+    const int warps = sub == 1 ? a.group : sub;
+    cfg.gridDim = dim3(static_cast<unsigned>(sub == 1 ? segs : segs * a.group), 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(32 * warps), 1, 1);
+    cfg.dynamicSmemBytes = merge_stage_bytes(warps);
+    {
+        int dev = -1;
+        cudaError_t e2 = cudaGetDevice(&dev);
+        if (e2 != cudaSuccess)
+            return e2;
+        if (dev < 0 || dev >= 64)
+            return cudaErrorInvalidDevice;
+        std::lock_guard<std::mutex> lk(g_merge_mu);
+        if (!g_merge_attr[dev]) {                // one warp per head of a group of up to 8: up to 64 KB
+            *site = "cudaFuncSetAttribute (merge shared memory)";
+            e2 = cudaFuncSetAttribute(splitk_merge_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(merge_stage_bytes(PKV_MAX_GROUP)));
+            if (e2 != cudaSuccess)
+                return e2;
+            g_merge_attr[dev] = true;
+            *site = "split-K merge kernel launch";
+        }
+    }
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
