@@ -274,6 +274,10 @@ pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dt
  * C(w) = 4 * (weights[0] + ... + weights[c-1]) + j * weights[c] for warp j
  * of CTA c, worker w covers list positions [T * C(w) / CT, T * C(w + 1) / CT)
  * of the T chunks, CT = C(4n).  Equal weights give exactly the default split.
+ * (The list the split cuts counts 3 empty chunks after every sequence's
+ * chunks of a kv head, the cost of the extra piece a range holding a
+ * sequence's end carries; a range's real edges are where its edges in that
+ * list fall.  Only when every range then holds a chunk: T * min weight >= CT.)
  * The math is unchanged; the pieces the split cuts (and so the last bits of
  * the result, within the accuracy bound) depend on the weights, and stay
  * deterministic for fixed weights.

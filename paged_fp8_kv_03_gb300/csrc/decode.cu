@@ -209,6 +209,29 @@ __device__ __forceinline__ int64_t range_lo(const Split &sp, int64_t total, int 
     return range_at(sp, total, c >= sp.ctas ? sp.ct : split_cw(sp, c, j, sp.pre[c], sp.pre[c + 1]));
 }
 
+// Real list position of virtual position xv in the list with `ghost` empty
+// chunks after every segment (ghost = 0: xv itself): in kv head h's part, the
+// largest sequence b with ps[b] + ghost * b <= rem holds it, at real offset
+// min(rem - ps[b] - ghost * b, its chunks).
+__device__ __forceinline__ int64_t real_position(const int *ps, int batch, int hkv, int ghost, int64_t xv)
+{
+    const int64_t per_head = ps[batch], per_head_v = per_head + static_cast<int64_t>(ghost) * batch;
+    if (per_head_v == 0 || xv >= per_head_v * hkv)
+        return per_head * hkv;
+    const int64_t h = xv / per_head_v, rem = xv - h * per_head_v;
+    int lo = 0, hi = batch - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (ps[mid] + static_cast<int64_t>(ghost) * mid <= rem)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int64_t c = rem - ps[lo] - static_cast<int64_t>(ghost) * lo;
+    const int np = ps[lo + 1] - ps[lo];
+    return h * per_head + ps[lo] + (c < np ? c : np);
+}
+
 struct Smem {
     static constexpr int kTile = kChunk * kHeadDim;         // bytes of one K (or V) chunk tile
     static constexpr int kStageBytes = 2 * kTile;
@@ -599,8 +622,18 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     }
     // Let the merge kernel get scheduled now; it waits for this grid to finish.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int64_t lo = range_at(sp, total, split_cw(sp, blockIdx.x, warp, pre_c0, pre_c1));
-    const int64_t hi = range_at(sp, total, split_cw(sp, blockIdx.x, warp + 1, pre_c0, pre_c1));
+    // The split runs over a virtual list with kGhostChunks empty chunks after
+    // every segment, so that a range holding a segment's end (one more piece:
+    // a partial state, the next query rows, the new token) gets that much less
+    // real work; its real edges are where the virtual ones fall (a ghost maps
+    // to the next segment's start).  Only while every range holds a chunk
+    // (T * wmin >= CT): otherwise the plain split, which the merge can walk.
+    const int ghost = total * (a.split ? a.split_wmin : 1) >= sp.ct ? kGhostChunks : 0;
+    // lane 0 works out the range's start, lane 1 its end
+    const int64_t edge = real_position(pstart, a.batch, a.hkv, ghost,
+                                       range_at(sp, total + static_cast<int64_t>(ghost) * a.batch * a.hkv,
+                                                split_cw(sp, blockIdx.x, warp + (lane & 1), pre_c0, pre_c1)));
+    const int64_t lo = __shfl_sync(kFull, edge, 0), hi = __shfl_sync(kFull, edge, 1);
     if (lo >= hi) {                              // warp-level: no CTA barrier follows
         if (a.probe && lane == 0)
             atomicMax(&g_split_probe[blockIdx.x][1], static_cast<unsigned long long>(global_timer_ns()));

@@ -43,6 +43,9 @@ struct AppendArgs {
 // zero (the tensor cores' fp32 accumulation rounds toward zero, so the error
 // of one unbroken chain grows with its length).
 constexpr int kFoldChunks = 128;
+// Empty chunks the decode split counts after every segment (the cost of one
+// more piece in a worker's range, two to three chunks' streaming time).
+constexpr int kGhostChunks = 3;
 
 // Weighted split.  Worker warp w = 4c + j of CTA c takes a share of the
 // chunk-head list proportional to its CTA's weight (an integer in
