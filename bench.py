@@ -31,6 +31,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -70,11 +71,19 @@ def _tensor_peak():
     return 1700.0, "fallback (sustained bf16; f16 same nominal rate)"
 
 
+def _code_only(text: str) -> str:
+    """C/CUDA source without comments and blank lines (a comment edit does
+    not change the kernel the counters were taken on)."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def _kernel_sha() -> str:
     h = hashlib.sha256()
     for f in ("decode.cu", "device.cuh", "internal.h"):
-        with open(os.path.join(ROOT, "paged_fp8_kv_03_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, "paged_fp8_kv_03_gb300", "csrc", f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -11,21 +11,25 @@
 // design streams every KV byte exactly once at full HBM rate.
 //
 // Work split.  The (sequence, kv head) segments are laid end to end as one
-// list of "page-heads" (one page of one kv head, 2 x P x 128 bytes), kv head
+// list of 16-token chunks (one chunk of one kv head, 2 x 16 x 128 bytes), kv head
 // by kv head (every sequence's segment of head 0, then of head 1, ...).  Every
 // warp of the persistent grid is an independent worker that takes a
 // contiguous range of that list, whatever the sequence lengths (split-K /
 // flash-decoding): an equal share, or a share proportional to its CTA's
 // weight when the host has installed weights for this grid (the CTAs land on
 // the same SMs call after call, and some SMs stream slower than others, so
-// calibrated weights let every worker finish at the same time).  A worker's
-// range cuts segments into
-// pieces; a piece covering a whole segment writes the final output, the
-// others write a partial softmax state (running max m, sum l, unnormalised
-// accumulator) into workspace slot worker + (the segment's rank in the list).  A second kernel, one
-// CTA per (segment, head) with a thread per dimension, merges the pieces in
-// worker order (deterministic); it is a programmatic dependent launch, so it
-// is already resident when the first kernel's last warps finish.
+// calibrated weights let every worker finish at the same time); the shares
+// count a few empty "ghost" chunks after every segment, the cost of the
+// extra piece a range holding a segment's end carries.  A worker's range
+// cuts segments into pieces; a piece covering a whole segment writes the
+// final output, the others write a partial softmax state (running max m, sum
+// l, unnormalised accumulator) into workspace slot worker + (the segment's
+// rank in the list).  A second kernel, one warp per (segment, query head),
+// merges the pieces in worker order (deterministic); it is a programmatic
+// dependent launch, so it is already resident when the first kernel's last
+// warps finish.  With the fused append, the worker that consumes the chunk
+// holding a new token stores it to the pool and patches its own copy of the
+// chunk, so the call never reads its own store back.
 //
 // Inside a worker (one warp): lane 0 issues two TMA tensor loads per page
 // (K tile, V tile; 128-byte swizzled, evict-first in L2) into the warp's own
