@@ -1,5 +1,6 @@
 """Host-side helpers of bench.py that need no GPU: the packed input staging
-used by the end-to-end measurements."""
+used by the end-to-end measurements, and the hash that ties the reported
+DRAM traffic to the decode sources it was measured on."""
 import os
 import sys
 
@@ -55,3 +56,27 @@ def test_host_stage_non_contiguous_input(no_pinning):
     t = torch.arange(24, dtype=torch.float32).view(4, 6).t()      # a transposed view
     st = bench._HostStage({"t": t})
     assert torch.equal(st.upload("cpu")["t"], t.contiguous())
+
+
+def test_kernel_hash_ignores_comments_but_not_code():
+    """The DRAM traffic bench.py reports is tied to the decode sources the
+    ncu counters were taken on: comments and blank lines may change without
+    invalidating it, any code token may not."""
+    src = (
+        "// header comment\n"
+        "#include \"internal.h\"\n"
+        "/* a block\n   comment */\n"
+        "__global__ void k(int *p)   // trailing\n"
+        "{\n"
+        "\n"
+        "    p[0] = 1;   /* inline */ p[1] = 2;\n"
+        "}\n"
+    )
+    base = bench._code_only(src)
+    assert "comment" not in base and "trailing" not in base and "inline" not in base
+    assert bench._code_only(src.replace("// header comment", "// another header")) == base
+    assert bench._code_only(src.replace("\n\n", "\n\n\n\n")) == base
+    assert bench._code_only(src.replace("p[1] = 2", "p[1] = 3")) != base
+    assert bench._code_only(src.replace("p[0]", "p [0]")) != base
+    # the committed traffic table is keyed by this hash of the current sources
+    assert len(bench._kernel_sha()) == 16
