@@ -282,6 +282,14 @@ pkv_status pkv_append_decode_fp8(const void *k_new, const void *v_new, int in_dt
  * the result, within the accuracy bound) depend on the weights, and stay
  * deterministic for fixed weights.
  *
+ * Weights belong to the device's current context: after a cudaDeviceReset
+ * they no longer apply (the calls split evenly and
+ * pkv_decode_get_split_weights reports none) until they are installed again.
+ * (A process that resets a device should restart before decoding on it
+ * again: the split-K merge kernel's raised shared-memory limit is not set up
+ * anew, so decode calls with more than 6 query heads per kv head then fail
+ * with PKV_ERR_CUDA.  Everything else is set up again on the next call.)
+ *
  * pkv_decode_set_split_weights installs n weights, each an integer in
  * [768, 1280] (1024 +- 25%), for the current device; they apply to decode calls
  * (pkv_paged_gqa_decode, pkv_append_decode_fp8 and the allocation-free entry

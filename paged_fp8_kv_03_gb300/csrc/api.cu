@@ -9,6 +9,7 @@
 #include <tuple>
 #include <vector>
 
+#include "context.h"
 #include "internal.h"
 
 namespace pkv {
@@ -18,11 +19,11 @@ namespace {
 std::mutex g_mu;
 std::map<int, int> g_sm_count;                              // device -> SMs
 std::map<std::tuple<int, const void *, size_t>, int> g_occupancy;   // (device, kernel, smem) -> CTAs per SM
-// (device, kernel) -> the kernel's dynamic shared memory limit set so far
-// (only ever raised: every page size runs the same kernel, so a limit per
-// page size would let one page size's smaller setting undercut another's
-// launch).
-std::map<std::tuple<int, const void *>, size_t> g_smem_attr;
+// (context, kernel) -> the kernel's dynamic shared memory limit set so far
+// in that context (only ever raised: every page size runs the same kernel, so
+// a limit per page size would let one page size's smaller setting undercut
+// another's launch; a device reset starts a new context at the default).
+std::map<std::tuple<unsigned long long, const void *>, size_t> g_smem_attr;
 std::atomic<int> g_withhold{-1};                            // failure-detection test facility (-1 = off)
 
 // Weighted split of each device: the per-CTA weights for one grid size (the
@@ -31,8 +32,26 @@ struct SplitState {
     std::vector<uint16_t> weights;
     long long ct = 0;                                       // 4 * sum of the weights
     int wmin = 0, wmax = 0;
+    unsigned long long ctx = 0;                             // context the device table was written in (0: unknown)
 };
 std::map<int, SplitState> g_split;                          // device -> weights
+
+// The device's installed weights, or nullptr.  Weights uploaded in an earlier
+// context of the device (before a device reset) are gone from the device
+// table the kernels read, so they are dropped: the device splits evenly until
+// weights are installed again.  Call with g_mu held.
+const SplitState *live_split(int dev)
+{
+    auto it = g_split.find(dev);
+    if (it == g_split.end())
+        return nullptr;
+    unsigned long long ctx = 0;
+    if (it->second.ctx != 0 && current_context_id(&ctx) && ctx != it->second.ctx) {
+        g_split.erase(it);
+        return nullptr;
+    }
+    return &it->second;
+}
 thread_local int t_last_cuda = 0;                           // error behind this thread's last PKV_ERR_CUDA
 thread_local const char *t_last_site = "";                  // the call that failed
 thread_local char t_last_text[160];
@@ -163,9 +182,11 @@ int decode_num_ctas(int page_size, int batch, int max_ctas)
     const void *kern = decode_kernel_for(page_size);
     int per_sm = 0;
     {
+        unsigned long long ctx = 0;
+        const bool known = current_context_id(&ctx);   // (no id yet: set the limit, remember nothing)
         std::lock_guard<std::mutex> lk(g_mu);
-        auto key_attr = std::make_tuple(dev, kern);
-        auto ia = g_smem_attr.find(key_attr);
+        auto key_attr = std::make_tuple(ctx, kern);
+        auto ia = known ? g_smem_attr.find(key_attr) : g_smem_attr.end();
         if (ia == g_smem_attr.end() || ia->second < smem) {
             const cudaError_t e =
                 cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -173,7 +194,8 @@ int decode_num_ctas(int page_size, int batch, int max_ctas)
                 cuda_failed(e, "cudaFuncSetAttribute (decode shared memory)");
                 return 0;
             }
-            g_smem_attr[key_attr] = smem;
+            if (known)
+                g_smem_attr[key_attr] = smem;
         }
         auto key = std::make_tuple(dev, kern, smem);
         auto it = g_occupancy.find(key);
@@ -329,12 +351,12 @@ pkv_status decode_impl(const void *k_new, const void *v_new, int in_dtype, int n
     a.probe = probe ? 1 : 0;
     {
         std::lock_guard<std::mutex> lk(g_mu);
-        auto it = g_split.find(current_device());
-        if (it != g_split.end() && static_cast<int>(it->second.weights.size()) == ctas) {
+        const SplitState *live = live_split(current_device());
+        if (live != nullptr && static_cast<int>(live->weights.size()) == ctas) {
             a.split = 1;
-            a.split_ct = it->second.ct;
-            a.split_wmin = it->second.wmin;
-            a.split_wmax = it->second.wmax;
+            a.split_ct = live->ct;
+            a.split_wmin = live->wmin;
+            a.split_wmax = live->wmax;
         }
     }
     if (probe_ctas)
@@ -375,6 +397,8 @@ pkv_status set_split(const uint16_t *weights, int n)
     const cudaError_t e = upload_split_prefix(prefix.data(), n);
     if (e != cudaSuccess)
         return cuda_failed(e);
+    unsigned long long ctx = 0;
+    st.ctx = current_context_id(&ctx) ? ctx : 0;
     st.weights.assign(weights, weights + n);
     st.ct = static_cast<long long>(kWarps) * prefix[n];
     g_split[dev] = st;
@@ -542,13 +566,13 @@ pkv_status pkv_decode_get_split_weights(uint16_t *weights, int capacity, int *n)
     if (dev < 0)
         return cuda_failed(cudaGetLastError());
     std::lock_guard<std::mutex> lk(g_mu);
-    auto it = g_split.find(dev);
-    const int have = it == g_split.end() ? 0 : static_cast<int>(it->second.weights.size());
+    const SplitState *live = live_split(dev);
+    const int have = live == nullptr ? 0 : static_cast<int>(live->weights.size());
     *n = have;
     if (have > capacity)
         return PKV_ERR_SHAPE;
     for (int c = 0; c < have; ++c)
-        weights[c] = it->second.weights[c];
+        weights[c] = live->weights[c];
     return PKV_OK;
 }
 

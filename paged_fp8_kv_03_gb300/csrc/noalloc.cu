@@ -31,6 +31,7 @@
 #include <algorithm>
 #include <mutex>
 
+#include "context.h"
 #include "internal.h"
 
 namespace {
@@ -42,9 +43,6 @@ constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
-typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
-
 struct ScratchEntry {
     unsigned long long ctx_id = 0;   // context the address belongs to (0: none yet)
     void *ptr = nullptr;
@@ -52,8 +50,9 @@ struct ScratchEntry {
 
 std::mutex g_noalloc_mu;
 ScratchEntry g_noalloc[64];
-CtxGetCurrentFn g_ctx_get_current = nullptr;
-CtxGetIdFn g_ctx_get_id = nullptr;
+
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
 
 template <typename Fn>
 Fn driver_fn(const char *name)
@@ -66,18 +65,6 @@ Fn driver_fn(const char *name)
     return reinterpret_cast<Fn>(fn);
 }
 
-// Unique id (for the life of the process) of the current device's context.
-bool current_context_id(unsigned long long *id)
-{
-    if (!g_ctx_get_current)
-        g_ctx_get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
-    if (!g_ctx_get_id)
-        g_ctx_get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
-    CUcontext ctx = nullptr;
-    return g_ctx_get_current && g_ctx_get_id && g_ctx_get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
-           g_ctx_get_id(ctx, id) == CUDA_SUCCESS;
-}
-
 void *scratch_for_current_device()
 {
     int dev = -1;
@@ -86,12 +73,12 @@ void *scratch_for_current_device()
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
     ScratchEntry &e = g_noalloc[dev];
     unsigned long long id = 0;
-    if (e.ptr != nullptr && current_context_id(&id) && id == e.ctx_id)
+    if (e.ptr != nullptr && pkv::current_context_id(&id) && id == e.ctx_id)
         return e.ptr;
     // Set-up for this device (or its new context): the lookup also makes the
     // device's primary context current if it was not yet.
     void *p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !current_context_id(&id))
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !pkv::current_context_id(&id))
         return nullptr;
     e.ptr = p;
     e.ctx_id = id;
@@ -99,6 +86,16 @@ void *scratch_for_current_device()
 }
 
 }  // namespace
+
+bool pkv::current_context_id(unsigned long long *id)
+{
+    // function-local statics: looked up once, thread-safely
+    static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    CUcontext ctx = nullptr;
+    return get_current && get_id && get_current(&ctx) == CUDA_SUCCESS && ctx != nullptr &&
+           get_id(ctx, id) == CUDA_SUCCESS;
+}
 
 extern "C" size_t pkv_decode_noalloc_scratch_bytes(void)
 {

@@ -54,6 +54,7 @@
 // drains its own copies and MMAs, frees TMEM and exits.
 #include <mutex>
 
+#include "context.h"
 #include "internal.h"
 #include "tcgen05.cuh"
 
@@ -814,7 +815,7 @@ __global__ void __launch_bounds__(kPThreads, 1)
 }
 
 std::mutex g_prefill_mu;
-bool g_prefill_attr[64] = {false};
+unsigned long long g_prefill_attr_ctx[64] = {0};   // per device: the context the kernel's limit was raised in
 
 }  // namespace
 
@@ -836,13 +837,15 @@ cudaError_t launch_paged_prefill(const PrefillArgs &a, const CUtensorMap &tm_q, 
     if (dev < 0 || dev >= 64)
         return cudaErrorInvalidDevice;
     {
+        unsigned long long ctx = 0;
+        const bool known = current_context_id(&ctx);
         std::lock_guard<std::mutex> lk(g_prefill_mu);
-        if (!g_prefill_attr[dev]) {
+        if (!known || g_prefill_attr_ctx[dev] != ctx) {
             e = cudaFuncSetAttribute(paged_prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      static_cast<int>(PS::bytes()));
             if (e != cudaSuccess)
                 return e;
-            g_prefill_attr[dev] = true;
+            g_prefill_attr_ctx[dev] = known ? ctx : 0;
         }
     }
     const int64_t pieces = a.rows_cap * 8;
